@@ -1,0 +1,101 @@
+/*
+ * moe_oracle.h -- plain CPU oracle for the top-k routed Mixture-of-Experts FFN layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may include, link or call this
+ * code: only the tests, the smoke check and the benchmark's CPU-baseline leg use it.  It
+ * shares no source, header, table or helper with the CUDA library.
+ *
+ * What the layer computes.  The pages define the layer only in prose: a sparse network of
+ * many expert sub-networks of which each token activates a small part ("AI MAX+ 395部署
+ * Qwen3大模型：GFX1151引擎实测优化解析", explanatory paragraph under "MOE 内核优化"), run on
+ * the timed path as a "selected-MoE" kernel ("AIMA AMD395 Qwen3.6 35B Windows Engine",
+ * section "性能优化做了什么").  The oracle follows the plainest standard reading of that
+ * layer, step by step:
+ *   1. router logits  l[t,e] = fp32( sum_h x[t,h] * Wr[e,h] )  (+ b[e], fp32 add)
+ *   2. selection      S = the k largest logits, lower expert index first on ties
+ *   3. weights        p = softmax over all E logits (fp64); w_j = p[S_j] / sum_i p[S_i] -> fp32
+ *   4. permutation    stable counting sort of the T*k (token, slot) pairs by expert
+ *   5. expert FFN     h = bf16( silu(Wg x) * (Wu x) ),  y = Wd h        (fp64 sums)
+ *   6. shared expert  same as 5 with the shared weights, weight 1, every token
+ *   7. combine        out[t] = bf16( sum_j w_j * y_j + y_shared )        (fp64 sum)
+ * All sums are taken in double; the only roundings are the ones listed (fp32 logits,
+ * fp32 weights, bf16 h, bf16 out).  "exact" mode skips the bf16 rounding of h.
+ *
+ * Layouts: row-major, [out, in] linear convention.  bf16 values travel as their 16-bit
+ * patterns (uint16_t).  x [T,H]; Wr [E,H]; b [E] or NULL; Wg, Wu [E,I,H]; Wd [E,H,I];
+ * Wsg, Wsu [Is,H]; Wsd [H,Is] (all NULL and Is = 0 when there is no shared expert).
+ * Logits are assumed finite.
+ */
+#ifndef MOE_ORACLE_H
+#define MOE_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* bf16 pattern -> double (exact). */
+double moe_ref_bf16_to_double(uint16_t b);
+/* double -> bf16 pattern, round to nearest, ties to even, in one rounding step. */
+uint16_t moe_ref_double_to_bf16(double v);
+/* silu(g) = g / (1 + exp(-g)) in double. */
+double moe_ref_silu(double g);
+
+/* Step 1: router logits [T,E] (fp32). b may be NULL. */
+void moe_ref_router_logits(int H, int E, int T, const uint16_t *x, const uint16_t *w_router,
+                           const float *b_router, float *logits);
+
+/* Steps 2-3 from given fp32 logits: ids [T,k] int32 in rank order, weights [T,k] fp32. */
+void moe_ref_route_from_logits(int E, int k, int T, const float *logits, int32_t *ids, float *w);
+
+/* Step 4: offsets [E+1], perm [T*k] (row -> pair index t*k+j), inv [T*k] (pair -> row).
+ * Returns 0, or -1 if an id lies outside [0,E). */
+int moe_ref_permute(int E, int k, int T, const int32_t *ids, int32_t *offsets, int32_t *perm,
+                    int32_t *inv);
+
+/* Step 5 for the rows of the permuted order: h_rows [T*k, I] (bf16 pattern) and
+ * y_rows [T*k, H] (fp32 rounding of the fp64 sum), computed from x, the permutation and
+ * the routed weights.  When h_in is not NULL the down projection uses those bf16 h rows
+ * instead of the oracle's own (to isolate the down projection).  When shared_y is not
+ * NULL and Is > 0, also step 6: shared_y [T,H] (fp32 rounding of the fp64 sum). */
+void moe_ref_expert_ffn(int H, int E, int k, int I, int Is, int T, const uint16_t *x,
+                        const int32_t *offsets, const int32_t *perm, const uint16_t *w_gate,
+                        const uint16_t *w_up, const uint16_t *w_down, const uint16_t *ws_gate,
+                        const uint16_t *ws_up, const uint16_t *ws_down, const uint16_t *h_in,
+                        uint16_t *h_rows, float *y_rows, float *shared_y);
+
+/* Step 7 from unfused rows: out[t] = bf16( sum_j w[t,j] * y_rows[inv[t*k+j]] + shared_y[t] ). */
+void moe_ref_combine(int H, int k, int T, const float *y_rows, const int32_t *inv,
+                     const float *topk_w, const float *shared_y, uint16_t *out);
+
+/* The whole layer, token by token (steps 1-7).  When ids_in/w_in are not NULL they replace
+ * steps 1-3 (the oracle then consumes a given routing).  exact != 0 skips the bf16 rounding
+ * of h.  out [T,H] bf16 pattern; out_f64 [T,H] (may be NULL) receives the unrounded sum.
+ * x_next (may be NULL) receives bf16( x + out ), the residual update of a layer stack.
+ * ids_out / w_out (may be NULL) receive the routing used.  n_threads <= 0 uses OpenMP's
+ * default; the loop over tokens is the only parallel loop. */
+void moe_ref_forward(int H, int E, int k, int I, int Is, int T, const uint16_t *x,
+                     const uint16_t *w_router, const float *b_router, const uint16_t *w_gate,
+                     const uint16_t *w_up, const uint16_t *w_down, const uint16_t *ws_gate,
+                     const uint16_t *ws_up, const uint16_t *ws_down, const int32_t *ids_in,
+                     const float *w_in, int exact, int n_threads, uint16_t *out,
+                     double *out_f64, uint16_t *x_next, int32_t *ids_out, float *w_out);
+
+/* Second, independent evaluation of the combine: expert-major over all E experts with a
+ * dense mask (weight w if the expert is among the token's k, else the expert is skipped),
+ * no permutation.  Consumes the given routing ids/w.  out_f64 [T,H], unrounded. */
+void moe_ref_dense_masked(int H, int E, int k, int I, int Is, int T, const uint16_t *x,
+                          const uint16_t *w_gate, const uint16_t *w_up, const uint16_t *w_down,
+                          const uint16_t *ws_gate, const uint16_t *ws_up,
+                          const uint16_t *ws_down, const int32_t *ids, const float *w,
+                          int exact, double *out_f64);
+
+/* Number of threads the OpenMP loop of moe_ref_forward would use for n_threads. */
+int moe_ref_threads(int n_threads);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_ORACLE_H */
