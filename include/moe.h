@@ -1,0 +1,171 @@
+/*
+ * moe.h -- C ABI of the GB300-native top-k routed Mixture-of-Experts FFN layer (libmoe.so).
+ *
+ * The layer.  The pages describe the layer only in prose: a network of many expert
+ * sub-networks of which each token activates a small part ("AI MAX+ 395部署Qwen3大模型：
+ * GFX1151引擎实测优化解析", explanatory MoE paragraph under "MOE 内核优化"), executed on the
+ * timed path of a batch-1 BF16 engine by a "selected-MoE" kernel ("AIMA AMD395 Qwen3.6 35B
+ * Windows Engine", section "性能优化做了什么").  This library computes the standard reading of
+ * that layer, for T tokens of hidden size H, E routed experts, top-k, expert intermediate I
+ * and a shared expert of intermediate Is:
+ *   logits   l[t,e] = sum_h x[t,h] Wr[e,h] (+ b[e])                     fp32
+ *   route    ids[t,0..k) = the k largest logits (lower index first on equal logits),
+ *            descending; w[t,j] = exp(l[t,ids_j]) / sum_i exp(l[t,ids_i])   (softmax over
+ *            all E followed by renormalisation over the k chosen; the full denominator cancels)
+ *   permute  stable counting sort of the T*k pairs p = t*k + j by expert id
+ *   experts  h = bf16( silu(Wg[e] x) * (Wu[e] x) ),  y = Wd[e] h        fp32 accumulate
+ *   shared   the same SwiGLU with the shared weights, weight 1, for every token
+ *   combine  out[t] = bf16( sum_j w[t,j] y[t,j] + y_shared[t] )
+ * and composes long prompts from q8192 / q4096 / q2048 / q1024 pieces plus an exact tail
+ * ("AIMA AMD395 Qwen3.6 35B Windows Engine", "性能优化做了什么": prompts split into a q8192
+ * tile, q1024 and a tail; "AIMA AMD395 Qwen3.6 35B Linux Engine", "Read this boundary first":
+ * resident q1024/q2048/q4096/q8192 buckets).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers (caller-allocated, caller-owned), row-major and
+ *     contiguous, 16-byte aligned, in the [out, in] linear convention.  bf16 tensors are passed
+ *     as moe_bf16 (the 16-bit pattern).  The library never allocates device memory and keeps no
+ *     state between calls other than per-device launch attributes and the optional timing table.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call is
+ *     asynchronous on that stream; inputs must stay valid until the stream reaches the work.
+ *   - Arguments are validated on the host before any launch; an invalid call launches
+ *     nothing and returns an error status.  T == 0 returns MOE_OK and does nothing.
+ *   - Device-side failures (a bounded wait that ran out, an expert id out of range) are
+ *     recorded in a status word in the workspace and read with moe_check_status().
+ *   - Supported shapes: H % 128 == 0, I % 128 == 0, Is % 128 == 0 (or Is == 0: no shared
+ *     expert), 1 <= k <= min(E, 32), E <= 1024, H <= 16384, I, Is <= 8192.  Router logits
+ *     must be finite.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16; /* bit pattern of a bfloat16 value */
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,        /* null pointer, negative size, k > E, misalignment, ... */
+    MOE_ERR_WORKSPACE_TOO_SMALL = 2,
+    MOE_ERR_UNSUPPORTED_SHAPE = 3,  /* outside the supported shapes listed above */
+    MOE_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed */
+    MOE_ERR_TIMEOUT = 5,            /* a device-side bounded wait ran out (see moe_check_status) */
+    MOE_ERR_NOT_IMPLEMENTED = 6
+} moe_status;
+
+/* Layer shape.  shared_inter == 0 means no shared expert. */
+typedef struct {
+    int hidden;       /* H */
+    int n_experts;    /* E */
+    int top_k;        /* k */
+    int inter;        /* I */
+    int shared_inter; /* Is */
+} moe_config;
+
+/* Device pointers to one layer's weights (bf16 unless noted). */
+typedef struct {
+    const moe_bf16 *w_router; /* [E, H] */
+    const float *b_router;    /* [E] fp32 router bias, or NULL (no bias) */
+    const moe_bf16 *w_gate;   /* [E, I, H] */
+    const moe_bf16 *w_up;     /* [E, I, H] */
+    const moe_bf16 *w_down;   /* [E, H, I] */
+    const moe_bf16 *ws_gate;  /* [Is, H]  (NULL when Is == 0) */
+    const moe_bf16 *ws_up;    /* [Is, H]  (NULL when Is == 0) */
+    const moe_bf16 *ws_down;  /* [H, Is]  (NULL when Is == 0) */
+} moe_weights;
+
+/* Text for a status code (static storage). */
+const char *moe_status_string(moe_status s);
+
+/* Bytes of device workspace needed by any call below for up to max_T tokens (moe_forward
+ * needs only min(max_T, 8192) tokens' worth, since it works piece by piece).  Returns 0 for
+ * an invalid or unsupported config.  The workspace must be 256-byte aligned. */
+size_t moe_workspace_size(const moe_config *cfg, int max_T);
+
+/* Router: logits, softmax, top-k and renormalisation.
+ * x [T,H] bf16 -> topk_ids [T,k] int32 and topk_w [T,k] fp32, slots in descending logit
+ * order.  logits_out [T,E] fp32 may be NULL; when given it receives the exact fp32 logits the
+ * selection used.  ws: workspace of moe_workspace_size(cfg, T) bytes (holds the logits when
+ * logits_out is NULL).  Computed on tensor cores (bf16 x bf16 -> fp32 accumulate). */
+moe_status moe_route(const moe_config *cfg, const moe_weights *w, const moe_bf16 *x, int T,
+                     float *logits_out, int32_t *topk_ids, float *topk_w, void *ws,
+                     size_t ws_bytes, void *stream);
+
+/* Softmax + top-k + renormalisation only, from given fp32 logits [T,E].  Bit-exact ids for
+ * identical logits (the selection compares fp32 values exactly, lower index first on ties). */
+moe_status moe_route_from_logits(const moe_config *cfg, const float *logits, int T,
+                                 int32_t *topk_ids, float *topk_w, void *stream);
+
+/* Permutation of the T*k (token, slot) pairs by expert: a stable counting sort.
+ * topk_ids [T,k] -> expert_offsets [E+1] (exclusive prefix sum of the per-expert counts,
+ * offsets[E] == T*k), perm [T*k] (row of the expert-sorted order -> pair index t*k+j),
+ * inv [T*k] (pair index -> row).  Pairs of one expert keep increasing pair order.  Bit-exact.
+ * ws: workspace of moe_workspace_size(cfg, T) bytes.  Ids outside [0,E) are a caller error:
+ * they are detected on the device, flagged in the status word, and the pair is dropped
+ * (inv = -1). */
+moe_status moe_permute(const moe_config *cfg, const int32_t *topk_ids, int T,
+                       int32_t *expert_offsets, int32_t *perm, int32_t *inv, void *ws,
+                       size_t ws_bytes, void *stream);
+
+/* Expert FFNs, unfused (for step-by-step checking).  Routed rows in the permuted order:
+ * h_rows [T*k, I] bf16 = bf16(silu(Wg[e] x_t) * (Wu[e] x_t)) and y_rows [T*k, H] fp32 =
+ * Wd[e] h, for row r of expert e holding pair perm[r] of token perm[r]/k.  When shared_y is not
+ * NULL and Is > 0, also shared_y [T,H] fp32 = the shared expert applied to every token.
+ * expert_offsets/perm as produced by moe_permute.  ws: moe_workspace_size(cfg, T) bytes. */
+moe_status moe_expert_ffn(const moe_config *cfg, const moe_weights *w, const moe_bf16 *x, int T,
+                          const int32_t *expert_offsets, const int32_t *perm, moe_bf16 *h_rows,
+                          float *y_rows, float *shared_y, void *ws, size_t ws_bytes,
+                          void *stream);
+
+/* Weighted combine: out[t] = bf16( sum_j topk_w[t,j] * y_rows[inv[t*k+j]] + shared_y[t] ).
+ * shared_y may be NULL (no shared term).  Deterministic (fixed slot order, fp32). */
+moe_status moe_combine(const moe_config *cfg, const float *y_rows, const int32_t *inv,
+                       const float *topk_w, const float *shared_y, int T, moe_bf16 *out,
+                       void *stream);
+
+/* The whole layer, fused: x [T,H] -> out [T,H] bf16.  T is split greedily into pieces of
+ * 8192, 4096, 2048 and 1024 tokens and an exact tail (no padding); every piece runs the same
+ * kernels, so the result equals the concatenation of per-piece calls.  T == 1 takes the
+ * decode path (HBM-streaming GEMVs).  x_next may be NULL; when given it receives
+ * bf16(x + out), the residual-stream update of a layer stack (fused into the last kernel).
+ * x_next may alias x.  ws: moe_workspace_size(cfg, T) bytes.  The fused combine adds fp32
+ * partial sums with atomics, so the fp32 summation order can differ from run to run (the
+ * result stays within the layer's tolerance, but is not bit-reproducible). */
+moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const moe_bf16 *x, int T,
+                       moe_bf16 *out, moe_bf16 *x_next, void *ws, size_t ws_bytes,
+                       void *stream);
+
+/* Reads and clears the device status word in `ws` (synchronises `stream`).  *device_status
+ * receives MOE_OK or the first error recorded by a kernel (MOE_ERR_TIMEOUT for a wait that
+ * ran out, MOE_ERR_INVALID_ARG for an out-of-range expert id).  Returns MOE_ERR_CUDA if the
+ * copy fails. */
+moe_status moe_check_status(void *ws, size_t ws_bytes, int *device_status, void *stream);
+
+/* Sizes of the pieces moe_forward splits T into: writes up to max_pieces sizes to `pieces`
+ * and returns the number of pieces (host only, no device work); -1 if T < 0. */
+int moe_plan_pieces(int T, int *pieces, int max_pieces);
+
+/* Number of kernels this library has launched in this process (host counter). */
+uint64_t moe_launch_count(void);
+
+/* Optional per-kernel timing.  While enabled, every kernel launch is bracketed by CUDA events
+ * on its stream; moe_timing_read() synchronises them and returns, for kernel class `name`
+ * (see moe_timing_name()), the number of launches and their total device time in ms, then
+ * forgets them.  Returns MOE_ERR_INVALID_ARG for an unknown name.  Not for use inside CUDA
+ * graph capture. */
+moe_status moe_timing_enable(int enable);
+moe_status moe_timing_read(const char *name, int *launches, double *total_ms);
+/* Name of kernel class i (0 <= i < moe_timing_classes()), or NULL. */
+const char *moe_timing_name(int i);
+int moe_timing_classes(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -1,0 +1,559 @@
+// moe_abi.cu -- the extern "C" entry points of include/moe.h: argument validation,
+// workspace carving, tensor-map encoding, and the order of kernel launches for each call.
+//
+// moe_forward composes a prompt of any length from pieces of 8192, 4096, 2048 and 1024
+// tokens and an exact tail ("AIMA AMD395 Qwen3.6 35B Windows Engine", "性能优化做了什么":
+// any prompt split into a q8192 tile, q1024 and a tail; "AIMA AMD395 Qwen3.6 35B Linux
+// Engine", "Read this boundary first": resident q1024/q2048/q4096/q8192 buckets).  The pages
+// pad the last bucket; here the tail runs at its exact length, because the layer treats every
+// token independently and the kernels take any token count (padding would only add work).
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ bookkeeping --
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+std::atomic<bool> g_timing{false};
+std::mutex g_timing_mu;
+struct TimedPair {
+    cudaEvent_t a, b;
+};
+std::vector<TimedPair> g_timed[KC_COUNT];
+
+const char *const kClassNames[KC_COUNT] = {
+    "router_gemm", "topk",          "permute",       "tile_prefix",   "gateup_gemm",
+    "down_gemm",   "shared_gateup", "shared_down",   "finalize",      "combine",
+    "zero",        "decode_router", "decode_gateup", "decode_down"};
+}  // namespace
+
+const char *kernel_class_name(int kc) { return (kc >= 0 && kc < KC_COUNT) ? kClassNames[kc] : nullptr; }
+
+LaunchScope::LaunchScope(int kc_, cudaStream_t s) : kc(kc_), stream(s), ev0(nullptr), ev1(nullptr), timed(false) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (g_timing.load(std::memory_order_relaxed)) {
+        if (cudaEventCreate(&ev0) == cudaSuccess && cudaEventCreate(&ev1) == cudaSuccess) {
+            timed = cudaEventRecord(ev0, s) == cudaSuccess;
+        }
+    }
+}
+
+LaunchScope::~LaunchScope() {
+    if (timed && cudaEventRecord(ev1, stream) == cudaSuccess) {
+        std::lock_guard<std::mutex> lk(g_timing_mu);
+        g_timed[kc].push_back({ev0, ev1});
+        return;
+    }
+    if (ev0) cudaEventDestroy(ev0);
+    if (ev1) cudaEventDestroy(ev1);
+}
+
+const DeviceInfo &device_info() {
+    static DeviceInfo infos[64];
+    static bool have[64] = {false};
+    static std::mutex mu;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!have[dev]) {
+        int sms = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        infos[dev].sm_count = sms > 0 ? sms : 1;
+        have[dev] = true;
+    }
+    return infos[dev];
+}
+
+// ------------------------------------------------------------------ tensor maps --
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+}  // namespace
+
+bool encode_tmap_2d_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                         uint32_t box_rows, uint32_t box_cols) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// -------------------------------------------------------------- workspace layout --
+
+namespace {
+
+constexpr int kMaxPiece = 8192;
+
+size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
+struct Layout {
+    size_t status, logits, ids, topw, offsets, tiles, perm, inv, h, h_s, acc, total;
+};
+
+Layout layout(const moe_config &c, int T) {
+    Layout L;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        size_t r = o;
+        o += align256(bytes);
+        return r;
+    };
+    const size_t Tt = (size_t)(T > 0 ? T : 1);
+    L.status = take(256);
+    L.logits = take(Tt * c.n_experts * 4);
+    L.ids = take(Tt * c.top_k * 4);
+    L.topw = take(Tt * c.top_k * 4);
+    L.offsets = take((size_t)(c.n_experts + 1) * 4);
+    L.tiles = take((size_t)(c.n_experts + 1) * 4);
+    L.perm = take(Tt * c.top_k * 4);
+    L.inv = take(Tt * c.top_k * 4);
+    L.h = take(Tt * c.top_k * c.inter * 2);
+    L.h_s = take(Tt * (size_t)c.shared_inter * 2);
+    L.acc = take(Tt * c.hidden * 4);
+    L.total = o;
+    return L;
+}
+
+template <typename T>
+T *at(void *ws, size_t off) {
+    return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status check_config(const moe_config *c) {
+    if (!c) return MOE_ERR_INVALID_ARG;
+    if (c->hidden <= 0 || c->n_experts <= 0 || c->top_k <= 0 || c->inter <= 0 || c->shared_inter < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (c->top_k > c->n_experts) return MOE_ERR_INVALID_ARG;
+    if (c->top_k > 32 || c->n_experts > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (c->hidden % 128 || c->inter % 128 || c->shared_inter % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (c->hidden > 16384 || c->inter > 8192 || c->shared_inter > 8192) return MOE_ERR_UNSUPPORTED_SHAPE;
+    return MOE_OK;
+}
+
+moe_status check_weights(const moe_config *c, const moe_weights *w, bool router, bool experts) {
+    if (!w) return MOE_ERR_INVALID_ARG;
+    if (router && (!w->w_router || !aligned16(w->w_router))) return MOE_ERR_INVALID_ARG;
+    if (experts) {
+        if (!w->w_gate || !w->w_up || !w->w_down) return MOE_ERR_INVALID_ARG;
+        if (!aligned16(w->w_gate) || !aligned16(w->w_up) || !aligned16(w->w_down)) return MOE_ERR_INVALID_ARG;
+        if (c->shared_inter > 0) {
+            if (!w->ws_gate || !w->ws_up || !w->ws_down) return MOE_ERR_INVALID_ARG;
+            if (!aligned16(w->ws_gate) || !aligned16(w->ws_up) || !aligned16(w->ws_down))
+                return MOE_ERR_INVALID_ARG;
+        }
+    }
+    return MOE_OK;
+}
+
+moe_status check_ws(const moe_config *c, void *ws, size_t ws_bytes, int T) {
+    if (!ws) return MOE_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < layout(*c, T).total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    return MOE_OK;
+}
+
+moe_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return MOE_OK;
+    return MOE_ERR_CUDA;
+}
+
+#define MOE_TRY(expr)                          \
+    do {                                       \
+        moe_status _st = (expr);               \
+        if (_st != MOE_OK) return _st;         \
+    } while (0)
+#define MOE_CUDA(expr) MOE_TRY(cuda_status(expr))
+
+// Router logits on tensor cores: logits[T,E] = x Wr^T + b.
+moe_status run_router_gemm(const moe_config &c, const moe_weights &w, const uint16_t *x, int T,
+                           float *logits, int *status, cudaStream_t s) {
+    CUtensorMap tm;
+    if (!encode_tmap_2d_bf16(&tm, w.w_router, (uint64_t)c.n_experts, (uint64_t)c.hidden, kTileM, 64))
+        return MOE_ERR_CUDA;
+    GemmArgs a{};
+    a.b_src = x;
+    a.K = c.hidden;
+    a.n_groups = 1;
+    a.M_single = T;
+    a.F = c.n_experts;
+    a.out = logits;
+    a.ld = c.n_experts;
+    a.bias = w.b_router;
+    a.status = status;
+    MOE_CUDA(launch_gemm(EPI_F32, a, tm, tm, KC_ROUTER_GEMM, s));
+    return MOE_OK;
+}
+
+// Shared expert over T tokens: h_s = SwiGLU(x), then Ws_down h_s stored (not added) into
+// out (fp32 [T,H]).
+moe_status run_shared(const moe_config &c, const moe_weights &w, const uint16_t *x, int T,
+                      uint16_t *h_s, float *out, int *status, cudaStream_t s) {
+    CUtensorMap tg, tu, td;
+    if (!encode_tmap_2d_bf16(&tg, w.ws_gate, c.shared_inter, c.hidden, kTileM, 64) ||
+        !encode_tmap_2d_bf16(&tu, w.ws_up, c.shared_inter, c.hidden, kTileM, 64) ||
+        !encode_tmap_2d_bf16(&td, w.ws_down, c.hidden, c.shared_inter, kTileM, 64))
+        return MOE_ERR_CUDA;
+    GemmArgs a{};
+    a.b_src = x;
+    a.K = c.hidden;
+    a.n_groups = 1;
+    a.M_single = T;
+    a.F = c.shared_inter;
+    a.out = h_s;
+    a.ld = c.shared_inter;
+    a.status = status;
+    MOE_CUDA(launch_gemm(EPI_SWIGLU, a, tg, tu, KC_SHARED_GATEUP, s));
+    GemmArgs d{};
+    d.b_src = h_s;
+    d.K = c.shared_inter;
+    d.n_groups = 1;
+    d.M_single = T;
+    d.F = c.hidden;
+    d.out = out;
+    d.ld = c.hidden;
+    d.status = status;
+    MOE_CUDA(launch_gemm(EPI_F32, d, td, td, KC_SHARED_DOWN, s));
+    return MOE_OK;
+}
+
+// Routed experts, grouped: h rows (permuted order) from x gathered through perm, then the down
+// projection either stored per row (y_rows) or weighted and added into acc[token].
+moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t *x,
+                      const int32_t *offsets, const int32_t *tiles, const int32_t *perm,
+                      const float *topw, uint16_t *h, float *y_rows, float *acc, int *status,
+                      cudaStream_t s) {
+    const uint64_t EI = (uint64_t)c.n_experts * c.inter;
+    CUtensorMap tg, tu, td;
+    if (!encode_tmap_2d_bf16(&tg, w.w_gate, EI, c.hidden, kTileM, 64) ||
+        !encode_tmap_2d_bf16(&tu, w.w_up, EI, c.hidden, kTileM, 64) ||
+        !encode_tmap_2d_bf16(&td, w.w_down, (uint64_t)c.n_experts * c.hidden, c.inter, kTileM, 64))
+        return MOE_ERR_CUDA;
+    GemmArgs a{};
+    a.b_src = x;
+    a.gather_perm = perm;
+    a.gather_k = c.top_k;
+    a.K = c.hidden;
+    a.n_groups = c.n_experts;
+    a.group_rows = offsets;
+    a.group_tiles = tiles;
+    a.F = c.inter;
+    a.out = h;
+    a.ld = c.inter;
+    a.status = status;
+    MOE_CUDA(launch_gemm(EPI_SWIGLU, a, tg, tu, KC_GATEUP_GEMM, s));
+    GemmArgs d{};
+    d.b_src = h;
+    d.K = c.inter;
+    d.n_groups = c.n_experts;
+    d.group_rows = offsets;
+    d.group_tiles = tiles;
+    d.F = c.hidden;
+    d.ld = c.hidden;
+    d.status = status;
+    if (y_rows) {
+        d.out = y_rows;
+        MOE_CUDA(launch_gemm(EPI_F32, d, td, td, KC_DOWN_GEMM, s));
+    } else {
+        d.out = acc;
+        d.epi_perm = perm;
+        d.epi_w = topw;
+        d.epi_k = c.top_k;
+        MOE_CUDA(launch_gemm(EPI_COMBINE, d, td, td, KC_DOWN_GEMM, s));
+    }
+    return MOE_OK;
+}
+
+// One prefill piece of T tokens (T >= 2), the whole layer.
+moe_status forward_piece(const moe_config &c, const moe_weights &w, const uint16_t *x, int T,
+                         uint16_t *out, uint16_t *x_next, void *ws, cudaStream_t s) {
+    const Layout L = layout(c, T);
+    int *status = at<int>(ws, L.status);
+    float *logits = at<float>(ws, L.logits);
+    int32_t *ids = at<int32_t>(ws, L.ids);
+    float *topw = at<float>(ws, L.topw);
+    int32_t *offsets = at<int32_t>(ws, L.offsets);
+    int32_t *tiles = at<int32_t>(ws, L.tiles);
+    int32_t *perm = at<int32_t>(ws, L.perm);
+    int32_t *inv = at<int32_t>(ws, L.inv);
+    uint16_t *h = at<uint16_t>(ws, L.h);
+    uint16_t *h_s = at<uint16_t>(ws, L.h_s);
+    float *acc = at<float>(ws, L.acc);
+    MOE_TRY(run_router_gemm(c, w, x, T, logits, status, s));
+    MOE_CUDA(launch_topk(logits, T, c.n_experts, c.top_k, ids, topw, s));
+    MOE_CUDA(launch_permute(ids, T, c.n_experts, c.top_k, offsets, perm, inv, tiles, kTileN, status, s));
+    if (c.shared_inter > 0) {
+        MOE_TRY(run_shared(c, w, x, T, h_s, acc, status, s));  // stores: initialises acc
+    } else {
+        MOE_CUDA(launch_zero(acc, (size_t)T * c.hidden, s));
+    }
+    MOE_TRY(run_routed(c, w, x, offsets, tiles, perm, topw, h, nullptr, acc, status, s));
+    MOE_CUDA(launch_finalize(acc, x, T, c.hidden, out, x_next, s));
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char *moe_status_string(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_TIMEOUT: return "device wait timed out";
+        case MOE_ERR_NOT_IMPLEMENTED: return "not implemented";
+    }
+    return "unknown status";
+}
+
+size_t moe_workspace_size(const moe_config *cfg, int max_T) {
+    if (check_config(cfg) != MOE_OK || max_T < 0) return 0;
+    return layout(*cfg, max_T).total;
+}
+
+moe_status moe_route(const moe_config *cfg, const moe_weights *w, const moe_bf16 *x, int T,
+                     float *logits_out, int32_t *topk_ids, float *topk_w, void *ws,
+                     size_t ws_bytes, void *stream) {
+    MOE_TRY(check_config(cfg));
+    if (T < 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    MOE_TRY(check_weights(cfg, w, true, false));
+    if (!x || !topk_ids || !topk_w || !aligned16(x)) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(check_ws(cfg, ws, ws_bytes, T));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Layout L = layout(*cfg, T);
+    float *logits = logits_out ? logits_out : at<float>(ws, L.logits);
+    MOE_TRY(run_router_gemm(*cfg, *w, x, T, logits, at<int>(ws, L.status), s));
+    MOE_CUDA(launch_topk(logits, T, cfg->n_experts, cfg->top_k, topk_ids, topk_w, s));
+    return MOE_OK;
+}
+
+moe_status moe_route_from_logits(const moe_config *cfg, const float *logits, int T,
+                                 int32_t *topk_ids, float *topk_w, void *stream) {
+    MOE_TRY(check_config(cfg));
+    if (T < 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+    MOE_CUDA(launch_topk(logits, T, cfg->n_experts, cfg->top_k, topk_ids, topk_w,
+                         static_cast<cudaStream_t>(stream)));
+    return MOE_OK;
+}
+
+moe_status moe_permute(const moe_config *cfg, const int32_t *topk_ids, int T,
+                       int32_t *expert_offsets, int32_t *perm, int32_t *inv, void *ws,
+                       size_t ws_bytes, void *stream) {
+    MOE_TRY(check_config(cfg));
+    if (T < 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!topk_ids || !expert_offsets || !perm || !inv) return MOE_ERR_INVALID_ARG;
+    if ((long long)T * cfg->top_k > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED_SHAPE;
+    MOE_TRY(check_ws(cfg, ws, ws_bytes, T));
+    const Layout L = layout(*cfg, T);
+    MOE_CUDA(launch_permute(topk_ids, T, cfg->n_experts, cfg->top_k, expert_offsets, perm, inv,
+                            at<int32_t>(ws, L.tiles), kTileN, at<int>(ws, L.status),
+                            static_cast<cudaStream_t>(stream)));
+    return MOE_OK;
+}
+
+moe_status moe_expert_ffn(const moe_config *cfg, const moe_weights *w, const moe_bf16 *x, int T,
+                          const int32_t *expert_offsets, const int32_t *perm, moe_bf16 *h_rows,
+                          float *y_rows, float *shared_y, void *ws, size_t ws_bytes,
+                          void *stream) {
+    MOE_TRY(check_config(cfg));
+    if (T < 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    MOE_TRY(check_weights(cfg, w, false, true));
+    if (!x || !expert_offsets || !perm || !h_rows || !y_rows) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(h_rows) || !aligned16(y_rows)) return MOE_ERR_INVALID_ARG;
+    if (shared_y && !aligned16(shared_y)) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(check_ws(cfg, ws, ws_bytes, T));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Layout L = layout(*cfg, T);
+    int *status = at<int>(ws, L.status);
+    int32_t *tiles = at<int32_t>(ws, L.tiles);
+    MOE_CUDA(launch_tile_prefix(expert_offsets, cfg->n_experts, tiles, kTileN, s));
+    MOE_TRY(run_routed(*cfg, *w, x, expert_offsets, tiles, perm, nullptr, h_rows, y_rows, nullptr, status, s));
+    if (shared_y && cfg->shared_inter > 0)
+        MOE_TRY(run_shared(*cfg, *w, x, T, at<uint16_t>(ws, L.h_s), shared_y, status, s));
+    return MOE_OK;
+}
+
+moe_status moe_combine(const moe_config *cfg, const float *y_rows, const int32_t *inv,
+                       const float *topk_w, const float *shared_y, int T, moe_bf16 *out,
+                       void *stream) {
+    MOE_TRY(check_config(cfg));
+    if (T < 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!y_rows || !inv || !topk_w || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(y_rows) || !aligned16(out) || (shared_y && !aligned16(shared_y))) return MOE_ERR_INVALID_ARG;
+    MOE_CUDA(launch_combine(y_rows, inv, topk_w, shared_y, T, cfg->hidden, cfg->top_k, out,
+                            static_cast<cudaStream_t>(stream)));
+    return MOE_OK;
+}
+
+int moe_plan_pieces(int T, int *pieces, int max_pieces) {
+    if (T < 0) return -1;
+    static const int kBuckets[4] = {8192, 4096, 2048, 1024};
+    int n = 0, rem = T;
+    for (int b = 0; b < 4; ++b) {
+        while (rem >= kBuckets[b]) {
+            if (pieces && n < max_pieces) pieces[n] = kBuckets[b];
+            ++n;
+            rem -= kBuckets[b];
+        }
+    }
+    if (rem > 0) {
+        if (pieces && n < max_pieces) pieces[n] = rem;
+        ++n;
+    }
+    return n;
+}
+
+moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const moe_bf16 *x, int T,
+                       moe_bf16 *out, moe_bf16 *x_next, void *ws, size_t ws_bytes,
+                       void *stream) {
+    MOE_TRY(check_config(cfg));
+    if (T < 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    MOE_TRY(check_weights(cfg, w, true, true));
+    if (!x || !out || !aligned16(x) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+    if (x_next && !aligned16(x_next)) return MOE_ERR_INVALID_ARG;
+    const int Tmax = T < kMaxPiece ? T : kMaxPiece;
+    MOE_TRY(check_ws(cfg, ws, ws_bytes, Tmax));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int H = cfg->hidden;
+    if (T == 1) {
+        const Layout L = layout(*cfg, 1);
+        DecodeArgs a{};
+        a.H = H;
+        a.E = cfg->n_experts;
+        a.k = cfg->top_k;
+        a.I = cfg->inter;
+        a.Is = cfg->shared_inter;
+        a.x = x;
+        a.w_router = w->w_router;
+        a.b_router = w->b_router;
+        a.w_gate = w->w_gate;
+        a.w_up = w->w_up;
+        a.w_down = w->w_down;
+        a.ws_gate = w->ws_gate;
+        a.ws_up = w->ws_up;
+        a.ws_down = w->ws_down;
+        a.logits = at<float>(ws, L.logits);
+        a.ids = at<int32_t>(ws, L.ids);
+        a.topw = at<float>(ws, L.topw);
+        a.h = at<uint16_t>(ws, L.h);
+        a.h_s = at<uint16_t>(ws, L.h_s);
+        a.out = out;
+        a.x_next = x_next;
+        MOE_CUDA(launch_decode(a, s));
+        return MOE_OK;
+    }
+    int pieces[64];
+    const int n = moe_plan_pieces(T, pieces, 64);
+    if (n > 64) return MOE_ERR_UNSUPPORTED_SHAPE;
+    size_t t0 = 0;
+    for (int i = 0; i < n; ++i) {
+        const int Tp = pieces[i];
+        uint16_t *xn = x_next ? x_next + t0 * H : nullptr;
+        if (Tp == 1) {
+            // a one-token tail takes the decode path of the same layer
+            MOE_TRY(moe_forward(cfg, w, x + t0 * H, 1, out + t0 * H, xn, ws, ws_bytes, stream));
+        } else {
+            MOE_TRY(forward_piece(*cfg, *w, x + t0 * H, Tp, out + t0 * H, xn, ws, s));
+        }
+        t0 += Tp;
+    }
+    return MOE_OK;
+}
+
+moe_status moe_check_status(void *ws, size_t ws_bytes, int *device_status, void *stream) {
+    if (!ws || !device_status || ws_bytes < 256) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int v = 0;
+    if (cudaMemcpyAsync(&v, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    *device_status = v;
+    if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+uint64_t moe_launch_count(void) { return g_launches.load(); }
+
+moe_status moe_timing_enable(int enable) {
+    g_timing.store(enable != 0);
+    return MOE_OK;
+}
+
+moe_status moe_timing_read(const char *name, int *launches, double *total_ms) {
+    if (!name || !launches || !total_ms) return MOE_ERR_INVALID_ARG;
+    int kc = -1;
+    for (int i = 0; i < KC_COUNT; ++i)
+        if (std::strcmp(name, kClassNames[i]) == 0) kc = i;
+    if (kc < 0) return MOE_ERR_INVALID_ARG;
+    std::vector<TimedPair> v;
+    {
+        std::lock_guard<std::mutex> lk(g_timing_mu);
+        v.swap(g_timed[kc]);
+    }
+    double tot = 0.0;
+    int n = 0;
+    moe_status st = MOE_OK;
+    for (auto &p : v) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(p.b) == cudaSuccess && cudaEventElapsedTime(&ms, p.a, p.b) == cudaSuccess) {
+            tot += ms;
+            ++n;
+        } else {
+            st = MOE_ERR_CUDA;
+        }
+        cudaEventDestroy(p.a);
+        cudaEventDestroy(p.b);
+    }
+    *launches = n;
+    *total_ms = tot;
+    return st;
+}
+
+const char *moe_timing_name(int i) { return kernel_class_name(i); }
+
+int moe_timing_classes(void) { return KC_COUNT; }
+
+}  // extern "C"

@@ -1,0 +1,364 @@
+// route.cu -- router softmax/top-k/renormalise, the stable expert permutation, and the
+// elementwise kernels (finalise, unfused combine, clear).
+//
+// Top-k routing ("AI MAX+ 395部署Qwen3大模型：GFX1151引擎实测优化解析", explanatory MoE
+// paragraph under "MOE 内核优化": each token activates only a few of many experts) is taken
+// on the fp32 logits: the k largest, lower expert index first on equal values, in descending
+// order; the weights are the softmax over all E logits renormalised over the k chosen, which
+// equals exp(l_j - m) / sum_i exp(l_i - m) over the chosen.
+#include <cuda_bf16.h>
+#include <float.h>
+
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+// ------------------------------------------------------------------------ top-k --
+// One warp per token.  Lane L holds logits e = L + 32*i.  k rounds of a warp arg-max with
+// the order (value descending, index ascending); the winner's owner marks it taken.
+template <int PER_LANE>
+__global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ logits, int T, int E,
+                                                   int k, int32_t *__restrict__ ids,
+                                                   float *__restrict__ w) {
+    const int warp = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (warp >= T) return;
+    const float *l = logits + (size_t)warp * E;
+    float v[PER_LANE];
+#pragma unroll
+    for (int i = 0; i < PER_LANE; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = e < E ? __ldg(&l[e]) : -INFINITY;
+    }
+    uint32_t taken = 0;
+    float my_val = 0.f;
+    int my_id = 0;
+    float top = 0.f;
+    for (int r = 0; r < k; ++r) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < PER_LANE; ++i) {
+            const int e = lane + 32 * i;
+            // increasing e within the lane: strict '>' keeps the lowest index among equals
+            if (e < E && !((taken >> i) & 1u) && (v[i] > bv || bi == 0x7fffffff)) {
+                bv = v[i];
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+            if (ov > bv || (ov == bv && oi < bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if (r == 0) top = bv;
+        if (lane == r) {
+            my_val = bv;
+            my_id = bi;
+        }
+    }
+    const float ej = lane < k ? expf(my_val - top) : 0.f;
+    float s = ej;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane < k) {
+        ids[(size_t)warp * k + lane] = my_id;
+        w[(size_t)warp * k + lane] = ej / s;
+    }
+}
+
+// --------------------------------------------------------------------- permute --
+// Stable counting sort of the P = T*k pairs by expert, in one CTA of 1024 threads with no
+// inter-CTA waits.  Warp w owns the contiguous pair range [w*chunk, (w+1)*chunk):
+//   1. per-warp histograms hist[w][e] (match_any groups equal ids inside a 32-pair batch);
+//   2. offsets = exclusive scan over e of sum_w hist[w][e]; then hist[w][e] becomes the
+//      first row of warp w's pairs of expert e (experts major, warps minor);
+//   3. each warp walks its range again in order; a pair's row is its warp's cursor for the
+//      expert plus its rank among equal ids earlier in the batch.
+// Pairs of one expert therefore keep increasing pair order: the result is bit-exact.
+constexpr int kPermThreads = 1024;
+constexpr int kPermWarps = kPermThreads / 32;
+
+__device__ __forceinline__ int block_excl_scan(int v, int *sh_warp, int *total) {
+    // exclusive scan of one value per thread across the 1024-thread block
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+    }
+    if (lane == 31) sh_warp[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        int s = sh_warp[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, s, off);
+            if (lane >= off) s += y;
+        }
+        sh_warp[lane] = s;  // inclusive
+    }
+    __syncthreads();
+    const int base = wid > 0 ? sh_warp[wid - 1] : 0;
+    const int incl = base + x;
+    *total = sh_warp[31];
+    __syncthreads();
+    return incl - v;
+}
+
+__global__ void __launch_bounds__(kPermThreads, 1)
+    permute_kernel(const int32_t *__restrict__ ids, int P, int E, int32_t *__restrict__ offsets,
+                   int32_t *__restrict__ perm, int32_t *__restrict__ inv,
+                   int32_t *__restrict__ tile_prefix, int tile_n, int *status) {
+    extern __shared__ int sh[];
+    int *hist = sh;                           // [kPermWarps][E]
+    int *sh_warp = sh + kPermWarps * E;       // [32]
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    for (int i = tid; i < kPermWarps * E; i += kPermThreads) hist[i] = 0;
+    __syncthreads();
+
+    const int chunk = (P + kPermWarps - 1) / kPermWarps;
+    const int beg = min(P, wid * chunk), end = min(P, beg + chunk);
+    int *myhist = hist + wid * E;
+    const uint32_t lt_mask = (1u << lane) - 1u;
+
+    // 1. histograms (8 batches of loads in flight)
+    for (int b0 = beg; b0 < end; b0 += 32 * 8) {
+        int e8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int pidx = b0 + 32 * u + lane;
+            e8[u] = pidx < end ? __ldg(&ids[pidx]) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            int e = e8[u];
+            if (e >= E || (e < 0 && b0 + 32 * u + lane < end)) {
+                if (status) atomicCAS(status, 0, (int)MOE_ERR_INVALID_ARG);
+                e = -1;
+            }
+            const uint32_t grp = __match_any_sync(0xffffffffu, e);
+            if (e >= 0 && (grp & lt_mask) == 0) myhist[e] += __popc(grp);
+        }
+    }
+    __syncthreads();
+
+    // 2. offsets and token-tile prefix (one expert per thread; E <= 1024)
+    int cnt = 0;
+    if (tid < E)
+        for (int w2 = 0; w2 < kPermWarps; ++w2) cnt += hist[w2 * E + tid];
+    int total = 0;
+    const int off = block_excl_scan(tid < E ? cnt : 0, sh_warp, &total);
+    const int tiles = tid < E ? (cnt + tile_n - 1) / tile_n : 0;
+    int total_tiles = 0;
+    const int toff = block_excl_scan(tiles, sh_warp, &total_tiles);
+    if (tid < E) {
+        offsets[tid] = off;
+        if (tile_prefix) tile_prefix[tid] = toff;
+        int run = off;
+        for (int w2 = 0; w2 < kPermWarps; ++w2) {
+            const int c = hist[w2 * E + tid];
+            hist[w2 * E + tid] = run;
+            run += c;
+        }
+    }
+    if (tid == 0) {
+        offsets[E] = total;
+        if (tile_prefix) tile_prefix[E] = total_tiles;
+    }
+    __syncthreads();
+
+    // 3. stable scatter
+    for (int b0 = beg; b0 < end; b0 += 32 * 8) {
+        int e8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int pidx = b0 + 32 * u + lane;
+            e8[u] = pidx < end ? __ldg(&ids[pidx]) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int pidx = b0 + 32 * u + lane;
+            int e = e8[u];
+            if (e >= E) e = -1;
+            const uint32_t grp = __match_any_sync(0xffffffffu, e);
+            int row = -1;
+            if (e >= 0) row = myhist[e] + __popc(grp & lt_mask);
+            __syncwarp();
+            if (e >= 0 && (grp & lt_mask) == 0) myhist[e] += __popc(grp);
+            __syncwarp();
+            if (pidx < end) {
+                inv[pidx] = row;
+                if (row >= 0) perm[row] = pidx;
+            }
+        }
+    }
+}
+
+// Token-tile prefix from given offsets (for the unfused expert entry point).
+__global__ void __launch_bounds__(kPermThreads, 1)
+    tile_prefix_kernel(const int32_t *__restrict__ offsets, int E, int32_t *__restrict__ tile_prefix,
+                       int tile_n) {
+    __shared__ int sh_warp[32];
+    const int tid = threadIdx.x;
+    const int cnt = tid < E ? offsets[tid + 1] - offsets[tid] : 0;
+    const int tiles = tid < E ? (max(cnt, 0) + tile_n - 1) / tile_n : 0;
+    int total = 0;
+    const int toff = block_excl_scan(tiles, sh_warp, &total);
+    if (tid < E) tile_prefix[tid] = toff;
+    if (tid == 0) tile_prefix[E] = total;
+}
+
+// ------------------------------------------------------------------- finalise --
+// out = bf16(acc); x_next = bf16(x + out).  8 elements per thread (H % 8 == 0).
+__global__ void __launch_bounds__(256) finalize_kernel(const float *__restrict__ acc,
+                                                       const uint16_t *x, size_t n8,
+                                                       uint16_t *__restrict__ out,
+                                                       uint16_t *x_next) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+        const float4 a0 = reinterpret_cast<const float4 *>(acc)[2 * i];
+        const float4 a1 = reinterpret_cast<const float4 *>(acc)[2 * i + 1];
+        const float v[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        __align__(16) __nv_bfloat16 o[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o[j] = __float2bfloat16_rn(v[j]);
+        reinterpret_cast<uint4 *>(out)[i] = *reinterpret_cast<const uint4 *>(o);
+        if (x_next) {
+            const uint4 xr = reinterpret_cast<const uint4 *>(x)[i];
+            const __nv_bfloat16 *xb = reinterpret_cast<const __nv_bfloat16 *>(&xr);
+            __align__(16) __nv_bfloat16 n[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                n[j] = __float2bfloat16_rn(__bfloat162float(xb[j]) + __bfloat162float(o[j]));
+            reinterpret_cast<uint4 *>(x_next)[i] = *reinterpret_cast<const uint4 *>(n);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- unfused combine --
+// out[t, n] = bf16( sum_j w[t,j] * y_rows[inv[t*k+j], n] + shared_y[t, n] ), slot order.
+__global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ y_rows,
+                                                      const int32_t *__restrict__ inv,
+                                                      const float *__restrict__ topk_w,
+                                                      const float *__restrict__ shared_y, int T,
+                                                      int H, int k, uint16_t *__restrict__ out) {
+    const int H4 = H / 4;
+    const size_t n = (size_t)T * H4;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const int t = (int)(i / H4), c = (int)(i % H4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < k; ++j) {
+            const int row = __ldg(&inv[(size_t)t * k + j]);
+            if (row < 0) continue;
+            const float wj = __ldg(&topk_w[(size_t)t * k + j]);
+            const float4 y = __ldg(reinterpret_cast<const float4 *>(y_rows + (size_t)row * H) + c);
+            acc.x += wj * y.x;
+            acc.y += wj * y.y;
+            acc.z += wj * y.z;
+            acc.w += wj * y.w;
+        }
+        if (shared_y) {
+            const float4 s = __ldg(reinterpret_cast<const float4 *>(shared_y + (size_t)t * H) + c);
+            acc.x += s.x;
+            acc.y += s.y;
+            acc.z += s.z;
+            acc.w += s.w;
+        }
+        __align__(8) __nv_bfloat16 o[4] = {__float2bfloat16_rn(acc.x), __float2bfloat16_rn(acc.y),
+                                           __float2bfloat16_rn(acc.z), __float2bfloat16_rn(acc.w)};
+        reinterpret_cast<uint2 *>(out + (size_t)t * H)[c] = *reinterpret_cast<const uint2 *>(o);
+    }
+}
+
+__global__ void __launch_bounds__(256) zero_kernel(float4 *__restrict__ p, size_t n4) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x)
+        p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+int grid_for(size_t work, int per_block) {
+    const DeviceInfo &di = device_info();
+    size_t b = (work + per_block - 1) / per_block;
+    const size_t cap = (size_t)di.sm_count * 8;
+    if (b > cap) b = cap;
+    if (b < 1) b = 1;
+    return (int)b;
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const float *logits, int T, int E, int k, int32_t *ids, float *w,
+                        cudaStream_t s) {
+    if (T <= 0) return cudaSuccess;
+    const int blocks = (T + 7) / 8;  // 8 warps per block
+    LaunchScope scope(KC_TOPK, s);
+    const int per = (E + 31) / 32;
+    if (per <= 1) topk_kernel<1><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
+    else if (per <= 2) topk_kernel<2><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
+    else if (per <= 4) topk_kernel<4><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
+    else if (per <= 8) topk_kernel<8><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
+    else if (per <= 16) topk_kernel<16><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
+    else topk_kernel<32><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int32_t *offsets,
+                           int32_t *perm, int32_t *inv, int32_t *tile_prefix, int tile_n,
+                           int *status, cudaStream_t s) {
+    const size_t smem = (size_t)(kPermWarps * E + 32) * sizeof(int);
+    static bool attr_done[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_done[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)((kPermWarps * 1024 + 32) * sizeof(int)));
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+    }
+    LaunchScope scope(KC_PERMUTE, s);
+    permute_kernel<<<1, kPermThreads, smem, s>>>(ids, T * k, E, offsets, perm, inv, tile_prefix,
+                                                 tile_n, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tile_prefix(const int32_t *offsets, int E, int32_t *tile_prefix, int tile_n,
+                               cudaStream_t s) {
+    LaunchScope scope(KC_TILE_PREFIX, s);
+    tile_prefix_kernel<<<1, kPermThreads, 0, s>>>(offsets, E, tile_prefix, tile_n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const float *acc, const uint16_t *x, int T, int H, uint16_t *out,
+                            uint16_t *x_next, cudaStream_t s) {
+    const size_t n8 = (size_t)T * H / 8;
+    if (n8 == 0) return cudaSuccess;
+    LaunchScope scope(KC_FINALIZE, s);
+    finalize_kernel<<<grid_for(n8, 256), 256, 0, s>>>(acc, x, n8, out, x_next);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float *y_rows, const int32_t *inv, const float *topk_w,
+                           const float *shared_y, int T, int H, int k, uint16_t *out,
+                           cudaStream_t s) {
+    const size_t n = (size_t)T * (H / 4);
+    if (n == 0) return cudaSuccess;
+    LaunchScope scope(KC_COMBINE, s);
+    combine_kernel<<<grid_for(n, 256), 256, 0, s>>>(y_rows, inv, topk_w, shared_y, T, H, k, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_zero(float *p, size_t n, cudaStream_t s) {
+    const size_t n4 = n / 4;
+    if (n4 == 0) return cudaSuccess;
+    LaunchScope scope(KC_ZERO, s);
+    zero_kernel<<<grid_for(n4, 256), 256, 0, s>>>(reinterpret_cast<float4 *>(p), n4);
+    return cudaGetLastError();
+}
+
+}  // namespace moe
