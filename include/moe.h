@@ -84,7 +84,10 @@ const char *moe_status_string(moe_status s);
 
 /* Bytes of device workspace needed by any call below for up to max_T tokens (moe_forward
  * needs only min(max_T, 8192) tokens' worth, since it works piece by piece).  Returns 0 for
- * an invalid or unsupported config.  The workspace must be 256-byte aligned. */
+ * an invalid or unsupported config.  The workspace must be 256-byte aligned.  Its first 256
+ * bytes hold the device status word: zero them once after allocating the workspace (kernels
+ * only ever change the word from 0 to an error code; moe_check_status clears it).  The rest
+ * is scratch that every call overwrites. */
 size_t moe_workspace_size(const moe_config *cfg, int max_T);
 
 /* Router: logits, softmax, top-k and renormalisation.

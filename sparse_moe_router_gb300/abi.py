@@ -1,0 +1,232 @@
+"""ctypes binding of libmoe.so (include/moe.h).  Argument marshalling only.
+
+Every function takes torch tensors that already live on the GPU and passes their device
+pointers to the C entry point of the same name; all computation happens in the library's
+CUDA kernels.  Loading fails loudly if the library has not been built: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+MOE_OK = 0
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_WORKSPACE_TOO_SMALL",
+                3: "MOE_ERR_UNSUPPORTED_SHAPE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT",
+                6: "MOE_ERR_NOT_IMPLEMENTED"}
+
+# Every symbol include/moe.h declares.
+EXPORTS = ["moe_status_string", "moe_workspace_size", "moe_route", "moe_route_from_logits",
+           "moe_permute", "moe_expert_ffn", "moe_combine", "moe_forward", "moe_check_status",
+           "moe_plan_pieces", "moe_launch_count", "moe_timing_enable", "moe_timing_read",
+           "moe_timing_name", "moe_timing_classes"]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__("%s failed: %s (%d)" % (fn, STATUS_NAMES.get(status, "?"), status))
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int), ("n_experts", ctypes.c_int), ("top_k", ctypes.c_int),
+                ("inter", ctypes.c_int), ("shared_inter", ctypes.c_int)]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("w_router", "b_router", "w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down")]
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libmoe.so (once).  Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError("libmoe.so not built (%s); run __graft_entry__.build() or "
+                          "python -m sparse_moe_router_gb300.build" % path)
+    L = ctypes.CDLL(path)
+    C, W = ctypes.POINTER(Config), ctypes.POINTER(Weights)
+    L.moe_status_string.argtypes = [_I]
+    L.moe_status_string.restype = ctypes.c_char_p
+    L.moe_workspace_size.argtypes = [C, _I]
+    L.moe_workspace_size.restype = _SZ
+    L.moe_route.argtypes = [C, W, _P, _I, _P, _P, _P, _P, _SZ, _P]
+    L.moe_route_from_logits.argtypes = [C, _P, _I, _P, _P, _P]
+    L.moe_permute.argtypes = [C, _P, _I, _P, _P, _P, _P, _SZ, _P]
+    L.moe_expert_ffn.argtypes = [C, W, _P, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]
+    L.moe_combine.argtypes = [C, _P, _P, _P, _P, _I, _P, _P]
+    L.moe_forward.argtypes = [C, W, _P, _I, _P, _P, _P, _SZ, _P]
+    L.moe_check_status.argtypes = [_P, _SZ, ctypes.POINTER(_I), _P]
+    L.moe_plan_pieces.argtypes = [_I, ctypes.POINTER(_I), _I]
+    L.moe_plan_pieces.restype = _I
+    L.moe_launch_count.argtypes = []
+    L.moe_launch_count.restype = ctypes.c_uint64
+    L.moe_timing_enable.argtypes = [_I]
+    L.moe_timing_read.argtypes = [ctypes.c_char_p, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_double)]
+    L.moe_timing_name.argtypes = [_I]
+    L.moe_timing_name.restype = ctypes.c_char_p
+    L.moe_timing_classes.argtypes = []
+    for fn in ("moe_route", "moe_route_from_logits", "moe_permute", "moe_expert_ffn",
+               "moe_combine", "moe_forward", "moe_check_status", "moe_timing_enable",
+               "moe_timing_read", "moe_timing_classes"):
+        getattr(L, fn).restype = _I
+    _lib = L
+    return L
+
+
+def lib():
+    return load()
+
+
+# ---------------------------------------------------------------------- helpers --
+
+def config(hidden, n_experts, top_k, inter, shared_inter) -> Config:
+    return Config(hidden, n_experts, top_k, inter, shared_inter)
+
+
+def config_of(shape) -> Config:
+    """Config from an object with hidden/n_experts/top_k/inter/shared_inter attributes."""
+    return Config(shape.hidden, shape.n_experts, shape.top_k, shape.inter, shape.shared_inter)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def weights(layer: dict) -> Weights:
+    """Weights struct from a dict of device tensors (keys as in include/moe.h)."""
+    w = Weights()
+    for name, _ in Weights._fields_:
+        t = layer.get(name)
+        setattr(w, name, None if t is None else t.data_ptr())
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("weight %s must be a contiguous CUDA tensor" % name)
+    return w
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn, st):
+    if st != MOE_OK:
+        raise MoeError(fn, st)
+
+
+def workspace_size(cfg: Config, max_T: int) -> int:
+    return int(lib().moe_workspace_size(ctypes.byref(cfg), int(max_T)))
+
+
+def alloc_workspace(cfg: Config, max_T: int, device="cuda") -> torch.Tensor:
+    n = workspace_size(cfg, max_T)
+    if n == 0:
+        raise MoeError("moe_workspace_size", 3)
+    # zeroed once: the first 256 bytes are the device status word
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+# ------------------------------------------------------------------ entry points --
+
+def moe_route(cfg, w: Weights, x, T, logits_out, topk_ids, topk_w, ws, stream=None):
+    st = lib().moe_route(ctypes.byref(cfg), ctypes.byref(w), _ptr(x), int(T), _ptr(logits_out),
+                         _ptr(topk_ids), _ptr(topk_w), _ptr(ws), ws.numel(), _stream(stream))
+    _check("moe_route", st)
+
+
+def moe_route_from_logits(cfg, logits, T, topk_ids, topk_w, stream=None):
+    st = lib().moe_route_from_logits(ctypes.byref(cfg), _ptr(logits), int(T), _ptr(topk_ids),
+                                     _ptr(topk_w), _stream(stream))
+    _check("moe_route_from_logits", st)
+
+
+def moe_permute(cfg, topk_ids, T, offsets, perm, inv, ws, stream=None):
+    st = lib().moe_permute(ctypes.byref(cfg), _ptr(topk_ids), int(T), _ptr(offsets), _ptr(perm),
+                           _ptr(inv), _ptr(ws), ws.numel(), _stream(stream))
+    _check("moe_permute", st)
+
+
+def moe_expert_ffn(cfg, w: Weights, x, T, offsets, perm, h_rows, y_rows, shared_y, ws, stream=None):
+    st = lib().moe_expert_ffn(ctypes.byref(cfg), ctypes.byref(w), _ptr(x), int(T), _ptr(offsets),
+                              _ptr(perm), _ptr(h_rows), _ptr(y_rows), _ptr(shared_y), _ptr(ws),
+                              ws.numel(), _stream(stream))
+    _check("moe_expert_ffn", st)
+
+
+def moe_combine(cfg, y_rows, inv, topk_w, shared_y, T, out, stream=None):
+    st = lib().moe_combine(ctypes.byref(cfg), _ptr(y_rows), _ptr(inv), _ptr(topk_w),
+                           _ptr(shared_y), int(T), _ptr(out), _stream(stream))
+    _check("moe_combine", st)
+
+
+def moe_forward(cfg, w: Weights, x, T, out, x_next, ws, stream=None):
+    st = lib().moe_forward(ctypes.byref(cfg), ctypes.byref(w), _ptr(x), int(T), _ptr(out),
+                           _ptr(x_next), _ptr(ws), ws.numel(), _stream(stream))
+    _check("moe_forward", st)
+
+
+def moe_forward_status(cfg, w: Weights, x, T, out, x_next, ws, stream=None) -> int:
+    """Like moe_forward but returns the status code instead of raising."""
+    return int(lib().moe_forward(ctypes.byref(cfg), ctypes.byref(w), _ptr(x), int(T), _ptr(out),
+                                 _ptr(x_next), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_check_status(ws, stream=None) -> int:
+    v = ctypes.c_int(0)
+    st = lib().moe_check_status(_ptr(ws), ws.numel(), ctypes.byref(v), _stream(stream))
+    _check("moe_check_status", st)
+    return v.value
+
+
+def moe_plan_pieces(T: int):
+    n = lib().moe_plan_pieces(int(T), None, 0)
+    if n < 0:
+        raise ValueError("T < 0")
+    buf = (ctypes.c_int * max(n, 1))()
+    lib().moe_plan_pieces(int(T), buf, n)
+    return [buf[i] for i in range(n)]
+
+
+def moe_launch_count() -> int:
+    return int(lib().moe_launch_count())
+
+
+def timing_enable(on: bool):
+    lib().moe_timing_enable(1 if on else 0)
+
+
+def timing_classes():
+    L = lib()
+    return [L.moe_timing_name(i).decode() for i in range(L.moe_timing_classes())]
+
+
+def timing_read(name: str):
+    n = ctypes.c_int(0)
+    ms = ctypes.c_double(0.0)
+    st = lib().moe_timing_read(name.encode(), ctypes.byref(n), ctypes.byref(ms))
+    _check("moe_timing_read", st)
+    return n.value, ms.value
+
+
+def status_string(code: int) -> str:
+    return lib().moe_status_string(int(code)).decode()

@@ -225,6 +225,14 @@ __global__ void __launch_bounds__(kBlock) decode_down_kernel(DecodeArgs a) {
 
 }  // namespace
 
+cudaError_t launch_decode_router(const DecodeArgs &a, cudaStream_t s) {
+    DecodeArgs r = a;
+    r.Is = 0;  // router rows only
+    LaunchScope scope(KC_DECODE_ROUTER, s);
+    decode_router_kernel<<<(r.E + kWarps - 1) / kWarps, kBlock, (size_t)r.H * 2, s>>>(r);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s) {
     static bool attr_done[64] = {false};
     int dev = 0;

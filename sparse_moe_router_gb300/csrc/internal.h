@@ -118,6 +118,8 @@ struct DecodeArgs {
     uint16_t *x_next;  // [H] or NULL
 };
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
+// Router logits of one token with the decode GEMV (the logits the decode path selects on).
+cudaError_t launch_decode_router(const DecodeArgs &a, cudaStream_t s);
 
 constexpr int kTileN = 128;   // tokens per GEMM tile (MMA N upper bound)
 constexpr int kTileM = 128;   // weight rows per GEMM tile (MMA M)

@@ -359,7 +359,20 @@ moe_status moe_route(const moe_config *cfg, const moe_weights *w, const moe_bf16
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const Layout L = layout(*cfg, T);
     float *logits = logits_out ? logits_out : at<float>(ws, L.logits);
-    MOE_TRY(run_router_gemm(*cfg, *w, x, T, logits, at<int>(ws, L.status), s));
+    if (T == 1) {
+        // one token: the decode path's GEMV, so the reported logits are the ones moe_forward
+        // selects on for T == 1
+        DecodeArgs a{};
+        a.H = cfg->hidden;
+        a.E = cfg->n_experts;
+        a.x = x;
+        a.w_router = w->w_router;
+        a.b_router = w->b_router;
+        a.logits = logits;
+        MOE_CUDA(launch_decode_router(a, s));
+    } else {
+        MOE_TRY(run_router_gemm(*cfg, *w, x, T, logits, at<int>(ws, L.status), s));
+    }
     MOE_CUDA(launch_topk(logits, T, cfg->n_experts, cfg->top_k, topk_ids, topk_w, s));
     return MOE_OK;
 }

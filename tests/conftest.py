@@ -25,3 +25,11 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_sessionstart(session):
+    # The CUDA library is built in-tree (nvcc cross-compiles without a GPU); the oracle too.
+    from sparse_moe_router_gb300 import build as lib_build
+    from oracle import build_oracle
+    build_oracle.build()
+    lib_build.build()

@@ -1,0 +1,104 @@
+"""Shared test helpers: seeded workloads on the GPU, host copies for the oracle, comparisons.
+
+The inputs come from sparse_moe_router_gb300.inputs (random draws only); the expected
+values come from the CPU oracle (oracle/), never from the CUDA path.
+"""
+import numpy as np
+import torch
+
+from oracle import moe_oracle as orc
+from sparse_moe_router_gb300 import abi, inputs
+
+# Layer-output tolerance: bf16 inputs, fp32 accumulation, bf16 output.
+MAX_ABS = 2e-2
+REL_L2 = 5e-3
+
+
+def logits_tol(ref):
+    return 1e-5 * (1.0 + np.abs(ref))
+
+
+def make(shape, T, seed, router_std=0.02, zipf_s=None, n_dead=0, n_layers=1, device="cuda"):
+    w = inputs.custom(shape, T=T, seed=seed, router_std=router_std, zipf_s=zipf_s, n_dead=n_dead,
+                      n_layers=n_layers)
+    layers, x = inputs.make(w, device=device)
+    return layers, x
+
+
+def host(layer):
+    return inputs.layer_to_host(layer)
+
+
+def u16(t):
+    return inputs.to_u16(t)
+
+
+def bf16_f64(bits):
+    return orc.bf16_to_f64(bits)
+
+
+def compare_out(got_u16, ref_u16, what="out"):
+    """Layer-output check: max |diff| and relative L2 error against the oracle's bf16 output."""
+    g = bf16_f64(got_u16)
+    r = bf16_f64(ref_u16)
+    assert np.all(np.isfinite(g)), what + ": non-finite values"
+    d = np.abs(g - r)
+    max_abs = float(d.max()) if d.size else 0.0
+    rel = float(np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-30)) if d.size else 0.0
+    assert max_abs <= MAX_ABS, "%s: max abs diff %.3g > %.3g" % (what, max_abs, MAX_ABS)
+    assert rel <= REL_L2, "%s: rel L2 %.3g > %.3g" % (what, rel, REL_L2)
+    return max_abs, rel
+
+
+def cfg_of(shape):
+    return abi.config_of(shape)
+
+
+def route_gpu(shape, layer, x, ws=None):
+    """moe_route through the C-ABI, returning host (logits, ids, w)."""
+    cfg = cfg_of(shape)
+    T = x.shape[0]
+    ws = ws if ws is not None else abi.alloc_workspace(cfg, T)
+    logits = torch.empty(T, shape.n_experts, dtype=torch.float32, device="cuda")
+    ids = torch.empty(T, shape.top_k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, shape.top_k, dtype=torch.float32, device="cuda")
+    abi.moe_route(cfg, abi.weights(layer), x, T, logits, ids, w, ws)
+    torch.cuda.synchronize()
+    return logits.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy()
+
+
+def forward_gpu(shape, layer, x, want_x_next=False, ws=None):
+    cfg = cfg_of(shape)
+    T = x.shape[0]
+    ws = ws if ws is not None else abi.alloc_workspace(cfg, min(T, 8192))
+    out = torch.empty_like(x)
+    xn = torch.empty_like(x) if want_x_next else None
+    abi.moe_forward(cfg, abi.weights(layer), x, T, out, xn, ws)
+    torch.cuda.synchronize()
+    assert abi.moe_check_status(ws) == 0
+    return out, xn
+
+
+def check_layer(shape, layer, x, rows=None, ws=None):
+    """Full-layer parity of moe_forward against the oracle consuming the GPU's routing.
+
+    The GPU routing (ids, weights) comes from moe_route on the same x; the ids are first
+    checked bit-exact against the oracle's selection on the GPU's own fp32 logits.  `rows`
+    (optional) restricts the oracle to a sample of token rows (the layer is per-token).
+    Returns (max_abs, rel_l2, n_routing_mismatch_vs_oracle_logits)."""
+    out, _ = forward_gpu(shape, layer, x, ws=ws)
+    logits, ids, w = route_gpu(shape, layer, x, ws=ws)
+    hl = host(layer)
+    ids_o, w_o = orc.route_from_logits(logits, shape.top_k)
+    assert np.array_equal(ids, ids_o), "routing ids differ from the oracle on identical logits"
+    np.testing.assert_allclose(w, w_o, rtol=2e-6, atol=1e-7)
+    xs = u16(x)
+    sel = np.arange(x.shape[0]) if rows is None else np.asarray(rows)
+    ref = orc.forward(np.ascontiguousarray(xs[sel]), hl, shape.top_k, ids=ids[sel], topk_w=w[sel])
+    ma, rl = compare_out(u16(out)[sel], ref["out"])
+    # Informational: how many tokens choose a different expert set from the oracle's own logits.
+    own_logits = orc.router_logits(np.ascontiguousarray(xs[sel]), hl["w_router"], hl.get("b_router"))
+    np.testing.assert_array_less(np.abs(logits[sel] - own_logits), logits_tol(own_logits) + 1e-30)
+    ids_own, _ = orc.route_from_logits(own_logits, shape.top_k)
+    mism = int(np.sum(np.any(np.sort(ids_own, 1) != np.sort(ids[sel], 1), axis=1)))
+    return ma, rl, mism
