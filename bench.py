@@ -1,0 +1,467 @@
+"""Benchmark of the top-k routed MoE layer on GB300 (one JSON line on rank 0).
+
+One step = one pass of the whole layer path over one batch: the prefill workload (T = 8192
+tokens, H = 2048, 256 experts top-8 + shared expert, I = 512, bf16; 4 distinct layers, layer
+l+1 reading bf16(x_0 + out_l)) through moe_forward.  `value` is MoE-layer tokens/s: tokens x
+layers / seconds.  The decode workload (T = 1, 40 distinct layers, ~64.7 GB of weights,
+captured as one CUDA graph) is timed in the same run and reported under "decode" as
+us/layer.  Inputs are resident in HBM when the timed region starts; the per-layer weights
+(1.6 GB) are larger than L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (plain C, fp64, OpenMP over tokens) on the host cores,
+on a bounded sample of the same workload per step.  Under torchrun each rank runs an
+independent replica (the layer has no exchange step at this scale: replicas only).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/s (prefill T=8192) & decode µs/layer; % of BF16 TC / HBM peak"
+UNIT = "tokens/s"
+
+
+def _dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if _cuda_ok() else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def _cuda_ok():
+    import torch
+    return torch.cuda.is_available()
+
+
+def _barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def _max_over_ranks(pg, v, device):
+    if pg is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(pw) if pw else None}
+
+
+# ------------------------------------------------------------------------ ours --
+
+def _algorithmic(shape, T):
+    """Flops of the layer's matrix products and bytes of the minimum weight+activation
+    traffic, per layer, for T tokens."""
+    H, E, k, I, Is = shape.hidden, shape.n_experts, shape.top_k, shape.inter, shape.shared_inter
+    gateup = 2.0 * T * k * H * 2 * I
+    down = 2.0 * T * k * I * H
+    shared = 2.0 * T * H * 2 * Is + 2.0 * T * Is * H
+    router = 2.0 * T * H * E
+    return {"gateup_flops": gateup, "down_flops": down, "shared_flops": shared,
+            "router_flops": router, "total_flops": gateup + down + shared + router}
+
+
+def _decode_bytes(shape):
+    H, E, k, I, Is = shape.hidden, shape.n_experts, shape.top_k, shape.inter, shape.shared_inter
+    return E * H * 2 + k * 3 * H * I * 2 + 3 * H * Is * 2
+
+
+def run_ours(args, world, rank, local, pg):
+    import torch
+    from sparse_moe_router_gb300 import abi, inputs
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    abi.load()
+    peaks = _peaks()
+
+    # ------------------------------------------------------------- prefill (value) --
+    wl = inputs.WORKLOADS["prefill8k"]
+    shape, T, L = wl.shape, wl.T, wl.n_layers
+    layers, x0 = inputs.make(wl, device=dev)
+    cfg = abi.config_of(shape)
+    ws = abi.alloc_workspace(cfg, min(T, 8192))
+    wts = [abi.weights(l) for l in layers]
+    xa = x0.clone()
+    xb = torch.empty_like(x0)
+    xc = torch.empty_like(x0)
+    out = torch.empty_like(x0)
+    stream = torch.cuda.current_stream()
+
+    def step(x_in):
+        # layer l+1 reads bf16(x_0 + out_l): the residual add is fused into moe_forward
+        x = x_in
+        for l in range(L):
+            nxt = xb if (x is not xb) else xc
+            abi.moe_forward(cfg, wts[l], x, T, out, nxt, ws, stream, resid=x_in)
+            x = nxt
+        return x
+
+    for _ in range(args.warmup):
+        step(xa)
+    torch.cuda.synchronize()
+    assert abi.moe_check_status(ws) == 0
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    _barrier(pg)
+    torch.cuda.synchronize()
+    n_launch0 = abi.moe_launch_count()
+    abi.timing_enable(True)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step(xa)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    abi.timing_enable(False)
+    launches = abi.moe_launch_count() - n_launch0
+    _barrier(pg)
+    clk = clocks.stop()
+    t_ms = ev0.elapsed_time(ev1)
+    t_ms = _max_over_ranks(pg, t_ms, dev)
+    per_kernel = {}
+    for name in abi.timing_classes():
+        n, ms = abi.timing_read(name)
+        if n:
+            per_kernel[name] = {"launches": n, "total_ms": round(ms, 4), "avg_us": round(1e3 * ms / n, 2)}
+    assert abi.moe_check_status(ws) == 0
+    ms_per_step = t_ms / args.steps
+    layer_tokens = T * L
+    value = world * layer_tokens * args.steps / (t_ms * 1e-3)
+    alg = _algorithmic(shape, T)
+    gu = per_kernel.get("gateup_gemm")
+    roofline = None
+    if gu:
+        achieved = alg["gateup_flops"] / (gu["avg_us"] * 1e-6) / 1e12
+        pk = peaks["bf16_tflops_sustained"]
+        roofline = {"bound": "tensor", "kernel": "gateup_gemm", "achieved": round(achieved, 1),
+                    "peak": pk, "unit": "TFLOP/s", "frac": round(achieved / pk, 4),
+                    "frac_of_burst_peak": round(achieved / peaks["bf16_tflops"], 4),
+                    "traffic": None, "peak_source": peaks["source"] + " bf16 sustained",
+                    "flops_per_launch": alg["gateup_flops"]}
+    layer_tflops = alg["total_flops"] * L * args.steps / (t_ms * 1e-3) / 1e12
+
+    # ------------------------------------------------------------------------ e2e --
+    e2e = None
+    if not args.skip_e2e:
+        x_host = x0.cpu().pin_memory()
+        out_host = torch.empty_like(x_host).pin_memory()
+        xd = torch.empty_like(x0)
+
+        def e2e_step():
+            xd.copy_(x_host, non_blocking=True)
+            x = step(xd)
+            out_host.copy_(x, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        _barrier(pg)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        te = _max_over_ranks(pg, e0.elapsed_time(e1), dev)
+        nbytes = x0.numel() * 2
+        e2e = {"value": round(world * layer_tokens * args.steps / (te * 1e-3), 1), "unit": UNIT,
+               "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes,
+               "ms_per_step": round(te / args.steps, 4),
+               "path": "pinned host x -> moe_forward x4 layers (C-ABI) -> pinned host out"}
+
+    del layers, wts
+    torch.cuda.empty_cache()
+
+    # --------------------------------------------------------------------- decode --
+    decode = None
+    if not args.skip_decode:
+        decode = run_decode(args, dev, pg, peaks)
+
+    # --------------------------------------------------------------- cpu baseline --
+    cpu = None
+    if rank == 0 and not args.skip_cpu:
+        cpu = cpu_baseline(wl, seconds=args.cpu_seconds)
+
+    res = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic (seeded normal weights/activations, random-init layer shape)",
+           "config": {"workload": "prefill T=8192, H=2048, E=256 top-8 + shared (I=Is=512), 4 distinct "
+                                  "layers, layer l+1 reads bf16(x_0 + out_l)",
+                      "tokens": T, "layers": L, "parallelism": "replicas" if world > 1 else "single GPU",
+                      "l2": "no flush: each layer's weights (1.6 GB) exceed the 129 MB L2",
+                      "value_definition": "tokens x layers / s (one token through one MoE layer)"},
+           "layer_tflops": round(layer_tflops, 1),
+           "roofline": roofline, "per_kernel": per_kernel, "gpu_launches": int(launches),
+           "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "decode": decode,
+           "peaks": peaks}
+    return res
+
+
+def run_decode(args, dev, pg, peaks):
+    import torch
+    from sparse_moe_router_gb300 import abi, inputs
+
+    wl = inputs.WORKLOADS["decode"]
+    shape, L = wl.shape, wl.n_layers
+    layers, x0 = inputs.make(wl, device=dev)
+    cfg = abi.config_of(shape)
+    ws = abi.alloc_workspace(cfg, 1)
+    wts = [abi.weights(l) for l in layers]
+    bufs = [x0.clone(), torch.empty_like(x0), torch.empty_like(x0)]
+    out = torch.empty_like(x0)
+    s = torch.cuda.Stream(device=dev)
+
+    def chain():
+        # layer l+1 reads bf16(x_0 + out_l), fused into the layer's last kernel
+        x = bufs[0]
+        for l in range(L):
+            nxt = bufs[1 + (l % 2)]
+            abi.moe_forward(cfg, wts[l], x, 1, out, nxt, ws, s, resid=bufs[0])
+            x = nxt
+
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            chain()
+    torch.cuda.synchronize()
+    assert abi.moe_check_status(ws) == 0
+    # capture the 40-layer chain as one graph
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            chain()
+    torch.cuda.synchronize()
+    reps = max(5, args.steps)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    times = []
+    n_launch0 = abi.moe_launch_count()
+    with torch.cuda.stream(s):   # replay() launches on the current stream: time on that stream
+        for _ in range(max(3, args.warmup)):
+            g.replay()
+        torch.cuda.synchronize()
+        for _ in range(reps):
+            e0.record(s)
+            g.replay()
+            e1.record(s)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+    assert abi.moe_launch_count() == n_launch0  # replays launch from the graph, not the library
+    t_med = statistics.median(times)
+    t_med = _max_over_ranks(pg, t_med, dev)
+    us_layer = 1e3 * t_med / L
+    nbytes = _decode_bytes(shape)
+    gbs = nbytes / (us_layer * 1e-6) / 1e9
+    # per-kernel split of one eager chain (outside the graph)
+    abi.timing_enable(True)
+    with torch.cuda.stream(s):
+        chain()
+    torch.cuda.synchronize()
+    abi.timing_enable(False)
+    split = {}
+    for name in ("decode_router", "decode_gateup", "decode_down"):
+        n, ms = abi.timing_read(name)
+        if n:
+            split[name] = {"launches": n, "avg_us": round(1e3 * ms / n, 2)}
+    del g
+    return {"workload": "decode T=1, 40 distinct layers (64.7 GB of weights), CUDA graph",
+            "us_per_layer": round(us_layer, 3), "graph_ms": round(t_med, 4), "reps": reps,
+            "p10_p90_ms": [round(sorted(times)[len(times) // 10], 4),
+                           round(sorted(times)[(9 * len(times)) // 10], 4)],
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                         "frac_of_8000": round(gbs / 8000.0, 4), "bytes_per_layer": nbytes,
+                         "traffic": None, "peak_source": peaks["source"] + " hbm copy"},
+            "eager_kernel_avg_us": split}
+
+
+def cpu_baseline(wl, seconds=12.0):
+    """The CPU oracle, as it stands, on a bounded sample of the prefill workload's tokens."""
+    import numpy as np
+    import torch
+
+    from oracle import moe_oracle as orc
+    from sparse_moe_router_gb300 import inputs
+
+    layers, x = inputs.make(wl, device="cuda" if torch.cuda.is_available() else "cpu", n_layers=1)
+    hl = inputs.layer_to_host(layers[0])
+    xs = inputs.to_u16(x)
+    del layers
+    threads = orc.threads(0)
+    k = wl.shape.top_k
+    # calibrate on a few tokens, then size the sample to about `seconds`
+    n0 = max(threads, 8)
+    t0 = time.perf_counter()
+    orc.forward(np.ascontiguousarray(xs[:n0]), hl, k)
+    dt = time.perf_counter() - t0
+    n = int(min(wl.T, max(n0, seconds / max(dt / n0, 1e-9))))
+    n = max(threads, (n // threads) * threads)
+    t0 = time.perf_counter()
+    orc.forward(np.ascontiguousarray(xs[:n]), hl, k)
+    dt = time.perf_counter() - t0
+    return {"value": round(n / dt, 2), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": "%d of the %d tokens of one layer of the prefill workload (fp64 C oracle, "
+                      "OpenMP over tokens), %.1f s" % (n, wl.T, dt)}
+
+
+def run_reference(args, world, rank):
+    """--impl reference: the CPU oracle on the host cores, a bounded sample per step."""
+    if rank != 0:
+        return None
+    import numpy as np
+    import torch
+
+    from oracle import moe_oracle as orc
+    from sparse_moe_router_gb300 import inputs
+
+    wl = inputs.WORKLOADS["prefill8k"]
+    layers, x = inputs.make(wl, device="cuda" if torch.cuda.is_available() else "cpu", n_layers=1)
+    hl = inputs.layer_to_host(layers[0])
+    xs = inputs.to_u16(x)
+    del layers
+    threads = orc.threads(0)
+    k = wl.shape.top_k
+    n0 = max(threads, 8)
+    t0 = time.perf_counter()
+    orc.forward(np.ascontiguousarray(xs[:n0]), hl, k)
+    per_tok = (time.perf_counter() - t0) / n0
+    # each step: about args.ref_step_seconds of oracle work
+    n = int(max(threads, min(wl.T, args.ref_step_seconds / max(per_tok, 1e-9))))
+    n = max(threads, (n // threads) * threads)
+    sample = np.ascontiguousarray(xs[:n])
+    for _ in range(args.warmup):
+        orc.forward(sample, hl, k)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        orc.forward(sample, hl, k)
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt
+    desc = "%d of the %d tokens of one prefill layer per step (fp64 C oracle, OpenMP over tokens)" % (n, wl.T)
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * dt / args.steps, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "prefill T=8192, H=2048, E=256 top-8 + shared (I=Is=512); "
+                                   "bounded token sample per step", "tokens_per_step": n},
+            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "kind": "oracle", "cores": threads,
+                             "sample": desc},
+            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--skip-decode", action="store_true")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=4.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local, pg = _dist_init()
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+    else:
+        res = run_ours(args, world, rank, local, pg)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if pg is not None:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

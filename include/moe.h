@@ -135,13 +135,14 @@ moe_status moe_combine(const moe_config *cfg, const float *y_rows, const int32_t
  * 8192, 4096, 2048 and 1024 tokens and an exact tail (no padding); every piece runs the same
  * kernels, so the result equals the concatenation of per-piece calls.  T == 1 takes the
  * decode path (HBM-streaming GEMVs).  x_next may be NULL; when given it receives
- * bf16(x + out), the residual-stream update of a layer stack (fused into the last kernel).
- * x_next may alias x.  ws: moe_workspace_size(cfg, T) bytes.  The fused combine adds fp32
- * partial sums with atomics, so the fp32 summation order can differ from run to run (the
- * result stays within the layer's tolerance, but is not bit-reproducible). */
+ * bf16(resid + out), the residual-stream update of a layer stack, fused into the last
+ * kernel; resid [T,H] may be NULL, meaning x.  x_next may alias resid (not x, when they
+ * differ).  ws: moe_workspace_size(cfg, T) bytes.  The fused combine adds fp32 partial sums
+ * with atomics, so the fp32 summation order can differ from run to run (the result stays
+ * within the layer's tolerance, but is not bit-reproducible). */
 moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const moe_bf16 *x, int T,
-                       moe_bf16 *out, moe_bf16 *x_next, void *ws, size_t ws_bytes,
-                       void *stream);
+                       moe_bf16 *out, const moe_bf16 *resid, moe_bf16 *x_next, void *ws,
+                       size_t ws_bytes, void *stream);
 
 /* Reads and clears the device status word in `ws` (synchronises `stream`).  *device_status
  * receives MOE_OK or the first error recorded by a kernel (MOE_ERR_TIMEOUT for a wait that

@@ -68,7 +68,7 @@ def load(path: str = LIB_PATH):
     L.moe_permute.argtypes = [C, _P, _I, _P, _P, _P, _P, _SZ, _P]
     L.moe_expert_ffn.argtypes = [C, W, _P, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]
     L.moe_combine.argtypes = [C, _P, _P, _P, _P, _I, _P, _P]
-    L.moe_forward.argtypes = [C, W, _P, _I, _P, _P, _P, _SZ, _P]
+    L.moe_forward.argtypes = [C, W, _P, _I, _P, _P, _P, _P, _SZ, _P]
     L.moe_check_status.argtypes = [_P, _SZ, ctypes.POINTER(_I), _P]
     L.moe_plan_pieces.argtypes = [_I, ctypes.POINTER(_I), _I]
     L.moe_plan_pieces.restype = _I
@@ -179,16 +179,16 @@ def moe_combine(cfg, y_rows, inv, topk_w, shared_y, T, out, stream=None):
     _check("moe_combine", st)
 
 
-def moe_forward(cfg, w: Weights, x, T, out, x_next, ws, stream=None):
+def moe_forward(cfg, w: Weights, x, T, out, x_next, ws, stream=None, resid=None):
     st = lib().moe_forward(ctypes.byref(cfg), ctypes.byref(w), _ptr(x), int(T), _ptr(out),
-                           _ptr(x_next), _ptr(ws), ws.numel(), _stream(stream))
+                           _ptr(resid), _ptr(x_next), _ptr(ws), ws.numel(), _stream(stream))
     _check("moe_forward", st)
 
 
-def moe_forward_status(cfg, w: Weights, x, T, out, x_next, ws, stream=None) -> int:
+def moe_forward_status(cfg, w: Weights, x, T, out, x_next, ws, stream=None, resid=None) -> int:
     """Like moe_forward but returns the status code instead of raising."""
     return int(lib().moe_forward(ctypes.byref(cfg), ctypes.byref(w), _ptr(x), int(T), _ptr(out),
-                                 _ptr(x_next), _ptr(ws), ws.numel(), _stream(stream)))
+                                 _ptr(resid), _ptr(x_next), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def moe_check_status(ws, stream=None) -> int:

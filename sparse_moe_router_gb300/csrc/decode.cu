@@ -10,7 +10,7 @@
 //             waits on another), then the k experts' gate/up row pairs -> h (bf16);
 //   kernel 3  for each output n: sum_j w_j * Wd[e_j][n,:].h_j + Ws_down[n,:].h_s, one warp
 //             per output, all k+1 rows of the output streamed together; bf16 out and the
-//             residual update x + out.
+//             residual update resid + out.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kBlock) decode_down_kernel(DecodeArgs a) {
         const __nv_bfloat16 o = __float2bfloat16_rn(acc);
         a.out[n] = *reinterpret_cast<const uint16_t *>(&o);
         if (a.x_next) {
-            const __nv_bfloat16 xv = *reinterpret_cast<const __nv_bfloat16 *>(&a.x[n]);
+            const __nv_bfloat16 xv = *reinterpret_cast<const __nv_bfloat16 *>(&a.resid[n]);
             a.x_next[n] = bf16_bits(__bfloat162float(xv) + __bfloat162float(o));
         }
     }

@@ -5,23 +5,29 @@
 // "MOE 内核优化": the MoE kernel bounds prefill) are, per expert e, products of the expert's
 // weight rows with the rows of the tokens routed to e.  The kernel computes them "swap-AB":
 //   D[f, j] = sum_k W[g*F + f, k] * B[row0 + j, k]
-// with the weight rows f on the MMA's M side (128 per tile) and the group's token rows j on
-// the N side (up to 128 per tile, N rounded up to 16).  A ragged expert with 257 rows thus
-// costs one extra 16-wide column block, not a second 128-row tile.
+// with 128 weight rows on the MMA's M side and up to 256 of the group's token rows on the N
+// side.  A group of c rows is cut into ceil(c/256) token tiles of equal size (rounded up to
+// 16), so an expert with 270 tokens costs two 144/126-wide tiles that each read the weight
+// tile once, not three tiles of 128/128/14.
+//   SwiGLU: the 128 weight rows of a tile are 64 gate rows and the same 64 features' up rows,
+//           so gate and up land in TMEM lanes i and 64 + i of one accumulator.
 //
-// Roles (288 threads):
-//   warps 0-3  epilogue: tcgen05.ld of the fp32 accumulator (warp w reads TMEM lanes
-//              32w..32w+31 = weight rows), fused epilogue, global stores / atomics;
-//   warps 4-7  producers: the B operand (token rows, optionally gathered through the expert
-//              permutation) with 16-byte cp.async into the 128-byte-swizzled K-major layout;
-//              thread 128 also issues the TMA loads of the weight tile(s);
-//   warp 8     allocates TMEM; lane 0 issues tcgen05.mma (kind::f16, bf16 -> fp32) and
-//              tcgen05.commit.
-// Pipelines: S shared-memory stages (full/empty mbarriers) and two TMEM accumulator buffers
-// (acc_full/acc_empty), so the epilogue of one tile overlaps the main loop of the next.
-// Tiles are walked statically (tile = blockIdx.x + i*gridDim.x), ordered (group, weight
-// tile, token tile) with the token tile fastest, so the CTAs that share a weight tile run
-// at the same time and the weight tile is fetched from HBM once.
+// Roles (one CTA per SM):
+//   warps 0..P-1  epilogue (P = 16 for the weighted scatter-add, else 8): warp w reads TMEM
+//               lanes 32*(w%4)..+31 (the hardware's lane quarters), and the P/4 warps of a
+//               quarter take every (P/4)-th 16-token chunk;
+//   warps P..P+3 producers.  Contiguous B (token rows in order): one thread issues the TMA
+//               loads of the weight tile and of the B tile.  Gathered B (token rows picked
+//               through the expert permutation): warp 8+s owns shared-memory stage s; it
+//               issues that stage's weight TMA, copies the gathered rows with 16-byte cp.async
+//               into the 128-byte-swizzled K-major layout, waits for its own copies, fences
+//               them into the async proxy and arrives, so all stages fill concurrently;
+//   warp P+4    allocates TMEM; lane 0 issues tcgen05.mma (kind::f16, bf16 -> fp32) and
+//               tcgen05.commit.
+// Pipelines: 4 shared-memory stages (full/empty mbarriers) and two TMEM accumulators of 256
+// columns (acc_full/acc_empty), so the epilogue of one tile overlaps the next main loop.
+// Tiles are walked statically (tile = blockIdx.x + i*gridDim.x), ordered (group, weight tile,
+// token tile) with the token tile fastest, so CTAs sharing a weight tile run together.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -33,23 +39,30 @@ namespace {
 constexpr int BM = kTileM;   // weight rows per tile (MMA M)
 constexpr int BN = kTileN;   // token rows per tile (max MMA N)
 constexpr int BK = 64;       // K elements per stage: one 128-byte swizzle row
-constexpr int kThreads = 288;
+constexpr int kStages = 4;
+constexpr int kABytes = BM * BK * 2;        // 16 KB
+constexpr int kBBytes = BN * BK * 2;        // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kAccCols = BN;                // fp32 accumulator columns per TMEM buffer
+constexpr uint32_t kTmemCols = 2 * kAccCols;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
 constexpr int kMaxGroups = 1025;                  // E <= 1024 experts (+1 spare)
+constexpr int kStgStride = BM + 4;                // SwiGLU staging row (floats), padded for banks
 
 template <int EPI>
 struct Cfg {
-    static constexpr int kAParts = (EPI == EPI_SWIGLU) ? 2 : 1;
-    static constexpr int kABytes = kAParts * BM * BK * 2;
-    static constexpr int kBBytes = BN * BK * 2;
-    static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kStages = (EPI == EPI_SWIGLU) ? 4 : 6;
-    static constexpr int kLag = kStages - 1;
-    static constexpr int kAccCols = kAParts * BN;
-    static constexpr uint32_t kTmemCols = 2 * kAccCols;
+    // epilogue warps: the weighted scatter-add needs many warps issuing reductions to keep
+    // enough of them in flight; the others need 8
+    static constexpr int kEpiWarps = (EPI == EPI_COMBINE) ? 16 : 8;
+    static constexpr int kProdWarp0 = kEpiWarps;    // 4 producer warps
+    static constexpr int kMmaWarp = kEpiWarps + 4;  // MMA + TMEM allocation warp
+    static constexpr int kThreads = (kEpiWarps + 5) * 32;
+    static constexpr int kFT = (EPI == EPI_SWIGLU) ? 64 : BM;    // output features per tile
+    static constexpr int kStagingBytes = (EPI == EPI_SWIGLU) ? 2 * 16 * kStgStride * 4 : 0;
     static constexpr int kBarBytes = (2 * kStages + 5) * 8;
-    static constexpr int kSmemBytes =
-        1024 /*alignment slack*/ + kStages * kStageBytes + kBarBytes + 16 + 2 * (kMaxGroups + 1) * 4;
+    static constexpr int kRowTableBytes = 4 * BN * 4;
+    static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + kStagingBytes +
+                                      kBarBytes + 16 + 2 * (kMaxGroups + 1) * 4 + kRowTableBytes;
 };
 
 struct TileInfo {
@@ -71,9 +84,11 @@ __device__ __forceinline__ TileInfo decode_tile(int tau, int nft, const int *g_t
     const int ntt = g_tiles[lo + 1] - g_tiles[lo];
     t.ftile = local / ntt;
     const int tt = local - t.ftile * ntt;
-    t.row0 = g_rows[lo] + tt * BN;
-    const int rem = g_rows[lo + 1] - t.row0;
-    t.nvalid = rem < BN ? rem : BN;
+    const int c = g_rows[lo + 1] - g_rows[lo];
+    const int tsz = token_tile_size(c);
+    t.row0 = g_rows[lo] + tt * tsz;
+    const int rem = c - tt * tsz;
+    t.nvalid = rem < tsz ? rem : tsz;
     return t;
 }
 
@@ -81,40 +96,58 @@ __device__ __forceinline__ void set_error(int *status, int code) {
     if (status) atomicCAS(status, 0, code);
 }
 
+__device__ __forceinline__ float sel4(float a0, float a1, float a2, float a3, int i) {
+    return i == 0 ? a0 : (i == 1 ? a1 : (i == 2 ? a2 : a3));
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
 template <int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
     gemm_kernel(const GemmArgs p, const __grid_constant__ CUtensorMap tm_a0,
-                const __grid_constant__ CUtensorMap tm_a1) {
+                const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_b) {
     using C = Cfg<EPI>;
+    constexpr int kEpiWarps = C::kEpiWarps;
+    constexpr int kProdWarp0 = C::kProdWarp0;
+    constexpr int kMmaWarp = C::kMmaWarp;
+    constexpr int kThreads = C::kThreads;
+    constexpr int kSubs = kEpiWarps / 4;  // warps per TMEM lane quarter
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kStages * C::kStageBytes);
+    float *staging = reinterpret_cast<float *>(smem + kStages * kStageBytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes + C::kStagingBytes);
     uint64_t *full = bars;
-    uint64_t *empty = bars + C::kStages;
-    uint64_t *acc_full = bars + 2 * C::kStages;
+    uint64_t *empty = bars + kStages;
+    uint64_t *acc_full = bars + 2 * kStages;
     uint64_t *acc_empty = acc_full + 2;
     uint64_t *drain = acc_empty + 2;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    volatile int *epi_vote = reinterpret_cast<volatile int *>(tmem_holder + 2);  // 2 slots
     int *g_tiles = reinterpret_cast<int *>(tmem_holder + 4);
     int *g_rows = g_tiles + (kMaxGroups + 1);
+    int *row_tables = g_rows + (kMaxGroups + 1);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
+    const bool gather = p.row_src != nullptr;  // only with EPI_SWIGLU
 
     if (tid == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
-            ptx::mbar_init(&full[s], 128 + 1);
+        for (int s = 0; s < kStages; ++s) {
+            // gathered B: the stage's warp arrives twice (weight expect_tx, then its copies)
+            ptx::mbar_init(&full[s], gather ? 2 : 1);
             ptx::mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&acc_full[b], 1);
-            ptx::mbar_init(&acc_empty[b], 128);
+            ptx::mbar_init(&acc_empty[b], kEpiWarps * 32);
         }
         ptx::mbar_init(drain, 1);
         *abort_flag = 0;
+        epi_vote[0] = 0;
+        epi_vote[1] = 0;
         ptx::fence_mbar_init();
     }
     int G;
@@ -124,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             g_rows[0] = 0;
             g_rows[1] = p.M_single;
             g_tiles[0] = 0;
-            g_tiles[1] = (p.M_single + BN - 1) / BN;
+            g_tiles[1] = token_tile_count(p.M_single);
         }
     } else {
         G = p.n_groups;
@@ -134,87 +167,116 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncthreads();
-    const int nft = (p.F + BM - 1) / BM;
+    const int nft = (p.F + C::kFT - 1) / C::kFT;
     const int total = nft * g_tiles[G];
     if ((int)blockIdx.x >= total) return;  // CTA-uniform; nothing allocated yet
 
-    if (warp == 8) ptx::tmem_alloc(tmem_holder, C::kTmemCols);
+    if (warp == kMmaWarp) ptx::tmem_alloc(tmem_holder, kTmemCols);
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
     const int nkb = p.K / BK;
 
-    if (warp >= 4 && warp < 8) {
+    if (warp >= kProdWarp0 && warp < kMmaWarp) {
         // ------------------------------------------------------------ producers --
-        const int q = tid - 128;
-        const int c = q & 7;        // 16-byte chunk within the 128-byte row segment
-        const int rbase = q >> 3;   // rows rbase + 16*i
-        const uint16_t *bsrc = static_cast<const uint16_t *>(p.b_src);
-        if (q == 0) {
-            ptx::tma_prefetch_desc(&tm_a0);
-            if (EPI == EPI_SWIGLU) ptx::tma_prefetch_desc(&tm_a1);
-        }
-        int it = 0;
         bool ok = true;
-        for (int tau = blockIdx.x; tau < total && ok; tau += gridDim.x) {
-            const TileInfo t = decode_tile(tau, nft, g_tiles, g_rows, G);
-            const int nmma = (t.nvalid + 15) & ~15;
-            const uint16_t *src[8];
-            uint32_t nbytes[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int j = rbase + 16 * i;
-                if (j < t.nvalid) {
-                    const int r = t.row0 + j;
-                    const int srow = p.gather_perm ? (__ldg(&p.gather_perm[r]) / p.gather_k) : r;
-                    src[i] = bsrc + (size_t)srow * p.K + c * 8;
-                    nbytes[i] = 16;
-                } else if (j < nmma) {
-                    src[i] = bsrc;
-                    nbytes[i] = 0;  // zero fill: read by the MMA, ignored by the epilogue
-                } else {
-                    src[i] = nullptr;
-                    nbytes[i] = 0;
-                }
-            }
-            const int arow = t.g * p.F + t.ftile * BM;
-            for (int kb = 0; kb < nkb; ++kb, ++it) {
-                const int s = it % C::kStages;
-                const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
-                if (!ptx::mbar_wait(&empty[s], ph ^ 1u, kWaitLimitNs, abort_flag)) { ok = false; break; }
-                uint8_t *st = smem + s * C::kStageBytes;
-                if (q == 0) {
-                    ptx::mbar_arrive_expect_tx(&full[s], C::kABytes);
-                    ptx::tma_load_2d(st, &tm_a0, kb * BK, arow, &full[s]);
-                    if (EPI == EPI_SWIGLU) ptx::tma_load_2d(st + BM * BK * 2, &tm_a1, kb * BK, arow, &full[s]);
-                }
-                const uint32_t bst = ptx::smem_u32(st + C::kABytes);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    if (src[i] != nullptr) {
-                        const int j = rbase + 16 * i;
-                        const uint32_t dst = bst + j * 128 + ((c ^ (j & 7)) << 4);
-                        const uint16_t *sp = nbytes[i] ? src[i] + kb * BK : src[i];
-                        ptx::cp_async_16(dst, sp, nbytes[i]);
+        if (!gather) {
+            if (tid == kProdWarp0 * 32) {
+                ptx::tma_prefetch_desc(&tm_a0);
+                if (EPI == EPI_SWIGLU) ptx::tma_prefetch_desc(&tm_a1);
+                ptx::tma_prefetch_desc(&tm_b);
+                int it = 0;
+                for (int tau = blockIdx.x; tau < total && ok; tau += gridDim.x) {
+                    const TileInfo t = decode_tile(tau, nft, g_tiles, g_rows, G);
+                    const int arow = t.g * p.F + t.ftile * C::kFT;
+                    for (int kb = 0; kb < nkb; ++kb, ++it) {
+                        const int s = it % kStages;
+                        const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+                        if (!ptx::mbar_wait(&empty[s], ph ^ 1u, kWaitLimitNs, abort_flag)) { ok = false; break; }
+                        uint8_t *st = smem + s * kStageBytes;
+                        ptx::mbar_arrive_expect_tx(&full[s], kABytes + kBBytes);
+                        if (EPI == EPI_SWIGLU) {
+                            ptx::tma_load_2d(st, &tm_a0, kb * BK, arow, &full[s]);
+                            ptx::tma_load_2d(st + kABytes / 2, &tm_a1, kb * BK, arow, &full[s]);
+                        } else {
+                            ptx::tma_load_2d(st, &tm_a0, kb * BK, arow, &full[s]);
+                        }
+                        ptx::tma_load_2d(st + kABytes, &tm_b, kb * BK, t.row0, &full[s]);
                     }
                 }
-                ptx::cp_async_commit();
-                if (it >= C::kLag) {
-                    ptx::cp_async_wait<C::kLag>();
-                    ptx::fence_proxy_async_smem();
-                    ptx::mbar_arrive(&full[(it - C::kLag) % C::kStages]);
-                }
             }
+        } else {
+            // warp kProdWarp0+slot owns stage `slot`: iterations it with it % kStages == slot
+            const int slot = warp - kProdWarp0;
+            uint32_t *table = reinterpret_cast<uint32_t *>(row_tables) + slot * BN;
+            const char *bsrc = static_cast<const char *>(p.b_src);
+            const int c = lane & 7;        // 16-byte chunk of the 128-byte row segment
+            const int rsub = lane >> 3;    // rows rsub + 4*m
+            if (lane == 0) {
+                ptx::tma_prefetch_desc(&tm_a0);
+                ptx::tma_prefetch_desc(&tm_a1);
+            }
+            int it = 0;
+            for (int tau = blockIdx.x; tau < total && ok; tau += gridDim.x) {
+                const TileInfo t = decode_tile(tau, nft, g_tiles, g_rows, G);
+                const int nmma = (t.nvalid + 15) & ~15;
+                const int first = (slot - it % kStages + kStages) % kStages;
+                if (first < nkb) {
+                    // byte offset of each gathered row's 16-byte chunk c (0xffffffff: zero row)
+                    __syncwarp();
+                    for (int j = lane; j < BN; j += 32)
+                        table[j] = j < t.nvalid ? (uint32_t)__ldg(&p.row_src[t.row0 + j]) * (uint32_t)(p.K * 2)
+                                               : 0xffffffffu;
+                    __syncwarp();
+                }
+                const int arow = t.g * p.F + t.ftile * C::kFT;
+                for (int kb = first; kb < nkb; kb += kStages) {
+                    const int itk = it + kb;
+                    const uint32_t ph = (uint32_t)(itk / kStages) & 1u;
+                    // every lane waits; the warp gives up together (it must stay converged)
+                    const bool got = ptx::mbar_wait(&empty[slot], ph ^ 1u, kWaitLimitNs, abort_flag);
+                    if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                    uint8_t *st = smem + slot * kStageBytes;
+                    if (lane == 0) {
+                        ptx::mbar_arrive_expect_tx(&full[slot], kABytes);
+                        ptx::tma_load_2d(st, &tm_a0, kb * BK, arow, &full[slot]);
+                        ptx::tma_load_2d(st + kABytes / 2, &tm_a1, kb * BK, arow, &full[slot]);
+                    }
+                    const uint32_t bst = ptx::smem_u32(st + kABytes);
+                    const char *kbase = bsrc + kb * BK * 2 + c * 16;
+                    // rows j = rsub + 4m, 8 per step; a step may run up to 16 rows past nmma:
+                    // those rows are zero-filled inside the stage buffer and the MMA never
+                    // reads them
+                    for (int j0 = rsub; j0 < nmma; j0 += 32) {
+                        uint32_t off[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) off[u] = table[j0 + 4 * u];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const int j = j0 + 4 * u;
+                            const uint32_t dst = bst + j * 128 + ((c ^ (j & 7)) << 4);
+                            if (off[u] != 0xffffffffu)
+                                ptx::cp_async_16(dst, kbase + off[u], 16);
+                            else
+                                ptx::cp_async_16(dst, bsrc, 0);  // zero rows up to the MMA's N
+                        }
+                    }
+                    ptx::cp_async_commit();
+                    ptx::cp_async_wait_all();
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(&full[slot]);
+                }
+                it += nkb;
+            }
+            ptx::cp_async_wait_all();
         }
-        ptx::cp_async_wait<0>();
-        ptx::fence_proxy_async_smem();
-        for (int d = (it > C::kLag ? it - C::kLag : 0); d < it; ++d) ptx::mbar_arrive(&full[d % C::kStages]);
         if (!ok) {
             set_error(p.status, MOE_ERR_TIMEOUT);
             *abort_flag = 1;
         }
-    } else if (warp == 8) {
+    } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA --
         if (lane == 0) {
             int it = 0, tc = 0;
@@ -226,24 +288,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
                 if (!ptx::mbar_wait(&acc_empty[buf], aph ^ 1u, kWaitLimitNs, abort_flag)) { ok = false; break; }
                 ptx::tc_fence_after();
-                const uint32_t d_base = tmem_base + (uint32_t)(buf * C::kAccCols);
+                const uint32_t d_base = tmem_base + (uint32_t)(buf * kAccCols);
                 const uint32_t idesc = ptx::idesc_bf16_f32(BM, nmma);
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
-                    const int s = it % C::kStages;
-                    const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
+                    const int s = it % kStages;
+                    const uint32_t ph = (uint32_t)(it / kStages) & 1u;
                     if (!ptx::mbar_wait(&full[s], ph, kWaitLimitNs, abort_flag)) { ok = false; break; }
                     ptx::tc_fence_after();
-                    const uint32_t a_addr = ptx::smem_u32(smem + s * C::kStageBytes);
-                    const uint32_t b_addr = a_addr + C::kABytes;
+                    const uint32_t a_addr = ptx::smem_u32(smem + s * kStageBytes);
+                    const uint32_t b_addr = a_addr + kABytes;
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t bd = ptx::sw128_desc(b_addr + kk * 32);
-                        const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
-                        ptx::mma_bf16(d_base, ptx::sw128_desc(a_addr + kk * 32), bd, idesc, acc);
-                        if (EPI == EPI_SWIGLU)
-                            ptx::mma_bf16(d_base + BN, ptx::sw128_desc(a_addr + BM * BK * 2 + kk * 32), bd,
-                                          idesc, acc);
-                    }
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        ptx::mma_bf16(d_base, ptx::sw128_desc(a_addr + kk * 32), ptx::sw128_desc(b_addr + kk * 32),
+                                      idesc, (kb | kk) != 0 ? 1u : 0u);
                     ptx::mma_commit(&empty[s]);
                 }
                 if (!ok) break;
@@ -260,70 +317,122 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue --
-        const int quarter = warp;  // warps 0..3 own TMEM lanes 32*warp .. 32*warp+31
+        const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+        const int sub = warp >> 2;     // this warp takes chunks cidx with cidx % kSubs == sub
         const int frow = quarter * 32 + lane;
+        float *stg = staging + sub * 16 * kStgStride;  // SwiGLU exchange buffer of this sub-group
         int tc = 0;
         bool ok = true;
         for (int tau = blockIdx.x; tau < total; tau += gridDim.x, ++tc) {
             const TileInfo t = decode_tile(tau, nft, g_tiles, g_rows, G);
             const int buf = tc & 1;
             const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
-            if (!ptx::mbar_wait(&acc_full[buf], aph, kWaitLimitNs, abort_flag)) { ok = false; break; }
+            // combine: each lane fetches (token, weight) of rows lane + 32m of the tile before
+            // the accumulator is ready, so the loads overlap the tile's main loop
+            int tok8[8];
+            float w8[8];
+            if (EPI == EPI_COMBINE) {
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const int j = lane + 32 * m;
+                    tok8[m] = 0;
+                    w8[m] = 0.f;
+                    if (j < t.nvalid) {
+                        const int row = t.row0 + j;
+                        tok8[m] = p.epi_tok ? __ldg(&p.epi_tok[row]) : row;
+                        w8[m] = p.epi_w ? __ldg(&p.epi_w[row]) : 1.f;
+                    }
+                }
+            }
+            // The epilogue warps share named barriers, so they give up together: lane 0 of
+            // each warp votes, and the vote is read by all after the barrier.
+            const bool got = ptx::mbar_wait(&acc_full[buf], aph, kWaitLimitNs, abort_flag);
+            if (lane == 0 && !got) epi_vote[tc & 1] = 1;
+            ptx::named_bar(1, kEpiWarps * 32);
+            const bool fail = epi_vote[tc & 1] != 0;
+            ptx::named_bar(1, kEpiWarps * 32);
+            if (fail) { ok = false; break; }
             ptx::tc_fence_after();
-            const int f = t.ftile * BM + frow;
-            const bool fvalid = f < p.F;
-            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * C::kAccCols);
+            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * kAccCols);
             float bias_f = 0.f;
-            if (EPI == EPI_F32 && p.bias != nullptr && fvalid) bias_f = __ldg(&p.bias[f]);
-            for (int j0 = 0; j0 < t.nvalid; j0 += 16) {
+            if (EPI == EPI_F32) {
+                const int f = t.ftile * BM + frow;
+                if (p.bias != nullptr && f < p.F) bias_f = __ldg(&p.bias[f]);
+            }
+#pragma unroll
+            for (int cidx = 0; cidx < BN / 16; ++cidx) {
+                const int j0 = 16 * cidx;
+                if (j0 >= t.nvalid) break;
+                if (cidx % kSubs != sub) continue;
                 uint32_t r[16];
                 ptx::tmem_ld_16(taddr + (uint32_t)j0, r);
+                ptx::tmem_ld_wait();
                 if (EPI == EPI_SWIGLU) {
-                    uint32_t u[16];
-                    ptx::tmem_ld_16(taddr + BN + (uint32_t)j0, u);
-                    ptx::tmem_ld_wait();
-                    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out);
+                    // lanes 0..63 hold gate, 64..127 the same features' up: exchange through
+                    // shared memory, then thread q computes token q/8, features 8*(q%8)..+7
+                    // and writes them as one 16-byte store.
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int j = j0 + jj;
-                        if (j < t.nvalid && fvalid) {
-                            const float g = __uint_as_float(r[jj]);
-                            const float uu = __uint_as_float(u[jj]);
-                            const float h = g / (1.0f + expf(-g)) * uu;
-                            o[(size_t)(t.row0 + j) * p.ld + f] = __float2bfloat16_rn(h);
-                        }
+                    for (int jj = 0; jj < 16; ++jj) stg[jj * kStgStride + frow] = __uint_as_float(r[jj]);
+                    ptx::named_bar(2 + sub, 128);
+                    const int q = frow;
+                    const int jj = q >> 3, fg = (q & 7) * 8;
+                    if (j0 + jj < t.nvalid) {
+                        const float4 g0 = *reinterpret_cast<const float4 *>(&stg[jj * kStgStride + fg]);
+                        const float4 g1 = *reinterpret_cast<const float4 *>(&stg[jj * kStgStride + fg + 4]);
+                        const float4 u0 = *reinterpret_cast<const float4 *>(&stg[jj * kStgStride + 64 + fg]);
+                        const float4 u1 = *reinterpret_cast<const float4 *>(&stg[jj * kStgStride + 64 + fg + 4]);
+                        __align__(16) __nv_bfloat16 h[8] = {
+                            __float2bfloat16_rn(silu_mul(g0.x, u0.x)), __float2bfloat16_rn(silu_mul(g0.y, u0.y)),
+                            __float2bfloat16_rn(silu_mul(g0.z, u0.z)), __float2bfloat16_rn(silu_mul(g0.w, u0.w)),
+                            __float2bfloat16_rn(silu_mul(g1.x, u1.x)), __float2bfloat16_rn(silu_mul(g1.y, u1.y)),
+                            __float2bfloat16_rn(silu_mul(g1.z, u1.z)), __float2bfloat16_rn(silu_mul(g1.w, u1.w))};
+                        __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out);
+                        *reinterpret_cast<uint4 *>(&o[(size_t)(t.row0 + j0 + jj) * p.ld + t.ftile * 64 + fg]) =
+                            *reinterpret_cast<const uint4 *>(h);
                     }
+                    ptx::named_bar(2 + sub, 128);
                 } else if (EPI == EPI_F32) {
-                    ptx::tmem_ld_wait();
+                    const int f = t.ftile * BM + frow;
                     float *o = static_cast<float *>(p.out);
+                    if (f < p.F) {
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int j = j0 + jj;
-                        if (j < t.nvalid && fvalid)
-                            o[(size_t)(t.row0 + j) * p.ld + f] = __uint_as_float(r[jj]) + bias_f;
+                        for (int jj = 0; jj < 16; ++jj)
+                            if (j0 + jj < t.nvalid)
+                                o[(size_t)(t.row0 + j0 + jj) * p.ld + f] = __uint_as_float(r[jj]) + bias_f;
                     }
                 } else {
-                    ptx::tmem_ld_wait();
-                    // token and routing weight of the 16 rows, spread over lanes 0..15
-                    int my_tok = 0;
-                    float my_w = 1.f;
-                    if (lane < 16 && j0 + lane < t.nvalid) {
-                        const int row = t.row0 + j0 + lane;
-                        if (p.epi_perm != nullptr) {
-                            const int pair = __ldg(&p.epi_perm[row]);
-                            my_tok = pair / p.epi_k;
-                            my_w = __ldg(&p.epi_w[pair]);
-                        } else {
-                            my_tok = row;
-                        }
-                    }
+                    // 4x4 transposes inside each lane quad turn (one feature, 4 tokens) per lane
+                    // into (4 consecutive features, one token) per lane: one fire-and-forget
+                    // 16-byte add per lane per 4 tokens.  (token, weight) of row j live in lane
+                    // j % 32, register j / 32.
+                    const int my_tok = tok8[cidx >> 1];
+                    const float my_w = w8[cidx >> 1];
                     float *o = static_cast<float *>(p.out);
+                    const int qd = lane & 3;
+                    const int fq = t.ftile * BM + quarter * 32 + (lane & ~3);
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int tok = __shfl_sync(0xffffffffu, my_tok, jj);
-                        const float w = __shfl_sync(0xffffffffu, my_w, jj);
-                        if (j0 + jj < t.nvalid && fvalid)
-                            atomicAdd(&o[(size_t)tok * p.ld + f], w * __uint_as_float(r[jj]));
+                    for (int g4 = 0; g4 < 4; ++g4) {
+                        const float a0 = __uint_as_float(r[4 * g4 + 0]);
+                        const float a1 = __uint_as_float(r[4 * g4 + 1]);
+                        const float a2 = __uint_as_float(r[4 * g4 + 2]);
+                        const float a3 = __uint_as_float(r[4 * g4 + 3]);
+                        float b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const float send = sel4(a0, a1, a2, a3, (qd - m) & 3);
+                            const int src = (lane & ~3) | ((qd + m) & 3);
+                            const float got2 = __shfl_sync(0xffffffffu, send, src);
+                            const int bi = (qd + m) & 3;
+                            b0 = bi == 0 ? got2 : b0;
+                            b1 = bi == 1 ? got2 : b1;
+                            b2 = bi == 2 ? got2 : b2;
+                            b3 = bi == 3 ? got2 : b3;
+                        }
+                        const int jt = 4 * g4 + qd;  // this lane's token within the 16
+                        const int tok = __shfl_sync(0xffffffffu, my_tok, 16 * (cidx & 1) + jt);
+                        const float w = __shfl_sync(0xffffffffu, my_w, 16 * (cidx & 1) + jt);
+                        if (j0 + jt < t.nvalid)
+                            ptx::red_add_v4(&o[(size_t)tok * p.ld + fq], w * b0, w * b1, w * b2, w * b3);
                     }
                 }
             }
@@ -338,15 +447,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 8) {
+    if (warp == kMmaWarp) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, C::kTmemCols);
+        ptx::tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
 template <int EPI>
-cudaError_t launch_impl(const GemmArgs &a, const CUtensorMap &m0, const CUtensorMap &m1, int kc,
-                        cudaStream_t s) {
+cudaError_t launch_impl(const GemmArgs &a, const CUtensorMap &m0, const CUtensorMap &m1,
+                        const CUtensorMap &mb, int kc, cudaStream_t s) {
     using C = Cfg<EPI>;
     static bool attr_done[64] = {false};
     int dev = 0;
@@ -360,26 +469,29 @@ cudaError_t launch_impl(const GemmArgs &a, const CUtensorMap &m0, const CUtensor
     const DeviceInfo &di = device_info();
     int grid = di.sm_count;
     if (a.group_rows == nullptr) {
-        const int nft = (a.F + BM - 1) / BM;
-        const int tiles = nft * ((a.M_single + BN - 1) / BN);
+        const int nft = (a.F + C::kFT - 1) / C::kFT;
+        const int tiles = nft * token_tile_count(a.M_single);
         if (tiles < grid) grid = tiles;
     }
     if (grid <= 0) return cudaSuccess;
     LaunchScope scope(kc, s);
-    gemm_kernel<EPI><<<grid, kThreads, C::kSmemBytes, s>>>(a, m0, m1);
+    gemm_kernel<EPI><<<grid, C::kThreads, C::kSmemBytes, s>>>(a, m0, m1, mb);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(GemmEpi epi, const GemmArgs &a, const CUtensorMap &tm_a0,
-                        const CUtensorMap &tm_a1, int kc, cudaStream_t s) {
+                        const CUtensorMap &tm_a1, const CUtensorMap &tm_b, int kc, cudaStream_t s) {
     if (a.n_groups > kMaxGroups - 1) return cudaErrorInvalidValue;
     if (a.K % BK != 0 || a.K <= 0) return cudaErrorInvalidValue;
+    if (a.row_src != nullptr && epi != EPI_SWIGLU) return cudaErrorInvalidValue;
+    if (epi == EPI_SWIGLU && (a.F % 64 != 0 || a.ld % 8 != 0)) return cudaErrorInvalidValue;
+    if (epi == EPI_COMBINE && (a.F % BM != 0 || a.ld % 4 != 0)) return cudaErrorInvalidValue;
     switch (epi) {
-        case EPI_F32: return launch_impl<EPI_F32>(a, tm_a0, tm_a1, kc, s);
-        case EPI_SWIGLU: return launch_impl<EPI_SWIGLU>(a, tm_a0, tm_a1, kc, s);
-        case EPI_COMBINE: return launch_impl<EPI_COMBINE>(a, tm_a0, tm_a1, kc, s);
+        case EPI_F32: return launch_impl<EPI_F32>(a, tm_a0, tm_a1, tm_b, kc, s);
+        case EPI_SWIGLU: return launch_impl<EPI_SWIGLU>(a, tm_a0, tm_a1, tm_b, kc, s);
+        case EPI_COMBINE: return launch_impl<EPI_COMBINE>(a, tm_a0, tm_a1, tm_b, kc, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/moe.h"
+#include "moe.h"
 
 namespace moe {
 
@@ -56,10 +56,9 @@ enum GemmEpi { EPI_F32 = 0, EPI_SWIGLU = 1, EPI_COMBINE = 2 };
 
 struct GemmArgs {
     // token side (B operand): row r of the group row space reads source row
-    // gather_perm ? gather_perm[r] / gather_k : r of b_src ([*, K] bf16)
+    // row_src ? row_src[r] : r of b_src ([*, K] bf16)
     const void *b_src;
-    const int32_t *gather_perm;
-    int gather_k;
+    const int32_t *row_src;
     int K;
     // groups: group_rows [G+1] row offsets and group_tiles [G+1] token-tile prefix, both on the
     // device; or NULL for one group of M_single rows.
@@ -73,27 +72,37 @@ struct GemmArgs {
     void *out;
     int ld;
     const float *bias;
-    const int32_t *epi_perm;
+    // EPI_COMBINE: row r adds epi_w[r] * D into out row epi_tok[r] (NULL: row r, weight 1)
+    const int32_t *epi_tok;
     const float *epi_w;
-    int epi_k;
     int *status;
 };
 
 // Launches the persistent grouped GEMM.  tm_a0 (and tm_a1 for EPI_SWIGLU: the up
-// projection) are 2-D tensor maps over the weight rows with a 128 x 64 box.
+// projection) are 2-D tensor maps over the weight rows with a 128 x 64 box; tm_b is a map
+// over the B rows ([rows, K], 128 x 64 box), used when row_src is NULL.  Gathered B
+// (row_src != NULL) is supported with EPI_SWIGLU only.
 cudaError_t launch_gemm(GemmEpi epi, const GemmArgs &a, const CUtensorMap &tm_a0,
-                        const CUtensorMap &tm_a1, int kc, cudaStream_t s);
+                        const CUtensorMap &tm_a1, const CUtensorMap &tm_b, int kc, cudaStream_t s);
 
 // ---- routing / permutation / elementwise ---------------------------------------------
 
 cudaError_t launch_topk(const float *logits, int T, int E, int k, int32_t *ids, float *w,
                         cudaStream_t s);
+// chunk_tab: device scratch of permute_scratch_ints(T, E, k) ints.  When row_tok / row_w are
+// not NULL the scatter also writes, per row of the sorted order, the token (pair / k) and the
+// routing weight topk_w[pair] (what the expert GEMMs read per row).
+size_t permute_scratch_ints(int T, int E, int k);
 cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int32_t *offsets,
                            int32_t *perm, int32_t *inv, int32_t *tile_prefix, int tile_n,
-                           int *status, cudaStream_t s);
+                           int32_t *chunk_tab, const float *topk_w, int32_t *row_tok,
+                           float *row_w, int *status, cudaStream_t s);
+// Token-tile prefix from given offsets, and row_tok[r] = perm[r] / k for the P rows.
 cudaError_t launch_tile_prefix(const int32_t *offsets, int E, int32_t *tile_prefix, int tile_n,
+                               const int32_t *perm, int P, int k, int32_t *row_tok,
                                cudaStream_t s);
-cudaError_t launch_finalize(const float *acc, const uint16_t *x, int T, int H, uint16_t *out,
+// out = bf16(acc); when x_next != NULL also x_next = bf16(resid + out).
+cudaError_t launch_finalize(const float *acc, const uint16_t *resid, int T, int H, uint16_t *out,
                             uint16_t *x_next, cudaStream_t s);
 cudaError_t launch_combine(const float *y_rows, const int32_t *inv, const float *topk_w,
                            const float *shared_y, int T, int H, int k, uint16_t *out,
@@ -115,13 +124,29 @@ struct DecodeArgs {
     uint16_t *h;       // [k, I]
     uint16_t *h_s;     // [Is]
     uint16_t *out;     // [H]
+    const uint16_t *resid;  // [H] residual added into x_next
     uint16_t *x_next;  // [H] or NULL
 };
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
 // Router logits of one token with the decode GEMV (the logits the decode path selects on).
 cudaError_t launch_decode_router(const DecodeArgs &a, cudaStream_t s);
 
-constexpr int kTileN = 128;   // tokens per GEMM tile (MMA N upper bound)
+constexpr int kTileN = 256;   // tokens per GEMM tile (MMA N upper bound)
 constexpr int kTileM = 128;   // weight rows per GEMM tile (MMA M)
+
+// Token tiles of a group of c rows: ceil(c / 256) tiles of equal size rounded up to 16 (the
+// MMA's N granularity); the last tile takes the remainder.  Shared by the permutation (tile
+// prefix) and the GEMM (tile decode), so both agree on every tile.
+__host__ __device__ __forceinline__ int token_tile_size(int c) {
+    if (c <= 0) return kTileN;
+    const int n = (c + kTileN - 1) / kTileN;
+    const int sz = (c + n - 1) / n;
+    return (sz + 15) & ~15;
+}
+__host__ __device__ __forceinline__ int token_tile_count(int c) {
+    if (c <= 0) return 0;
+    const int sz = token_tile_size(c);
+    return (c + sz - 1) / sz;
+}
 
 }  // namespace moe

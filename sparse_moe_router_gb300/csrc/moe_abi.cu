@@ -116,7 +116,7 @@ constexpr int kMaxPiece = 8192;
 size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
 struct Layout {
-    size_t status, logits, ids, topw, offsets, tiles, perm, inv, h, h_s, acc, total;
+    size_t status, logits, ids, topw, offsets, tiles, chunks, perm, inv, row_tok, row_w, h, h_s, acc, total;
 };
 
 Layout layout(const moe_config &c, int T) {
@@ -134,8 +134,11 @@ Layout layout(const moe_config &c, int T) {
     L.topw = take(Tt * c.top_k * 4);
     L.offsets = take((size_t)(c.n_experts + 1) * 4);
     L.tiles = take((size_t)(c.n_experts + 1) * 4);
+    L.chunks = take(permute_scratch_ints((int)Tt, c.n_experts, c.top_k) * 4);
     L.perm = take(Tt * c.top_k * 4);
     L.inv = take(Tt * c.top_k * 4);
+    L.row_tok = take(Tt * c.top_k * 4);
+    L.row_w = take(Tt * c.top_k * 4);
     L.h = take(Tt * c.top_k * c.inter * 2);
     L.h_s = take(Tt * (size_t)c.shared_inter * 2);
     L.acc = take(Tt * c.hidden * 4);
@@ -198,8 +201,9 @@ moe_status cuda_status(cudaError_t e) {
 // Router logits on tensor cores: logits[T,E] = x Wr^T + b.
 moe_status run_router_gemm(const moe_config &c, const moe_weights &w, const uint16_t *x, int T,
                            float *logits, int *status, cudaStream_t s) {
-    CUtensorMap tm;
-    if (!encode_tmap_2d_bf16(&tm, w.w_router, (uint64_t)c.n_experts, (uint64_t)c.hidden, kTileM, 64))
+    CUtensorMap tm, tb;
+    if (!encode_tmap_2d_bf16(&tm, w.w_router, (uint64_t)c.n_experts, (uint64_t)c.hidden, kTileM, 64) ||
+        !encode_tmap_2d_bf16(&tb, x, (uint64_t)T, (uint64_t)c.hidden, kTileN, 64))
         return MOE_ERR_CUDA;
     GemmArgs a{};
     a.b_src = x;
@@ -211,18 +215,21 @@ moe_status run_router_gemm(const moe_config &c, const moe_weights &w, const uint
     a.ld = c.n_experts;
     a.bias = w.b_router;
     a.status = status;
-    MOE_CUDA(launch_gemm(EPI_F32, a, tm, tm, KC_ROUTER_GEMM, s));
+    MOE_CUDA(launch_gemm(EPI_F32, a, tm, tm, tb, KC_ROUTER_GEMM, s));
     return MOE_OK;
 }
 
 // Shared expert over T tokens: h_s = SwiGLU(x), then Ws_down h_s stored (not added) into
-// out (fp32 [T,H]).
+// out (fp32 [T,H]).  Gate/up maps use 64-row boxes: a SwiGLU tile holds 64 features' gate
+// rows and the same features' up rows.
 moe_status run_shared(const moe_config &c, const moe_weights &w, const uint16_t *x, int T,
                       uint16_t *h_s, float *out, int *status, cudaStream_t s) {
-    CUtensorMap tg, tu, td;
-    if (!encode_tmap_2d_bf16(&tg, w.ws_gate, c.shared_inter, c.hidden, kTileM, 64) ||
-        !encode_tmap_2d_bf16(&tu, w.ws_up, c.shared_inter, c.hidden, kTileM, 64) ||
-        !encode_tmap_2d_bf16(&td, w.ws_down, c.hidden, c.shared_inter, kTileM, 64))
+    CUtensorMap tg, tu, td, tx, th;
+    if (!encode_tmap_2d_bf16(&tg, w.ws_gate, c.shared_inter, c.hidden, kTileM / 2, 64) ||
+        !encode_tmap_2d_bf16(&tu, w.ws_up, c.shared_inter, c.hidden, kTileM / 2, 64) ||
+        !encode_tmap_2d_bf16(&td, w.ws_down, c.hidden, c.shared_inter, kTileM, 64) ||
+        !encode_tmap_2d_bf16(&tx, x, (uint64_t)T, c.hidden, kTileN, 64) ||
+        !encode_tmap_2d_bf16(&th, h_s, (uint64_t)T, c.shared_inter, kTileN, 64))
         return MOE_ERR_CUDA;
     GemmArgs a{};
     a.b_src = x;
@@ -233,7 +240,7 @@ moe_status run_shared(const moe_config &c, const moe_weights &w, const uint16_t 
     a.out = h_s;
     a.ld = c.shared_inter;
     a.status = status;
-    MOE_CUDA(launch_gemm(EPI_SWIGLU, a, tg, tu, KC_SHARED_GATEUP, s));
+    MOE_CUDA(launch_gemm(EPI_SWIGLU, a, tg, tu, tx, KC_SHARED_GATEUP, s));
     GemmArgs d{};
     d.b_src = h_s;
     d.K = c.shared_inter;
@@ -243,26 +250,26 @@ moe_status run_shared(const moe_config &c, const moe_weights &w, const uint16_t 
     d.out = out;
     d.ld = c.hidden;
     d.status = status;
-    MOE_CUDA(launch_gemm(EPI_F32, d, td, td, KC_SHARED_DOWN, s));
+    MOE_CUDA(launch_gemm(EPI_F32, d, td, td, th, KC_SHARED_DOWN, s));
     return MOE_OK;
 }
 
 // Routed experts, grouped: h rows (permuted order) from x gathered through perm, then the down
 // projection either stored per row (y_rows) or weighted and added into acc[token].
-moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t *x,
-                      const int32_t *offsets, const int32_t *tiles, const int32_t *perm,
-                      const float *topw, uint16_t *h, float *y_rows, float *acc, int *status,
+moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t *x, int T,
+                      const int32_t *offsets, const int32_t *tiles, const int32_t *row_tok,
+                      const float *row_w, uint16_t *h, float *y_rows, float *acc, int *status,
                       cudaStream_t s) {
     const uint64_t EI = (uint64_t)c.n_experts * c.inter;
-    CUtensorMap tg, tu, td;
-    if (!encode_tmap_2d_bf16(&tg, w.w_gate, EI, c.hidden, kTileM, 64) ||
-        !encode_tmap_2d_bf16(&tu, w.w_up, EI, c.hidden, kTileM, 64) ||
-        !encode_tmap_2d_bf16(&td, w.w_down, (uint64_t)c.n_experts * c.hidden, c.inter, kTileM, 64))
+    CUtensorMap tg, tu, td, th;
+    if (!encode_tmap_2d_bf16(&tg, w.w_gate, EI, c.hidden, kTileM / 2, 64) ||
+        !encode_tmap_2d_bf16(&tu, w.w_up, EI, c.hidden, kTileM / 2, 64) ||
+        !encode_tmap_2d_bf16(&td, w.w_down, (uint64_t)c.n_experts * c.hidden, c.inter, kTileM, 64) ||
+        !encode_tmap_2d_bf16(&th, h, (uint64_t)T * c.top_k, c.inter, kTileN, 64))
         return MOE_ERR_CUDA;
     GemmArgs a{};
     a.b_src = x;
-    a.gather_perm = perm;
-    a.gather_k = c.top_k;
+    a.row_src = row_tok;
     a.K = c.hidden;
     a.n_groups = c.n_experts;
     a.group_rows = offsets;
@@ -271,7 +278,7 @@ moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t 
     a.out = h;
     a.ld = c.inter;
     a.status = status;
-    MOE_CUDA(launch_gemm(EPI_SWIGLU, a, tg, tu, KC_GATEUP_GEMM, s));
+    MOE_CUDA(launch_gemm(EPI_SWIGLU, a, tg, tu, tg, KC_GATEUP_GEMM, s));
     GemmArgs d{};
     d.b_src = h;
     d.K = c.inter;
@@ -283,20 +290,20 @@ moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t 
     d.status = status;
     if (y_rows) {
         d.out = y_rows;
-        MOE_CUDA(launch_gemm(EPI_F32, d, td, td, KC_DOWN_GEMM, s));
+        MOE_CUDA(launch_gemm(EPI_F32, d, td, td, th, KC_DOWN_GEMM, s));
     } else {
         d.out = acc;
-        d.epi_perm = perm;
-        d.epi_w = topw;
-        d.epi_k = c.top_k;
-        MOE_CUDA(launch_gemm(EPI_COMBINE, d, td, td, KC_DOWN_GEMM, s));
+        d.epi_tok = row_tok;
+        d.epi_w = row_w;
+        MOE_CUDA(launch_gemm(EPI_COMBINE, d, td, td, th, KC_DOWN_GEMM, s));
     }
     return MOE_OK;
 }
 
 // One prefill piece of T tokens (T >= 2), the whole layer.
 moe_status forward_piece(const moe_config &c, const moe_weights &w, const uint16_t *x, int T,
-                         uint16_t *out, uint16_t *x_next, void *ws, cudaStream_t s) {
+                         uint16_t *out, const uint16_t *resid, uint16_t *x_next, void *ws,
+                         cudaStream_t s) {
     const Layout L = layout(c, T);
     int *status = at<int>(ws, L.status);
     float *logits = at<float>(ws, L.logits);
@@ -311,14 +318,17 @@ moe_status forward_piece(const moe_config &c, const moe_weights &w, const uint16
     float *acc = at<float>(ws, L.acc);
     MOE_TRY(run_router_gemm(c, w, x, T, logits, status, s));
     MOE_CUDA(launch_topk(logits, T, c.n_experts, c.top_k, ids, topw, s));
-    MOE_CUDA(launch_permute(ids, T, c.n_experts, c.top_k, offsets, perm, inv, tiles, kTileN, status, s));
+    int32_t *row_tok = at<int32_t>(ws, L.row_tok);
+    float *row_w = at<float>(ws, L.row_w);
+    MOE_CUDA(launch_permute(ids, T, c.n_experts, c.top_k, offsets, perm, inv, tiles, kTileN,
+                            at<int32_t>(ws, L.chunks), topw, row_tok, row_w, status, s));
     if (c.shared_inter > 0) {
         MOE_TRY(run_shared(c, w, x, T, h_s, acc, status, s));  // stores: initialises acc
     } else {
         MOE_CUDA(launch_zero(acc, (size_t)T * c.hidden, s));
     }
-    MOE_TRY(run_routed(c, w, x, offsets, tiles, perm, topw, h, nullptr, acc, status, s));
-    MOE_CUDA(launch_finalize(acc, x, T, c.hidden, out, x_next, s));
+    MOE_TRY(run_routed(c, w, x, T, offsets, tiles, row_tok, row_w, h, nullptr, acc, status, s));
+    MOE_CUDA(launch_finalize(acc, resid, T, c.hidden, out, x_next, s));
     return MOE_OK;
 }
 
@@ -399,7 +409,8 @@ moe_status moe_permute(const moe_config *cfg, const int32_t *topk_ids, int T,
     MOE_TRY(check_ws(cfg, ws, ws_bytes, T));
     const Layout L = layout(*cfg, T);
     MOE_CUDA(launch_permute(topk_ids, T, cfg->n_experts, cfg->top_k, expert_offsets, perm, inv,
-                            at<int32_t>(ws, L.tiles), kTileN, at<int>(ws, L.status),
+                            at<int32_t>(ws, L.tiles), kTileN, at<int32_t>(ws, L.chunks), nullptr,
+                            at<int32_t>(ws, L.row_tok), nullptr, at<int>(ws, L.status),
                             static_cast<cudaStream_t>(stream)));
     return MOE_OK;
 }
@@ -420,8 +431,11 @@ moe_status moe_expert_ffn(const moe_config *cfg, const moe_weights *w, const moe
     const Layout L = layout(*cfg, T);
     int *status = at<int>(ws, L.status);
     int32_t *tiles = at<int32_t>(ws, L.tiles);
-    MOE_CUDA(launch_tile_prefix(expert_offsets, cfg->n_experts, tiles, kTileN, s));
-    MOE_TRY(run_routed(*cfg, *w, x, expert_offsets, tiles, perm, nullptr, h_rows, y_rows, nullptr, status, s));
+    int32_t *row_tok = at<int32_t>(ws, L.row_tok);
+    MOE_CUDA(launch_tile_prefix(expert_offsets, cfg->n_experts, tiles, kTileN, perm, T * cfg->top_k,
+                                cfg->top_k, row_tok, s));
+    MOE_TRY(run_routed(*cfg, *w, x, T, expert_offsets, tiles, row_tok, nullptr, h_rows, y_rows, nullptr, status,
+                       s));
     if (shared_y && cfg->shared_inter > 0)
         MOE_TRY(run_shared(*cfg, *w, x, T, at<uint16_t>(ws, L.h_s), shared_y, status, s));
     return MOE_OK;
@@ -459,14 +473,16 @@ int moe_plan_pieces(int T, int *pieces, int max_pieces) {
 }
 
 moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const moe_bf16 *x, int T,
-                       moe_bf16 *out, moe_bf16 *x_next, void *ws, size_t ws_bytes,
-                       void *stream) {
+                       moe_bf16 *out, const moe_bf16 *resid, moe_bf16 *x_next, void *ws,
+                       size_t ws_bytes, void *stream) {
     MOE_TRY(check_config(cfg));
     if (T < 0) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
     MOE_TRY(check_weights(cfg, w, true, true));
     if (!x || !out || !aligned16(x) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
     if (x_next && !aligned16(x_next)) return MOE_ERR_INVALID_ARG;
+    if (resid && !aligned16(resid)) return MOE_ERR_INVALID_ARG;
+    if (!resid) resid = x;
     const int Tmax = T < kMaxPiece ? T : kMaxPiece;
     MOE_TRY(check_ws(cfg, ws, ws_bytes, Tmax));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -494,6 +510,7 @@ moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const moe_bf
         a.h = at<uint16_t>(ws, L.h);
         a.h_s = at<uint16_t>(ws, L.h_s);
         a.out = out;
+        a.resid = resid;
         a.x_next = x_next;
         MOE_CUDA(launch_decode(a, s));
         return MOE_OK;
@@ -507,9 +524,10 @@ moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const moe_bf
         uint16_t *xn = x_next ? x_next + t0 * H : nullptr;
         if (Tp == 1) {
             // a one-token tail takes the decode path of the same layer
-            MOE_TRY(moe_forward(cfg, w, x + t0 * H, 1, out + t0 * H, xn, ws, ws_bytes, stream));
+            MOE_TRY(moe_forward(cfg, w, x + t0 * H, 1, out + t0 * H, resid + t0 * H, xn, ws, ws_bytes,
+                                stream));
         } else {
-            MOE_TRY(forward_piece(*cfg, *w, x + t0 * H, Tp, out + t0 * H, xn, ws, s));
+            MOE_TRY(forward_piece(*cfg, *w, x + t0 * H, Tp, out + t0 * H, resid + t0 * H, xn, ws, s));
         }
         t0 += Tp;
     }

@@ -89,6 +89,45 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *tmap, in
         : "memory");
 }
 
+// Hint: bring the box at (c0, c1) into L2 ahead of its TMA load (no completion tracking).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void *tmap, int c0, int c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
+// Fire-and-forget 16-byte vector add into global memory (no value returned, so the issuing
+// thread never waits on it).
+__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+// Bulk (TMA) element-wise add of `bytes` (multiple of 16) from shared memory into global
+// memory, tracked by the issuing thread's bulk groups.
+__device__ __forceinline__ void bulk_reduce_add_f32(float *gdst, const void *ssrc, uint32_t bytes) {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst),
+                 "r"(smem_u32(ssrc)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until at most N bulk groups of this thread still read their shared-memory source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Wait until all bulk groups of this thread have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Barrier among `count` threads on named barrier `id` (id 0 is __syncthreads).
+__device__ __forceinline__ void named_bar(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ------------------------------------------------------------------------- cp.async --
 
 // 16-byte global -> shared copy; src_bytes == 0 fills the 16 bytes with zeros.
@@ -100,6 +139,10 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint3
 
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 template <int N>

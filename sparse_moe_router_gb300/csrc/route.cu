@@ -15,8 +15,32 @@ namespace moe {
 namespace {
 
 // ------------------------------------------------------------------------ top-k --
-// One warp per token.  Lane L holds logits e = L + 32*i.  k rounds of a warp arg-max with
-// the order (value descending, index ascending); the winner's owner marks it taken.
+// One warp per token.  Lane L holds the logits e = L + 32*i (i < PER_LANE) and first sorts
+// them (bitonic network on the total order: value descending, index ascending).  Each of the
+// k rounds is then a warp arg-max over the lanes' list heads only; the winning lane pops its
+// head.  The order makes ties go to the lower expert index.
+template <int N>
+__device__ __forceinline__ void sort_desc(float (&v)[N], int (&e)[N]) {
+#pragma unroll
+    for (int k = 2; k <= N; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                const int l = i ^ j;
+                if (l > i) {
+                    const bool l_first = v[l] > v[i] || (v[l] == v[i] && e[l] < e[i]);
+                    const bool swap = ((i & k) == 0) ? l_first : !l_first;
+                    if (swap) {
+                        const float tv = v[i]; v[i] = v[l]; v[l] = tv;
+                        const int te = e[i]; e[i] = e[l]; e[l] = te;
+                    }
+                }
+            }
+        }
+    }
+}
+
 template <int PER_LANE>
 __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ logits, int T, int E,
                                                    int k, int32_t *__restrict__ ids,
@@ -26,27 +50,18 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ log
     if (warp >= T) return;
     const float *l = logits + (size_t)warp * E;
     float v[PER_LANE];
+    int e[PER_LANE];
 #pragma unroll
     for (int i = 0; i < PER_LANE; ++i) {
-        const int e = lane + 32 * i;
-        v[i] = e < E ? __ldg(&l[e]) : -INFINITY;
+        e[i] = lane + 32 * i;
+        v[i] = e[i] < E ? __ldg(&l[e[i]]) : -INFINITY;
     }
-    uint32_t taken = 0;
-    float my_val = 0.f;
+    sort_desc<PER_LANE>(v, e);
+    float my_val = 0.f, top = 0.f;
     int my_id = 0;
-    float top = 0.f;
     for (int r = 0; r < k; ++r) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < PER_LANE; ++i) {
-            const int e = lane + 32 * i;
-            // increasing e within the lane: strict '>' keeps the lowest index among equals
-            if (e < E && !((taken >> i) & 1u) && (v[i] > bv || bi == 0x7fffffff)) {
-                bv = v[i];
-                bi = e;
-            }
-        }
+        float bv = v[0];
+        int bi = e[0] < E ? e[0] : 0x7fffffff;  // padding never wins over a real logit
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
             const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
@@ -56,7 +71,15 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ log
                 bi = oi;
             }
         }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if ((bi & 31) == lane) {  // pop the head of the winner's list
+#pragma unroll
+            for (int i = 0; i + 1 < PER_LANE; ++i) {
+                v[i] = v[i + 1];
+                e[i] = e[i + 1];
+            }
+            v[PER_LANE - 1] = -INFINITY;
+            e[PER_LANE - 1] = 0x7fffffff;
+        }
         if (r == 0) top = bv;
         if (lane == r) {
             my_val = bv;
@@ -74,16 +97,20 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ log
 }
 
 // --------------------------------------------------------------------- permute --
-// Stable counting sort of the P = T*k pairs by expert, in one CTA of 1024 threads with no
-// inter-CTA waits.  Warp w owns the contiguous pair range [w*chunk, (w+1)*chunk):
-//   1. per-warp histograms hist[w][e] (match_any groups equal ids inside a 32-pair batch);
-//   2. offsets = exclusive scan over e of sum_w hist[w][e]; then hist[w][e] becomes the
-//      first row of warp w's pairs of expert e (experts major, warps minor);
-//   3. each warp walks its range again in order; a pair's row is its warp's cursor for the
-//      expert plus its rank among equal ids earlier in the batch.
+// Stable counting sort of the P = T*k pairs by expert in three launches, with no block ever
+// waiting on another:
+//   1. perm_hist:    block c counts the experts of its chunk of kChunk consecutive pairs;
+//   2. perm_scan:    one block: per expert, the exclusive prefix over chunks, then the
+//                    exclusive prefix over experts (the offsets) and the token-tile prefix;
+//                    the chunk table now holds each chunk's first row per expert;
+//   3. perm_scatter: block c walks its chunk again; warp w owns pairs [64w, 64w+64) of the
+//                    chunk, per-warp counts give each warp its first row per expert, and a
+//                    pair's rank among equal ids earlier in its 32-pair batch (match_any)
+//                    finishes its row.
 // Pairs of one expert therefore keep increasing pair order: the result is bit-exact.
 constexpr int kPermThreads = 1024;
 constexpr int kPermWarps = kPermThreads / 32;
+constexpr int kChunk = 2048;                 // pairs per block (64 per warp)
 
 __device__ __forceinline__ int block_excl_scan(int v, int *sh_warp, int *total) {
     // exclusive scan of one value per thread across the 1024-thread block
@@ -113,90 +140,106 @@ __device__ __forceinline__ int block_excl_scan(int v, int *sh_warp, int *total) 
     return incl - v;
 }
 
-__global__ void __launch_bounds__(kPermThreads, 1)
-    permute_kernel(const int32_t *__restrict__ ids, int P, int E, int32_t *__restrict__ offsets,
-                   int32_t *__restrict__ perm, int32_t *__restrict__ inv,
-                   int32_t *__restrict__ tile_prefix, int tile_n, int *status) {
-    extern __shared__ int sh[];
-    int *hist = sh;                           // [kPermWarps][E]
-    int *sh_warp = sh + kPermWarps * E;       // [32]
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    for (int i = tid; i < kPermWarps * E; i += kPermThreads) hist[i] = 0;
+__global__ void __launch_bounds__(kPermThreads) perm_hist_kernel(const int32_t *__restrict__ ids, int P,
+                                                                  int E, int32_t *__restrict__ chunk_tab,
+                                                                  int *status) {
+    extern __shared__ int cnt[];  // [E]
+    const int tid = threadIdx.x;
+    for (int i = tid; i < E; i += kPermThreads) cnt[i] = 0;
     __syncthreads();
-
-    const int chunk = (P + kPermWarps - 1) / kPermWarps;
-    const int beg = min(P, wid * chunk), end = min(P, beg + chunk);
-    int *myhist = hist + wid * E;
-    const uint32_t lt_mask = (1u << lane) - 1u;
-
-    // 1. histograms (8 batches of loads in flight)
-    for (int b0 = beg; b0 < end; b0 += 32 * 8) {
-        int e8[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int pidx = b0 + 32 * u + lane;
-            e8[u] = pidx < end ? __ldg(&ids[pidx]) : -1;
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            int e = e8[u];
-            if (e >= E || (e < 0 && b0 + 32 * u + lane < end)) {
-                if (status) atomicCAS(status, 0, (int)MOE_ERR_INVALID_ARG);
-                e = -1;
-            }
-            const uint32_t grp = __match_any_sync(0xffffffffu, e);
-            if (e >= 0 && (grp & lt_mask) == 0) myhist[e] += __popc(grp);
-        }
+    const int beg = blockIdx.x * kChunk;
+    for (int p = beg + tid; p < min(P, beg + kChunk); p += kPermThreads) {
+        const int e = __ldg(&ids[p]);
+        if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+        else if (status) atomicCAS(status, 0, (int)MOE_ERR_INVALID_ARG);
     }
     __syncthreads();
+    for (int i = tid; i < E; i += kPermThreads) chunk_tab[(size_t)blockIdx.x * E + i] = cnt[i];
+}
 
-    // 2. offsets and token-tile prefix (one expert per thread; E <= 1024)
+__global__ void __launch_bounds__(kPermThreads, 1)
+    perm_scan_kernel(int32_t *__restrict__ chunk_tab, int n_chunks, int E, int32_t *__restrict__ offsets,
+                     int32_t *__restrict__ tile_prefix, int tile_n) {
+    __shared__ int sh_warp[32];
+    const int tid = threadIdx.x;
     int cnt = 0;
     if (tid < E)
-        for (int w2 = 0; w2 < kPermWarps; ++w2) cnt += hist[w2 * E + tid];
+        for (int c = 0; c < n_chunks; ++c) {
+            const int h = chunk_tab[(size_t)c * E + tid];
+            chunk_tab[(size_t)c * E + tid] = cnt;
+            cnt += h;
+        }
     int total = 0;
     const int off = block_excl_scan(tid < E ? cnt : 0, sh_warp, &total);
-    const int tiles = tid < E ? (cnt + tile_n - 1) / tile_n : 0;
+    const int tiles = tid < E ? token_tile_count(cnt) : 0;
     int total_tiles = 0;
     const int toff = block_excl_scan(tiles, sh_warp, &total_tiles);
     if (tid < E) {
         offsets[tid] = off;
         if (tile_prefix) tile_prefix[tid] = toff;
-        int run = off;
-        for (int w2 = 0; w2 < kPermWarps; ++w2) {
-            const int c = hist[w2 * E + tid];
-            hist[w2 * E + tid] = run;
-            run += c;
-        }
+        for (int c = 0; c < n_chunks; ++c) chunk_tab[(size_t)c * E + tid] += off;
     }
     if (tid == 0) {
         offsets[E] = total;
         if (tile_prefix) tile_prefix[E] = total_tiles;
     }
-    __syncthreads();
+}
 
-    // 3. stable scatter
-    for (int b0 = beg; b0 < end; b0 += 32 * 8) {
-        int e8[8];
+__global__ void __launch_bounds__(kPermThreads) perm_scatter_kernel(const int32_t *__restrict__ ids, int P,
+                                                                     int E, int k, const int32_t *__restrict__ chunk_tab,
+                                                                     int32_t *__restrict__ perm,
+                                                                     int32_t *__restrict__ inv,
+                                                                     const float *__restrict__ topk_w,
+                                                                     int32_t *__restrict__ row_tok,
+                                                                     float *__restrict__ row_w) {
+    extern __shared__ int wh[];  // [kPermWarps][E]
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    for (int i = tid; i < kPermWarps * E; i += kPermThreads) wh[i] = 0;
+    const int base = blockIdx.x * kChunk + wid * (kChunk / kPermWarps);
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    int e2[2];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int pidx = b0 + 32 * u + lane;
-            e8[u] = pidx < end ? __ldg(&ids[pidx]) : -1;
+    for (int b = 0; b < 2; ++b) {
+        const int p = base + 32 * b + lane;
+        int e = p < P ? __ldg(&ids[p]) : -1;
+        if (e >= E) e = -1;
+        e2[b] = e;
+    }
+    __syncthreads();
+    int *my = wh + wid * E;
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+        const uint32_t grp = __match_any_sync(0xffffffffu, e2[b]);
+        if (e2[b] >= 0 && (grp & lt_mask) == 0) my[e2[b]] += __popc(grp);
+        __syncwarp();
+    }
+    __syncthreads();
+    // per expert: first row of each warp's pairs = chunk's first row + earlier warps' counts
+    for (int e = tid; e < E; e += kPermThreads) {
+        int run = chunk_tab[(size_t)blockIdx.x * E + e];
+        for (int w2 = 0; w2 < kPermWarps; ++w2) {
+            const int c = wh[w2 * E + e];
+            wh[w2 * E + e] = run;
+            run += c;
         }
+    }
+    __syncthreads();
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int pidx = b0 + 32 * u + lane;
-            int e = e8[u];
-            if (e >= E) e = -1;
-            const uint32_t grp = __match_any_sync(0xffffffffu, e);
-            int row = -1;
-            if (e >= 0) row = myhist[e] + __popc(grp & lt_mask);
-            __syncwarp();
-            if (e >= 0 && (grp & lt_mask) == 0) myhist[e] += __popc(grp);
-            __syncwarp();
-            if (pidx < end) {
-                inv[pidx] = row;
-                if (row >= 0) perm[row] = pidx;
+    for (int b = 0; b < 2; ++b) {
+        const int p = base + 32 * b + lane;
+        const int e = e2[b];
+        const uint32_t grp = __match_any_sync(0xffffffffu, e);
+        int row = -1;
+        if (e >= 0) row = my[e] + __popc(grp & lt_mask);
+        __syncwarp();
+        if (e >= 0 && (grp & lt_mask) == 0) my[e] += __popc(grp);
+        __syncwarp();
+        if (p < P) {
+            inv[p] = row;
+            if (row >= 0) {
+                perm[row] = p;
+                if (row_tok) row_tok[row] = p / k;
+                if (row_w) row_w[row] = __ldg(&topk_w[p]);
             }
         }
     }
@@ -205,11 +248,13 @@ __global__ void __launch_bounds__(kPermThreads, 1)
 // Token-tile prefix from given offsets (for the unfused expert entry point).
 __global__ void __launch_bounds__(kPermThreads, 1)
     tile_prefix_kernel(const int32_t *__restrict__ offsets, int E, int32_t *__restrict__ tile_prefix,
-                       int tile_n) {
+                       int tile_n, const int32_t *__restrict__ perm, int P, int k,
+                       int32_t *__restrict__ row_tok) {
     __shared__ int sh_warp[32];
     const int tid = threadIdx.x;
+    for (int r = tid; r < P; r += kPermThreads) row_tok[r] = perm[r] / k;
     const int cnt = tid < E ? offsets[tid + 1] - offsets[tid] : 0;
-    const int tiles = tid < E ? (max(cnt, 0) + tile_n - 1) / tile_n : 0;
+    const int tiles = tid < E ? token_tile_count(cnt) : 0;
     int total = 0;
     const int toff = block_excl_scan(tiles, sh_warp, &total);
     if (tid < E) tile_prefix[tid] = toff;
@@ -217,9 +262,9 @@ __global__ void __launch_bounds__(kPermThreads, 1)
 }
 
 // ------------------------------------------------------------------- finalise --
-// out = bf16(acc); x_next = bf16(x + out).  8 elements per thread (H % 8 == 0).
+// out = bf16(acc); x_next = bf16(resid + out).  8 elements per thread (H % 8 == 0).
 __global__ void __launch_bounds__(256) finalize_kernel(const float *__restrict__ acc,
-                                                       const uint16_t *x, size_t n8,
+                                                       const uint16_t *resid, size_t n8,
                                                        uint16_t *__restrict__ out,
                                                        uint16_t *x_next) {
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
@@ -231,7 +276,7 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float *__restrict__
         for (int j = 0; j < 8; ++j) o[j] = __float2bfloat16_rn(v[j]);
         reinterpret_cast<uint4 *>(out)[i] = *reinterpret_cast<const uint4 *>(o);
         if (x_next) {
-            const uint4 xr = reinterpret_cast<const uint4 *>(x)[i];
+            const uint4 xr = reinterpret_cast<const uint4 *>(resid)[i];
             const __nv_bfloat16 *xb = reinterpret_cast<const __nv_bfloat16 *>(&xr);
             __align__(16) __nv_bfloat16 n[8];
 #pragma unroll
@@ -308,38 +353,54 @@ cudaError_t launch_topk(const float *logits, int T, int E, int k, int32_t *ids, 
     return cudaGetLastError();
 }
 
+size_t permute_scratch_ints(int T, int E, int k) {
+    const long P = (long)T * k;
+    return (size_t)((P + kChunk - 1) / kChunk) * E;
+}
+
 cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int32_t *offsets,
                            int32_t *perm, int32_t *inv, int32_t *tile_prefix, int tile_n,
-                           int *status, cudaStream_t s) {
-    const size_t smem = (size_t)(kPermWarps * E + 32) * sizeof(int);
+                           int32_t *chunk_tab, const float *topk_w, int32_t *row_tok,
+                           float *row_w, int *status, cudaStream_t s) {
+    const int P = T * k;
+    const int n_chunks = (P + kChunk - 1) / kChunk;
     static bool attr_done[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)((kPermWarps * 1024 + 32) * sizeof(int)));
+        cudaError_t e = cudaFuncSetAttribute(perm_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)(kPermWarps * 1024 * sizeof(int)));
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
+    {
+        LaunchScope scope(KC_PERMUTE, s);
+        perm_hist_kernel<<<n_chunks, kPermThreads, E * sizeof(int), s>>>(ids, P, E, chunk_tab, status);
+    }
+    {
+        LaunchScope scope(KC_PERMUTE, s);
+        perm_scan_kernel<<<1, kPermThreads, 0, s>>>(chunk_tab, n_chunks, E, offsets, tile_prefix, tile_n);
+    }
     LaunchScope scope(KC_PERMUTE, s);
-    permute_kernel<<<1, kPermThreads, smem, s>>>(ids, T * k, E, offsets, perm, inv, tile_prefix,
-                                                 tile_n, status);
+    perm_scatter_kernel<<<n_chunks, kPermThreads, kPermWarps * E * sizeof(int), s>>>(
+        ids, P, E, k, chunk_tab, perm, inv, topk_w, row_tok, row_w);
     return cudaGetLastError();
 }
 
 cudaError_t launch_tile_prefix(const int32_t *offsets, int E, int32_t *tile_prefix, int tile_n,
+                               const int32_t *perm, int P, int k, int32_t *row_tok,
                                cudaStream_t s) {
     LaunchScope scope(KC_TILE_PREFIX, s);
-    tile_prefix_kernel<<<1, kPermThreads, 0, s>>>(offsets, E, tile_prefix, tile_n);
+    tile_prefix_kernel<<<1, kPermThreads, 0, s>>>(offsets, E, tile_prefix, tile_n, perm, P, k, row_tok);
     return cudaGetLastError();
 }
 
-cudaError_t launch_finalize(const float *acc, const uint16_t *x, int T, int H, uint16_t *out,
+cudaError_t launch_finalize(const float *acc, const uint16_t *resid, int T, int H, uint16_t *out,
                             uint16_t *x_next, cudaStream_t s) {
     const size_t n8 = (size_t)T * H / 8;
     if (n8 == 0) return cudaSuccess;
     LaunchScope scope(KC_FINALIZE, s);
-    finalize_kernel<<<grid_for(n8, 256), 256, 0, s>>>(acc, x, n8, out, x_next);
+    finalize_kernel<<<grid_for(n8, 256), 256, 0, s>>>(acc, resid, n8, out, x_next);
     return cudaGetLastError();
 }
 

@@ -37,15 +37,29 @@ def bf16_f64(bits):
     return orc.bf16_to_f64(bits)
 
 
+def abs_bound(ref_f64):
+    """Per-element absolute bound: 2e-2, or two bf16 spacings at |ref| where that is larger.
+
+    Both sides round the same sum (fp32 on the GPU, fp64 in the oracle) to bf16 once, so a
+    one-step difference is always possible; one bf16 step exceeds 2e-2 only for |ref| > 2.56,
+    which the chained multi-layer workloads reach (the residual stream grows layer by layer).
+    For unit-scale outputs the bound is exactly 2e-2."""
+    spacing = np.ldexp(1.0, np.frexp(np.maximum(np.abs(ref_f64), 2.0 ** -126))[1] - 8)
+    return np.maximum(MAX_ABS, 2.0 * spacing)
+
+
 def compare_out(got_u16, ref_u16, what="out"):
-    """Layer-output check: max |diff| and relative L2 error against the oracle's bf16 output."""
+    """Layer-output check against the oracle's bf16 output: every |diff| within abs_bound
+    (2e-2 at unit scale) and relative L2 error <= 5e-3.  Returns (max |diff|, rel L2)."""
     g = bf16_f64(got_u16)
     r = bf16_f64(ref_u16)
     assert np.all(np.isfinite(g)), what + ": non-finite values"
     d = np.abs(g - r)
     max_abs = float(d.max()) if d.size else 0.0
     rel = float(np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-30)) if d.size else 0.0
-    assert max_abs <= MAX_ABS, "%s: max abs diff %.3g > %.3g" % (what, max_abs, MAX_ABS)
+    bad = d > abs_bound(r)
+    assert not bad.any(), "%s: %d elements beyond the abs bound (max diff %.3g at |ref| %.3g)" % (
+        what, int(bad.sum()), float(d[bad].max()), float(np.abs(r[bad]).max()))
     assert rel <= REL_L2, "%s: rel L2 %.3g > %.3g" % (what, rel, REL_L2)
     return max_abs, rel
 

@@ -67,26 +67,26 @@ def test_entry_points_reject_bad_arguments_without_device_work():
     P = ctypes.c_void_p
     fake = P(0x10000)          # never dereferenced: validation fails first
     # null config / null pointers / negative T
-    assert L.moe_forward(None, ctypes.byref(w), fake, 4, fake, None, fake, 1 << 30, None) == 1
-    assert L.moe_forward(ctypes.byref(cfg), ctypes.byref(w), fake, 4, fake, None, fake, 1 << 30, None) == 1
-    assert L.moe_forward(ctypes.byref(cfg), ctypes.byref(w), fake, -1, fake, None, fake, 1 << 30, None) == 1
+    assert L.moe_forward(None, ctypes.byref(w), fake, 4, fake, None, None, fake, 1 << 30, None) == 1
+    assert L.moe_forward(ctypes.byref(cfg), ctypes.byref(w), fake, 4, fake, None, None, fake, 1 << 30, None) == 1
+    assert L.moe_forward(ctypes.byref(cfg), ctypes.byref(w), fake, -1, fake, None, None, fake, 1 << 30, None) == 1
     assert L.moe_route_from_logits(ctypes.byref(cfg), None, 5, fake, fake, None) == 1
     assert L.moe_permute(ctypes.byref(cfg), fake, 5, None, fake, fake, fake, 1 << 30, None) == 1
     assert L.moe_combine(ctypes.byref(cfg), None, fake, fake, None, 3, fake, None) == 1
     # unsupported shape
     assert L.moe_route_from_logits(ctypes.byref(_cfg(top_k=40, n_experts=64)), fake, 5, fake, fake, None) == 3
     # T == 0 is a no-op that succeeds, even with null tensors
-    assert L.moe_forward(ctypes.byref(cfg), None, None, 0, None, None, None, 0, None) == 0
+    assert L.moe_forward(ctypes.byref(cfg), None, None, 0, None, None, None, None, 0, None) == 0
     assert L.moe_permute(ctypes.byref(cfg), None, 0, None, None, None, None, 0, None) == 0
     # workspace checks: misaligned, too small
     wt = abi.Weights(*(0x10000 for _ in range(8)))
-    assert L.moe_forward(ctypes.byref(cfg), ctypes.byref(wt), fake, 4, fake, None, P(0x10010), 1 << 30, None) == 1
-    assert L.moe_forward(ctypes.byref(cfg), ctypes.byref(wt), fake, 4, fake, None, fake, 1000, None) == 2
+    assert L.moe_forward(ctypes.byref(cfg), ctypes.byref(wt), fake, 4, fake, None, None, P(0x10010), 1 << 30, None) == 1
+    assert L.moe_forward(ctypes.byref(cfg), ctypes.byref(wt), fake, 4, fake, None, None, fake, 1000, None) == 2
     # misaligned tensor
-    assert L.moe_forward(ctypes.byref(cfg), ctypes.byref(wt), P(0x10002), 4, fake, None, fake, 1 << 30, None) == 1
+    assert L.moe_forward(ctypes.byref(cfg), ctypes.byref(wt), P(0x10002), 4, fake, None, None, fake, 1 << 30, None) == 1
     # missing shared-expert weights when Is > 0
     wn = abi.Weights(*(0x10000 for _ in range(5)), None, None, None)
-    assert L.moe_forward(ctypes.byref(cfg), ctypes.byref(wn), fake, 4, fake, None, fake, 1 << 30, None) == 1
+    assert L.moe_forward(ctypes.byref(cfg), ctypes.byref(wn), fake, 4, fake, None, None, fake, 1 << 30, None) == 1
 
 
 def test_plan_pieces():

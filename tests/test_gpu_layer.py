@@ -113,8 +113,17 @@ def test_forward_x_next_and_alias():
     ref = orc.bf16_to_f64(u16(x)) + orc.bf16_to_f64(u16(out))
     want = torch.as_tensor(ref, dtype=torch.float32).to(torch.bfloat16)
     assert np.array_equal(u16(xn), u16(want))
-    # x_next may alias x
+    # a separate residual input: x_next = bf16(resid + out)
     cfg = cfg_of(TINY)
+    resid = torch.randn_like(x.float()).to(torch.bfloat16)
+    ws0 = abi.alloc_workspace(cfg, 77)
+    out_r = torch.empty_like(x)
+    xn_r = torch.empty_like(x)
+    abi.moe_forward(cfg, abi.weights(layers[0]), x, 77, out_r, xn_r, ws0, resid=resid)
+    torch.cuda.synchronize()
+    assert torch.equal(xn_r, (resid.float() + out_r.float()).to(torch.bfloat16))
+    compare_out(u16(out_r), u16(out))
+    # x_next may alias x (resid defaults to x)
     ws = abi.alloc_workspace(cfg, 77)
     x2 = x.clone()
     out2 = torch.empty_like(x)

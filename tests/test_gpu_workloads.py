@@ -1,7 +1,9 @@
 """Parity on the five named workloads at full size, through moe_forward (the call the
 benchmark times), against the CPU oracle.
 
-Multi-layer workloads chain layers through the residual stream x_{l+1} = bf16(x_l + out_l);
+Multi-layer workloads chain layers as x_{l+1} = bf16(x_0 + out_l) (the first layer's input
+plus this layer's output, fused into moe_forward through its residual input), which keeps the
+unit-RMS input of a pre-norm layer stack while every layer still waits on the previous one;
 each layer is checked with the oracle fed the GPU's bf16 input to that layer.  Where the
 oracle would take minutes, a seeded sample of token rows is checked (the layer treats every
 token independently), plus the full routing and permutation.
@@ -54,10 +56,11 @@ def _run_chain(wl, sample, n_layers=None):
     ws = abi.alloc_workspace(cfg, min(T, 8192))
     rng = np.random.default_rng(wl.seed)
     results = []
+    x0 = x
     for l, layer in enumerate(layers):
         out = torch.empty_like(x)
         xn = torch.empty_like(x)
-        abi.moe_forward(cfg, abi.weights(layer), x, T, out, xn, ws)
+        abi.moe_forward(cfg, abi.weights(layer), x, T, out, xn, ws, resid=x0)
         torch.cuda.synchronize()
         assert abi.moe_check_status(ws) == 0
         if sample is None or sample >= T:
@@ -66,6 +69,8 @@ def _run_chain(wl, sample, n_layers=None):
             rows = np.unique(np.concatenate([rng.choice(T, size=sample, replace=False), [0, T - 1]]))
         (ma, rl), ids = _check_rows(shape, layer, x, out, rows)
         results.append((l, ma, rl, ids))
+        ref_next = (x0.float() + out.float()).to(torch.bfloat16)
+        assert torch.equal(xn, ref_next)
         x = xn
     return results
 
