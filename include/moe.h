@@ -115,6 +115,22 @@ moe_status moe_permute(const moe_config *cfg, const int32_t *topk_ids, int T,
                        int32_t *expert_offsets, int32_t *perm, int32_t *inv, void *ws,
                        size_t ws_bytes, void *stream);
 
+/* moe_permute without a workspace, for callers that cannot allocate device memory where
+ * they route tokens (a serving process that reserves all device memory at start-up, host
+ * code with no allocator at hand).  The pages have no counterpart: this is a convenience of
+ * this library.  Same outputs as moe_permute (bit-identical), but the per-chunk count table
+ * lives in a fixed array inside the library (128 KiB on every device that loads it, kept
+ * until the process exits), so the call allocates nothing and takes no workspace.
+ * Limits: T*k <= 65536 pairs, E <= 1024, k <= 32; larger problems return
+ * MOE_ERR_UNSUPPORTED_SHAPE (use moe_permute).  Ids outside [0,E) get inv = -1 and are not
+ * otherwise reported (no status word).  The first call on each device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the one array: calls that overlap on the GPU
+ * (different streams or threads) race and must be serialised by the caller. */
+moe_status moe_permute_noalloc(const moe_config *cfg, const int32_t *topk_ids, int T,
+                               int32_t *expert_offsets, int32_t *perm, int32_t *inv,
+                               void *stream);
+
 /* Expert FFNs, unfused (for step-by-step checking).  Routed rows in the permuted order:
  * h_rows [T*k, I] bf16 = bf16(silu(Wg[e] x_t) * (Wu[e] x_t)) and y_rows [T*k, H] fp32 =
  * Wd[e] h, for row r of expert e holding pair perm[r] of token perm[r]/k.  When shared_y is not

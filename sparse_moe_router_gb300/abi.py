@@ -22,7 +22,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_WORKSPACE_TOO
 
 # Every symbol include/moe.h declares.
 EXPORTS = ["moe_status_string", "moe_workspace_size", "moe_route", "moe_route_from_logits",
-           "moe_permute", "moe_expert_ffn", "moe_combine", "moe_forward", "moe_check_status",
+           "moe_permute", "moe_permute_noalloc", "moe_expert_ffn", "moe_combine", "moe_forward", "moe_check_status",
            "moe_plan_pieces", "moe_launch_count", "moe_timing_enable", "moe_timing_read",
            "moe_timing_name", "moe_timing_classes"]
 
@@ -66,6 +66,7 @@ def load(path: str = LIB_PATH):
     L.moe_route.argtypes = [C, W, _P, _I, _P, _P, _P, _P, _SZ, _P]
     L.moe_route_from_logits.argtypes = [C, _P, _I, _P, _P, _P]
     L.moe_permute.argtypes = [C, _P, _I, _P, _P, _P, _P, _SZ, _P]
+    L.moe_permute_noalloc.argtypes = [C, _P, _I, _P, _P, _P, _P]
     L.moe_expert_ffn.argtypes = [C, W, _P, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]
     L.moe_combine.argtypes = [C, _P, _P, _P, _P, _I, _P, _P]
     L.moe_forward.argtypes = [C, W, _P, _I, _P, _P, _P, _P, _SZ, _P]
@@ -79,7 +80,7 @@ def load(path: str = LIB_PATH):
     L.moe_timing_name.argtypes = [_I]
     L.moe_timing_name.restype = ctypes.c_char_p
     L.moe_timing_classes.argtypes = []
-    for fn in ("moe_route", "moe_route_from_logits", "moe_permute", "moe_expert_ffn",
+    for fn in ("moe_route", "moe_route_from_logits", "moe_permute", "moe_permute_noalloc", "moe_expert_ffn",
                "moe_combine", "moe_forward", "moe_check_status", "moe_timing_enable",
                "moe_timing_read", "moe_timing_classes"):
         getattr(L, fn).restype = _I
@@ -164,6 +165,13 @@ def moe_permute(cfg, topk_ids, T, offsets, perm, inv, ws, stream=None):
     st = lib().moe_permute(ctypes.byref(cfg), _ptr(topk_ids), int(T), _ptr(offsets), _ptr(perm),
                            _ptr(inv), _ptr(ws), ws.numel(), _stream(stream))
     _check("moe_permute", st)
+
+
+def moe_permute_noalloc(cfg, topk_ids, T, offsets, perm, inv, stream=None):
+    """moe_permute for callers that cannot allocate: no workspace argument."""
+    st = lib().moe_permute_noalloc(ctypes.byref(cfg), _ptr(topk_ids), int(T), _ptr(offsets),
+                                   _ptr(perm), _ptr(inv), _stream(stream))
+    _check("moe_permute_noalloc", st)
 
 
 def moe_expert_ffn(cfg, w: Weights, x, T, offsets, perm, h_rows, y_rows, shared_y, ws, stream=None):
