@@ -153,9 +153,10 @@ moe_status moe_combine(const moe_config *cfg, const float *y_rows, const int32_t
  * decode path (HBM-streaming GEMVs).  x_next may be NULL; when given it receives
  * bf16(resid + out), the residual-stream update of a layer stack, fused into the last
  * kernel; resid [T,H] may be NULL, meaning x.  x_next may alias resid (not x, when they
- * differ).  ws: moe_workspace_size(cfg, T) bytes.  The fused combine adds fp32 partial sums
- * with atomics, so the fp32 summation order can differ from run to run (the result stays
- * within the layer's tolerance, but is not bit-reproducible). */
+ * differ).  ws: moe_workspace_size(cfg, T) bytes.  Rounding: h is rounded to bf16 once, each
+ * weighted expert row w*y is stored as bf16 and the k rows of a token are summed in fp32 in
+ * slot order with the shared expert's fp32 row, and the sum is rounded to bf16 once.  No
+ * atomics: the result is bit-reproducible. */
 moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const moe_bf16 *x, int T,
                        moe_bf16 *out, const moe_bf16 *resid, moe_bf16 *x_next, void *ws,
                        size_t ws_bytes, void *stream);

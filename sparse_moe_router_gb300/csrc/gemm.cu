@@ -1,5 +1,5 @@
 // gemm.cu -- persistent grouped GEMM on the 5th-generation tensor cores (tcgen05 + TMEM),
-// with the MoE epilogues fused: fp32 store (+bias), SwiGLU -> bf16, weighted scatter-add.
+// with the MoE epilogues fused: fp32 store (+bias), SwiGLU -> bf16, weighted row scatter.
 //
 // The layer's expert projections ("AI MAX+ 395部署Qwen3大模型：GFX1151引擎实测优化解析",
 // "MOE 内核优化": the MoE kernel bounds prefill) are, per expert e, products of the expert's
@@ -13,7 +13,7 @@
 //           so gate and up land in TMEM lanes i and 64 + i of one accumulator.
 //
 // Roles (one CTA per SM):
-//   warps 0..P-1  epilogue (P = 16 for the weighted scatter-add, else 8): warp w reads TMEM
+//   warps 0..P-1  epilogue (P = 16 for the weighted row scatter, else 8): warp w reads TMEM
 //               lanes 32*(w%4)..+31 (the hardware's lane quarters), and the P/4 warps of a
 //               quarter take every (P/4)-th 16-token chunk;
 //   warps P..P+3 producers.  Contiguous B (token rows in order): one thread issues the TMA
@@ -51,18 +51,22 @@ constexpr int kStgStride = BM + 4;                // SwiGLU staging row (floats)
 
 template <int EPI>
 struct Cfg {
-    // epilogue warps: the weighted scatter-add needs many warps issuing reductions to keep
-    // enough of them in flight; the others need 8
+    // epilogue warps: the weighted row scatter keeps many warps storing; the others need 8
     static constexpr int kEpiWarps = (EPI == EPI_COMBINE) ? 16 : 8;
     static constexpr int kProdWarp0 = kEpiWarps;    // 4 producer warps
     static constexpr int kMmaWarp = kEpiWarps + 4;  // MMA + TMEM allocation warp
     static constexpr int kThreads = (kEpiWarps + 5) * 32;
     static constexpr int kFT = (EPI == EPI_SWIGLU) ? 64 : BM;    // output features per tile
-    static constexpr int kStagingBytes = (EPI == EPI_SWIGLU) ? 2 * 16 * kStgStride * 4 : 0;
+    // SwiGLU: gate/up exchange, fp32 [2 sub-groups][16 rows][kStgStride];
+    // combine: per-warp bf16 transpose buffers [warps][16 rows][32 features]
+    static constexpr int kStagingBytes =
+        (EPI == EPI_SWIGLU) ? 2 * 16 * kStgStride * 4 : (EPI == EPI_COMBINE ? kEpiWarps * 16 * 32 * 2 : 0);
+    // combine: per-tile (output row, weight) of the BN tile rows, double-buffered
+    static constexpr int kMetaBytes = (EPI == EPI_COMBINE) ? 2 * BN * 8 : 0;
     static constexpr int kBarBytes = (2 * kStages + 5) * 8;
-    static constexpr int kRowTableBytes = 4 * BN * 4;
+    static constexpr int kRowTableBytes = (EPI == EPI_SWIGLU) ? 4 * BN * 4 : 0;
     static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + kStagingBytes +
-                                      kBarBytes + 16 + 2 * (kMaxGroups + 1) * 4 + kRowTableBytes;
+                                      kMetaBytes + kBarBytes + 16 + 2 * (kMaxGroups + 1) * 4 + kRowTableBytes;
 };
 
 struct TileInfo {
@@ -96,10 +100,6 @@ __device__ __forceinline__ void set_error(int *status, int code) {
     if (status) atomicCAS(status, 0, code);
 }
 
-__device__ __forceinline__ float sel4(float a0, float a1, float a2, float a3, int i) {
-    return i == 0 ? a0 : (i == 1 ? a1 : (i == 2 ? a2 : a3));
-}
-
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
 template <int EPI>
@@ -116,7 +116,9 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *staging = reinterpret_cast<float *>(smem + kStages * kStageBytes);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes + C::kStagingBytes);
+    int32_t *meta_row = reinterpret_cast<int32_t *>(smem + kStages * kStageBytes + C::kStagingBytes);
+    float *meta_w = reinterpret_cast<float *>(meta_row + 2 * BN);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes + C::kStagingBytes + C::kMetaBytes);
     uint64_t *full = bars;
     uint64_t *empty = bars + kStages;
     uint64_t *acc_full = bars + 2 * kStages;
@@ -327,22 +329,20 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
             const TileInfo t = decode_tile(tau, nft, g_tiles, g_rows, G);
             const int buf = tc & 1;
             const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
-            // combine: each lane fetches (token, weight) of rows lane + 32m of the tile before
-            // the accumulator is ready, so the loads overlap the tile's main loop
-            int tok8[8];
-            float w8[8];
-            if (EPI == EPI_COMBINE) {
-#pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const int j = lane + 32 * m;
-                    tok8[m] = 0;
-                    w8[m] = 0.f;
-                    if (j < t.nvalid) {
-                        const int row = t.row0 + j;
-                        tok8[m] = p.epi_tok ? __ldg(&p.epi_tok[row]) : row;
-                        w8[m] = p.epi_w ? __ldg(&p.epi_w[row]) : 1.f;
-                    }
+            // combine: the 16 warps fetch (output row, weight) of the tile's rows into shared
+            // memory before the accumulator is ready (the loads overlap the main loop); the
+            // vote barrier below publishes them to all epilogue warps
+            if (EPI == EPI_COMBINE && lane < BN / kEpiWarps) {
+                const int j = warp * (BN / kEpiWarps) + lane;
+                int orow = 0;
+                float w = 0.f;
+                if (j < t.nvalid) {
+                    const int row = t.row0 + j;
+                    orow = p.epi_tok ? __ldg(&p.epi_tok[row]) : row;
+                    w = p.epi_w ? __ldg(&p.epi_w[row]) : 1.f;
                 }
+                meta_row[buf * BN + j] = orow;
+                meta_w[buf * BN + j] = w;
             }
             // The epilogue warps share named barriers, so they give up together: lane 0 of
             // each warp votes, and the vote is read by all after the barrier.
@@ -401,39 +401,30 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
                                 o[(size_t)(t.row0 + j0 + jj) * p.ld + f] = __uint_as_float(r[jj]) + bias_f;
                     }
                 } else {
-                    // 4x4 transposes inside each lane quad turn (one feature, 4 tokens) per lane
-                    // into (4 consecutive features, one token) per lane: one fire-and-forget
-                    // 16-byte add per lane per 4 tokens.  (token, weight) of row j live in lane
-                    // j % 32, register j / 32.
-                    const int my_tok = tok8[cidx >> 1];
-                    const float my_w = w8[cidx >> 1];
-                    float *o = static_cast<float *>(p.out);
-                    const int qd = lane & 3;
-                    const int fq = t.ftile * BM + quarter * 32 + (lane & ~3);
+                    // Weighted row scatter: tile row r is stored as bf16(w_r * D[:, r]) into
+                    // output row meta_row[r] (the pair index, so the k rows of a token end up
+                    // adjacent).  The warp's 32 features x 16 rows go through its own 1 KB
+                    // buffer, transposed, and leave as 16-byte stores (8 features of a row).
+                    uint16_t *tb = reinterpret_cast<uint16_t *>(staging) + warp * (16 * 32);
+                    const int mb = buf * BN + j0;
 #pragma unroll
-                    for (int g4 = 0; g4 < 4; ++g4) {
-                        const float a0 = __uint_as_float(r[4 * g4 + 0]);
-                        const float a1 = __uint_as_float(r[4 * g4 + 1]);
-                        const float a2 = __uint_as_float(r[4 * g4 + 2]);
-                        const float a3 = __uint_as_float(r[4 * g4 + 3]);
-                        float b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;
-#pragma unroll
-                        for (int m = 0; m < 4; ++m) {
-                            const float send = sel4(a0, a1, a2, a3, (qd - m) & 3);
-                            const int src = (lane & ~3) | ((qd + m) & 3);
-                            const float got2 = __shfl_sync(0xffffffffu, send, src);
-                            const int bi = (qd + m) & 3;
-                            b0 = bi == 0 ? got2 : b0;
-                            b1 = bi == 1 ? got2 : b1;
-                            b2 = bi == 2 ? got2 : b2;
-                            b3 = bi == 3 ? got2 : b3;
-                        }
-                        const int jt = 4 * g4 + qd;  // this lane's token within the 16
-                        const int tok = __shfl_sync(0xffffffffu, my_tok, 16 * (cidx & 1) + jt);
-                        const float w = __shfl_sync(0xffffffffu, my_w, 16 * (cidx & 1) + jt);
-                        if (j0 + jt < t.nvalid)
-                            ptx::red_add_v4(&o[(size_t)tok * p.ld + fq], w * b0, w * b1, w * b2, w * b3);
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const __nv_bfloat16 v = __float2bfloat16_rn(meta_w[mb + jj] * __uint_as_float(r[jj]));
+                        tb[jj * 32 + lane] = *reinterpret_cast<const uint16_t *>(&v);
                     }
+                    __syncwarp();
+                    uint16_t *o = static_cast<uint16_t *>(p.out);
+                    const int seg = lane & 3;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const int jj = (lane >> 2) + 8 * half;
+                        if (j0 + jj < t.nvalid) {
+                            const uint4 v = *reinterpret_cast<const uint4 *>(&tb[jj * 32 + seg * 8]);
+                            const int orow = meta_row[mb + jj];
+                            *reinterpret_cast<uint4 *>(&o[(size_t)orow * p.ld + t.ftile * BM + quarter * 32 + seg * 8]) = v;
+                        }
+                    }
+                    __syncwarp();
                 }
             }
             ptx::tc_fence_before();
@@ -487,7 +478,7 @@ cudaError_t launch_gemm(GemmEpi epi, const GemmArgs &a, const CUtensorMap &tm_a0
     if (a.K % BK != 0 || a.K <= 0) return cudaErrorInvalidValue;
     if (a.row_src != nullptr && epi != EPI_SWIGLU) return cudaErrorInvalidValue;
     if (epi == EPI_SWIGLU && (a.F % 64 != 0 || a.ld % 8 != 0)) return cudaErrorInvalidValue;
-    if (epi == EPI_COMBINE && (a.F % BM != 0 || a.ld % 4 != 0)) return cudaErrorInvalidValue;
+    if (epi == EPI_COMBINE && (a.F % BM != 0 || a.ld % 8 != 0)) return cudaErrorInvalidValue;
     switch (epi) {
         case EPI_F32: return launch_impl<EPI_F32>(a, tm_a0, tm_a1, tm_b, kc, s);
         case EPI_SWIGLU: return launch_impl<EPI_SWIGLU>(a, tm_a0, tm_a1, tm_b, kc, s);

@@ -52,6 +52,9 @@ bool encode_tmap_2d_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint
 
 // ---- GEMM (tcgen05, swap-AB: weight rows on M, tokens on N) ---------------------------
 
+// EPI_F32: out[r, f] = D + bias[f] (fp32).  EPI_SWIGLU: h = bf16(silu(gate) * up).
+// EPI_COMBINE: out[epi_tok[r], f] = bf16(epi_w[r] * D) -- the weighted expert rows, stored in
+// pair order for the combine that follows.
 enum GemmEpi { EPI_F32 = 0, EPI_SWIGLU = 1, EPI_COMBINE = 2 };
 
 struct GemmArgs {
@@ -72,7 +75,7 @@ struct GemmArgs {
     void *out;
     int ld;
     const float *bias;
-    // EPI_COMBINE: row r adds epi_w[r] * D into out row epi_tok[r] (NULL: row r, weight 1)
+    // EPI_COMBINE: row r stores bf16(epi_w[r] * D) into out row epi_tok[r] (NULL: row r, weight 1)
     const int32_t *epi_tok;
     const float *epi_w;
     int *status;
@@ -101,9 +104,11 @@ cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int32_t *off
 cudaError_t launch_tile_prefix(const int32_t *offsets, int E, int32_t *tile_prefix, int tile_n,
                                const int32_t *perm, int P, int k, int32_t *row_tok,
                                cudaStream_t s);
-// out = bf16(acc); when x_next != NULL also x_next = bf16(resid + out).
-cudaError_t launch_finalize(const float *acc, const uint16_t *resid, int T, int H, uint16_t *out,
-                            uint16_t *x_next, cudaStream_t s);
+// out[t] = bf16( sum_j y[t*k + j] + acc[t] ) with y bf16 [T*k, H] (the weighted expert rows in
+// pair order) and acc fp32 [T, H] (the shared expert, or NULL); when x_next != NULL also
+// x_next = bf16(resid + out).  The sum runs in fp32, slots in order, then the shared term.
+cudaError_t launch_finalize(const uint16_t *y, int k, const float *acc, const uint16_t *resid, int T,
+                            int H, uint16_t *out, uint16_t *x_next, cudaStream_t s);
 cudaError_t launch_combine(const float *y_rows, const int32_t *inv, const float *topk_w,
                            const float *shared_y, int T, int H, int k, uint16_t *out,
                            cudaStream_t s);

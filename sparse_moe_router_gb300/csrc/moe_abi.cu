@@ -116,7 +116,7 @@ constexpr int kMaxPiece = 8192;
 size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
 struct Layout {
-    size_t status, logits, ids, topw, offsets, tiles, chunks, perm, inv, row_tok, row_w, h, h_s, acc, total;
+    size_t status, logits, ids, topw, offsets, tiles, chunks, perm, inv, row_tok, row_w, h, h_s, acc, y, total;
 };
 
 Layout layout(const moe_config &c, int T) {
@@ -142,6 +142,7 @@ Layout layout(const moe_config &c, int T) {
     L.h = take(Tt * c.top_k * c.inter * 2);
     L.h_s = take(Tt * (size_t)c.shared_inter * 2);
     L.acc = take(Tt * c.hidden * 4);
+    L.y = take(Tt * c.top_k * c.hidden * 2);
     L.total = o;
     return L;
 }
@@ -256,10 +257,13 @@ moe_status run_shared(const moe_config &c, const moe_weights &w, const uint16_t 
 
 // Routed experts, grouped: h rows (permuted order) from x gathered through perm, then the down
 // projection either stored per row (y_rows) or weighted and added into acc[token].
+// Routed experts, grouped: h rows (permuted order) from x gathered through row_tok, then the
+// down projection either stored per row in fp32 (y_rows, unfused) or weighted and stored as
+// bf16 rows in pair order (y_pairs[perm[r]] = bf16(row_w[r] * y)) for the combine.
 moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t *x, int T,
                       const int32_t *offsets, const int32_t *tiles, const int32_t *row_tok,
-                      const float *row_w, uint16_t *h, float *y_rows, float *acc, int *status,
-                      cudaStream_t s) {
+                      const int32_t *perm, const float *row_w, uint16_t *h, float *y_rows,
+                      uint16_t *y_pairs, int *status, cudaStream_t s) {
     const uint64_t EI = (uint64_t)c.n_experts * c.inter;
     CUtensorMap tg, tu, td, th;
     if (!encode_tmap_2d_bf16(&tg, w.w_gate, EI, c.hidden, kTileM / 2, 64) ||
@@ -292,8 +296,8 @@ moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t 
         d.out = y_rows;
         MOE_CUDA(launch_gemm(EPI_F32, d, td, td, th, KC_DOWN_GEMM, s));
     } else {
-        d.out = acc;
-        d.epi_tok = row_tok;
+        d.out = y_pairs;
+        d.epi_tok = perm;
         d.epi_w = row_w;
         MOE_CUDA(launch_gemm(EPI_COMBINE, d, td, td, th, KC_DOWN_GEMM, s));
     }
@@ -322,13 +326,11 @@ moe_status forward_piece(const moe_config &c, const moe_weights &w, const uint16
     float *row_w = at<float>(ws, L.row_w);
     MOE_CUDA(launch_permute(ids, T, c.n_experts, c.top_k, offsets, perm, inv, tiles, kTileN,
                             at<int32_t>(ws, L.chunks), topw, row_tok, row_w, status, s));
-    if (c.shared_inter > 0) {
-        MOE_TRY(run_shared(c, w, x, T, h_s, acc, status, s));  // stores: initialises acc
-    } else {
-        MOE_CUDA(launch_zero(acc, (size_t)T * c.hidden, s));
-    }
-    MOE_TRY(run_routed(c, w, x, T, offsets, tiles, row_tok, row_w, h, nullptr, acc, status, s));
-    MOE_CUDA(launch_finalize(acc, resid, T, c.hidden, out, x_next, s));
+    uint16_t *y = at<uint16_t>(ws, L.y);
+    if (c.shared_inter > 0) MOE_TRY(run_shared(c, w, x, T, h_s, acc, status, s));
+    MOE_TRY(run_routed(c, w, x, T, offsets, tiles, row_tok, perm, row_w, h, nullptr, y, status, s));
+    MOE_CUDA(launch_finalize(y, c.top_k, c.shared_inter > 0 ? acc : nullptr, resid, T, c.hidden, out,
+                             x_next, s));
     return MOE_OK;
 }
 
@@ -434,8 +436,8 @@ moe_status moe_expert_ffn(const moe_config *cfg, const moe_weights *w, const moe
     int32_t *row_tok = at<int32_t>(ws, L.row_tok);
     MOE_CUDA(launch_tile_prefix(expert_offsets, cfg->n_experts, tiles, kTileN, perm, T * cfg->top_k,
                                 cfg->top_k, row_tok, s));
-    MOE_TRY(run_routed(*cfg, *w, x, T, expert_offsets, tiles, row_tok, nullptr, h_rows, y_rows, nullptr, status,
-                       s));
+    MOE_TRY(run_routed(*cfg, *w, x, T, expert_offsets, tiles, row_tok, perm, nullptr, h_rows, y_rows, nullptr,
+                       status, s));
     if (shared_y && cfg->shared_inter > 0)
         MOE_TRY(run_shared(*cfg, *w, x, T, at<uint16_t>(ws, L.h_s), shared_y, status, s));
     return MOE_OK;

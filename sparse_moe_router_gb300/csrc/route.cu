@@ -262,15 +262,34 @@ __global__ void __launch_bounds__(kPermThreads, 1)
 }
 
 // ------------------------------------------------------------------- finalise --
-// out = bf16(acc); x_next = bf16(resid + out).  8 elements per thread (H % 8 == 0).
-__global__ void __launch_bounds__(256) finalize_kernel(const float *__restrict__ acc,
-                                                       const uint16_t *resid, size_t n8,
+// out[t] = bf16( sum_j y[t*k+j] + acc[t] ) in fp32 (slots in order, then the shared term);
+// x_next = bf16(resid + out).  8 features per thread (H % 8 == 0): the k bf16 rows of a
+// token are adjacent, so every load is a 16-byte coalesced read.
+__global__ void __launch_bounds__(256) finalize_kernel(const uint16_t *__restrict__ y, int k,
+                                                       const float *__restrict__ acc,
+                                                       const uint16_t *resid, int H8, size_t n8,
                                                        uint16_t *__restrict__ out,
                                                        uint16_t *x_next) {
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
-        const float4 a0 = reinterpret_cast<const float4 *>(acc)[2 * i];
-        const float4 a1 = reinterpret_cast<const float4 *>(acc)[2 * i + 1];
-        const float v[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const size_t t = i / H8, c = i % H8;
+        float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        const uint4 *yr = reinterpret_cast<const uint4 *>(y) + (t * k) * H8 + c;
+        for (int j = 0; j < k; ++j) {
+            const uint4 q = __ldg(yr + (size_t)j * H8);
+            const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&q);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float2 f = __bfloat1622float2(b[m]);
+                v[2 * m] += f.x;
+                v[2 * m + 1] += f.y;
+            }
+        }
+        if (acc) {
+            const float4 a0 = __ldg(reinterpret_cast<const float4 *>(acc) + 2 * i);
+            const float4 a1 = __ldg(reinterpret_cast<const float4 *>(acc) + 2 * i + 1);
+            v[0] += a0.x; v[1] += a0.y; v[2] += a0.z; v[3] += a0.w;
+            v[4] += a1.x; v[5] += a1.y; v[6] += a1.z; v[7] += a1.w;
+        }
         __align__(16) __nv_bfloat16 o[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) o[j] = __float2bfloat16_rn(v[j]);
@@ -395,12 +414,12 @@ cudaError_t launch_tile_prefix(const int32_t *offsets, int E, int32_t *tile_pref
     return cudaGetLastError();
 }
 
-cudaError_t launch_finalize(const float *acc, const uint16_t *resid, int T, int H, uint16_t *out,
-                            uint16_t *x_next, cudaStream_t s) {
+cudaError_t launch_finalize(const uint16_t *y, int k, const float *acc, const uint16_t *resid, int T,
+                            int H, uint16_t *out, uint16_t *x_next, cudaStream_t s) {
     const size_t n8 = (size_t)T * H / 8;
     if (n8 == 0) return cudaSuccess;
     LaunchScope scope(KC_FINALIZE, s);
-    finalize_kernel<<<grid_for(n8, 256), 256, 0, s>>>(acc, resid, n8, out, x_next);
+    finalize_kernel<<<grid_for(n8, 256), 256, 0, s>>>(y, k, acc, resid, H / 8, n8, out, x_next);
     return cudaGetLastError();
 }
 

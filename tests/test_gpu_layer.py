@@ -190,3 +190,12 @@ def test_launch_counter_and_timing():
     n, ms = abi.timing_read("gateup_gemm")
     assert n == 1 and ms > 0
     assert "down_gemm" in abi.timing_classes()
+
+
+def test_forward_is_bit_reproducible():
+    """No atomics in the fused path: two runs on the same input give identical bits."""
+    shape = inputs.Shape(512, 32, 4, 256, 256)
+    layers, x = make(shape, 777, seed=13)
+    a, _ = forward_gpu(shape, layers[0], x)
+    b, _ = forward_gpu(shape, layers[0], x)
+    assert torch.equal(a, b)
