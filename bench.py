@@ -348,7 +348,7 @@ def run_decode(args, dev, pg, peaks):
     torch.cuda.synchronize()
     abi.timing_enable(False)
     split = {}
-    for name in ("decode_router", "decode_gateup", "decode_down"):
+    for name in ("decode_router", "decode_experts"):
         n, ms = abi.timing_read(name)
         if n:
             split[name] = {"launches": n, "avg_us": round(1e3 * ms / n, 2)}

@@ -23,8 +23,7 @@ enum KernelClass {
     KC_COMBINE,           // unfused weighted combine
     KC_ZERO,              // accumulator clear
     KC_DECODE_ROUTER,     // decode: router GEMV + shared gate/up GEMV
-    KC_DECODE_GATEUP,     // decode: top-k + routed gate/up GEMV
-    KC_DECODE_DOWN,       // decode: down GEMVs + combine + residual
+    KC_DECODE_EXPERTS,    // decode: top-k, expert gate/up slices, split-K down, combine
     KC_COUNT
 };
 
@@ -46,9 +45,10 @@ struct DeviceInfo {
 const DeviceInfo &device_info();
 
 // cuTensorMapEncodeTiled obtained through the runtime's driver entry point: a 2-D bf16 map
-// over [rows, cols] (cols contiguous) with a box_rows x box_cols box, 128-byte swizzle.
+// over [rows, cols] (cols contiguous) with a box_rows x box_cols box, 128-byte swizzle (or
+// none: plain row-major boxes).
 bool encode_tmap_2d_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
-                         uint32_t box_rows, uint32_t box_cols);
+                         uint32_t box_rows, uint32_t box_cols, bool swizzle128 = true);
 
 // ---- GEMM (tcgen05, swap-AB: weight rows on M, tokens on N) ---------------------------
 
@@ -131,8 +131,16 @@ struct DecodeArgs {
     uint16_t *out;     // [H]
     const uint16_t *resid;  // [H] residual added into x_next
     uint16_t *x_next;  // [H] or NULL
+    float *acc;        // [H] fp32 accumulator (cleared by the first kernel)
+    int *counter;      // ticket counter, zero between calls (the last block resets it)
+    int *status;       // device status word or NULL
 };
-cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
+// tm_down: map over w_down as [E*H, I], tm_sdown: over ws_down as [H, Is] (or any map when
+// Is == 0); both unswizzled with a 128-row x decode_slice()-column box.
+cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &tm_down, const CUtensorMap &tm_sdown,
+                          cudaStream_t s);
+int decode_slice();
+int decode_box_rows();
 // Router logits of one token with the decode GEMV (the logits the decode path selects on).
 cudaError_t launch_decode_router(const DecodeArgs &a, cudaStream_t s);
 

@@ -32,9 +32,9 @@ struct TimedPair {
 std::vector<TimedPair> g_timed[KC_COUNT];
 
 const char *const kClassNames[KC_COUNT] = {
-    "router_gemm", "topk",          "permute",       "tile_prefix",   "gateup_gemm",
-    "down_gemm",   "shared_gateup", "shared_down",   "finalize",      "combine",
-    "zero",        "decode_router", "decode_gateup", "decode_down"};
+    "router_gemm", "topk",          "permute",     "tile_prefix",   "gateup_gemm",
+    "down_gemm",   "shared_gateup", "shared_down", "finalize",      "combine",
+    "zero",        "decode_router", "decode_experts"};
 }  // namespace
 
 const char *kernel_class_name(int kc) { return (kc >= 0 && kc < KC_COUNT) ? kClassNames[kc] : nullptr; }
@@ -94,7 +94,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }  // namespace
 
 bool encode_tmap_2d_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
-                         uint32_t box_rows, uint32_t box_cols) {
+                         uint32_t box_rows, uint32_t box_cols, bool swizzle128) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
     if (!enc) return false;
     cuuint64_t dims[2] = {cols, rows};
@@ -102,7 +102,8 @@ bool encode_tmap_2d_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -514,7 +515,19 @@ moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const moe_bf
         a.out = out;
         a.resid = resid;
         a.x_next = x_next;
-        MOE_CUDA(launch_decode(a, s));
+        a.acc = at<float>(ws, L.acc);
+        a.counter = at<int>(ws, L.status) + 1;  // in the status area: zero between calls
+        a.status = at<int>(ws, L.status);
+        CUtensorMap td, tsd;
+        const uint32_t sl = (uint32_t)decode_slice(), br = (uint32_t)decode_box_rows();
+        if (!encode_tmap_2d_bf16(&td, w->w_down, (uint64_t)cfg->n_experts * H, cfg->inter, br, sl, false))
+            return MOE_ERR_CUDA;
+        if (cfg->shared_inter > 0) {
+            if (!encode_tmap_2d_bf16(&tsd, w->ws_down, H, cfg->shared_inter, br, sl, false)) return MOE_ERR_CUDA;
+        } else {
+            tsd = td;
+        }
+        MOE_CUDA(launch_decode(a, td, tsd, s));
         return MOE_OK;
     }
     int pieces[64];

@@ -106,6 +106,6 @@ def test_status_strings_and_timing_names():
     assert abi.status_string(0) == "ok"
     assert abi.status_string(2) == "workspace too small"
     names = abi.timing_classes()
-    assert "gateup_gemm" in names and "decode_down" in names
+    assert "gateup_gemm" in names and "decode_experts" in names
     with pytest.raises(abi.MoeError):
         abi.timing_read("no_such_kernel")
