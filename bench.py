@@ -162,8 +162,8 @@ def run_ours(args, world, rank, local, pg):
 
     # ------------------------------------------------------------- prefill (value) --
     wl = inputs.WORKLOADS["prefill8k"]
-    shape, T, L = wl.shape, wl.T, wl.n_layers
-    layers, x0 = inputs.make(wl, device=dev)
+    shape, T, L = wl.shape, wl.T, (args.layers or wl.n_layers)
+    layers, x0 = inputs.make(wl, device=dev, n_layers=L)
     cfg = abi.config_of(shape)
     ws = abi.alloc_workspace(cfg, min(T, 8192))
     wts = [abi.weights(l) for l in layers]
@@ -446,6 +446,8 @@ def main():
     ap.add_argument("--skip-decode", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="prefill layers per step (default: the workload's 4); fewer only for profiler captures")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=4.0)
     args = ap.parse_args()

@@ -22,8 +22,9 @@ enum KernelClass {
     KC_FINALIZE,          // fp32 accumulator -> bf16 out (+ residual)
     KC_COMBINE,           // unfused weighted combine
     KC_ZERO,              // accumulator clear
-    KC_DECODE_ROUTER,     // decode: router GEMV + shared gate/up GEMV
+    KC_DECODE_ROUTER,     // decode: router GEMV
     KC_DECODE_EXPERTS,    // decode: top-k, expert gate/up slices, split-K down, combine
+    KC_GATHER_X,          // token rows copied into expert-sorted order
     KC_COUNT
 };
 
@@ -107,6 +108,10 @@ cudaError_t launch_tile_prefix(const int32_t *offsets, int E, int32_t *tile_pref
 // out[t] = bf16( sum_j y[t*k + j] + acc[t] ) with y bf16 [T*k, H] (the weighted expert rows in
 // pair order) and acc fp32 [T, H] (the shared expert, or NULL); when x_next != NULL also
 // x_next = bf16(resid + out).  The sum runs in fp32, slots in order, then the shared term.
+// xp[r] = x[row_tok[r]] for the P expert-sorted rows (H bf16 each); a row whose token index is
+// outside [0, T) is written as zeros.
+cudaError_t launch_gather_rows(const uint16_t *x, int T, int H, const int32_t *row_tok, int P,
+                               uint16_t *xp, cudaStream_t s);
 cudaError_t launch_finalize(const uint16_t *y, int k, const float *acc, const uint16_t *resid, int T,
                             int H, uint16_t *out, uint16_t *x_next, cudaStream_t s);
 cudaError_t launch_combine(const float *y_rows, const int32_t *inv, const float *topk_w,

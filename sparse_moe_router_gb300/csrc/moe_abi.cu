@@ -34,7 +34,7 @@ std::vector<TimedPair> g_timed[KC_COUNT];
 const char *const kClassNames[KC_COUNT] = {
     "router_gemm", "topk",          "permute",     "tile_prefix",   "gateup_gemm",
     "down_gemm",   "shared_gateup", "shared_down", "finalize",      "combine",
-    "zero",        "decode_router", "decode_experts"};
+    "zero",        "decode_router", "decode_experts", "gather_x"};
 }  // namespace
 
 const char *kernel_class_name(int kc) { return (kc >= 0 && kc < KC_COUNT) ? kClassNames[kc] : nullptr; }
@@ -263,18 +263,21 @@ moe_status run_shared(const moe_config &c, const moe_weights &w, const uint16_t 
 // bf16 rows in pair order (y_pairs[perm[r]] = bf16(row_w[r] * y)) for the combine.
 moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t *x, int T,
                       const int32_t *offsets, const int32_t *tiles, const int32_t *row_tok,
-                      const int32_t *perm, const float *row_w, uint16_t *h, float *y_rows,
+                      const int32_t *perm, const float *row_w, uint16_t *xp, uint16_t *h, float *y_rows,
                       uint16_t *y_pairs, int *status, cudaStream_t s) {
     const uint64_t EI = (uint64_t)c.n_experts * c.inter;
-    CUtensorMap tg, tu, td, th;
+    const uint64_t P = (uint64_t)T * c.top_k;
+    CUtensorMap tg, tu, td, tx, th;
     if (!encode_tmap_2d_bf16(&tg, w.w_gate, EI, c.hidden, kTileM / 2, 64) ||
         !encode_tmap_2d_bf16(&tu, w.w_up, EI, c.hidden, kTileM / 2, 64) ||
         !encode_tmap_2d_bf16(&td, w.w_down, (uint64_t)c.n_experts * c.hidden, c.inter, kTileM, 64) ||
-        !encode_tmap_2d_bf16(&th, h, (uint64_t)T * c.top_k, c.inter, kTileN, 64))
+        !encode_tmap_2d_bf16(&tx, xp, P, c.hidden, kTileN, 64) ||
+        !encode_tmap_2d_bf16(&th, h, P, c.inter, kTileN, 64))
         return MOE_ERR_CUDA;
+    // the token rows in expert-sorted order, so that both GEMM operands load as TMA tiles
+    MOE_CUDA(launch_gather_rows(x, T, c.hidden, row_tok, (int)P, xp, s));
     GemmArgs a{};
-    a.b_src = x;
-    a.row_src = row_tok;
+    a.b_src = xp;
     a.K = c.hidden;
     a.n_groups = c.n_experts;
     a.group_rows = offsets;
@@ -283,7 +286,7 @@ moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t 
     a.out = h;
     a.ld = c.inter;
     a.status = status;
-    MOE_CUDA(launch_gemm(EPI_SWIGLU, a, tg, tu, tg, KC_GATEUP_GEMM, s));
+    MOE_CUDA(launch_gemm(EPI_SWIGLU, a, tg, tu, tx, KC_GATEUP_GEMM, s));
     GemmArgs d{};
     d.b_src = h;
     d.K = c.inter;
@@ -329,7 +332,9 @@ moe_status forward_piece(const moe_config &c, const moe_weights &w, const uint16
                             at<int32_t>(ws, L.chunks), topw, row_tok, row_w, status, s));
     uint16_t *y = at<uint16_t>(ws, L.y);
     if (c.shared_inter > 0) MOE_TRY(run_shared(c, w, x, T, h_s, acc, status, s));
-    MOE_TRY(run_routed(c, w, x, T, offsets, tiles, row_tok, perm, row_w, h, nullptr, y, status, s));
+    // y doubles as the expert-sorted copy of x: the gate/up GEMM is done reading it before the
+    // down GEMM writes y (same stream)
+    MOE_TRY(run_routed(c, w, x, T, offsets, tiles, row_tok, perm, row_w, y, h, nullptr, y, status, s));
     MOE_CUDA(launch_finalize(y, c.top_k, c.shared_inter > 0 ? acc : nullptr, resid, T, c.hidden, out,
                              x_next, s));
     return MOE_OK;
@@ -437,8 +442,8 @@ moe_status moe_expert_ffn(const moe_config *cfg, const moe_weights *w, const moe
     int32_t *row_tok = at<int32_t>(ws, L.row_tok);
     MOE_CUDA(launch_tile_prefix(expert_offsets, cfg->n_experts, tiles, kTileN, perm, T * cfg->top_k,
                                 cfg->top_k, row_tok, s));
-    MOE_TRY(run_routed(*cfg, *w, x, T, expert_offsets, tiles, row_tok, perm, nullptr, h_rows, y_rows, nullptr,
-                       status, s));
+    MOE_TRY(run_routed(*cfg, *w, x, T, expert_offsets, tiles, row_tok, perm, nullptr, at<uint16_t>(ws, L.y), h_rows,
+                       y_rows, nullptr, status, s));
     if (shared_y && cfg->shared_inter > 0)
         MOE_TRY(run_shared(*cfg, *w, x, T, at<uint16_t>(ws, L.h_s), shared_y, status, s));
     return MOE_OK;

@@ -414,6 +414,42 @@ cudaError_t launch_tile_prefix(const int32_t *offsets, int E, int32_t *tile_pref
     return cudaGetLastError();
 }
 
+// One warp per expert-sorted row: 16-byte loads of the token's row, four in flight per lane.
+__global__ void __launch_bounds__(256)
+    gather_rows_kernel(const uint4 *__restrict__ x, int T, const int32_t *__restrict__ row_tok, int P,
+                       int H8, uint4 *__restrict__ xp) {
+    const int lane = threadIdx.x & 31;
+    const int wpb = blockDim.x >> 5;
+    for (int r = blockIdx.x * wpb + (threadIdx.x >> 5); r < P; r += gridDim.x * wpb) {
+        const int t = __ldg(&row_tok[r]);
+        uint4 *dst = xp + (size_t)r * H8;
+        if (t < 0 || t >= T) {
+            for (int i = lane; i < H8; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
+            continue;
+        }
+        const uint4 *src = x + (size_t)t * H8;
+        int i = lane;
+        for (; i + 96 < H8; i += 128) {
+            const uint4 v0 = __ldg(&src[i]), v1 = __ldg(&src[i + 32]);
+            const uint4 v2 = __ldg(&src[i + 64]), v3 = __ldg(&src[i + 96]);
+            dst[i] = v0;
+            dst[i + 32] = v1;
+            dst[i + 64] = v2;
+            dst[i + 96] = v3;
+        }
+        for (; i < H8; i += 32) dst[i] = __ldg(&src[i]);
+    }
+}
+
+cudaError_t launch_gather_rows(const uint16_t *x, int T, int H, const int32_t *row_tok, int P,
+                               uint16_t *xp, cudaStream_t s) {
+    if (P <= 0) return cudaSuccess;
+    LaunchScope scope(KC_GATHER_X, s);
+    gather_rows_kernel<<<grid_for((size_t)P, 8), 256, 0, s>>>(reinterpret_cast<const uint4 *>(x), T, row_tok, P,
+                                                              H / 8, reinterpret_cast<uint4 *>(xp));
+    return cudaGetLastError();
+}
+
 cudaError_t launch_finalize(const uint16_t *y, int k, const float *acc, const uint16_t *resid, int T,
                             int H, uint16_t *out, uint16_t *x_next, cudaStream_t s) {
     const size_t n8 = (size_t)T * H / 8;
