@@ -127,6 +127,8 @@ __device__ __forceinline__ uint16_t bf16_bits(float v) {
     return *reinterpret_cast<const uint16_t *>(&h);
 }
 
+__device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
 // ---------------------------------------------------------------------- kernel 1 --
 __global__ void __launch_bounds__(kK1Block) decode_k1_kernel(DecodeArgs a) {
     extern __shared__ uint4 xs[];  // H bf16
@@ -216,17 +218,57 @@ __device__ __forceinline__ void warp_topk_t(const float *logits, int E, int k, i
     }
 }
 
-__device__ __forceinline__ void warp_topk(const float *logits, int E, int k, int *s_ids, float *s_w) {
+// The same selection for E > 256 without holding the logits in registers: they are staged in
+// shared memory (lg, E <= 1024) with a bitmask of the experts already chosen; each of the k
+// rounds is a warp arg-max over the unchosen ones.
+__device__ __noinline__ void warp_topk_smem(const float *logits, int E, int k, int *s_ids, float *s_w, float *lg,
+                                            unsigned *chosen) {
+    const int lane = threadIdx.x & 31;
+    for (int e = lane; e < E; e += 32) lg[e] = logits[e];
+    chosen[lane] = 0u;  // 32 words: 1024 experts
+    __syncwarp();
+    float top = 0.f, my_val = 0.f;
+    int my_id = 0;
+    for (int r = 0; r < k; ++r) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+        for (int e = lane; e < E; e += 32) {
+            if ((chosen[e >> 5] >> (e & 31)) & 1u) continue;
+            const float v = lg[e];
+            if (v > bv || (v == bv && e < bi)) { bv = v; bi = e; }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+        }
+        if (lane == 0 && bi >= 0 && bi < E) chosen[bi >> 5] |= 1u << (bi & 31);
+        __syncwarp();
+        if (r == 0) top = bv;
+        if (lane == r) { my_val = bv; my_id = bi; }
+    }
+    const float ej = lane < k ? expf(my_val - top) : 0.f;
+    const float sum = warp_sum(ej);
+    if (lane < k) {
+        s_ids[lane] = (my_id >= 0 && my_id < E) ? my_id : 0;
+        s_w[lane] = ej / sum;
+    }
+}
+
+__device__ __forceinline__ void warp_topk(const float *logits, int E, int k, int *s_ids, float *s_w, float *lg,
+                                          unsigned *chosen) {
     const int per = (E + 31) / 32;
     if (per <= 1) warp_topk_t<1>(logits, E, k, s_ids, s_w);
     else if (per <= 2) warp_topk_t<2>(logits, E, k, s_ids, s_w);
     else if (per <= 4) warp_topk_t<4>(logits, E, k, s_ids, s_w);
     else if (per <= 8) warp_topk_t<8>(logits, E, k, s_ids, s_w);
-    else if (per <= 16) warp_topk_t<16>(logits, E, k, s_ids, s_w);
-    else warp_topk_t<32>(logits, E, k, s_ids, s_w);
+    else warp_topk_smem(logits, E, k, s_ids, s_w, lg, chosen);
 }
 
-__global__ void __launch_bounds__(kK2Threads, 1)
+// 96 registers a thread (512 threads: 48K of the SM's 64K) leave room for a K1 block of the next
+// layer on the same SM, so the router spreads over the GPU instead of the few SMs K2 leaves idle.
+__global__ void __maxnreg__(96)
     decode_k2_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tm_down,
                      const __grid_constant__ CUtensorMap tm_sdown, int n_routed_blocks) {
     extern __shared__ uint8_t smem_raw[];
@@ -237,6 +279,8 @@ __global__ void __launch_bounds__(kK2Threads, 1)
     float *hsl = reinterpret_cast<float *>(xs + a.H / 8);                        // [kSlice] fp32
     __shared__ int s_ids[32];
     __shared__ float s_w[32];
+    __shared__ float s_lg[1024];       // logits staging for E > 256
+    __shared__ unsigned s_chosen[32];
     __shared__ __align__(8) uint64_t bar;
     __shared__ int s_last;
     __shared__ int s_ok;
@@ -252,20 +296,24 @@ __global__ void __launch_bounds__(kK2Threads, 1)
         s_ok = 1;
         s_abort = 0;
         ptx::fence_mbar_init();
+        ptx::tma_prefetch_desc(tm);
     }
     pdl_launch_dependents();
     __syncthreads();
-    // TMA of rows [r0, r0 + rows) of the slice's columns into shared memory, on `bar`
+    // TMA of rows [r0, r0 + rows) of the slice's columns into shared memory, on `bar`; run by a
+    // whole warp: lane 0 posts the byte count, then lane b issues box b (at most 16 boxes)
+    constexpr int kLoadWarp = kK2Warps - 1;
     auto load_chunk = [&](int base_row, int r0, int rows) {
-        ptx::mbar_arrive_expect_tx(&bar, (uint32_t)(rows * kSlice * 2));
-        for (int b = 0; b < rows / kBoxRows; ++b)
-            ptx::tma_load_2d(wd + (size_t)b * kBoxRows * kSlice, tm, i0, base_row + r0 + b * kBoxRows, &bar);
+        if (lane == 0) ptx::mbar_arrive_expect_tx(&bar, (uint32_t)(rows * kSlice * 2));
+        __syncwarp();
+        if (lane < rows / kBoxRows)
+            ptx::tma_load_2d(wd + (size_t)lane * kBoxRows * kSlice, tm, i0, base_row + r0 + lane * kBoxRows, &bar);
     };
     const int rows0 = a.H < kChunkRows ? a.H : kChunkRows;
     if (shared_task) {
         // the shared expert's weights do not depend on the routing: start its down columns
         // into shared memory and its gate/up rows into L2 before waiting for K1
-        if (tid == 0) load_chunk(0, 0, rows0);
+        if (warp == kLoadWarp) load_chunk(0, 0, rows0);
         const int row_bytes = a.H * 2;
         for (int f = warp; f < kSlice; f += kK2Warps) {
             const char *g = reinterpret_cast<const char *>(a.ws_gate + (size_t)(i0 + f) * a.H);
@@ -277,7 +325,7 @@ __global__ void __launch_bounds__(kK2Threads, 1)
         }
     }
     pdl_wait();  // x, the logits and the cleared accumulator come after K1
-    if (warp == 0 && !shared_task) warp_topk(a.logits, a.E, a.k, s_ids, s_w);
+    if (warp == 0 && !shared_task) warp_topk(a.logits, a.E, a.k, s_ids, s_w, s_lg, s_chosen);
     const uint4 *xg = reinterpret_cast<const uint4 *>(a.x);
     for (int i = tid; i < a.H / 8; i += kK2Threads) xs[i] = xg[i];
     __syncthreads();
@@ -288,7 +336,7 @@ __global__ void __launch_bounds__(kK2Threads, 1)
         const int e = s_ids[slot];
         wj = s_w[slot];
         base_row = e * a.H;
-        if (tid == 0) load_chunk(base_row, 0, rows0);
+        if (warp == kLoadWarp) load_chunk(base_row, 0, rows0);
         wg = a.w_gate + (size_t)e * a.I * a.H;
         wu = a.w_up + (size_t)e * a.I * a.H;
     }
@@ -308,6 +356,7 @@ __global__ void __launch_bounds__(kK2Threads, 1)
         if (tid == 0 && !ptx::mbar_wait(&bar, (uint32_t)ph, kWaitLimitNs, (volatile int *)&s_abort)) s_ok = 0;
         __syncthreads();
         if (!s_ok) break;
+        // rows is a multiple of 128, so every warp runs the same number of iterations
         for (int n = tid; n < rows; n += kK2Threads) {
             const uint4 *rw = reinterpret_cast<const uint4 *>(wd + (size_t)n * kSlice);
             float acc = 0.f;
@@ -323,10 +372,14 @@ __global__ void __launch_bounds__(kK2Threads, 1)
                     acc = fmaf(f.y, hsl[c * 8 + 2 * m + 1], acc);
                 }
             }
-            atomicAdd(&a.acc[r0 + n], wj * acc);
+            // lanes 4q..4q+3 hold rows n..n+3: one 16-byte reduction per four rows
+            const float v1 = __shfl_down_sync(0xffffffffu, acc, 1);
+            const float v2 = __shfl_down_sync(0xffffffffu, acc, 2);
+            const float v3 = __shfl_down_sync(0xffffffffu, acc, 3);
+            if ((lane & 3) == 0) ptx::red_add_v4(&a.acc[r0 + n], wj * acc, wj * v1, wj * v2, wj * v3);
         }
         __syncthreads();  // the chunk buffer is free again
-        if (r0 + kChunkRows < a.H && tid == 0) {
+        if (r0 + kChunkRows < a.H && warp == kLoadWarp) {
             const int next = (a.H - r0 - kChunkRows) < kChunkRows ? (a.H - r0 - kChunkRows) : kChunkRows;
             load_chunk(base_row, r0 + kChunkRows, next);
         }
@@ -342,13 +395,24 @@ __global__ void __launch_bounds__(kK2Threads, 1)
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    for (int n = tid; n < a.H; n += kK2Threads) {
-        const float v = __ldcg(&a.acc[n]);
-        const __nv_bfloat16 o = __float2bfloat16_rn(v);
-        a.out[n] = *reinterpret_cast<const uint16_t *>(&o);
+    // four outputs a thread: one 16-byte accumulator load, 8-byte bf16 loads and stores
+    for (int n4 = tid; n4 < a.H / 4; n4 += kK2Threads) {
+        const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.acc) + n4);
+        const float vv[4] = {v.x, v.y, v.z, v.w};
+        uint16_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) o[q] = bf16_bits(vv[q]);
+        *reinterpret_cast<uint2 *>(a.out + 4 * n4) =
+            make_uint2((uint32_t)o[0] | ((uint32_t)o[1] << 16), (uint32_t)o[2] | ((uint32_t)o[3] << 16));
         if (a.x_next) {
-            const __nv_bfloat16 rv = *reinterpret_cast<const __nv_bfloat16 *>(&a.resid[n]);
-            a.x_next[n] = bf16_bits(__bfloat162float(rv) + __bfloat162float(o));
+            const uint2 r = *reinterpret_cast<const uint2 *>(a.resid + 4 * n4);
+            const uint16_t rr[4] = {(uint16_t)(r.x & 0xffffu), (uint16_t)(r.x >> 16), (uint16_t)(r.y & 0xffffu),
+                                    (uint16_t)(r.y >> 16)};
+            uint16_t xn[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) xn[q] = bf16_bits(bf16_to_f(rr[q]) + bf16_to_f(o[q]));
+            *reinterpret_cast<uint2 *>(a.x_next + 4 * n4) =
+                make_uint2((uint32_t)xn[0] | ((uint32_t)xn[1] << 16), (uint32_t)xn[2] | ((uint32_t)xn[3] << 16));
         }
     }
     if (tid == 0) atomicExch(a.counter, 0);

@@ -85,7 +85,9 @@ def test_forward_length_sweep(T):
 
 
 @pytest.mark.parametrize("shape", [inputs.Shape(512, 8, 2, 256, 0), inputs.Shape(384, 1, 1, 128, 0),
-                                   inputs.Shape(256, 16, 16, 128, 256), inputs.Shape(1024, 128, 1, 128, 128)])
+                                   inputs.Shape(256, 16, 16, 128, 256), inputs.Shape(1024, 128, 1, 128, 128),
+                                   # more than 256 experts: the decode top-k stages logits in shared memory
+                                   inputs.Shape(256, 600, 8, 128, 128), inputs.Shape(256, 1024, 32, 128, 0)])
 def test_forward_shapes(shape):
     layers, x = make(shape, 150, seed=7)
     check_layer(shape, layers[0], x)
