@@ -193,15 +193,15 @@ __device__ __forceinline__ void warp_topk_t(const float *logits, int E, int k, i
     float top = 0.f, my_val = 0.f;
     int my_id = 0;
     for (int r = 0; r < k; ++r) {
-        float bv = v[0];
-        int bi = id[0] < E ? id[0] : 0x7fffffff;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-        }
-        if ((bi & 31) == lane) {
+        // two warp reductions a round: the largest head, then the lowest expert index among
+        // the lanes whose head equals it
+        const uint32_t key = order_key(v[0]);
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, key);
+        const uint32_t cand = (key == mk && id[0] < E) ? (uint32_t)id[0] : 0xffffffffu;
+        const uint32_t sel = __reduce_min_sync(0xffffffffu, cand);
+        const float bv = key_value(mk);
+        const int bi = (int)sel;
+        if (sel != 0xffffffffu && (int)(sel & 31u) == lane) {
 #pragma unroll
             for (int i = 0; i + 1 < PER; ++i) { v[i] = v[i + 1]; id[i] = id[i + 1]; }
             v[PER - 1] = -INFINITY;

@@ -58,6 +58,19 @@ bool encode_tmap_2d_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint
 // pair order for the combine that follows.
 enum GemmEpi { EPI_F32 = 0, EPI_SWIGLU = 1, EPI_COMBINE = 2 };
 
+#ifdef __CUDACC__
+// Order-preserving map of fp32 onto uint32 (-0 folded onto +0, so equal values get equal keys)
+// and its inverse: top-k rounds compare logits with one integer warp reduction.
+__device__ __forceinline__ uint32_t order_key(float x) {
+    uint32_t u = __float_as_uint(x);
+    if ((u << 1) == 0u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+#endif
+
 struct GemmArgs {
     // token side (B operand): row r of the group row space reads source row
     // row_src ? row_src[r] : r of b_src ([*, K] bf16)

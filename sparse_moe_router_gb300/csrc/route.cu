@@ -60,18 +60,15 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ log
     float my_val = 0.f, top = 0.f;
     int my_id = 0;
     for (int r = 0; r < k; ++r) {
-        float bv = v[0];
-        int bi = e[0] < E ? e[0] : 0x7fffffff;  // padding never wins over a real logit
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-            if (ov > bv || (ov == bv && oi < bi)) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-        if ((bi & 31) == lane) {  // pop the head of the winner's list
+        // the largest head, then the lowest expert index among the lanes holding it (padding,
+        // e >= E, never wins)
+        const uint32_t key = order_key(v[0]);
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, key);
+        const uint32_t cand = (key == mk && e[0] < E) ? (uint32_t)e[0] : 0xffffffffu;
+        const uint32_t sel = __reduce_min_sync(0xffffffffu, cand);
+        const float bv = key_value(mk);
+        const int bi = (int)sel;
+        if (sel != 0xffffffffu && (int)(sel & 31u) == lane) {  // pop the head of the winner's list
 #pragma unroll
             for (int i = 0; i + 1 < PER_LANE; ++i) {
                 v[i] = v[i + 1];
