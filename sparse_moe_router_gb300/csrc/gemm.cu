@@ -74,7 +74,7 @@ struct TileInfo {
 };
 
 __device__ __forceinline__ TileInfo decode_tile(int tau, int nft, const int *g_tiles,
-                                                const int *g_rows, int G) {
+                                                const int *g_rows, int G, int cap) {
     // Largest group g with nft*g_tiles[g] <= tau (empty groups share their successor's base,
     // and the largest index picks the non-empty one).
     int lo = 0, hi = G - 1;
@@ -89,7 +89,7 @@ __device__ __forceinline__ TileInfo decode_tile(int tau, int nft, const int *g_t
     t.ftile = local / ntt;
     const int tt = local - t.ftile * ntt;
     const int c = g_rows[lo + 1] - g_rows[lo];
-    const int tsz = token_tile_size(c);
+    const int tsz = token_tile_size(c, cap);
     t.row0 = g_rows[lo] + tt * tsz;
     const int rem = c - tt * tsz;
     t.nvalid = rem < tsz ? rem : tsz;
@@ -133,6 +133,8 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
+    const int cap = p.tile_cap > 0 ? p.tile_cap : BN;           // token tile cap
+    const uint32_t b_bytes = (uint32_t)cap * BK * 2;            // B box bytes per stage
     const int lane = tid & 31;
     const bool gather = p.row_src != nullptr;  // only with EPI_SWIGLU
 
@@ -159,7 +161,7 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
             g_rows[0] = 0;
             g_rows[1] = p.M_single;
             g_tiles[0] = 0;
-            g_tiles[1] = token_tile_count(p.M_single);
+            g_tiles[1] = token_tile_count(p.M_single, cap);
         }
     } else {
         G = p.n_groups;
@@ -190,14 +192,14 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
                 ptx::tma_prefetch_desc(&tm_b);
                 int it = 0;
                 for (int tau = blockIdx.x; tau < total && ok; tau += gridDim.x) {
-                    const TileInfo t = decode_tile(tau, nft, g_tiles, g_rows, G);
+                    const TileInfo t = decode_tile(tau, nft, g_tiles, g_rows, G, cap);
                     const int arow = t.g * p.F + t.ftile * C::kFT;
                     for (int kb = 0; kb < nkb; ++kb, ++it) {
                         const int s = it % kStages;
                         const uint32_t ph = (uint32_t)(it / kStages) & 1u;
                         if (!ptx::mbar_wait(&empty[s], ph ^ 1u, kWaitLimitNs, abort_flag)) { ok = false; break; }
                         uint8_t *st = smem + s * kStageBytes;
-                        ptx::mbar_arrive_expect_tx(&full[s], kABytes + kBBytes);
+                        ptx::mbar_arrive_expect_tx(&full[s], kABytes + b_bytes);
                         if (EPI == EPI_SWIGLU) {
                             ptx::tma_load_2d(st, &tm_a0, kb * BK, arow, &full[s]);
                             ptx::tma_load_2d(st + kABytes / 2, &tm_a1, kb * BK, arow, &full[s]);
@@ -221,7 +223,7 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
             }
             int it = 0;
             for (int tau = blockIdx.x; tau < total && ok; tau += gridDim.x) {
-                const TileInfo t = decode_tile(tau, nft, g_tiles, g_rows, G);
+                const TileInfo t = decode_tile(tau, nft, g_tiles, g_rows, G, cap);
                 const int nmma = (t.nvalid + 15) & ~15;
                 const int first = (slot - it % kStages + kStages) % kStages;
                 if (first < nkb) {
@@ -284,7 +286,7 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
             int it = 0, tc = 0;
             bool ok = true;
             for (int tau = blockIdx.x; tau < total && ok; tau += gridDim.x, ++tc) {
-                const TileInfo t = decode_tile(tau, nft, g_tiles, g_rows, G);
+                const TileInfo t = decode_tile(tau, nft, g_tiles, g_rows, G, cap);
                 const uint32_t nmma = (uint32_t)((t.nvalid + 15) & ~15);
                 const int buf = tc & 1;
                 const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
@@ -326,7 +328,7 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
         int tc = 0;
         bool ok = true;
         for (int tau = blockIdx.x; tau < total; tau += gridDim.x, ++tc) {
-            const TileInfo t = decode_tile(tau, nft, g_tiles, g_rows, G);
+            const TileInfo t = decode_tile(tau, nft, g_tiles, g_rows, G, cap);
             const int buf = tc & 1;
             const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
             // combine: the 16 warps fetch (output row, weight) of the tile's rows into shared
@@ -461,7 +463,7 @@ cudaError_t launch_impl(const GemmArgs &a, const CUtensorMap &m0, const CUtensor
     int grid = di.sm_count;
     if (a.group_rows == nullptr) {
         const int nft = (a.F + C::kFT - 1) / C::kFT;
-        const int tiles = nft * token_tile_count(a.M_single);
+        const int tiles = nft * token_tile_count(a.M_single, a.tile_cap > 0 ? a.tile_cap : BN);
         if (tiles < grid) grid = tiles;
     }
     if (grid <= 0) return cudaSuccess;
@@ -476,6 +478,8 @@ cudaError_t launch_gemm(GemmEpi epi, const GemmArgs &a, const CUtensorMap &tm_a0
                         const CUtensorMap &tm_a1, const CUtensorMap &tm_b, int kc, cudaStream_t s) {
     if (a.n_groups > kMaxGroups - 1) return cudaErrorInvalidValue;
     if (a.K % BK != 0 || a.K <= 0) return cudaErrorInvalidValue;
+    if (a.tile_cap < 0 || a.tile_cap > BN || a.tile_cap % 16 != 0) return cudaErrorInvalidValue;
+    if (a.tile_cap != 0 && a.group_rows != nullptr) return cudaErrorInvalidValue;  // groups use 256
     if (a.row_src != nullptr && epi != EPI_SWIGLU) return cudaErrorInvalidValue;
     if (epi == EPI_SWIGLU && (a.F % 64 != 0 || a.ld % 8 != 0)) return cudaErrorInvalidValue;
     if (epi == EPI_COMBINE && (a.F % BM != 0 || a.ld % 8 != 0)) return cudaErrorInvalidValue;

@@ -93,6 +93,8 @@ struct GemmArgs {
     const int32_t *epi_tok;
     const float *epi_w;
     int *status;
+    // token tile cap (a multiple of 16, <= 256; 0 = 256); the B tensor map's box has this many rows
+    int tile_cap;
 };
 
 // Launches the persistent grouped GEMM.  tm_a0 (and tm_a1 for EPI_SWIGLU: the up
@@ -168,15 +170,16 @@ constexpr int kTileM = 128;   // weight rows per GEMM tile (MMA M)
 // Token tiles of a group of c rows: ceil(c / 256) tiles of equal size rounded up to 16 (the
 // MMA's N granularity); the last tile takes the remainder.  Shared by the permutation (tile
 // prefix) and the GEMM (tile decode), so both agree on every tile.
-__host__ __device__ __forceinline__ int token_tile_size(int c) {
-    if (c <= 0) return kTileN;
-    const int n = (c + kTileN - 1) / kTileN;
+// (A launch may lower the cap below 256 for more, smaller tiles: the router GEMM.)
+__host__ __device__ __forceinline__ int token_tile_size(int c, int cap = kTileN) {
+    if (c <= 0) return cap;
+    const int n = (c + cap - 1) / cap;
     const int sz = (c + n - 1) / n;
     return (sz + 15) & ~15;
 }
-__host__ __device__ __forceinline__ int token_tile_count(int c) {
+__host__ __device__ __forceinline__ int token_tile_count(int c, int cap = kTileN) {
     if (c <= 0) return 0;
-    const int sz = token_tile_size(c);
+    const int sz = token_tile_size(c, cap);
     return (c + sz - 1) / sz;
 }
 

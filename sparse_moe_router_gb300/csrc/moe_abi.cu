@@ -200,18 +200,24 @@ moe_status cuda_status(cudaError_t e) {
     } while (0)
 #define MOE_CUDA(expr) MOE_TRY(cuda_status(expr))
 
-// Router logits on tensor cores: logits[T,E] = x Wr^T + b.
+// Router logits on tensor cores: logits[T,E] = x Wr^T + b.  The router has few weight tiles
+// (E/128), so its token tiles are capped lower than the experts' to occupy more SMs.
+#ifndef MOE_ROUTER_TILE_N
+#define MOE_ROUTER_TILE_N 128
+#endif
+constexpr int kRouterTileN = MOE_ROUTER_TILE_N;
 moe_status run_router_gemm(const moe_config &c, const moe_weights &w, const uint16_t *x, int T,
                            float *logits, int *status, cudaStream_t s) {
     CUtensorMap tm, tb;
     if (!encode_tmap_2d_bf16(&tm, w.w_router, (uint64_t)c.n_experts, (uint64_t)c.hidden, kTileM, 64) ||
-        !encode_tmap_2d_bf16(&tb, x, (uint64_t)T, (uint64_t)c.hidden, kTileN, 64))
+        !encode_tmap_2d_bf16(&tb, x, (uint64_t)T, (uint64_t)c.hidden, kRouterTileN, 64))
         return MOE_ERR_CUDA;
     GemmArgs a{};
     a.b_src = x;
     a.K = c.hidden;
     a.n_groups = 1;
     a.M_single = T;
+    a.tile_cap = kRouterTileN;
     a.F = c.n_experts;
     a.out = logits;
     a.ld = c.n_experts;

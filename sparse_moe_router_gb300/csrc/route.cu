@@ -97,8 +97,9 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ log
 // Stable counting sort of the P = T*k pairs by expert in three launches, with no block ever
 // waiting on another:
 //   1. perm_hist:    block c counts the experts of its chunk of kChunk consecutive pairs;
-//   2. perm_scan:    one block: per expert, the exclusive prefix over chunks, then the
-//                    exclusive prefix over experts (the offsets) and the token-tile prefix;
+//   2. perm_scan:    one block: per expert (a group of adjacent lanes, each summing a range
+//                    of chunks), the exclusive prefix over chunks, then the exclusive prefix
+//                    over experts (the offsets) and the token-tile prefix;
 //                    the chunk table now holds each chunk's first row per expert;
 //   3. perm_scatter: block c walks its chunk again; warp w owns pairs [64w, 64w+64) of the
 //                    chunk, per-warp counts give each warp its first row per expert, and a
@@ -159,26 +160,61 @@ __global__ void __launch_bounds__(kPermThreads, 1)
                      int32_t *__restrict__ tile_prefix, int tile_n) {
     __shared__ int sh_warp[32];
     const int tid = threadIdx.x;
-    int cnt = 0;
-    if (tid < E)
-        for (int c = 0; c < n_chunks; ++c) {
-            const int h = chunk_tab[(size_t)c * E + tid];
-            chunk_tab[(size_t)c * E + tid] = cnt;
-            cnt += h;
+    // tpe adjacent lanes per expert (a power of two <= 32 with E * tpe <= 1024); lane `sub` of
+    // expert e owns chunks [c0, c1) of e's column of the table
+    int tpe = 1;
+    while (tpe < 32 && E * tpe * 2 <= kPermThreads) tpe *= 2;
+    const int e = tid / tpe, sub = tid % tpe;
+    const bool live = e < E;
+    const int cpt = (n_chunks + tpe - 1) / tpe;
+    const int c0 = sub * cpt, c1 = min(n_chunks, c0 + cpt);
+    // pass 1: this lane's share of expert e's count, eight loads in flight
+    int part = 0;
+    if (live)
+        for (int c = c0; c < c1; c += 8) {
+            int h[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) h[u] = (c + u < c1) ? chunk_tab[(size_t)(c + u) * E + e] : 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) part += h[u];
         }
+    // the lanes' exclusive prefix within the expert, and the expert's total
+    int incl = part;
+    for (int d = 1; d < tpe; d <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, d, tpe);
+        if (sub >= d) incl += y;
+    }
+    const int excl = incl - part;
+    const int cnt = __shfl_sync(0xffffffffu, incl, tpe - 1, tpe);
+    // offsets over experts (the first lane of each group carries its expert's count)
     int total = 0;
-    const int off = block_excl_scan(tid < E ? cnt : 0, sh_warp, &total);
-    const int tiles = tid < E ? token_tile_count(cnt) : 0;
+    const int off_first = block_excl_scan((live && sub == 0) ? cnt : 0, sh_warp, &total);
+    const int off = __shfl_sync(0xffffffffu, off_first, 0, tpe);
+    const int tiles = (live && sub == 0) ? token_tile_count(cnt) : 0;
     int total_tiles = 0;
     const int toff = block_excl_scan(tiles, sh_warp, &total_tiles);
-    if (tid < E) {
-        offsets[tid] = off;
-        if (tile_prefix) tile_prefix[tid] = toff;
-        for (int c = 0; c < n_chunks; ++c) chunk_tab[(size_t)c * E + tid] += off;
+    if (live && sub == 0) {
+        offsets[e] = off;
+        if (tile_prefix) tile_prefix[e] = toff;
     }
     if (tid == 0) {
         offsets[E] = total;
         if (tile_prefix) tile_prefix[E] = total_tiles;
+    }
+    // pass 2: each chunk's first row for expert e
+    if (live) {
+        int run = off + excl;
+        for (int c = c0; c < c1; c += 8) {
+            int h[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) h[u] = (c + u < c1) ? chunk_tab[(size_t)(c + u) * E + e] : 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (c + u < c1) {
+                    chunk_tab[(size_t)(c + u) * E + e] = run;
+                    run += h[u];
+                }
+        }
     }
 }
 
