@@ -46,7 +46,7 @@ constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kAccCols = BN;                // fp32 accumulator columns per TMEM buffer
 constexpr uint32_t kTmemCols = 2 * kAccCols;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
-constexpr int kMaxGroups = 1025;                  // E <= 1024 experts (+1 spare)
+constexpr int kMaxGroups = 1026;                  // E <= 1024 experts, the shared expert, a spare
 constexpr int kStgStride = BM + 4;                // SwiGLU staging row (floats), padded for banks
 
 template <int EPI>
@@ -74,7 +74,19 @@ struct TileInfo {
 };
 
 __device__ __forceinline__ TileInfo decode_tile(int tau, int nft, const int *g_tiles,
-                                                const int *g_rows, int G, int cap) {
+                                                const int *g_rows, int G, int cap, bool shared_last) {
+    if (shared_last) {
+        // S shared-expert tiles (group G-1, L2-resident weights) spread evenly among the R
+        // routed ones: position iQ holds shared tile i, the others the routed tiles in order
+        const int R = nft * g_tiles[G - 1];
+        const int S = nft * (g_tiles[G] - g_tiles[G - 1]);
+        if (S > 0) {
+            const int Q = (R + S) / S;
+            const int q = tau / Q;
+            if (tau % Q == 0 && q < S) tau = R + q;
+            else tau -= (q + 1 < S ? q + 1 : S);
+        }
+    }
     // Largest group g with nft*g_tiles[g] <= tau (empty groups share their successor's base,
     // and the largest index picks the non-empty one).
     int lo = 0, hi = G - 1;
@@ -105,7 +117,8 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f +
 template <int EPI>
 __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
     gemm_kernel(const GemmArgs p, const __grid_constant__ CUtensorMap tm_a0,
-                const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_b) {
+                const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_b,
+                const __grid_constant__ CUtensorMap tm_s0, const __grid_constant__ CUtensorMap tm_s1) {
     using C = Cfg<EPI>;
     constexpr int kEpiWarps = C::kEpiWarps;
     constexpr int kProdWarp0 = C::kProdWarp0;
@@ -190,10 +203,17 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
                 ptx::tma_prefetch_desc(&tm_a0);
                 if (EPI == EPI_SWIGLU) ptx::tma_prefetch_desc(&tm_a1);
                 ptx::tma_prefetch_desc(&tm_b);
+                if (p.shared_last) {
+                    ptx::tma_prefetch_desc(&tm_s0);
+                    if (EPI == EPI_SWIGLU) ptx::tma_prefetch_desc(&tm_s1);
+                }
                 int it = 0;
                 for (int tau = blockIdx.x; tau < total && ok; tau += gridDim.x) {
-                    const TileInfo t = decode_tile(tau, nft, g_tiles, g_rows, G, cap);
-                    const int arow = t.g * p.F + t.ftile * C::kFT;
+                    const TileInfo t = decode_tile(tau, nft, g_tiles, g_rows, G, cap, p.shared_last);
+                    const bool shg = p.shared_last && t.g == G - 1;
+                    const int arow = (shg ? 0 : t.g * p.F) + t.ftile * C::kFT;
+                    const void *ma0 = shg ? (const void *)&tm_s0 : (const void *)&tm_a0;
+                    const void *ma1 = shg ? (const void *)&tm_s1 : (const void *)&tm_a1;
                     for (int kb = 0; kb < nkb; ++kb, ++it) {
                         const int s = it % kStages;
                         const uint32_t ph = (uint32_t)(it / kStages) & 1u;
@@ -201,10 +221,10 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
                         uint8_t *st = smem + s * kStageBytes;
                         ptx::mbar_arrive_expect_tx(&full[s], kABytes + b_bytes);
                         if (EPI == EPI_SWIGLU) {
-                            ptx::tma_load_2d(st, &tm_a0, kb * BK, arow, &full[s]);
-                            ptx::tma_load_2d(st + kABytes / 2, &tm_a1, kb * BK, arow, &full[s]);
+                            ptx::tma_load_2d(st, ma0, kb * BK, arow, &full[s]);
+                            ptx::tma_load_2d(st + kABytes / 2, ma1, kb * BK, arow, &full[s]);
                         } else {
-                            ptx::tma_load_2d(st, &tm_a0, kb * BK, arow, &full[s]);
+                            ptx::tma_load_2d(st, ma0, kb * BK, arow, &full[s]);
                         }
                         ptx::tma_load_2d(st + kABytes, &tm_b, kb * BK, t.row0, &full[s]);
                     }
@@ -223,7 +243,7 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
             }
             int it = 0;
             for (int tau = blockIdx.x; tau < total && ok; tau += gridDim.x) {
-                const TileInfo t = decode_tile(tau, nft, g_tiles, g_rows, G, cap);
+                const TileInfo t = decode_tile(tau, nft, g_tiles, g_rows, G, cap, p.shared_last);
                 const int nmma = (t.nvalid + 15) & ~15;
                 const int first = (slot - it % kStages + kStages) % kStages;
                 if (first < nkb) {
@@ -286,7 +306,7 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
             int it = 0, tc = 0;
             bool ok = true;
             for (int tau = blockIdx.x; tau < total && ok; tau += gridDim.x, ++tc) {
-                const TileInfo t = decode_tile(tau, nft, g_tiles, g_rows, G, cap);
+                const TileInfo t = decode_tile(tau, nft, g_tiles, g_rows, G, cap, p.shared_last);
                 const uint32_t nmma = (uint32_t)((t.nvalid + 15) & ~15);
                 const int buf = tc & 1;
                 const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
@@ -328,7 +348,7 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
         int tc = 0;
         bool ok = true;
         for (int tau = blockIdx.x; tau < total; tau += gridDim.x, ++tc) {
-            const TileInfo t = decode_tile(tau, nft, g_tiles, g_rows, G, cap);
+            const TileInfo t = decode_tile(tau, nft, g_tiles, g_rows, G, cap, p.shared_last);
             const int buf = tc & 1;
             const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
             // combine: the 16 warps fetch (output row, weight) of the tile's rows into shared
@@ -340,8 +360,13 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
                 float w = 0.f;
                 if (j < t.nvalid) {
                     const int row = t.row0 + j;
-                    orow = p.epi_tok ? __ldg(&p.epi_tok[row]) : row;
-                    w = p.epi_w ? __ldg(&p.epi_w[row]) : 1.f;
+                    if (p.shared_last && t.g == G - 1) {  // shared expert: in place, weight 1
+                        orow = row;
+                        w = 1.f;
+                    } else {
+                        orow = p.epi_tok ? __ldg(&p.epi_tok[row]) : row;
+                        w = p.epi_w ? __ldg(&p.epi_w[row]) : 1.f;
+                    }
                 }
                 meta_row[buf * BN + j] = orow;
                 meta_w[buf * BN + j] = w;
@@ -448,7 +473,8 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
 
 template <int EPI>
 cudaError_t launch_impl(const GemmArgs &a, const CUtensorMap &m0, const CUtensorMap &m1,
-                        const CUtensorMap &mb, int kc, cudaStream_t s) {
+                        const CUtensorMap &mb, const CUtensorMap &s0, const CUtensorMap &s1, int kc,
+                        cudaStream_t s) {
     using C = Cfg<EPI>;
     static bool attr_done[64] = {false};
     int dev = 0;
@@ -468,25 +494,28 @@ cudaError_t launch_impl(const GemmArgs &a, const CUtensorMap &m0, const CUtensor
     }
     if (grid <= 0) return cudaSuccess;
     LaunchScope scope(kc, s);
-    gemm_kernel<EPI><<<grid, C::kThreads, C::kSmemBytes, s>>>(a, m0, m1, mb);
+    gemm_kernel<EPI><<<grid, C::kThreads, C::kSmemBytes, s>>>(a, m0, m1, mb, s0, s1);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(GemmEpi epi, const GemmArgs &a, const CUtensorMap &tm_a0,
-                        const CUtensorMap &tm_a1, const CUtensorMap &tm_b, int kc, cudaStream_t s) {
+cudaError_t launch_gemm(GemmEpi epi, const GemmArgs &a, const CUtensorMap &tm_a0, const CUtensorMap &tm_a1,
+                        const CUtensorMap &tm_b, const CUtensorMap &tm_s0, const CUtensorMap &tm_s1, int kc,
+                        cudaStream_t s) {
     if (a.n_groups > kMaxGroups - 1) return cudaErrorInvalidValue;
     if (a.K % BK != 0 || a.K <= 0) return cudaErrorInvalidValue;
     if (a.tile_cap < 0 || a.tile_cap > BN || a.tile_cap % 16 != 0) return cudaErrorInvalidValue;
     if (a.tile_cap != 0 && a.group_rows != nullptr) return cudaErrorInvalidValue;  // groups use 256
+    if (a.shared_last && (a.group_rows == nullptr || a.n_groups < 2 || a.row_src != nullptr))
+        return cudaErrorInvalidValue;
     if (a.row_src != nullptr && epi != EPI_SWIGLU) return cudaErrorInvalidValue;
     if (epi == EPI_SWIGLU && (a.F % 64 != 0 || a.ld % 8 != 0)) return cudaErrorInvalidValue;
     if (epi == EPI_COMBINE && (a.F % BM != 0 || a.ld % 8 != 0)) return cudaErrorInvalidValue;
     switch (epi) {
-        case EPI_F32: return launch_impl<EPI_F32>(a, tm_a0, tm_a1, tm_b, kc, s);
-        case EPI_SWIGLU: return launch_impl<EPI_SWIGLU>(a, tm_a0, tm_a1, tm_b, kc, s);
-        case EPI_COMBINE: return launch_impl<EPI_COMBINE>(a, tm_a0, tm_a1, tm_b, kc, s);
+        case EPI_F32: return launch_impl<EPI_F32>(a, tm_a0, tm_a1, tm_b, tm_s0, tm_s1, kc, s);
+        case EPI_SWIGLU: return launch_impl<EPI_SWIGLU>(a, tm_a0, tm_a1, tm_b, tm_s0, tm_s1, kc, s);
+        case EPI_COMBINE: return launch_impl<EPI_COMBINE>(a, tm_a0, tm_a1, tm_b, tm_s0, tm_s1, kc, s);
     }
     return cudaErrorInvalidValue;
 }

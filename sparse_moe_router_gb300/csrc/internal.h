@@ -95,14 +95,20 @@ struct GemmArgs {
     int *status;
     // token tile cap (a multiple of 16, <= 256; 0 = 256); the B tensor map's box has this many rows
     int tile_cap;
+    // the last group is the shared expert: its weight rows come from the tm_s* maps (row
+    // ftile*kFT of the shared matrix), its tiles are interleaved evenly among the routed ones,
+    // and the combine epilogue stores its rows in place with weight 1
+    bool shared_last;
 };
 
-// Launches the persistent grouped GEMM.  tm_a0 (and tm_a1 for EPI_SWIGLU: the up
-// projection) are 2-D tensor maps over the weight rows with a 128 x 64 box; tm_b is a map
-// over the B rows ([rows, K], 128 x 64 box), used when row_src is NULL.  Gathered B
-// (row_src != NULL) is supported with EPI_SWIGLU only.
-cudaError_t launch_gemm(GemmEpi epi, const GemmArgs &a, const CUtensorMap &tm_a0,
-                        const CUtensorMap &tm_a1, const CUtensorMap &tm_b, int kc, cudaStream_t s);
+// Launch the persistent grouped GEMM.  tm_a0 (and tm_a1 for EPI_SWIGLU: the up projection)
+// are 2-D tensor maps over the weight rows (64- or 128-row box, 64 columns); tm_b is a map over
+// the B rows ([rows, K], box of tile_cap rows x 64).  tm_s0 / tm_s1 are the shared expert's
+// weight maps, read for the last group when a.shared_last (pass any map otherwise).
+// Gathered B (row_src != NULL) is supported with EPI_SWIGLU only.
+cudaError_t launch_gemm(GemmEpi epi, const GemmArgs &a, const CUtensorMap &tm_a0, const CUtensorMap &tm_a1,
+                        const CUtensorMap &tm_b, const CUtensorMap &tm_s0, const CUtensorMap &tm_s1, int kc,
+                        cudaStream_t s);
 
 // ---- routing / permutation / elementwise ---------------------------------------------
 
@@ -110,12 +116,14 @@ cudaError_t launch_topk(const float *logits, int T, int E, int k, int32_t *ids, 
                         cudaStream_t s);
 // chunk_tab: device scratch of permute_scratch_ints(T, E, k) ints.  When row_tok / row_w are
 // not NULL the scatter also writes, per row of the sorted order, the token (pair / k) and the
-// routing weight topk_w[pair] (what the expert GEMMs read per row).
+// routing weight topk_w[pair] (what the expert GEMMs read per row).  extra_rows > 0 appends one
+// more group of that many rows after the experts (offsets[E+1], tile_prefix[E+1]): the shared
+// expert's rows when it runs inside the routed GEMMs.
 size_t permute_scratch_ints(int T, int E, int k);
 cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int32_t *offsets,
                            int32_t *perm, int32_t *inv, int32_t *tile_prefix, int tile_n,
                            int32_t *chunk_tab, const float *topk_w, int32_t *row_tok,
-                           float *row_w, int *status, cudaStream_t s);
+                           float *row_w, int *status, cudaStream_t s, int extra_rows = 0);
 // Token-tile prefix from given offsets, and row_tok[r] = perm[r] / k for the P rows.
 cudaError_t launch_tile_prefix(const int32_t *offsets, int E, int32_t *tile_prefix, int tile_n,
                                const int32_t *perm, int P, int k, int32_t *row_tok,
@@ -125,10 +133,14 @@ cudaError_t launch_tile_prefix(const int32_t *offsets, int E, int32_t *tile_pref
 // x_next = bf16(resid + out).  The sum runs in fp32, slots in order, then the shared term.
 // xp[r] = x[row_tok[r]] for the P expert-sorted rows (H bf16 each); a row whose token index is
 // outside [0, T) is written as zeros.
+// n_tail > 0: rows P .. P+n_tail-1 of xp are x's rows 0 .. n_tail-1 in order (the shared
+// expert's group).
 cudaError_t launch_gather_rows(const uint16_t *x, int T, int H, const int32_t *row_tok, int P,
-                               uint16_t *xp, cudaStream_t s);
+                               uint16_t *xp, cudaStream_t s, int n_tail = 0);
+// y_tail (bf16 [T, H], or NULL) is added like one more expert row of weight 1.
 cudaError_t launch_finalize(const uint16_t *y, int k, const float *acc, const uint16_t *resid, int T,
-                            int H, uint16_t *out, uint16_t *x_next, cudaStream_t s);
+                            int H, uint16_t *out, uint16_t *x_next, cudaStream_t s,
+                            const uint16_t *y_tail = nullptr);
 cudaError_t launch_combine(const float *y_rows, const int32_t *inv, const float *topk_w,
                            const float *shared_y, int T, int H, int k, uint16_t *out,
                            cudaStream_t s);

@@ -133,17 +133,18 @@ Layout layout(const moe_config &c, int T) {
     L.logits = take(Tt * c.n_experts * 4);
     L.ids = take(Tt * c.top_k * 4);
     L.topw = take(Tt * c.top_k * 4);
-    L.offsets = take((size_t)(c.n_experts + 1) * 4);
-    L.tiles = take((size_t)(c.n_experts + 1) * 4);
+    // E + 2 entries: the experts and, when it runs inside the routed GEMMs, the shared expert
+    L.offsets = take((size_t)(c.n_experts + 2) * 4);
+    L.tiles = take((size_t)(c.n_experts + 2) * 4);
     L.chunks = take(permute_scratch_ints((int)Tt, c.n_experts, c.top_k) * 4);
     L.perm = take(Tt * c.top_k * 4);
     L.inv = take(Tt * c.top_k * 4);
     L.row_tok = take(Tt * c.top_k * 4);
     L.row_w = take(Tt * c.top_k * 4);
-    L.h = take(Tt * c.top_k * c.inter * 2);
+    L.h = take(Tt * (c.top_k + 1) * c.inter * 2);  // + the shared expert's rows
     L.h_s = take(Tt * (size_t)c.shared_inter * 2);
     L.acc = take(Tt * c.hidden * 4);
-    L.y = take(Tt * c.top_k * c.hidden * 2);
+    L.y = take(Tt * (c.top_k + 1) * c.hidden * 2);
     L.total = o;
     return L;
 }
@@ -223,7 +224,7 @@ moe_status run_router_gemm(const moe_config &c, const moe_weights &w, const uint
     a.ld = c.n_experts;
     a.bias = w.b_router;
     a.status = status;
-    MOE_CUDA(launch_gemm(EPI_F32, a, tm, tm, tb, KC_ROUTER_GEMM, s));
+    MOE_CUDA(launch_gemm(EPI_F32, a, tm, tm, tb, tm, tm, KC_ROUTER_GEMM, s));
     return MOE_OK;
 }
 
@@ -248,7 +249,7 @@ moe_status run_shared(const moe_config &c, const moe_weights &w, const uint16_t 
     a.out = h_s;
     a.ld = c.shared_inter;
     a.status = status;
-    MOE_CUDA(launch_gemm(EPI_SWIGLU, a, tg, tu, tx, KC_SHARED_GATEUP, s));
+    MOE_CUDA(launch_gemm(EPI_SWIGLU, a, tg, tu, tx, tg, tu, KC_SHARED_GATEUP, s));
     GemmArgs d{};
     d.b_src = h_s;
     d.K = c.shared_inter;
@@ -258,58 +259,74 @@ moe_status run_shared(const moe_config &c, const moe_weights &w, const uint16_t 
     d.out = out;
     d.ld = c.hidden;
     d.status = status;
-    MOE_CUDA(launch_gemm(EPI_F32, d, td, td, th, KC_SHARED_DOWN, s));
+    MOE_CUDA(launch_gemm(EPI_F32, d, td, td, th, td, td, KC_SHARED_DOWN, s));
     return MOE_OK;
 }
 
-// Routed experts, grouped: h rows (permuted order) from x gathered through perm, then the down
-// projection either stored per row (y_rows) or weighted and added into acc[token].
-// Routed experts, grouped: h rows (permuted order) from x gathered through row_tok, then the
-// down projection either stored per row in fp32 (y_rows, unfused) or weighted and stored as
-// bf16 rows in pair order (y_pairs[perm[r]] = bf16(row_w[r] * y)) for the combine.
+// Routed experts, grouped: h rows (expert-sorted order) from the expert-sorted copy of x
+// (xp), then the down projection either stored per row in fp32 (y_rows, unfused) or weighted
+// and stored as bf16 rows in pair order (y_pairs[perm[r]] = bf16(row_w[r] * y)) for the
+// combine.  with_shared: the shared expert (I_s == I) runs as one more group of the T tokens
+// in order: rows P .. P+T-1 of xp, h and y_pairs (weight 1); offsets/tiles then hold E + 2
+// entries.
 moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t *x, int T,
                       const int32_t *offsets, const int32_t *tiles, const int32_t *row_tok,
                       const int32_t *perm, const float *row_w, uint16_t *xp, uint16_t *h, float *y_rows,
-                      uint16_t *y_pairs, int *status, cudaStream_t s) {
+                      uint16_t *y_pairs, int *status, cudaStream_t s, bool with_shared = false) {
     const uint64_t EI = (uint64_t)c.n_experts * c.inter;
     const uint64_t P = (uint64_t)T * c.top_k;
-    CUtensorMap tg, tu, td, tx, th;
+    const uint64_t rows = P + (with_shared ? (uint64_t)T : 0);
+    CUtensorMap tg, tu, td, tx, th, tsg, tsu, tsd;
     if (!encode_tmap_2d_bf16(&tg, w.w_gate, EI, c.hidden, kTileM / 2, 64) ||
         !encode_tmap_2d_bf16(&tu, w.w_up, EI, c.hidden, kTileM / 2, 64) ||
         !encode_tmap_2d_bf16(&td, w.w_down, (uint64_t)c.n_experts * c.hidden, c.inter, kTileM, 64) ||
-        !encode_tmap_2d_bf16(&tx, xp, P, c.hidden, kTileN, 64) ||
-        !encode_tmap_2d_bf16(&th, h, P, c.inter, kTileN, 64))
+        !encode_tmap_2d_bf16(&tx, xp, rows, c.hidden, kTileN, 64) ||
+        !encode_tmap_2d_bf16(&th, h, rows, c.inter, kTileN, 64))
         return MOE_ERR_CUDA;
-    // the token rows in expert-sorted order, so that both GEMM operands load as TMA tiles
-    MOE_CUDA(launch_gather_rows(x, T, c.hidden, row_tok, (int)P, xp, s));
+    if (with_shared) {
+        if (!encode_tmap_2d_bf16(&tsg, w.ws_gate, c.shared_inter, c.hidden, kTileM / 2, 64) ||
+            !encode_tmap_2d_bf16(&tsu, w.ws_up, c.shared_inter, c.hidden, kTileM / 2, 64) ||
+            !encode_tmap_2d_bf16(&tsd, w.ws_down, c.hidden, c.shared_inter, kTileM, 64))
+            return MOE_ERR_CUDA;
+    } else {
+        tsg = tg;
+        tsu = tu;
+        tsd = td;
+    }
+    // the token rows in expert-sorted order (then x itself for the shared expert), so that both
+    // GEMM operands load as TMA tiles
+    MOE_CUDA(launch_gather_rows(x, T, c.hidden, row_tok, (int)P, xp, s, with_shared ? T : 0));
     GemmArgs a{};
     a.b_src = xp;
     a.K = c.hidden;
-    a.n_groups = c.n_experts;
+    a.n_groups = c.n_experts + (with_shared ? 1 : 0);
     a.group_rows = offsets;
     a.group_tiles = tiles;
     a.F = c.inter;
     a.out = h;
     a.ld = c.inter;
     a.status = status;
-    MOE_CUDA(launch_gemm(EPI_SWIGLU, a, tg, tu, tx, KC_GATEUP_GEMM, s));
+    a.shared_last = with_shared;
+    MOE_CUDA(launch_gemm(EPI_SWIGLU, a, tg, tu, tx, tsg, tsu, KC_GATEUP_GEMM, s));
     GemmArgs d{};
     d.b_src = h;
     d.K = c.inter;
-    d.n_groups = c.n_experts;
+    d.n_groups = a.n_groups;
     d.group_rows = offsets;
     d.group_tiles = tiles;
     d.F = c.hidden;
     d.ld = c.hidden;
     d.status = status;
+    d.shared_last = with_shared;
     if (y_rows) {
+        if (with_shared) return MOE_ERR_INVALID_ARG;
         d.out = y_rows;
-        MOE_CUDA(launch_gemm(EPI_F32, d, td, td, th, KC_DOWN_GEMM, s));
+        MOE_CUDA(launch_gemm(EPI_F32, d, td, td, th, td, td, KC_DOWN_GEMM, s));
     } else {
         d.out = y_pairs;
         d.epi_tok = perm;
         d.epi_w = row_w;
-        MOE_CUDA(launch_gemm(EPI_COMBINE, d, td, td, th, KC_DOWN_GEMM, s));
+        MOE_CUDA(launch_gemm(EPI_COMBINE, d, td, td, th, tsd, tsd, KC_DOWN_GEMM, s));
     }
     return MOE_OK;
 }
@@ -334,15 +351,18 @@ moe_status forward_piece(const moe_config &c, const moe_weights &w, const uint16
     MOE_CUDA(launch_topk(logits, T, c.n_experts, c.top_k, ids, topw, s));
     int32_t *row_tok = at<int32_t>(ws, L.row_tok);
     float *row_w = at<float>(ws, L.row_w);
+    // a shared expert as wide as the routed ones runs inside the routed GEMMs, as group E
+    const bool merged = c.shared_inter > 0 && c.shared_inter == c.inter;
     MOE_CUDA(launch_permute(ids, T, c.n_experts, c.top_k, offsets, perm, inv, tiles, kTileN,
-                            at<int32_t>(ws, L.chunks), topw, row_tok, row_w, status, s));
+                            at<int32_t>(ws, L.chunks), topw, row_tok, row_w, status, s, merged ? T : 0));
     uint16_t *y = at<uint16_t>(ws, L.y);
-    if (c.shared_inter > 0) MOE_TRY(run_shared(c, w, x, T, h_s, acc, status, s));
+    if (c.shared_inter > 0 && !merged) MOE_TRY(run_shared(c, w, x, T, h_s, acc, status, s));
     // y doubles as the expert-sorted copy of x: the gate/up GEMM is done reading it before the
     // down GEMM writes y (same stream)
-    MOE_TRY(run_routed(c, w, x, T, offsets, tiles, row_tok, perm, row_w, y, h, nullptr, y, status, s));
-    MOE_CUDA(launch_finalize(y, c.top_k, c.shared_inter > 0 ? acc : nullptr, resid, T, c.hidden, out,
-                             x_next, s));
+    MOE_TRY(run_routed(c, w, x, T, offsets, tiles, row_tok, perm, row_w, y, h, nullptr, y, status, s, merged));
+    const size_t P = (size_t)T * c.top_k;
+    MOE_CUDA(launch_finalize(y, c.top_k, (c.shared_inter > 0 && !merged) ? acc : nullptr, resid, T, c.hidden, out,
+                             x_next, s, merged ? y + P * c.hidden : nullptr));
     return MOE_OK;
 }
 

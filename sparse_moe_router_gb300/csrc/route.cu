@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(kPermThreads) perm_hist_kernel(const int32_t *
 
 __global__ void __launch_bounds__(kPermThreads, 1)
     perm_scan_kernel(int32_t *__restrict__ chunk_tab, int n_chunks, int E, int32_t *__restrict__ offsets,
-                     int32_t *__restrict__ tile_prefix, int tile_n) {
+                     int32_t *__restrict__ tile_prefix, int tile_n, int extra_rows) {
     __shared__ int sh_warp[32];
     const int tid = threadIdx.x;
     // tpe adjacent lanes per expert (a power of two <= 32 with E * tpe <= 1024); lane `sub` of
@@ -200,6 +200,10 @@ __global__ void __launch_bounds__(kPermThreads, 1)
     if (tid == 0) {
         offsets[E] = total;
         if (tile_prefix) tile_prefix[E] = total_tiles;
+        if (extra_rows > 0) {  // one more group after the experts
+            offsets[E + 1] = total + extra_rows;
+            if (tile_prefix) tile_prefix[E + 1] = total_tiles + token_tile_count(extra_rows);
+        }
     }
     // pass 2: each chunk's first row for expert e
     if (live) {
@@ -299,6 +303,7 @@ __global__ void __launch_bounds__(kPermThreads, 1)
 // x_next = bf16(resid + out).  8 features per thread (H % 8 == 0): the k bf16 rows of a
 // token are adjacent, so every load is a 16-byte coalesced read.
 __global__ void __launch_bounds__(256) finalize_kernel(const uint16_t *__restrict__ y, int k,
+                                                       const uint16_t *__restrict__ y_tail,
                                                        const float *__restrict__ acc,
                                                        const uint16_t *resid, int H8, size_t n8,
                                                        uint16_t *__restrict__ out,
@@ -309,6 +314,16 @@ __global__ void __launch_bounds__(256) finalize_kernel(const uint16_t *__restric
         const uint4 *yr = reinterpret_cast<const uint4 *>(y) + (t * k) * H8 + c;
         for (int j = 0; j < k; ++j) {
             const uint4 q = __ldg(yr + (size_t)j * H8);
+            const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&q);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float2 f = __bfloat1622float2(b[m]);
+                v[2 * m] += f.x;
+                v[2 * m + 1] += f.y;
+            }
+        }
+        if (y_tail) {
+            const uint4 q = __ldg(reinterpret_cast<const uint4 *>(y_tail) + i);
             const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&q);
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
@@ -413,7 +428,7 @@ size_t permute_scratch_ints(int T, int E, int k) {
 cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int32_t *offsets,
                            int32_t *perm, int32_t *inv, int32_t *tile_prefix, int tile_n,
                            int32_t *chunk_tab, const float *topk_w, int32_t *row_tok,
-                           float *row_w, int *status, cudaStream_t s) {
+                           float *row_w, int *status, cudaStream_t s, int extra_rows) {
     const int P = T * k;
     const int n_chunks = (P + kChunk - 1) / kChunk;
     static bool attr_done[64] = {false};
@@ -431,7 +446,8 @@ cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int32_t *off
     }
     {
         LaunchScope scope(KC_PERMUTE, s);
-        perm_scan_kernel<<<1, kPermThreads, 0, s>>>(chunk_tab, n_chunks, E, offsets, tile_prefix, tile_n);
+        perm_scan_kernel<<<1, kPermThreads, 0, s>>>(chunk_tab, n_chunks, E, offsets, tile_prefix, tile_n,
+                                                    extra_rows);
     }
     LaunchScope scope(KC_PERMUTE, s);
     perm_scatter_kernel<<<n_chunks, kPermThreads, kPermWarps * E * sizeof(int), s>>>(
@@ -450,11 +466,11 @@ cudaError_t launch_tile_prefix(const int32_t *offsets, int E, int32_t *tile_pref
 // One warp per expert-sorted row: 16-byte loads of the token's row, four in flight per lane.
 __global__ void __launch_bounds__(256)
     gather_rows_kernel(const uint4 *__restrict__ x, int T, const int32_t *__restrict__ row_tok, int P,
-                       int H8, uint4 *__restrict__ xp) {
+                       int n_tail, int H8, uint4 *__restrict__ xp) {
     const int lane = threadIdx.x & 31;
     const int wpb = blockDim.x >> 5;
-    for (int r = blockIdx.x * wpb + (threadIdx.x >> 5); r < P; r += gridDim.x * wpb) {
-        const int t = __ldg(&row_tok[r]);
+    for (int r = blockIdx.x * wpb + (threadIdx.x >> 5); r < P + n_tail; r += gridDim.x * wpb) {
+        const int t = r < P ? __ldg(&row_tok[r]) : r - P;
         uint4 *dst = xp + (size_t)r * H8;
         if (t < 0 || t >= T) {
             for (int i = lane; i < H8; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
@@ -475,20 +491,20 @@ __global__ void __launch_bounds__(256)
 }
 
 cudaError_t launch_gather_rows(const uint16_t *x, int T, int H, const int32_t *row_tok, int P,
-                               uint16_t *xp, cudaStream_t s) {
-    if (P <= 0) return cudaSuccess;
+                               uint16_t *xp, cudaStream_t s, int n_tail) {
+    if (P + n_tail <= 0) return cudaSuccess;
     LaunchScope scope(KC_GATHER_X, s);
-    gather_rows_kernel<<<grid_for((size_t)P, 8), 256, 0, s>>>(reinterpret_cast<const uint4 *>(x), T, row_tok, P,
-                                                              H / 8, reinterpret_cast<uint4 *>(xp));
+    gather_rows_kernel<<<grid_for((size_t)(P + n_tail), 8), 256, 0, s>>>(
+        reinterpret_cast<const uint4 *>(x), T, row_tok, P, n_tail, H / 8, reinterpret_cast<uint4 *>(xp));
     return cudaGetLastError();
 }
 
 cudaError_t launch_finalize(const uint16_t *y, int k, const float *acc, const uint16_t *resid, int T,
-                            int H, uint16_t *out, uint16_t *x_next, cudaStream_t s) {
+                            int H, uint16_t *out, uint16_t *x_next, cudaStream_t s, const uint16_t *y_tail) {
     const size_t n8 = (size_t)T * H / 8;
     if (n8 == 0) return cudaSuccess;
     LaunchScope scope(KC_FINALIZE, s);
-    finalize_kernel<<<grid_for(n8, 256), 256, 0, s>>>(y, k, acc, resid, H / 8, n8, out, x_next);
+    finalize_kernel<<<grid_for(n8, 256), 256, 0, s>>>(y, k, y_tail, acc, resid, H / 8, n8, out, x_next);
     return cudaGetLastError();
 }
 
