@@ -112,7 +112,10 @@ __device__ __forceinline__ void set_error(int *status, int code) {
     if (status) atomicCAS(status, 0, code);
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+// silu(g) * u = g * u / (1 + e^-g), with the fast exponential and an IEEE reciprocal: its error
+// (a few fp32 ulp) is far below the bf16 rounding of h that follows.  g -> -inf gives
+// 1 / inf = 0, so the product stays 0.
+__device__ __forceinline__ float silu_mul(float g, float u) { return g * u * __frcp_rn(1.0f + __expf(-g)); }
 
 template <int EPI>
 __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
@@ -386,14 +389,18 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
                 const int f = t.ftile * BM + frow;
                 if (p.bias != nullptr && f < p.F) bias_f = __ldg(&p.bias[f]);
             }
-#pragma unroll
-            for (int cidx = 0; cidx < BN / 16; ++cidx) {
+            // this warp's chunks are cidx = sub, sub + kSubs, ...; the TMEM load of the next
+            // chunk is issued before the current one is processed, hiding its latency
+            const int n_chunks = (t.nvalid + 15) >> 4;
+            uint32_t rn[16];
+            if (sub < n_chunks) ptx::tmem_ld_16(taddr + (uint32_t)(16 * sub), rn);
+            for (int cidx = sub; cidx < n_chunks; cidx += kSubs) {
                 const int j0 = 16 * cidx;
-                if (j0 >= t.nvalid) break;
-                if (cidx % kSubs != sub) continue;
                 uint32_t r[16];
-                ptx::tmem_ld_16(taddr + (uint32_t)j0, r);
                 ptx::tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < 16; ++q) r[q] = rn[q];
+                if (cidx + kSubs < n_chunks) ptx::tmem_ld_16(taddr + (uint32_t)(j0 + 16 * kSubs), rn);
                 if (EPI == EPI_SWIGLU) {
                     // lanes 0..63 hold gate, 64..127 the same features' up: exchange through
                     // shared memory, then thread q computes token q/8, features 8*(q%8)..+7
