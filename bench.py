@@ -81,12 +81,16 @@ class ClockSampler:
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,timestamp")
 
     def __init__(self, index):
         self.index = index
         self.proc = None
         self.path = None
+        self.window = None  # (t0, t1) wall-clock seconds of the timed region
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
 
     def start(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -115,6 +119,19 @@ class ClockSampler:
                 if len(parts) >= 9:
                     rows.append(parts)
         os.unlink(self.path)
+        if self.window and rows:
+            # keep the samples taken inside the timed region (timestamps are local wall time)
+            inside = []
+            for r in rows:
+                try:
+                    ts = time.mktime(time.strptime(r[9].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    ts += float("0." + r[9].split(".")[1]) if "." in r[9] else 0.0
+                except (IndexError, ValueError):
+                    continue
+                if self.window[0] - 0.05 <= ts <= self.window[1] + 0.05:
+                    inside.append(r)
+            if inside:
+                rows = inside
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
@@ -134,11 +151,11 @@ class ClockSampler:
 
 # ------------------------------------------------------------------------ ours --
 
-# dram__bytes_read.sum + dram__bytes_write.sum of one routed gate/up launch (T=8192, H=2048, E=256,
-# k=8, I=512) from an ncu capture of the current kernel: 1.343 GB read + 0.064 GB written.  The
-# algorithmic minimum is 1.074 GB of weights + 0.268 GB of expert-sorted x read + 0.067 GB of h
-# written, so the kernel reads nothing twice from HBM.
-GATEUP_DRAM_BYTES = 1_407_297_000
+# dram__bytes_read.sum + dram__bytes_write.sum of one gate/up launch (routed experts + the shared
+# expert, T=8192, H=2048, E=256, k=8, I=I_s=512) from an ncu capture of the current kernel:
+# 1.616 GB read + 0.073 GB written.  The algorithmic minimum reads 1.076 GB of weights and 0.302 GB
+# of token rows (expert-sorted x and x) and writes 0.075 GB of h.
+GATEUP_DRAM_BYTES = 1_688_690_000
 
 
 def _algorithmic(shape, T):
@@ -147,10 +164,13 @@ def _algorithmic(shape, T):
     H, E, k, I, Is = shape.hidden, shape.n_experts, shape.top_k, shape.inter, shape.shared_inter
     gateup = 2.0 * T * k * H * 2 * I
     down = 2.0 * T * k * I * H
-    shared = 2.0 * T * H * 2 * Is + 2.0 * T * Is * H
+    shared_gu = 2.0 * T * H * 2 * Is
+    shared = shared_gu + 2.0 * T * Is * H
     router = 2.0 * T * H * E
-    return {"gateup_flops": gateup, "down_flops": down, "shared_flops": shared,
-            "router_flops": router, "total_flops": gateup + down + shared + router}
+    # a shared expert as wide as the routed ones runs inside the routed gate/up launch
+    gateup_launch = gateup + (shared_gu if Is == I else 0.0)
+    return {"gateup_flops": gateup, "gateup_launch_flops": gateup_launch, "down_flops": down,
+            "shared_flops": shared, "router_flops": router, "total_flops": gateup + down + shared + router}
 
 
 def _decode_bytes(shape):
@@ -202,11 +222,13 @@ def run_ours(args, world, rank, local, pg):
     abi.timing_enable(True)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
+    t_w0 = time.time()
     ev0.record(stream)
     for _ in range(args.steps):
         step(xa)
     ev1.record(stream)
     torch.cuda.synchronize()
+    clocks.mark(t_w0, time.time())
     abi.timing_enable(False)
     launches = abi.moe_launch_count() - n_launch0
     _barrier(pg)
@@ -226,13 +248,13 @@ def run_ours(args, world, rank, local, pg):
     gu = per_kernel.get("gateup_gemm")
     roofline = None
     if gu:
-        achieved = alg["gateup_flops"] / (gu["avg_us"] * 1e-6) / 1e12
+        achieved = alg["gateup_launch_flops"] / (gu["avg_us"] * 1e-6) / 1e12
         pk = peaks["bf16_tflops_sustained"]
         roofline = {"bound": "tensor", "kernel": "gateup_gemm", "achieved": round(achieved, 1),
                     "peak": pk, "unit": "TFLOP/s", "frac": round(achieved / pk, 4),
                     "frac_of_burst_peak": round(achieved / peaks["bf16_tflops"], 4),
                     "traffic": GATEUP_DRAM_BYTES, "peak_source": peaks["source"] + " bf16 sustained",
-                    "flops_per_launch": alg["gateup_flops"]}
+                    "flops_per_launch": alg["gateup_launch_flops"]}
     layer_tflops = alg["total_flops"] * L * args.steps / (t_ms * 1e-3) / 1e12
 
     # ------------------------------------------------------------------------ e2e --
@@ -447,7 +469,7 @@ def run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=300)  # ~1 s timed: several clock samples
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-decode", action="store_true")
