@@ -98,8 +98,16 @@ __device__ __forceinline__ TileInfo decode_tile(int tau, int nft, const int *g_t
     t.g = lo;
     const int local = tau - nft * g_tiles[lo];
     const int ntt = g_tiles[lo + 1] - g_tiles[lo];
-    t.ftile = local / ntt;
-    const int tt = local - t.ftile * ntt;
+    int tt;
+    if (shared_last && lo == G - 1) {
+        // shared expert: its weights (a few MB) stay in L2 anyway, so walk the weight tiles
+        // fastest and let the nft tiles that read one token tile run close together
+        tt = local / nft;
+        t.ftile = local - tt * nft;
+    } else {
+        t.ftile = local / ntt;
+        tt = local - t.ftile * ntt;
+    }
     const int c = g_rows[lo + 1] - g_rows[lo];
     const int tsz = token_tile_size(c, cap);
     t.row0 = g_rows[lo] + tt * tsz;
