@@ -16,18 +16,17 @@
 //   warps 0..P-1  epilogue (P = 16 for the weighted row scatter, else 8): warp w reads TMEM
 //               lanes 32*(w%4)..+31 (the hardware's lane quarters), and the P/4 warps of a
 //               quarter take every (P/4)-th 16-token chunk;
-//   warps P..P+3 producers.  Contiguous B (token rows in order): one thread issues the TMA
-//               loads of the weight tile and of the B tile.  Gathered B (token rows picked
-//               through the expert permutation): warp 8+s owns shared-memory stage s; it
-//               issues that stage's weight TMA, copies the gathered rows with 16-byte cp.async
-//               into the 128-byte-swizzled K-major layout, waits for its own copies, fences
-//               them into the async proxy and arrives, so all stages fill concurrently;
+//   warps P..P+3 producers: one thread issues the TMA loads of the weight tile and of the
+//               token tile (the other three warps idle);
 //   warp P+4    allocates TMEM; lane 0 issues tcgen05.mma (kind::f16, bf16 -> fp32) and
 //               tcgen05.commit.
 // Pipelines: 4 shared-memory stages (full/empty mbarriers) and two TMEM accumulators of 256
 // columns (acc_full/acc_empty), so the epilogue of one tile overlaps the next main loop.
 // Tiles are walked statically (tile = blockIdx.x + i*gridDim.x), ordered (group, weight tile,
 // token tile) with the token tile fastest, so CTAs sharing a weight tile run together.
+// Clusters of 2 (GemmArgs::cluster): the pair walks units of two adjacent weight tiles of one
+// token tile; each CTA loads half of the token tile and multicasts it to both, and each CTA's
+// MMA commits release the stage in both, so every token tile leaves L2 once per pair.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -64,9 +63,8 @@ struct Cfg {
     // combine: per-tile (output row, weight) of the BN tile rows, double-buffered
     static constexpr int kMetaBytes = (EPI == EPI_COMBINE) ? 2 * BN * 8 : 0;
     static constexpr int kBarBytes = (2 * kStages + 5) * 8;
-    static constexpr int kRowTableBytes = (EPI == EPI_SWIGLU) ? 4 * BN * 4 : 0;
     static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + kStagingBytes +
-                                      kMetaBytes + kBarBytes + 16 + 2 * (kMaxGroups + 1) * 4 + kRowTableBytes;
+                                      kMetaBytes + kBarBytes + 16 + 2 * (kMaxGroups + 1) * 4;
 };
 
 struct TileInfo {
@@ -153,20 +151,20 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
     volatile int *epi_vote = reinterpret_cast<volatile int *>(tmem_holder + 2);  // 2 slots
     int *g_tiles = reinterpret_cast<int *>(tmem_holder + 4);
     int *g_rows = g_tiles + (kMaxGroups + 1);
-    int *row_tables = g_rows + (kMaxGroups + 1);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int cap = p.tile_cap > 0 ? p.tile_cap : BN;           // token tile cap
     const uint32_t b_bytes = (uint32_t)cap * BK * 2;            // B box bytes per stage
     const int lane = tid & 31;
-    const bool gather = p.row_src != nullptr;  // only with EPI_SWIGLU
+    const int CL = p.cluster > 1 ? p.cluster : 1;                // CTAs per cluster
+    const uint32_t crank = CL > 1 ? ptx::cluster_ctarank() : 0u;
+    const uint16_t cmask = (uint16_t)((1u << CL) - 1u);
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
-            // gathered B: the stage's warp arrives twice (weight expect_tx, then its copies)
-            ptx::mbar_init(&full[s], gather ? 2 : 1);
-            ptx::mbar_init(&empty[s], 1);
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], CL);  // released by the MMA commits of every CTA of the cluster
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&acc_full[b], 1);
@@ -195,9 +193,23 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
         }
     }
     __syncthreads();
+    // the other CTAs of the cluster see this CTA's barriers initialised before anything is
+    // multicast into them
+    if (CL > 1) ptx::cluster_sync();
     const int nft = (p.F + C::kFT - 1) / C::kFT;
-    const int total = nft * g_tiles[G];
-    if ((int)blockIdx.x >= total) return;  // CTA-uniform; nothing allocated yet
+    const int nft_u = nft / CL;                      // units of CL adjacent weight tiles
+    const int total = nft_u * g_tiles[G];
+    const int cid = (int)blockIdx.x / CL, ncl = (int)gridDim.x / CL;
+    if (cid >= total) {  // cluster-uniform; nothing allocated yet
+        if (CL > 1) ptx::cluster_sync();
+        return;
+    }
+    // unit u -> this CTA's tile: weight tile unit*CL + rank of the unit's token tile
+    auto tile_of = [&](int u) {
+        TileInfo t = decode_tile(u, nft_u, g_tiles, g_rows, G, cap, p.shared_last);
+        t.ftile = t.ftile * CL + (int)crank;
+        return t;
+    };
 
     if (warp == kMmaWarp) ptx::tmem_alloc(tmem_holder, kTmemCols);
     ptx::tc_fence_before();
@@ -209,103 +221,42 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
     if (warp >= kProdWarp0 && warp < kMmaWarp) {
         // ------------------------------------------------------------ producers --
         bool ok = true;
-        if (!gather) {
-            if (tid == kProdWarp0 * 32) {
-                ptx::tma_prefetch_desc(&tm_a0);
-                if (EPI == EPI_SWIGLU) ptx::tma_prefetch_desc(&tm_a1);
-                ptx::tma_prefetch_desc(&tm_b);
-                if (p.shared_last) {
-                    ptx::tma_prefetch_desc(&tm_s0);
-                    if (EPI == EPI_SWIGLU) ptx::tma_prefetch_desc(&tm_s1);
-                }
-                int it = 0;
-                for (int tau = blockIdx.x; tau < total && ok; tau += gridDim.x) {
-                    const TileInfo t = decode_tile(tau, nft, g_tiles, g_rows, G, cap, p.shared_last);
-                    const bool shg = p.shared_last && t.g == G - 1;
-                    const int arow = (shg ? 0 : t.g * p.F) + t.ftile * C::kFT;
-                    const void *ma0 = shg ? (const void *)&tm_s0 : (const void *)&tm_a0;
-                    const void *ma1 = shg ? (const void *)&tm_s1 : (const void *)&tm_a1;
-                    for (int kb = 0; kb < nkb; ++kb, ++it) {
-                        const int s = it % kStages;
-                        const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-                        if (!ptx::mbar_wait(&empty[s], ph ^ 1u, kWaitLimitNs, abort_flag)) { ok = false; break; }
-                        uint8_t *st = smem + s * kStageBytes;
-                        ptx::mbar_arrive_expect_tx(&full[s], kABytes + b_bytes);
-                        if (EPI == EPI_SWIGLU) {
-                            ptx::tma_load_2d(st, ma0, kb * BK, arow, &full[s]);
-                            ptx::tma_load_2d(st + kABytes / 2, ma1, kb * BK, arow, &full[s]);
-                        } else {
-                            ptx::tma_load_2d(st, ma0, kb * BK, arow, &full[s]);
-                        }
-                        ptx::tma_load_2d(st + kABytes, &tm_b, kb * BK, t.row0, &full[s]);
-                    }
-                }
-            }
-        } else {
-            // warp kProdWarp0+slot owns stage `slot`: iterations it with it % kStages == slot
-            const int slot = warp - kProdWarp0;
-            uint32_t *table = reinterpret_cast<uint32_t *>(row_tables) + slot * BN;
-            const char *bsrc = static_cast<const char *>(p.b_src);
-            const int c = lane & 7;        // 16-byte chunk of the 128-byte row segment
-            const int rsub = lane >> 3;    // rows rsub + 4*m
-            if (lane == 0) {
-                ptx::tma_prefetch_desc(&tm_a0);
-                ptx::tma_prefetch_desc(&tm_a1);
+        if (tid == kProdWarp0 * 32) {
+            ptx::tma_prefetch_desc(&tm_a0);
+            if (EPI == EPI_SWIGLU) ptx::tma_prefetch_desc(&tm_a1);
+            ptx::tma_prefetch_desc(&tm_b);
+            if (p.shared_last) {
+                ptx::tma_prefetch_desc(&tm_s0);
+                if (EPI == EPI_SWIGLU) ptx::tma_prefetch_desc(&tm_s1);
             }
             int it = 0;
-            for (int tau = blockIdx.x; tau < total && ok; tau += gridDim.x) {
-                const TileInfo t = decode_tile(tau, nft, g_tiles, g_rows, G, cap, p.shared_last);
-                const int nmma = (t.nvalid + 15) & ~15;
-                const int first = (slot - it % kStages + kStages) % kStages;
-                if (first < nkb) {
-                    // byte offset of each gathered row's 16-byte chunk c (0xffffffff: zero row)
-                    __syncwarp();
-                    for (int j = lane; j < BN; j += 32)
-                        table[j] = j < t.nvalid ? (uint32_t)__ldg(&p.row_src[t.row0 + j]) * (uint32_t)(p.K * 2)
-                                               : 0xffffffffu;
-                    __syncwarp();
-                }
-                const int arow = t.g * p.F + t.ftile * C::kFT;
-                for (int kb = first; kb < nkb; kb += kStages) {
-                    const int itk = it + kb;
-                    const uint32_t ph = (uint32_t)(itk / kStages) & 1u;
-                    // every lane waits; the warp gives up together (it must stay converged)
-                    const bool got = ptx::mbar_wait(&empty[slot], ph ^ 1u, kWaitLimitNs, abort_flag);
-                    if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-                    uint8_t *st = smem + slot * kStageBytes;
-                    if (lane == 0) {
-                        ptx::mbar_arrive_expect_tx(&full[slot], kABytes);
-                        ptx::tma_load_2d(st, &tm_a0, kb * BK, arow, &full[slot]);
-                        ptx::tma_load_2d(st + kABytes / 2, &tm_a1, kb * BK, arow, &full[slot]);
+            for (int tau = cid; tau < total && ok; tau += ncl) {
+                const TileInfo t = tile_of(tau);
+                const bool shg = p.shared_last && t.g == G - 1;
+                const int arow = (shg ? 0 : t.g * p.F) + t.ftile * C::kFT;
+                const void *ma0 = shg ? (const void *)&tm_s0 : (const void *)&tm_a0;
+                const void *ma1 = shg ? (const void *)&tm_s1 : (const void *)&tm_a1;
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+                    if (!ptx::mbar_wait(&empty[s], ph ^ 1u, kWaitLimitNs, abort_flag)) { ok = false; break; }
+                    uint8_t *st = smem + s * kStageBytes;
+                    ptx::mbar_arrive_expect_tx(&full[s], kABytes + b_bytes);
+                    if (EPI == EPI_SWIGLU) {
+                        ptx::tma_load_2d(st, ma0, kb * BK, arow, &full[s]);
+                        ptx::tma_load_2d(st + kABytes / 2, ma1, kb * BK, arow, &full[s]);
+                    } else {
+                        ptx::tma_load_2d(st, ma0, kb * BK, arow, &full[s]);
                     }
-                    const uint32_t bst = ptx::smem_u32(st + kABytes);
-                    const char *kbase = bsrc + kb * BK * 2 + c * 16;
-                    // rows j = rsub + 4m, 8 per step; a step may run up to 16 rows past nmma:
-                    // those rows are zero-filled inside the stage buffer and the MMA never
-                    // reads them
-                    for (int j0 = rsub; j0 < nmma; j0 += 32) {
-                        uint32_t off[8];
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) off[u] = table[j0 + 4 * u];
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            const int j = j0 + 4 * u;
-                            const uint32_t dst = bst + j * 128 + ((c ^ (j & 7)) << 4);
-                            if (off[u] != 0xffffffffu)
-                                ptx::cp_async_16(dst, kbase + off[u], 16);
-                            else
-                                ptx::cp_async_16(dst, bsrc, 0);  // zero rows up to the MMA's N
-                        }
+                    if (CL == 1) {
+                        ptx::tma_load_2d(st + kABytes, &tm_b, kb * BK, t.row0, &full[s]);
+                    } else {  // this CTA's share of the token tile, to every CTA of the cluster
+                        const int part = cap / CL;
+                        ptx::tma_load_2d_mc(st + kABytes + (int)crank * part * (BK * 2), &tm_b, kb * BK,
+                                            t.row0 + (int)crank * part, &full[s], cmask);
                     }
-                    ptx::cp_async_commit();
-                    ptx::cp_async_wait_all();
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(&full[slot]);
                 }
-                it += nkb;
             }
-            ptx::cp_async_wait_all();
         }
         if (!ok) {
             set_error(p.status, MOE_ERR_TIMEOUT);
@@ -316,8 +267,8 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
         if (lane == 0) {
             int it = 0, tc = 0;
             bool ok = true;
-            for (int tau = blockIdx.x; tau < total && ok; tau += gridDim.x, ++tc) {
-                const TileInfo t = decode_tile(tau, nft, g_tiles, g_rows, G, cap, p.shared_last);
+            for (int tau = cid; tau < total && ok; tau += ncl, ++tc) {
+                const TileInfo t = tile_of(tau);
                 const uint32_t nmma = (uint32_t)((t.nvalid + 15) & ~15);
                 const int buf = tc & 1;
                 const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
@@ -336,7 +287,8 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
                     for (int kk = 0; kk < BK / 16; ++kk)
                         ptx::mma_bf16(d_base, ptx::sw128_desc(a_addr + kk * 32), ptx::sw128_desc(b_addr + kk * 32),
                                       idesc, (kb | kk) != 0 ? 1u : 0u);
-                    ptx::mma_commit(&empty[s]);
+                    if (CL == 1) ptx::mma_commit(&empty[s]);
+                    else ptx::mma_commit_mc(&empty[s], cmask);
                 }
                 if (!ok) break;
                 ptx::mma_commit(&acc_full[buf]);
@@ -358,8 +310,8 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
         float *stg = staging + sub * 16 * kStgStride;  // SwiGLU exchange buffer of this sub-group
         int tc = 0;
         bool ok = true;
-        for (int tau = blockIdx.x; tau < total; tau += gridDim.x, ++tc) {
-            const TileInfo t = decode_tile(tau, nft, g_tiles, g_rows, G, cap, p.shared_last);
+        for (int tau = cid; tau < total; tau += ncl, ++tc) {
+            const TileInfo t = tile_of(tau);
             const int buf = tc & 1;
             const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
             // combine: the 16 warps fetch (output row, weight) of the tile's rows into shared
@@ -480,6 +432,8 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
 
     ptx::tc_fence_before();
     __syncthreads();
+    // no CTA leaves while another may still multicast into its shared memory or barriers
+    if (CL > 1) ptx::cluster_sync();
     if (warp == kMmaWarp) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, kTmemCols);
@@ -509,6 +463,24 @@ cudaError_t launch_impl(const GemmArgs &a, const CUtensorMap &m0, const CUtensor
     }
     if (grid <= 0) return cudaSuccess;
     LaunchScope scope(kc, s);
+    if (a.cluster > 1) {
+        // whole clusters only; the kernel gives the units out per cluster
+        grid = (grid / a.cluster) * a.cluster;
+        if (grid <= 0) return cudaErrorInvalidValue;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(C::kThreads);
+        cfg.dynamicSmemBytes = C::kSmemBytes;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = a.cluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, gemm_kernel<EPI>, a, m0, m1, mb, s0, s1);
+    }
     gemm_kernel<EPI><<<grid, C::kThreads, C::kSmemBytes, s>>>(a, m0, m1, mb, s0, s1);
     return cudaGetLastError();
 }
@@ -522,9 +494,14 @@ cudaError_t launch_gemm(GemmEpi epi, const GemmArgs &a, const CUtensorMap &tm_a0
     if (a.K % BK != 0 || a.K <= 0) return cudaErrorInvalidValue;
     if (a.tile_cap < 0 || a.tile_cap > BN || a.tile_cap % 16 != 0) return cudaErrorInvalidValue;
     if (a.tile_cap != 0 && a.group_rows != nullptr) return cudaErrorInvalidValue;  // groups use 256
-    if (a.shared_last && (a.group_rows == nullptr || a.n_groups < 2 || a.row_src != nullptr))
+    if (a.shared_last && (a.group_rows == nullptr || a.n_groups < 2))
         return cudaErrorInvalidValue;
-    if (a.row_src != nullptr && epi != EPI_SWIGLU) return cudaErrorInvalidValue;
+    if (a.cluster > 1) {
+        const int kft = (epi == EPI_SWIGLU) ? 64 : BM;
+        const int nft = (a.F + kft - 1) / kft;
+        const int cap = a.tile_cap > 0 ? a.tile_cap : BN;
+        if (a.cluster != 2 || nft % a.cluster != 0 || cap % (16 * a.cluster) != 0) return cudaErrorInvalidValue;
+    }
     if (epi == EPI_SWIGLU && (a.F % 64 != 0 || a.ld % 8 != 0)) return cudaErrorInvalidValue;
     if (epi == EPI_COMBINE && (a.F % BM != 0 || a.ld % 8 != 0)) return cudaErrorInvalidValue;
     switch (epi) {

@@ -72,10 +72,9 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 #endif
 
 struct GemmArgs {
-    // token side (B operand): row r of the group row space reads source row
-    // row_src ? row_src[r] : r of b_src ([*, K] bf16)
+    // token side (B operand): row r of the group row space is row r of b_src ([*, K] bf16),
+    // loaded through the B tensor map
     const void *b_src;
-    const int32_t *row_src;
     int K;
     // groups: group_rows [G+1] row offsets and group_tiles [G+1] token-tile prefix, both on the
     // device; or NULL for one group of M_single rows.
@@ -99,13 +98,16 @@ struct GemmArgs {
     // ftile*kFT of the shared matrix), its tiles are interleaved evenly among the routed ones,
     // and the combine epilogue stores its rows in place with weight 1
     bool shared_last;
+    // CTAs per cluster (0/1: none; 2: the CTAs of a pair take adjacent weight tiles of the same
+    // token tile, and each TMA-multicasts half of the token tile to both; the B tensor map's box
+    // then has tile_cap/2 rows)
+    int cluster;
 };
 
 // Launch the persistent grouped GEMM.  tm_a0 (and tm_a1 for EPI_SWIGLU: the up projection)
 // are 2-D tensor maps over the weight rows (64- or 128-row box, 64 columns); tm_b is a map over
 // the B rows ([rows, K], box of tile_cap rows x 64).  tm_s0 / tm_s1 are the shared expert's
 // weight maps, read for the last group when a.shared_last (pass any map otherwise).
-// Gathered B (row_src != NULL) is supported with EPI_SWIGLU only.
 cudaError_t launch_gemm(GemmEpi epi, const GemmArgs &a, const CUtensorMap &tm_a0, const CUtensorMap &tm_a1,
                         const CUtensorMap &tm_b, const CUtensorMap &tm_s0, const CUtensorMap &tm_s1, int kc,
                         cudaStream_t s);

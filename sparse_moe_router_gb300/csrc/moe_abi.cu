@@ -263,6 +263,11 @@ moe_status run_shared(const moe_config &c, const moe_weights &w, const uint16_t 
     return MOE_OK;
 }
 
+#ifndef MOE_GEMM_CLUSTER
+#define MOE_GEMM_CLUSTER 1
+#endif
+constexpr int kGemmCluster = MOE_GEMM_CLUSTER;  // CTAs per cluster of the routed GEMMs (1 or 2)
+
 // Routed experts, grouped: h rows (expert-sorted order) from the expert-sorted copy of x
 // (xp), then the down projection either stored per row in fp32 (y_rows, unfused) or weighted
 // and stored as bf16 rows in pair order (y_pairs[perm[r]] = bf16(row_w[r] * y)) for the
@@ -276,12 +281,16 @@ moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t 
     const uint64_t EI = (uint64_t)c.n_experts * c.inter;
     const uint64_t P = (uint64_t)T * c.top_k;
     const uint64_t rows = P + (with_shared ? (uint64_t)T : 0);
+    // pairs of CTAs share each token tile (multicast) when the weight tiles come in pairs:
+    // always for gate/up (I / 64 is even), for the down projection when H / 128 is even
+    const int cl_gu = kGemmCluster;
+    const int cl_dn = (c.hidden / kTileM) % 2 == 0 ? kGemmCluster : 1;
     CUtensorMap tg, tu, td, tx, th, tsg, tsu, tsd;
     if (!encode_tmap_2d_bf16(&tg, w.w_gate, EI, c.hidden, kTileM / 2, 64) ||
         !encode_tmap_2d_bf16(&tu, w.w_up, EI, c.hidden, kTileM / 2, 64) ||
         !encode_tmap_2d_bf16(&td, w.w_down, (uint64_t)c.n_experts * c.hidden, c.inter, kTileM, 64) ||
-        !encode_tmap_2d_bf16(&tx, xp, rows, c.hidden, kTileN, 64) ||
-        !encode_tmap_2d_bf16(&th, h, rows, c.inter, kTileN, 64))
+        !encode_tmap_2d_bf16(&tx, xp, rows, c.hidden, kTileN / cl_gu, 64) ||
+        !encode_tmap_2d_bf16(&th, h, rows, c.inter, kTileN / cl_dn, 64))
         return MOE_ERR_CUDA;
     if (with_shared) {
         if (!encode_tmap_2d_bf16(&tsg, w.ws_gate, c.shared_inter, c.hidden, kTileM / 2, 64) ||
@@ -307,6 +316,7 @@ moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t 
     a.ld = c.inter;
     a.status = status;
     a.shared_last = with_shared;
+    a.cluster = cl_gu;
     MOE_CUDA(launch_gemm(EPI_SWIGLU, a, tg, tu, tx, tsg, tsu, KC_GATEUP_GEMM, s));
     GemmArgs d{};
     d.b_src = h;
@@ -318,6 +328,7 @@ moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t 
     d.ld = c.hidden;
     d.status = status;
     d.shared_last = with_shared;
+    d.cluster = cl_dn;
     if (y_rows) {
         if (with_shared) return MOE_ERR_INVALID_ARG;
         d.out = y_rows;
