@@ -77,47 +77,67 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Lane-partial dot products of two weight rows with the shared-memory vector xs (len bf16,
-// len % 8 == 0), eight 16-byte loads per row in flight per lane.
-__device__ __forceinline__ void dot2_rows(const uint16_t *r0, const uint16_t *r1, const uint4 *xs,
-                                          int len, int lane, float &a0, float &a1) {
-    const int n16 = len / 8;
+// The same for up to NT token vectors: token i of the list is xs + tl[i] * n16 (n of them).
+// One row load feeds every token; U loads per row stay in flight.
+template <int NT>
+__device__ __forceinline__ void dot2_rows_t(const uint16_t *r0, const uint16_t *r1, const uint4 *xs, int n16,
+                                            int lane, const int *tl, int n, float (&a0)[NT], float (&a1)[NT]) {
+    constexpr int U = 8;
     const uint4 *p0 = reinterpret_cast<const uint4 *>(r0);
     const uint4 *p1 = reinterpret_cast<const uint4 *>(r1);
     int c = lane;
-    for (; c + 32 * 7 < n16; c += 32 * 8) {
-        uint4 w0[8], w1[8];
+    for (; c + 32 * (U - 1) < n16; c += 32 * U) {
+        uint4 w0[U], w1[U];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < U; ++u) {
             w0[u] = ld_stream(p0 + c + 32 * u);
             w1[u] = ld_stream(p1 + c + 32 * u);
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const uint4 xv = xs[c + 32 * u];
-            a0 += dot8(w0[u], xv);
-            a1 += dot8(w1[u], xv);
-        }
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+                if (t < n) {
+                    const uint4 xv = xs[tl[t] * n16 + c + 32 * u];
+                    a0[t] += dot8(w0[u], xv);
+                    a1[t] += dot8(w1[u], xv);
+                }
     }
     for (; c < n16; c += 32) {
-        const uint4 xv = xs[c];
-        a0 += dot8(ld_stream(p0 + c), xv);
-        a1 += dot8(ld_stream(p1 + c), xv);
+        const uint4 w0 = ld_stream(p0 + c), w1 = ld_stream(p1 + c);
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+            if (t < n) {
+                const uint4 xv = xs[tl[t] * n16 + c];
+                a0[t] += dot8(w0, xv);
+                a1[t] += dot8(w1, xv);
+            }
     }
 }
 
-__device__ __forceinline__ void dot1_row(const uint16_t *r0, const uint4 *xs, int len, int lane, float &a0) {
-    const int n16 = len / 8;
+// One row against the first n (<= NT) token vectors of xs (token t at xs + t * n16).
+template <int NT>
+__device__ __forceinline__ void dot1_row_t(const uint16_t *r0, const uint4 *xs, int n16, int lane, int n,
+                                           float (&a0)[NT]) {
+    constexpr int U = NT == 1 ? 8 : 4;
     const uint4 *p0 = reinterpret_cast<const uint4 *>(r0);
     int c = lane;
-    for (; c + 32 * 7 < n16; c += 32 * 8) {
-        uint4 w0[8];
+    for (; c + 32 * (U - 1) < n16; c += 32 * U) {
+        uint4 w0[U];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) w0[u] = ld_stream(p0 + c + 32 * u);
+        for (int u = 0; u < U; ++u) w0[u] = ld_stream(p0 + c + 32 * u);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) a0 += dot8(w0[u], xs[c + 32 * u]);
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+                if (t < n) a0[t] += dot8(w0[u], xs[t * n16 + c + 32 * u]);
     }
-    for (; c < n16; c += 32) a0 += dot8(ld_stream(p0 + c), xs[c]);
+    for (; c < n16; c += 32) {
+        const uint4 w0 = ld_stream(p0 + c);
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+            if (t < n) a0[t] += dot8(w0, xs[t * n16 + c]);
+    }
 }
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
@@ -130,8 +150,9 @@ __device__ __forceinline__ uint16_t bf16_bits(float v) {
 __device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
 // ---------------------------------------------------------------------- kernel 1 --
+template <int NT>
 __global__ void __launch_bounds__(kK1Block) decode_k1_kernel(DecodeArgs a) {
-    extern __shared__ uint4 xs[];  // H bf16
+    extern __shared__ uint4 xs[];  // [T][H] bf16
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int task = blockIdx.x * kK1Warps + warp;
     // The weights do not depend on the previous kernel: start them towards L2 right away.
@@ -142,18 +163,27 @@ __global__ void __launch_bounds__(kK1Block) decode_k1_kernel(DecodeArgs a) {
     }
     pdl_launch_dependents();
     pdl_wait();  // x (and the accumulator's last reader) come from the previous kernels
+    const int n16 = a.H / 8;
     if (a.acc) {
         // clear the fp32 accumulator K2 adds into
-        for (int n = blockIdx.x * kK1Block + tid; n < a.H; n += gridDim.x * kK1Block) a.acc[n] = 0.f;
+        for (int n = blockIdx.x * kK1Block + tid; n < a.T * a.H; n += gridDim.x * kK1Block) a.acc[n] = 0.f;
     }
     const uint4 *xg = reinterpret_cast<const uint4 *>(a.x);
-    for (int i = tid; i < a.H / 8; i += kK1Block) xs[i] = xg[i];
+    for (int i = tid; i < a.T * n16; i += kK1Block) xs[i] = xg[i];
     __syncthreads();
     if (task < a.E) {
-        float s0 = 0.f;
-        dot1_row(a.w_router + (size_t)task * a.H, xs, a.H, lane, s0);
-        s0 = warp_sum(s0);
-        if (lane == 0) a.logits[task] = s0 + (a.b_router ? a.b_router[task] : 0.f);
+        // one pass over the router row for all T tokens
+        float sc[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) sc[t] = 0.f;
+        dot1_row_t<NT>(a.w_router + (size_t)task * a.H, xs, n16, lane, a.T, sc);
+        const float b = a.b_router ? a.b_router[task] : 0.f;
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+            if (t < a.T) {  // the same for the whole warp
+                const float v = warp_sum(sc[t]);
+                if (lane == 0) a.logits[(size_t)t * a.E + task] = v + b;
+            }
     }
 }
 
@@ -267,53 +297,71 @@ __device__ __forceinline__ void warp_topk(const float *logits, int E, int k, int
 }
 
 // 96 registers a thread (512 threads: 48K of the SM's 64K) leave room for a K1 block of the next
-// layer on the same SM, so the router spreads over the GPU instead of the few SMs K2 leaves idle.
-__global__ void __maxnreg__(96)
+// layer on the same SM, so the router spreads over the GPU instead of the few SMs K2 leaves idle
+// (with several tokens the gate/up accumulators need 128).
+//
+// T tokens (NT = 1, or 8 for 2 <= T <= 8).  Work items: the shared expert's 32-feature slices
+// first (a block whose first item is one starts its loads before K1 finishes), then one item per
+// (token t, slot j, slice).  A routed item works only for the first (token, slot) in token order
+// that selected its expert e, and then serves every token that selected e: the expert's
+// weights leave HBM once however many of the T tokens chose it; its other items are skipped.
+// Blocks walk items w = blockIdx.x + i * gridDim.x; the launch gives every item its own block.
+template <int NT>
+__global__ void __maxnreg__(NT == 1 ? 96 : 128)
     decode_k2_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tm_down,
-                     const __grid_constant__ CUtensorMap tm_sdown, int n_routed_blocks) {
+                     const __grid_constant__ CUtensorMap tm_sdown, int n_shared_blocks) {
     extern __shared__ uint8_t smem_raw[];
     // TMA destinations: align the dynamic shared memory up to 1024 bytes (the launch adds slack)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint16_t *wd = reinterpret_cast<uint16_t *>(smem);                           // [kChunkRows][kSlice]
-    uint4 *xs = reinterpret_cast<uint4 *>(smem + (size_t)kChunkRows * kSlice * 2);  // [H] bf16
-    float *hsl = reinterpret_cast<float *>(xs + a.H / 8);                        // [kSlice] fp32
-    __shared__ int s_ids[32];
-    __shared__ float s_w[32];
+    uint4 *xs = reinterpret_cast<uint4 *>(smem + (size_t)kChunkRows * kSlice * 2);  // [T][H] bf16
+    float *hsl = reinterpret_cast<float *>(xs + (size_t)a.T * (a.H / 8));          // [NT][kSlice] fp32
+    __shared__ int s_ids[kMaxDecodeT][32];
+    __shared__ float s_w[kMaxDecodeT][32];
     __shared__ float s_lg[1024];       // logits staging for E > 256
     __shared__ unsigned s_chosen[32];
+    __shared__ int s_tl[kMaxDecodeT];  // tokens this block serves, and their routing weights
+    __shared__ float s_tw[kMaxDecodeT];
+    __shared__ int s_n;
     __shared__ __align__(8) uint64_t bar;
     __shared__ int s_last;
     __shared__ int s_ok;
     __shared__ int s_abort;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const bool shared_task = (int)blockIdx.x >= n_routed_blocks;
+    const int T = a.T;
+    const int n16 = a.H / 8;
     const int slices = a.I / kSlice;
-    const int slot = shared_task ? 0 : (int)blockIdx.x / slices;
-    const int i0 = shared_task ? ((int)blockIdx.x - n_routed_blocks) * kSlice : ((int)blockIdx.x % slices) * kSlice;
-    const CUtensorMap *tm = shared_task ? &tm_sdown : &tm_down;
+    const int n_items = n_shared_blocks + T * a.k * slices;  // shared slices, then routed
+    // item w: shared slice w, or routed (token, slot, slice) w - n_shared_blocks
+    auto item_shared = [&](int w) { return w < n_shared_blocks; };
+    auto item_i0 = [&](int w) { return w < n_shared_blocks ? w * kSlice : ((w - n_shared_blocks) % slices) * kSlice; };
+    const int w0 = (int)blockIdx.x;  // this block's first item (blocks <= items)
     if (tid == 0) {
         ptx::mbar_init(&bar, 1);
         s_ok = 1;
         s_abort = 0;
         ptx::fence_mbar_init();
-        ptx::tma_prefetch_desc(tm);
+        ptx::tma_prefetch_desc(&tm_down);
+        ptx::tma_prefetch_desc(&tm_sdown);
     }
     pdl_launch_dependents();
     __syncthreads();
-    // TMA of rows [r0, r0 + rows) of the slice's columns into shared memory, on `bar`; run by a
+    // TMA of rows [r0, r0 + rows) of a slice's columns into shared memory, on `bar`; run by a
     // whole warp: lane 0 posts the byte count, then lane b issues box b (at most 16 boxes)
     constexpr int kLoadWarp = kK2Warps - 1;
-    auto load_chunk = [&](int base_row, int r0, int rows) {
+    auto load_chunk = [&](const CUtensorMap *tm, int i0, int base_row, int r0, int rows) {
         if (lane == 0) ptx::mbar_arrive_expect_tx(&bar, (uint32_t)(rows * kSlice * 2));
         __syncwarp();
         if (lane < rows / kBoxRows)
             ptx::tma_load_2d(wd + (size_t)lane * kBoxRows * kSlice, tm, i0, base_row + r0 + lane * kBoxRows, &bar);
     };
     const int rows0 = a.H < kChunkRows ? a.H : kChunkRows;
-    if (shared_task) {
-        // the shared expert's weights do not depend on the routing: start its down columns
-        // into shared memory and its gate/up rows into L2 before waiting for K1
-        if (warp == kLoadWarp) load_chunk(0, 0, rows0);
+    const bool first_shared = item_shared(w0);
+    if (first_shared) {
+        // the shared expert's weights do not depend on the routing: start the first item's down
+        // columns into shared memory and its gate/up rows into L2 before waiting for K1
+        const int i0 = item_i0(w0);
+        if (warp == kLoadWarp) load_chunk(&tm_sdown, i0, 0, 0, rows0);
         const int row_bytes = a.H * 2;
         for (int f = warp; f < kSlice; f += kK2Warps) {
             const char *g = reinterpret_cast<const char *>(a.ws_gate + (size_t)(i0 + f) * a.H);
@@ -325,63 +373,132 @@ __global__ void __maxnreg__(96)
         }
     }
     pdl_wait();  // x, the logits and the cleared accumulator come after K1
-    if (warp == 0 && !shared_task) warp_topk(a.logits, a.E, a.k, s_ids, s_w, s_lg, s_chosen);
+    if (n_items > n_shared_blocks) {
+        // every token's top-k: one warp per token (warp 0 for all of them above 256 experts,
+        // whose selection stages the logits in shared memory)
+        if (a.E <= 256) {
+            if (warp < T) warp_topk(a.logits + (size_t)warp * a.E, a.E, a.k, s_ids[warp], s_w[warp], s_lg, s_chosen);
+        } else if (warp == 0) {
+            for (int t = 0; t < T; ++t) warp_topk(a.logits + (size_t)t * a.E, a.E, a.k, s_ids[t], s_w[t], s_lg, s_chosen);
+        }
+    }
     const uint4 *xg = reinterpret_cast<const uint4 *>(a.x);
-    for (int i = tid; i < a.H / 8; i += kK2Threads) xs[i] = xg[i];
+    for (int i = tid; i < T * n16; i += kK2Threads) xs[i] = xg[i];
     __syncthreads();
-    float wj = 1.f;
-    int base_row = 0;  // first row of this block's weight matrix in the tensor map
-    const uint16_t *wg = a.ws_gate, *wu = a.ws_up;  // shared expert: rows i0.. of [Is, H]
-    if (!shared_task) {
-        const int e = s_ids[slot];
-        wj = s_w[slot];
-        base_row = e * a.H;
-        if (warp == kLoadWarp) load_chunk(base_row, 0, rows0);
-        wg = a.w_gate + (size_t)e * a.I * a.H;
-        wu = a.w_up + (size_t)e * a.I * a.H;
-    }
-    // h for features i0 .. i0+31: 16 warps x 2 features (gate and up rows)
-    for (int f = warp; f < kSlice; f += kK2Warps) {
-        const size_t row = (size_t)(i0 + f);
-        float g = 0.f, u = 0.f;
-        dot2_rows(wg + row * a.H, wu + row * a.H, xs, a.H, lane, g, u);
-        g = warp_sum(g);
-        u = warp_sum(u);
-        if (lane == 0) hsl[f] = __bfloat162float(__float2bfloat16_rn(silu_mul(g, u)));
-    }
-    // split-K partial of the down projection, chunk by chunk: rows n of the chunk, 32 columns
-    // each from shared memory (chunk order rotated per row against bank conflicts)
-    for (int r0 = 0, ph = 0; r0 < a.H; r0 += kChunkRows, ph ^= 1) {
-        const int rows = (a.H - r0) < kChunkRows ? (a.H - r0) : kChunkRows;
-        if (tid == 0 && !ptx::mbar_wait(&bar, (uint32_t)ph, kWaitLimitNs, (volatile int *)&s_abort)) s_ok = 0;
+    uint32_t ph = 0;  // parity of the next chunk load on `bar`
+    for (int w = w0; w < n_items && s_ok; w += (int)gridDim.x) {
+        const bool shared_task = item_shared(w);
+        const int i0 = item_i0(w);
+        const int rb = w - n_shared_blocks;  // routed item index
+        const int tok = shared_task ? 0 : rb / (a.k * slices);
+        const int slot = shared_task ? 0 : (rb / slices) % a.k;
+        if (warp == 0) {
+            // the tokens this item serves: pair p = t*k + j (32 per round, T*k <= 4*32) holds token
+            // t's slot-j expert; the item works when (tok, slot) is the expert's first pair
+            if (shared_task) {
+                if (lane < T) {
+                    s_tl[lane] = lane;
+                    s_tw[lane] = 1.f;
+                }
+                if (lane == 0) s_n = T;
+            } else {
+                const int e = s_ids[tok][slot];
+                const int pme = tok * a.k + slot;  // this item's pair
+                int base = 0;
+                bool first = true;  // no earlier pair selected e (the same for the whole warp)
+                for (int half = 0; 32 * half < T * a.k; ++half) {
+                    const int pp = lane + 32 * half;
+                    const bool hit = pp < T * a.k && s_ids[pp / a.k][pp % a.k] == e;
+                    const unsigned m = __ballot_sync(0xffffffffu, hit);
+                    const int lo = pme - 32 * half;  // this round's pairs before pme: bits [0, lo)
+                    const unsigned before = lo <= 0 ? 0u : (lo >= 32 ? 0xffffffffu : ((1u << lo) - 1u));
+                    if (m & before) first = false;
+                    const unsigned later = m & ~before;  // pairs from pme on: one per token at most
+                    if ((later >> lane) & 1u) {
+                        const int rank = base + __popc(later & ((1u << lane) - 1u));
+                        s_tl[rank] = pp / a.k;
+                        s_tw[rank] = s_w[pp / a.k][pp % a.k];
+                    }
+                    base += __popc(later);
+                }
+                if (lane == 0) s_n = first ? base : 0;
+            }
+        }
         __syncthreads();
-        if (!s_ok) break;
-        // rows is a multiple of 128, so every warp runs the same number of iterations
-        for (int n = tid; n < rows; n += kK2Threads) {
-            const uint4 *rw = reinterpret_cast<const uint4 *>(wd + (size_t)n * kSlice);
-            float acc = 0.f;
+        const int nt = s_n;  // 0: another item serves this expert
+        if (nt == 0) {
+            __syncthreads();  // s_n is rewritten by the next item
+            continue;
+        }
+        const CUtensorMap *tm = shared_task ? &tm_sdown : &tm_down;
+        int base_row = 0;  // first row of this item's weight matrix in its tensor map
+        const uint16_t *wg = a.ws_gate, *wu = a.ws_up;  // shared expert: rows i0.. of [Is, H]
+        if (!shared_task) {
+            const int e = s_ids[tok][slot];
+            base_row = e * a.H;
+            wg = a.w_gate + (size_t)e * a.I * a.H;
+            wu = a.w_up + (size_t)e * a.I * a.H;
+        }
+        if (!(w == w0 && first_shared) && warp == kLoadWarp) load_chunk(tm, i0, base_row, 0, rows0);
+        // h for features i0 .. i0+31 and each served token: 16 warps x 2 features
+        for (int f = warp; f < kSlice; f += kK2Warps) {
+            const size_t row = (size_t)(i0 + f);
+            float g[NT], u[NT];
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const int c = (cc + (n >> 1)) & 3;
-                const uint4 q = rw[c];
-                const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&q);
+            for (int t = 0; t < NT; ++t) g[t] = u[t] = 0.f;
+            dot2_rows_t<NT>(wg + row * a.H, wu + row * a.H, xs, n16, lane, s_tl, nt, g, u);
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const float2 f = __bfloat1622float2(b[m]);
-                    acc = fmaf(f.x, hsl[c * 8 + 2 * m], acc);
-                    acc = fmaf(f.y, hsl[c * 8 + 2 * m + 1], acc);
+            for (int t = 0; t < NT; ++t)
+                if (t < nt) {  // the same for the whole warp
+                    const float gs = warp_sum(g[t]), us = warp_sum(u[t]);
+                    if (lane == 0) hsl[t * kSlice + f] = __bfloat162float(__float2bfloat16_rn(silu_mul(gs, us)));
+                }
+        }
+        // split-K partial of the down projection, chunk by chunk: rows n of the chunk, 32 columns
+        // each from shared memory (chunk order rotated per row against bank conflicts)
+        for (int r0 = 0; r0 < a.H; r0 += kChunkRows, ph ^= 1u) {
+            const int rows = (a.H - r0) < kChunkRows ? (a.H - r0) : kChunkRows;
+            if (tid == 0 && !ptx::mbar_wait(&bar, ph, kWaitLimitNs, (volatile int *)&s_abort)) s_ok = 0;
+            __syncthreads();
+            if (!s_ok) break;
+            // rows is a multiple of 128, so every warp runs the same number of iterations
+            for (int n = tid; n < rows; n += kK2Threads) {
+                const uint4 *rw = reinterpret_cast<const uint4 *>(wd + (size_t)n * kSlice);
+                // the row's four 16-byte chunks, read in an order rotated per row (against bank
+                // conflicts); chunk cc of q holds features 8*((cc + n/2) % 4) ..
+                uint4 q[4];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) q[cc] = rw[(cc + (n >> 1)) & 3];
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    if (t >= nt) break;  // the same for the whole block
+                    float acc = 0.f;
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const int c = (cc + (n >> 1)) & 3;
+                        const __nv_bfloat162 *bq = reinterpret_cast<const __nv_bfloat162 *>(&q[cc]);
+                        const float *hf = hsl + t * kSlice + c * 8;
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const float2 fv = __bfloat1622float2(bq[m]);
+                            acc = fmaf(fv.x, hf[2 * m], acc);
+                            acc = fmaf(fv.y, hf[2 * m + 1], acc);
+                        }
+                    }
+                    // lanes 4q..4q+3 hold rows n..n+3: one 16-byte reduction per four rows
+                    const float v1 = __shfl_down_sync(0xffffffffu, acc, 1);
+                    const float v2 = __shfl_down_sync(0xffffffffu, acc, 2);
+                    const float v3 = __shfl_down_sync(0xffffffffu, acc, 3);
+                    const float wt = s_tw[t];
+                    if ((lane & 3) == 0)
+                        ptx::red_add_v4(&a.acc[(size_t)s_tl[t] * a.H + r0 + n], wt * acc, wt * v1, wt * v2, wt * v3);
                 }
             }
-            // lanes 4q..4q+3 hold rows n..n+3: one 16-byte reduction per four rows
-            const float v1 = __shfl_down_sync(0xffffffffu, acc, 1);
-            const float v2 = __shfl_down_sync(0xffffffffu, acc, 2);
-            const float v3 = __shfl_down_sync(0xffffffffu, acc, 3);
-            if ((lane & 3) == 0) ptx::red_add_v4(&a.acc[r0 + n], wj * acc, wj * v1, wj * v2, wj * v3);
-        }
-        __syncthreads();  // the chunk buffer is free again
-        if (r0 + kChunkRows < a.H && warp == kLoadWarp) {
-            const int next = (a.H - r0 - kChunkRows) < kChunkRows ? (a.H - r0 - kChunkRows) : kChunkRows;
-            load_chunk(base_row, r0 + kChunkRows, next);
+            __syncthreads();  // the chunk buffer, hsl and the token list are free again
+            if (r0 + kChunkRows < a.H && warp == kLoadWarp) {
+                const int next = (a.H - r0 - kChunkRows) < kChunkRows ? (a.H - r0 - kChunkRows) : kChunkRows;
+                load_chunk(tm, i0, base_row, r0 + kChunkRows, next);
+            }
         }
     }
     if (!s_ok && tid == 0 && a.status) atomicCAS(a.status, 0, (int)MOE_ERR_TIMEOUT);
@@ -396,7 +513,7 @@ __global__ void __maxnreg__(96)
     if (!s_last) return;
     __threadfence();
     // four outputs a thread: one 16-byte accumulator load, 8-byte bf16 loads and stores
-    for (int n4 = tid; n4 < a.H / 4; n4 += kK2Threads) {
+    for (int n4 = tid; n4 < T * a.H / 4; n4 += kK2Threads) {
         const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.acc) + n4);
         const float vv[4] = {v.x, v.y, v.z, v.w};
         uint16_t o[4];
@@ -432,7 +549,29 @@ cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, size_t smem, cudaS
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
-size_t k2_smem(int H) { return 1024 + (size_t)kChunkRows * kSlice * 2 + (size_t)H * 2 + kSlice * 4; }
+size_t k2_smem(int T, int H, int nt) {
+    return 1024 + (size_t)kChunkRows * kSlice * 2 + (size_t)T * H * 2 + (size_t)nt * kSlice * 4;
+}
+
+// Shared-memory limits of both instantiations (T = 1 up to H = 16384; T <= 8 with T*H <= 32768).
+cudaError_t decode_attrs() {
+    static bool done[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && done[dev]) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(decode_k2_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)k2_smem(1, 16384, 1));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(decode_k2_kernel<kMaxDecodeT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)k2_smem(1, kMaxDecodeTH, kMaxDecodeT));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(decode_k1_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 32 * 1024);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(decode_k1_kernel<kMaxDecodeT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kMaxDecodeTH * 2);
+    if (e == cudaSuccess && dev < 64) done[dev] = true;
+    return e;
+}
 
 }  // namespace
 
@@ -440,46 +579,46 @@ int decode_slice() { return kSlice; }
 int decode_box_rows() { return kBoxRows; }
 
 cudaError_t launch_decode_router(const DecodeArgs &a, cudaStream_t s) {
+    if (!decode_fits(a.T, a.H)) return cudaErrorInvalidValue;
+    const cudaError_t e = decode_attrs();
+    if (e != cudaSuccess) return e;
     DecodeArgs r = a;
     r.acc = nullptr;  // router rows only, no accumulator to clear
     LaunchScope scope(KC_DECODE_ROUTER, s);
-    decode_k1_kernel<<<(r.E + kK1Warps - 1) / kK1Warps, kK1Block, (size_t)r.H * 2, s>>>(r);
+    const dim3 grid((r.E + kK1Warps - 1) / kK1Warps);
+    const size_t smem = (size_t)r.T * r.H * 2;
+    if (r.T == 1) decode_k1_kernel<1><<<grid, kK1Block, smem, s>>>(r);
+    else decode_k1_kernel<kMaxDecodeT><<<grid, kK1Block, smem, s>>>(r);
     return cudaGetLastError();
 }
 
 cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &tm_down, const CUtensorMap &tm_sdown,
                           cudaStream_t s) {
-    static bool attr_done[64] = {false};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !attr_done[dev]) {
-        // largest supported H (16384): 128 KB of slice columns + 32 KB of x
-        cudaError_t e = cudaFuncSetAttribute(decode_k2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)k2_smem(16384));
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(decode_k1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 32 * 1024);
-        if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
-    }
+    if (!decode_fits(a.T, a.H)) return cudaErrorInvalidValue;
+    cudaError_t e = decode_attrs();
+    if (e != cudaSuccess) return e;
+    const bool one = a.T == 1;
     {
         DecodeArgs k1 = a;
-        const int tasks = a.E;
         void *args[] = {&k1};
         LaunchScope scope(KC_DECODE_ROUTER, s);
-        const cudaError_t e = launch_pdl(reinterpret_cast<const void *>(decode_k1_kernel),
-                                         dim3((tasks + kK1Warps - 1) / kK1Warps), dim3(kK1Block),
-                                         (size_t)a.H * 2, s, args);
+        e = launch_pdl(one ? reinterpret_cast<const void *>(decode_k1_kernel<1>)
+                           : reinterpret_cast<const void *>(decode_k1_kernel<kMaxDecodeT>),
+                       dim3((a.E + kK1Warps - 1) / kK1Warps), dim3(kK1Block), (size_t)a.T * a.H * 2, s, args);
         if (e != cudaSuccess) return e;
     }
     {
         DecodeArgs k2 = a;
-        int n_routed = a.k * (a.I / kSlice);
-        const int blocks = n_routed + a.Is / kSlice;
+        int n_shared = a.Is / kSlice;
+        // one block per item: with one block per SM resident, a finished item's SM takes the next
+        // item at once (measured faster than blocks that walk several items)
+        const int blocks = a.T * a.k * (a.I / kSlice) + n_shared;
         CUtensorMap m0 = tm_down, m1 = tm_sdown;
-        void *args[] = {&k2, &m0, &m1, &n_routed};
+        void *args[] = {&k2, &m0, &m1, &n_shared};
         LaunchScope scope(KC_DECODE_EXPERTS, s);
-        return launch_pdl(reinterpret_cast<const void *>(decode_k2_kernel), dim3(blocks), dim3(kK2Threads),
-                          k2_smem(a.H), s, args);
+        return launch_pdl(one ? reinterpret_cast<const void *>(decode_k2_kernel<1>)
+                              : reinterpret_cast<const void *>(decode_k2_kernel<kMaxDecodeT>),
+                          dim3(blocks), dim3(kK2Threads), k2_smem(a.T, a.H, one ? 1 : kMaxDecodeT), s, args);
     }
 }
 

@@ -414,10 +414,11 @@ moe_status moe_route(const moe_config *cfg, const moe_weights *w, const moe_bf16
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const Layout L = layout(*cfg, T);
     float *logits = logits_out ? logits_out : at<float>(ws, L.logits);
-    if (T == 1) {
-        // one token: the decode path's GEMV, so the reported logits are the ones moe_forward
-        // selects on for T == 1
+    if (decode_fits(T, cfg->hidden)) {
+        // a few tokens: the decode path's GEMV, so the reported logits are the ones moe_forward
+        // selects on for such T
         DecodeArgs a{};
+        a.T = T;
         a.H = cfg->hidden;
         a.E = cfg->n_experts;
         a.x = x;
@@ -532,9 +533,12 @@ moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const moe_bf
     MOE_TRY(check_ws(cfg, ws, ws_bytes, Tmax));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int H = cfg->hidden;
-    if (T == 1) {
-        const Layout L = layout(*cfg, 1);
+    if (decode_fits(T, H)) {
+        // up to kMaxDecodeT tokens: router GEMV, then each selected expert's weights streamed once
+        // for all tokens that chose it
+        const Layout L = layout(*cfg, T);
         DecodeArgs a{};
+        a.T = T;
         a.H = H;
         a.E = cfg->n_experts;
         a.k = cfg->top_k;
@@ -579,9 +583,9 @@ moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const moe_bf
     for (int i = 0; i < n; ++i) {
         const int Tp = pieces[i];
         uint16_t *xn = x_next ? x_next + t0 * H : nullptr;
-        if (Tp == 1) {
-            // a one-token tail takes the decode path of the same layer
-            MOE_TRY(moe_forward(cfg, w, x + t0 * H, 1, out + t0 * H, resid + t0 * H, xn, ws, ws_bytes,
+        if (decode_fits(Tp, H)) {
+            // a tail of a few tokens takes the decode path of the same layer
+            MOE_TRY(moe_forward(cfg, w, x + t0 * H, Tp, out + t0 * H, resid + t0 * H, xn, ws, ws_bytes,
                                 stream));
         } else {
             MOE_TRY(forward_piece(*cfg, *w, x + t0 * H, Tp, out + t0 * H, resid + t0 * H, xn, ws, s));

@@ -201,3 +201,31 @@ def test_forward_is_bit_reproducible():
     a, _ = forward_gpu(shape, layers[0], x)
     b, _ = forward_gpu(shape, layers[0], x)
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("T", [2, 3, 4, 5, 8])
+def test_small_batch_decode_layer_shape(T):
+    """2..4 tokens take the decode path (each selected expert's weights streamed once for every
+    token that chose it), 5 and more the prefill path: parity at the 2048-wide, 256-expert top-8
+    shape on both sides of the switch."""
+    shape = inputs.Shape(2048, 256, 8, 512, 512)
+    layers, x = make(shape, T, seed=40 + T)
+    check_layer(shape, layers[0], x)
+
+
+def test_small_batch_decode_repeated_tokens():
+    """Identical token rows select identical experts: one block serves all of them."""
+    shape = inputs.Shape(2048, 256, 8, 512, 512)
+    layers, x = make(shape, 4, seed=47)
+    x = x[torch.tensor([0, 1, 0, 0], device=x.device)].contiguous()
+    check_layer(shape, layers[0], x)
+    out, _ = forward_gpu(shape, layers[0], x)
+    # rows 0, 2, 3 are the same token: the same output within the fp32 summation order
+    compare_out(u16(out)[[2, 3]], u16(out)[[0, 0]])
+
+
+@pytest.mark.parametrize("shape,T", [(inputs.Shape(256, 600, 8, 128, 128), 3), (TINY, 4), (TINY, 2),
+                                     (inputs.Shape(256, 64, 32, 128, 128), 3)])
+def test_small_batch_decode_other_shapes(shape, T):
+    layers, x = make(shape, T, seed=60 + T)
+    check_layer(shape, layers[0], x)
