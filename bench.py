@@ -323,47 +323,56 @@ def run_decode(args, dev, pg, peaks):
     shape, L = wl.shape, wl.n_layers
     layers, x0 = inputs.make(wl, device=dev)
     cfg = abi.config_of(shape)
-    ws = abi.alloc_workspace(cfg, 1)
     wts = [abi.weights(l) for l in layers]
-    bufs = [x0.clone(), torch.empty_like(x0), torch.empty_like(x0)]
-    out = torch.empty_like(x0)
     s = torch.cuda.Stream(device=dev)
 
-    def chain():
-        # layer l+1 reads bf16(x_0 + out_l), fused into the layer's last kernel
-        x = bufs[0]
-        for l in range(L):
-            nxt = bufs[1 + (l % 2)]
-            abi.moe_forward(cfg, wts[l], x, 1, out, nxt, ws, s, resid=bufs[0])
-            x = nxt
+    def graph_time(x_start):
+        """Median time of the 40-layer chain for x_start's tokens, captured as one CUDA graph."""
+        T = x_start.shape[0]
+        ws = abi.alloc_workspace(cfg, T)
+        bufs = [x_start.clone(), torch.empty_like(x_start), torch.empty_like(x_start)]
+        out = torch.empty_like(x_start)
 
-    with torch.cuda.stream(s):
-        for _ in range(3):
-            chain()
-    torch.cuda.synchronize()
-    assert abi.moe_check_status(ws) == 0
-    # capture the 40-layer chain as one graph
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(s):
-        with torch.cuda.graph(g, stream=s):
-            chain()
-    torch.cuda.synchronize()
-    reps = max(5, args.steps)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    times = []
-    n_launch0 = abi.moe_launch_count()
-    with torch.cuda.stream(s):   # replay() launches on the current stream: time on that stream
-        for _ in range(max(3, args.warmup)):
-            g.replay()
+        def chain():
+            # layer l+1 reads bf16(x_0 + out_l), fused into the layer's last kernel
+            x = bufs[0]
+            for l in range(L):
+                nxt = bufs[1 + (l % 2)]
+                abi.moe_forward(cfg, wts[l], x, T, out, nxt, ws, s, resid=bufs[0])
+                x = nxt
+
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                chain()
         torch.cuda.synchronize()
-        for _ in range(reps):
-            e0.record(s)
-            g.replay()
-            e1.record(s)
-            e1.synchronize()
-            times.append(e0.elapsed_time(e1))
-    assert abi.moe_launch_count() == n_launch0  # replays launch from the graph, not the library
+        assert abi.moe_check_status(ws) == 0
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                chain()
+        torch.cuda.synchronize()
+        reps = max(5, args.steps)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        times = []
+        n_launch0 = abi.moe_launch_count()
+        with torch.cuda.stream(s):   # replay() launches on the current stream: time on that stream
+            for _ in range(max(3, args.warmup)):
+                g.replay()
+            torch.cuda.synchronize()
+            for _ in range(reps):
+                e0.record(s)
+                g.replay()
+                e1.record(s)
+                e1.synchronize()
+                times.append(e0.elapsed_time(e1))
+        assert abi.moe_launch_count() == n_launch0  # replays launch from the graph, not the library
+        assert abi.moe_check_status(ws) == 0
+        del g
+        return times, chain
+
+    times, chain = graph_time(x0)
+    reps = len(times)
     t_med = statistics.median(times)
     t_med = _max_over_ranks(pg, t_med, dev)
     us_layer = 1e3 * t_med / L
@@ -380,7 +389,14 @@ def run_decode(args, dev, pg, peaks):
         n, ms = abi.timing_read(name)
         if n:
             split[name] = {"launches": n, "avg_us": round(1e3 * ms / n, 2)}
-    del g
+    # a few tokens at once (multi-token prediction, speculative verification): 2..4 tokens take
+    # the decode path, each selected expert streamed once for all tokens that chose it
+    small = []
+    for T in (2, 3, 4):
+        _, xT = inputs.make(inputs.custom(shape, T=T, seed=100 + T), device=dev, n_layers=0)
+        tT = _max_over_ranks(pg, statistics.median(graph_time(xT)[0]), dev)
+        small.append({"T": T, "us_per_layer": round(1e3 * tT / L, 3),
+                      "tokens_per_s": round(T * L / (tT * 1e-3), 1)})
     return {"workload": "decode T=1, 40 distinct layers (64.7 GB of weights), CUDA graph",
             "us_per_layer": round(us_layer, 3), "graph_ms": round(t_med, 4), "reps": reps,
             "p10_p90_ms": [round(sorted(times)[len(times) // 10], 4),
@@ -389,7 +405,7 @@ def run_decode(args, dev, pg, peaks):
                          "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
                          "frac_of_8000": round(gbs / 8000.0, 4), "bytes_per_layer": nbytes,
                          "traffic": None, "peak_source": peaks["source"] + " hbm copy"},
-            "eager_kernel_avg_us": split}
+            "eager_kernel_avg_us": split, "small_batch": small}
 
 
 def cpu_baseline(wl, seconds=12.0):

@@ -94,7 +94,9 @@ size_t moe_workspace_size(const moe_config *cfg, int max_T);
  * x [T,H] bf16 -> topk_ids [T,k] int32 and topk_w [T,k] fp32, slots in descending logit
  * order.  logits_out [T,E] fp32 may be NULL; when given it receives the exact fp32 logits the
  * selection used.  ws: workspace of moe_workspace_size(cfg, T) bytes (holds the logits when
- * logits_out is NULL).  Computed on tensor cores (bf16 x bf16 -> fp32 accumulate). */
+ * logits_out is NULL).  Computed on tensor cores (bf16 x bf16 -> fp32 accumulate); for the
+ * 1 to 4 tokens moe_forward runs on the decode path, by that path's GEMV, so the logits are
+ * the ones moe_forward selects on. */
 moe_status moe_route(const moe_config *cfg, const moe_weights *w, const moe_bf16 *x, int T,
                      float *logits_out, int32_t *topk_ids, float *topk_w, void *ws,
                      size_t ws_bytes, void *stream);
@@ -149,14 +151,16 @@ moe_status moe_combine(const moe_config *cfg, const float *y_rows, const int32_t
 
 /* The whole layer, fused: x [T,H] -> out [T,H] bf16.  T is split greedily into pieces of
  * 8192, 4096, 2048 and 1024 tokens and an exact tail (no padding); every piece runs the same
- * kernels, so the result equals the concatenation of per-piece calls.  T == 1 takes the
- * decode path (HBM-streaming GEMVs).  x_next may be NULL; when given it receives
- * bf16(resid + out), the residual-stream update of a layer stack, fused into the last
- * kernel; resid [T,H] may be NULL, meaning x.  x_next may alias resid (not x, when they
- * differ).  ws: moe_workspace_size(cfg, T) bytes.  Rounding: h is rounded to bf16 once, each
- * weighted expert row w*y is stored as bf16 and the k rows of a token are summed in fp32 in
- * slot order with the shared expert's fp32 row, and the sum is rounded to bf16 once.  No
- * atomics: the result is bit-reproducible. */
+ * kernels, so the result equals the concatenation of per-piece calls.  A call (or tail) of 1
+ * to 4 tokens with T*H <= 32768 takes the decode path: a router GEMV, then every selected
+ * expert's weights streamed once for all the tokens that chose it, its partial products
+ * added in fp32 with atomics (so not bit-reproducible) and rounded to bf16 once.  x_next may
+ * be NULL; when given it receives bf16(resid + out), the residual-stream update of a layer
+ * stack, fused into the last kernel; resid [T,H] may be NULL, meaning x.  x_next may alias
+ * resid (not x, when they differ).  ws: moe_workspace_size(cfg, T) bytes.  Rounding on the
+ * prefill path: h is rounded to bf16 once, each weighted expert row w*y (and the shared
+ * expert's row) is stored as bf16, the k+1 rows of a token are summed in fp32 in slot order,
+ * and the sum is rounded to bf16 once.  No atomics there: the result is bit-reproducible. */
 moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const moe_bf16 *x, int T,
                        moe_bf16 *out, const moe_bf16 *resid, moe_bf16 *x_next, void *ws,
                        size_t ws_bytes, void *stream);
