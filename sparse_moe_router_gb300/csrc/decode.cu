@@ -296,7 +296,7 @@ __device__ __forceinline__ void warp_topk(const float *logits, int E, int k, int
     else warp_topk_smem(logits, E, k, s_ids, s_w, lg, chosen);
 }
 
-// 96 registers a thread (512 threads: 48K of the SM's 64K) leave room for a K1 block of the next
+// 104 registers a thread (512 threads: 52K of the SM's 64K) leave room for a K1 block of the next
 // layer on the same SM, so the router spreads over the GPU instead of the few SMs K2 leaves idle
 // (with several tokens the gate/up accumulators need 128).
 //
@@ -307,7 +307,7 @@ __device__ __forceinline__ void warp_topk(const float *logits, int E, int k, int
 // weights leave HBM once however many of the T tokens chose it; its other items are skipped.
 // Blocks walk items w = blockIdx.x + i * gridDim.x; the launch gives every item its own block.
 template <int NT>
-__global__ void __maxnreg__(NT == 1 ? 96 : 128)
+__global__ void __maxnreg__(NT == 1 ? 104 : 128)
     decode_k2_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tm_down,
                      const __grid_constant__ CUtensorMap tm_sdown, int n_shared_blocks) {
     extern __shared__ uint8_t smem_raw[];
@@ -382,6 +382,15 @@ __global__ void __maxnreg__(NT == 1 ? 96 : 128)
             for (int t = 0; t < T; ++t) warp_topk(a.logits + (size_t)t * a.E, a.E, a.k, s_ids[t], s_w[t], s_lg, s_chosen);
         }
     }
+    if (NT == 1 && warp == 0) {
+        // one token (one item per block): the item serves that token, with no duplicates to skip
+        __syncwarp();  // s_w of the top-k above, written by other lanes
+        if (lane == 0) {
+            s_tl[0] = 0;
+            s_tw[0] = item_shared(w0) ? 1.f : s_w[0][((w0 - n_shared_blocks) / slices) % a.k];
+            s_n = 1;
+        }
+    }
     const uint4 *xg = reinterpret_cast<const uint4 *>(a.x);
     for (int i = tid; i < T * n16; i += kK2Threads) xs[i] = xg[i];
     __syncthreads();
@@ -392,7 +401,7 @@ __global__ void __maxnreg__(NT == 1 ? 96 : 128)
         const int rb = w - n_shared_blocks;  // routed item index
         const int tok = shared_task ? 0 : rb / (a.k * slices);
         const int slot = shared_task ? 0 : (rb / slices) % a.k;
-        if (warp == 0) {
+        if (NT > 1 && warp == 0) {
             // the tokens this item serves: pair p = t*k + j (32 per round, T*k <= 4*32) holds token
             // t's slot-j expert; the item works when (tok, slot) is the expert's first pair
             if (shared_task) {
@@ -424,7 +433,7 @@ __global__ void __maxnreg__(NT == 1 ? 96 : 128)
                 if (lane == 0) s_n = first ? base : 0;
             }
         }
-        __syncthreads();
+        if (NT > 1) __syncthreads();
         const int nt = s_n;  // 0: another item serves this expert
         if (nt == 0) {
             __syncthreads();  // s_n is rewritten by the next item
@@ -502,16 +511,17 @@ __global__ void __maxnreg__(NT == 1 ? 96 : 128)
         }
     }
     if (!s_ok && tid == 0 && a.status) atomicCAS(a.status, 0, (int)MOE_ERR_TIMEOUT);
-    // last block: every other block's adds are in the accumulator
-    __threadfence();
+    // last block: every other block's adds are in the accumulator.  The block's reductions are
+    // ordered before thread 0's ticket by the barrier and the ticket's release; the last block
+    // sees all of them through the ticket's acquire.
     __syncthreads();
     if (tid == 0) {
-        const int ticket = atomicAdd(a.counter, 1);
+        int ticket;
+        asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(ticket) : "l"(a.counter) : "memory");
         s_last = (ticket == (int)gridDim.x - 1) ? 1 : 0;
     }
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
     // four outputs a thread: one 16-byte accumulator load, 8-byte bf16 loads and stores
     for (int n4 = tid; n4 < T * a.H / 4; n4 += kK2Threads) {
         const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.acc) + n4);
