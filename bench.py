@@ -419,6 +419,7 @@ def cpu_baseline(wl, seconds=12.0):
     layers, x = inputs.make(wl, device="cuda" if torch.cuda.is_available() else "cpu", n_layers=1)
     hl = inputs.layer_to_host(layers[0])
     xs = inputs.to_u16(x)
+    layers0 = layers[0]
     del layers
     threads = orc.threads(0)
     k = wl.shape.top_k
@@ -432,9 +433,45 @@ def cpu_baseline(wl, seconds=12.0):
     t0 = time.perf_counter()
     orc.forward(np.ascontiguousarray(xs[:n]), hl, k)
     dt = time.perf_counter() - t0
-    return {"value": round(n / dt, 2), "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": "%d of the %d tokens of one layer of the prefill workload (fp64 C oracle, "
-                      "OpenMP over tokens), %.1f s" % (n, wl.T, dt)}
+    res = {"value": round(n / dt, 2), "unit": UNIT, "cores": threads, "kind": "oracle",
+           "sample": "%d of the %d tokens of one layer of the prefill workload (fp64 C oracle, "
+                     "OpenMP over tokens), %.1f s" % (n, wl.T, dt)}
+    if torch.cuda.is_available():
+        res["parity"] = _parity_sample(wl, layers0, x, hl, xs, orc)
+    return res
+
+
+def _parity_sample(wl, layer, x, hl, xs, orc, rows=512):
+    """The GPU layer (moe_forward on the workload's first layer) against the oracle on a row
+    sample, with the oracle taking the GPU's routing (as the parity tests do): max |diff|, rel L2
+    and the rows whose ids differ from the oracle's own selection on the GPU's logits."""
+    import numpy as np
+    import torch
+
+    from sparse_moe_router_gb300 import abi, inputs
+
+    T, k = wl.T, wl.shape.top_k
+    cfg = abi.config_of(wl.shape)
+    ws = abi.alloc_workspace(cfg, min(T, 8192))
+    wts = abi.weights(layer)
+    out = torch.empty_like(x)
+    abi.moe_forward(cfg, wts, x, T, out, None, ws)
+    logits = torch.empty(T, wl.shape.n_experts, dtype=torch.float32, device=x.device)
+    ids = torch.empty(T, k, dtype=torch.int32, device=x.device)
+    w = torch.empty(T, k, dtype=torch.float32, device=x.device)
+    abi.moe_route(cfg, wts, x, T, logits, ids, w, ws)
+    torch.cuda.synchronize()
+    assert abi.moe_check_status(ws) == 0
+    sel = np.linspace(0, T - 1, rows).astype(np.int64)
+    ids_h, w_h, lg = ids.cpu().numpy()[sel], w.cpu().numpy()[sel], logits.cpu().numpy()[sel]
+    ref = orc.forward(np.ascontiguousarray(xs[sel]), hl, k, ids=ids_h, topk_w=w_h)["out"]
+    f = lambda u: (u.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    g, r = f(inputs.to_u16(out)[sel]), f(ref)
+    ids_o, _ = orc.route_from_logits(lg, k)
+    return {"rows": rows, "max_abs": float(np.abs(g - r).max()),
+            "rel_l2": float(np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-30)),
+            "ids_mismatch_rows": int(np.sum(np.any(ids_o != ids_h, axis=1))),
+            "bound": {"max_abs": 2e-2, "rel_l2": 5e-3}}
 
 
 def run_reference(args, world, rank):

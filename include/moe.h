@@ -171,6 +171,16 @@ moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const moe_bf
  * copy fails. */
 moe_status moe_check_status(void *ws, size_t ws_bytes, int *device_status, void *stream);
 
+/* Diagnostics, not a step of the layer: one device thread waits on a barrier with the same
+ * bounded wait every pipeline of this library uses.  With arrive != 0 the barrier completes
+ * first and the wait returns at once; with arrive == 0 nothing arrives, the wait gives up after
+ * limit_ns nanoseconds (at most 1e9) and records MOE_ERR_TIMEOUT in the workspace status word,
+ * which moe_check_status then reports.  No fault, trap or hang: the kernel returns, and the
+ * stream and context stay usable.  ws: at least the 256-byte status area of a workspace
+ * (256-byte aligned).  Returns MOE_ERR_INVALID_ARG for a bad workspace or limit. */
+moe_status moe_selftest_wait(void *ws, size_t ws_bytes, unsigned long long limit_ns, int arrive,
+                             void *stream);
+
 /* Sizes of the pieces moe_forward splits T into: writes up to max_pieces sizes to `pieces`
  * and returns the number of pieces (host only, no device work); -1 if T < 0. */
 int moe_plan_pieces(int T, int *pieces, int max_pieces);

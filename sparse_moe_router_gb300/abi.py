@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_WORKSPACE_TOO
 EXPORTS = ["moe_status_string", "moe_workspace_size", "moe_route", "moe_route_from_logits",
            "moe_permute", "moe_permute_noalloc", "moe_expert_ffn", "moe_combine", "moe_forward", "moe_check_status",
            "moe_plan_pieces", "moe_launch_count", "moe_timing_enable", "moe_timing_read",
-           "moe_timing_name", "moe_timing_classes"]
+           "moe_timing_name", "moe_timing_classes", "moe_selftest_wait"]
 
 
 class MoeError(RuntimeError):
@@ -71,6 +71,7 @@ def load(path: str = LIB_PATH):
     L.moe_combine.argtypes = [C, _P, _P, _P, _P, _I, _P, _P]
     L.moe_forward.argtypes = [C, W, _P, _I, _P, _P, _P, _P, _SZ, _P]
     L.moe_check_status.argtypes = [_P, _SZ, ctypes.POINTER(_I), _P]
+    L.moe_selftest_wait.argtypes = [_P, _SZ, ctypes.c_ulonglong, _I, _P]
     L.moe_plan_pieces.argtypes = [_I, ctypes.POINTER(_I), _I]
     L.moe_plan_pieces.restype = _I
     L.moe_launch_count.argtypes = []
@@ -82,7 +83,7 @@ def load(path: str = LIB_PATH):
     L.moe_timing_classes.argtypes = []
     for fn in ("moe_route", "moe_route_from_logits", "moe_permute", "moe_permute_noalloc", "moe_expert_ffn",
                "moe_combine", "moe_forward", "moe_check_status", "moe_timing_enable",
-               "moe_timing_read", "moe_timing_classes"):
+               "moe_timing_read", "moe_timing_classes", "moe_selftest_wait"):
         getattr(L, fn).restype = _I
     _lib = L
     return L
@@ -204,6 +205,12 @@ def moe_check_status(ws, stream=None) -> int:
     st = lib().moe_check_status(_ptr(ws), ws.numel(), ctypes.byref(v), _stream(stream))
     _check("moe_check_status", st)
     return v.value
+
+
+def moe_selftest_wait(ws, limit_ns: int, arrive: bool, stream=None):
+    """Run the library's bounded device wait on a barrier that completes (arrive) or never does."""
+    st = lib().moe_selftest_wait(_ptr(ws), ws.numel(), int(limit_ns), 1 if arrive else 0, _stream(stream))
+    _check("moe_selftest_wait", st)
 
 
 def moe_plan_pieces(T: int):

@@ -24,9 +24,6 @@
 // columns (acc_full/acc_empty), so the epilogue of one tile overlaps the next main loop.
 // Tiles are walked statically (tile = blockIdx.x + i*gridDim.x), ordered (group, weight tile,
 // token tile) with the token tile fastest, so CTAs sharing a weight tile run together.
-// Clusters of 2 (GemmArgs::cluster): the pair walks units of two adjacent weight tiles of one
-// token tile; each CTA loads half of the token tile and multicasts it to both, and each CTA's
-// MMA commits release the stage in both, so every token tile leaves L2 once per pair.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -64,7 +61,7 @@ struct Cfg {
     static constexpr int kMetaBytes = (EPI == EPI_COMBINE) ? 2 * BN * 8 : 0;
     static constexpr int kBarBytes = (2 * kStages + 5) * 8;
     static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + kStagingBytes +
-                                      kMetaBytes + kBarBytes + 16 + 2 * (kMaxGroups + 1) * 4;
+                                      kMetaBytes + kBarBytes + 32 + 2 * (kMaxGroups + 1) * 4;
 };
 
 struct TileInfo {
@@ -149,7 +146,9 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     volatile int *epi_vote = reinterpret_cast<volatile int *>(tmem_holder + 2);  // 2 slots
-    int *g_tiles = reinterpret_cast<int *>(tmem_holder + 4);
+    // stage fills issued by the producer / consumed by the MMA (read on abort), a zero flag
+    volatile int *fills = reinterpret_cast<volatile int *>(tmem_holder + 4);
+    int *g_tiles = reinterpret_cast<int *>(tmem_holder + 8);
     int *g_rows = g_tiles + (kMaxGroups + 1);
 
     const int tid = threadIdx.x;
@@ -157,14 +156,11 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
     const int cap = p.tile_cap > 0 ? p.tile_cap : BN;           // token tile cap
     const uint32_t b_bytes = (uint32_t)cap * BK * 2;            // B box bytes per stage
     const int lane = tid & 31;
-    const int CL = p.cluster > 1 ? p.cluster : 1;                // CTAs per cluster
-    const uint32_t crank = CL > 1 ? ptx::cluster_ctarank() : 0u;
-    const uint16_t cmask = (uint16_t)((1u << CL) - 1u);
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(&full[s], 1);
-            ptx::mbar_init(&empty[s], CL);  // released by the MMA commits of every CTA of the cluster
+            ptx::mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&acc_full[b], 1);
@@ -174,6 +170,7 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
         *abort_flag = 0;
         epi_vote[0] = 0;
         epi_vote[1] = 0;
+        fills[0] = fills[1] = fills[2] = 0;
         ptx::fence_mbar_init();
     }
     int G;
@@ -193,23 +190,11 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
         }
     }
     __syncthreads();
-    // the other CTAs of the cluster see this CTA's barriers initialised before anything is
-    // multicast into them
-    if (CL > 1) ptx::cluster_sync();
     const int nft = (p.F + C::kFT - 1) / C::kFT;
-    const int nft_u = nft / CL;                      // units of CL adjacent weight tiles
-    const int total = nft_u * g_tiles[G];
-    const int cid = (int)blockIdx.x / CL, ncl = (int)gridDim.x / CL;
-    if (cid >= total) {  // cluster-uniform; nothing allocated yet
-        if (CL > 1) ptx::cluster_sync();
-        return;
-    }
-    // unit u -> this CTA's tile: weight tile unit*CL + rank of the unit's token tile
-    auto tile_of = [&](int u) {
-        TileInfo t = decode_tile(u, nft_u, g_tiles, g_rows, G, cap, p.shared_last);
-        t.ftile = t.ftile * CL + (int)crank;
-        return t;
-    };
+    const int total = nft * g_tiles[G];
+    const int cid = (int)blockIdx.x, ncl = (int)gridDim.x;
+    if (cid >= total) return;  // CTA-uniform; nothing allocated yet
+    auto tile_of = [&](int u) { return decode_tile(u, nft, g_tiles, g_rows, G, cap, p.shared_last); };
 
     if (warp == kMmaWarp) ptx::tmem_alloc(tmem_holder, kTmemCols);
     ptx::tc_fence_before();
@@ -248,15 +233,10 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
                     } else {
                         ptx::tma_load_2d(st, ma0, kb * BK, arow, &full[s]);
                     }
-                    if (CL == 1) {
-                        ptx::tma_load_2d(st + kABytes, &tm_b, kb * BK, t.row0, &full[s]);
-                    } else {  // this CTA's share of the token tile, to every CTA of the cluster
-                        const int part = cap / CL;
-                        ptx::tma_load_2d_mc(st + kABytes + (int)crank * part * (BK * 2), &tm_b, kb * BK,
-                                            t.row0 + (int)crank * part, &full[s], cmask);
-                    }
+                    ptx::tma_load_2d(st + kABytes, &tm_b, kb * BK, t.row0, &full[s]);
                 }
             }
+            fills[0] = it;
         }
         if (!ok) {
             set_error(p.status, MOE_ERR_TIMEOUT);
@@ -287,12 +267,12 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
                     for (int kk = 0; kk < BK / 16; ++kk)
                         ptx::mma_bf16(d_base, ptx::sw128_desc(a_addr + kk * 32), ptx::sw128_desc(b_addr + kk * 32),
                                       idesc, (kb | kk) != 0 ? 1u : 0u);
-                    if (CL == 1) ptx::mma_commit(&empty[s]);
-                    else ptx::mma_commit_mc(&empty[s], cmask);
+                    ptx::mma_commit(&empty[s]);
                 }
                 if (!ok) break;
                 ptx::mma_commit(&acc_full[buf]);
             }
+            fills[1] = it;
             // Wait for every MMA of this CTA before TMEM is released.
             ptx::mma_commit(drain);
             if (!ptx::mbar_wait(drain, 0, kWaitLimitNs, abort_flag)) ok = false;
@@ -432,8 +412,14 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
 
     ptx::tc_fence_before();
     __syncthreads();
-    // no CTA leaves while another may still multicast into its shared memory or barriers
-    if (CL > 1) ptx::cluster_sync();
+    if (*abort_flag) {
+        // a wait gave up: the stage fills issued but not consumed may still be landing in shared
+        // memory; let them finish (bounded) before the CTA's shared memory is released
+        if (tid == kProdWarp0 * 32)
+            for (int i = fills[1]; i < fills[0]; ++i)
+                ptx::mbar_wait(&full[i % kStages], (uint32_t)(i / kStages) & 1u, kWaitLimitNs, fills + 2);
+        __syncthreads();
+    }
     if (warp == kMmaWarp) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, kTmemCols);
@@ -463,24 +449,6 @@ cudaError_t launch_impl(const GemmArgs &a, const CUtensorMap &m0, const CUtensor
     }
     if (grid <= 0) return cudaSuccess;
     LaunchScope scope(kc, s);
-    if (a.cluster > 1) {
-        // whole clusters only; the kernel gives the units out per cluster
-        grid = (grid / a.cluster) * a.cluster;
-        if (grid <= 0) return cudaErrorInvalidValue;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(grid);
-        cfg.blockDim = dim3(C::kThreads);
-        cfg.dynamicSmemBytes = C::kSmemBytes;
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = a.cluster;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, gemm_kernel<EPI>, a, m0, m1, mb, s0, s1);
-    }
     gemm_kernel<EPI><<<grid, C::kThreads, C::kSmemBytes, s>>>(a, m0, m1, mb, s0, s1);
     return cudaGetLastError();
 }
@@ -496,12 +464,6 @@ cudaError_t launch_gemm(GemmEpi epi, const GemmArgs &a, const CUtensorMap &tm_a0
     if (a.tile_cap != 0 && a.group_rows != nullptr) return cudaErrorInvalidValue;  // groups use 256
     if (a.shared_last && (a.group_rows == nullptr || a.n_groups < 2))
         return cudaErrorInvalidValue;
-    if (a.cluster > 1) {
-        const int kft = (epi == EPI_SWIGLU) ? 64 : BM;
-        const int nft = (a.F + kft - 1) / kft;
-        const int cap = a.tile_cap > 0 ? a.tile_cap : BN;
-        if (a.cluster != 2 || nft % a.cluster != 0 || cap % (16 * a.cluster) != 0) return cudaErrorInvalidValue;
-    }
     if (epi == EPI_SWIGLU && (a.F % 64 != 0 || a.ld % 8 != 0)) return cudaErrorInvalidValue;
     if (epi == EPI_COMBINE && (a.F % BM != 0 || a.ld % 8 != 0)) return cudaErrorInvalidValue;
     switch (epi) {

@@ -98,10 +98,6 @@ struct GemmArgs {
     // ftile*kFT of the shared matrix), its tiles are interleaved evenly among the routed ones,
     // and the combine epilogue stores its rows in place with weight 1
     bool shared_last;
-    // CTAs per cluster (0/1: none; 2: the CTAs of a pair take adjacent weight tiles of the same
-    // token tile, and each TMA-multicasts half of the token tile to both; the B tensor map's box
-    // then has tile_cap/2 rows)
-    int cluster;
 };
 
 // Launch the persistent grouped GEMM.  tm_a0 (and tm_a1 for EPI_SWIGLU: the up projection)

@@ -15,6 +15,7 @@
 #include <vector>
 
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "internal.h"
 
@@ -111,6 +112,12 @@ bool encode_tmap_2d_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint
 // -------------------------------------------------------------- workspace layout --
 
 namespace {
+
+// NVTX range around an entry point (visible in profilers that record NVTX; a few ns otherwise).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+};
 
 constexpr int kMaxPiece = 8192;
 
@@ -263,11 +270,6 @@ moe_status run_shared(const moe_config &c, const moe_weights &w, const uint16_t 
     return MOE_OK;
 }
 
-#ifndef MOE_GEMM_CLUSTER
-#define MOE_GEMM_CLUSTER 1
-#endif
-constexpr int kGemmCluster = MOE_GEMM_CLUSTER;  // CTAs per cluster of the routed GEMMs (1 or 2)
-
 // Routed experts, grouped: h rows (expert-sorted order) from the expert-sorted copy of x
 // (xp), then the down projection either stored per row in fp32 (y_rows, unfused) or weighted
 // and stored as bf16 rows in pair order (y_pairs[perm[r]] = bf16(row_w[r] * y)) for the
@@ -281,16 +283,12 @@ moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t 
     const uint64_t EI = (uint64_t)c.n_experts * c.inter;
     const uint64_t P = (uint64_t)T * c.top_k;
     const uint64_t rows = P + (with_shared ? (uint64_t)T : 0);
-    // pairs of CTAs share each token tile (multicast) when the weight tiles come in pairs:
-    // always for gate/up (I / 64 is even), for the down projection when H / 128 is even
-    const int cl_gu = kGemmCluster;
-    const int cl_dn = (c.hidden / kTileM) % 2 == 0 ? kGemmCluster : 1;
     CUtensorMap tg, tu, td, tx, th, tsg, tsu, tsd;
     if (!encode_tmap_2d_bf16(&tg, w.w_gate, EI, c.hidden, kTileM / 2, 64) ||
         !encode_tmap_2d_bf16(&tu, w.w_up, EI, c.hidden, kTileM / 2, 64) ||
         !encode_tmap_2d_bf16(&td, w.w_down, (uint64_t)c.n_experts * c.hidden, c.inter, kTileM, 64) ||
-        !encode_tmap_2d_bf16(&tx, xp, rows, c.hidden, kTileN / cl_gu, 64) ||
-        !encode_tmap_2d_bf16(&th, h, rows, c.inter, kTileN / cl_dn, 64))
+        !encode_tmap_2d_bf16(&tx, xp, rows, c.hidden, kTileN, 64) ||
+        !encode_tmap_2d_bf16(&th, h, rows, c.inter, kTileN, 64))
         return MOE_ERR_CUDA;
     if (with_shared) {
         if (!encode_tmap_2d_bf16(&tsg, w.ws_gate, c.shared_inter, c.hidden, kTileM / 2, 64) ||
@@ -316,7 +314,6 @@ moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t 
     a.ld = c.inter;
     a.status = status;
     a.shared_last = with_shared;
-    a.cluster = cl_gu;
     MOE_CUDA(launch_gemm(EPI_SWIGLU, a, tg, tu, tx, tsg, tsu, KC_GATEUP_GEMM, s));
     GemmArgs d{};
     d.b_src = h;
@@ -328,7 +325,6 @@ moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t 
     d.ld = c.hidden;
     d.status = status;
     d.shared_last = with_shared;
-    d.cluster = cl_dn;
     if (y_rows) {
         if (with_shared) return MOE_ERR_INVALID_ARG;
         d.out = y_rows;
@@ -405,6 +401,7 @@ size_t moe_workspace_size(const moe_config *cfg, int max_T) {
 moe_status moe_route(const moe_config *cfg, const moe_weights *w, const moe_bf16 *x, int T,
                      float *logits_out, int32_t *topk_ids, float *topk_w, void *ws,
                      size_t ws_bytes, void *stream) {
+    NvtxRange nvtx_range("moe_route");
     MOE_TRY(check_config(cfg));
     if (T < 0) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
@@ -435,6 +432,7 @@ moe_status moe_route(const moe_config *cfg, const moe_weights *w, const moe_bf16
 
 moe_status moe_route_from_logits(const moe_config *cfg, const float *logits, int T,
                                  int32_t *topk_ids, float *topk_w, void *stream) {
+    NvtxRange nvtx_range("moe_route_from_logits");
     MOE_TRY(check_config(cfg));
     if (T < 0) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
@@ -447,6 +445,7 @@ moe_status moe_route_from_logits(const moe_config *cfg, const float *logits, int
 moe_status moe_permute(const moe_config *cfg, const int32_t *topk_ids, int T,
                        int32_t *expert_offsets, int32_t *perm, int32_t *inv, void *ws,
                        size_t ws_bytes, void *stream) {
+    NvtxRange nvtx_range("moe_permute");
     MOE_TRY(check_config(cfg));
     if (T < 0) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
@@ -465,6 +464,7 @@ moe_status moe_expert_ffn(const moe_config *cfg, const moe_weights *w, const moe
                           const int32_t *expert_offsets, const int32_t *perm, moe_bf16 *h_rows,
                           float *y_rows, float *shared_y, void *ws, size_t ws_bytes,
                           void *stream) {
+    NvtxRange nvtx_range("moe_expert_ffn");
     MOE_TRY(check_config(cfg));
     if (T < 0) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
@@ -490,6 +490,7 @@ moe_status moe_expert_ffn(const moe_config *cfg, const moe_weights *w, const moe
 moe_status moe_combine(const moe_config *cfg, const float *y_rows, const int32_t *inv,
                        const float *topk_w, const float *shared_y, int T, moe_bf16 *out,
                        void *stream) {
+    NvtxRange nvtx_range("moe_combine");
     MOE_TRY(check_config(cfg));
     if (T < 0) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
@@ -521,6 +522,7 @@ int moe_plan_pieces(int T, int *pieces, int max_pieces) {
 moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const moe_bf16 *x, int T,
                        moe_bf16 *out, const moe_bf16 *resid, moe_bf16 *x_next, void *ws,
                        size_t ws_bytes, void *stream) {
+    NvtxRange nvtx_range("moe_forward");
     MOE_TRY(check_config(cfg));
     if (T < 0) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;

@@ -89,29 +89,6 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *tmap, in
         : "memory");
 }
 
-// The same tile, written to shared memory at the same offset (and its bytes signalled on the
-// mbarrier at the same offset) in every CTA of the cluster named by `mask`.
-__device__ __forceinline__ void tma_load_2d_mc(void *smem_dst, const void *tmap, int c0, int c1, uint64_t *bar,
-                                               uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(mask)
-        : "memory");
-}
-
-// ---------------------------------------------------------------------------- cluster --
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-// All threads of all CTAs of the cluster (release / acquire: shared-memory state written before
-// it, barrier initialisation included, is visible to the other CTAs after it).
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // Hint: bring the box at (c0, c1) into L2 ahead of its TMA load (no completion tracking).
 __device__ __forceinline__ void tma_prefetch_l2_2d(const void *tmap, int c0, int c1) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
@@ -222,16 +199,6 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
-        : "memory");
-}
-
-// Arrive (once every MMA issued so far has completed) on the mbarrier at the same offset in
-// every CTA of the cluster named by `mask`.
-__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(mask)
         : "memory");
 }
 
