@@ -153,8 +153,12 @@ class ClockSampler:
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one gate/up launch (routed experts + the shared
 # expert, T=8192, H=2048, E=256, k=8, I=I_s=512) from an ncu capture of the current kernel, or None
-# while the kernel has changed since the last capture.
-GATEUP_DRAM_BYTES = None
+# while the kernel has changed since the last capture: 1.4116 GB read + 72.19 MB written.
+GATEUP_DRAM_BYTES = 1_483_835_000
+# the same for the one-token decode kernel that streams the selected experts' and the shared
+# expert's weights (decode_k2_kernel<1>, H=2048, E=256, k=8, I=I_s=512): 56.71 MB read + 39 KB
+# written.  The router GEMV kernel before it reads the 1 MB router matrix and is not counted here.
+DECODE_K2_DRAM_BYTES = 56_752_000
 
 
 def _algorithmic(shape, T):
@@ -170,6 +174,12 @@ def _algorithmic(shape, T):
     gateup_launch = gateup + (shared_gu if Is == I else 0.0)
     return {"gateup_flops": gateup, "gateup_launch_flops": gateup_launch, "down_flops": down,
             "shared_flops": shared, "router_flops": router, "total_flops": gateup + down + shared + router}
+
+
+def _decode_layer_bytes(shape):
+    """All of one layer's weights (what the decode chain keeps resident)."""
+    H, E, I, Is = shape.hidden, shape.n_experts, shape.inter, shape.shared_inter
+    return 2 * (E * H + 3 * E * H * I + 3 * H * Is)
 
 
 def _decode_bytes(shape):
@@ -315,13 +325,25 @@ def run_ours(args, world, rank, local, pg):
     return res
 
 
+def run_decode_only(args, world, rank, local, pg):
+    """--decode-only: the decode measurement alone, as its own JSON line."""
+    import torch
+    from sparse_moe_router_gb300 import abi
+
+    torch.cuda.set_device(local)
+    abi.load()
+    d = run_decode(args, torch.device("cuda", local), pg, _peaks())
+    return {"metric": "MoE layer decode us/layer (T=1)", "value": d["us_per_layer"], "unit": "us/layer",
+            "n_gpus": world, "higher_is_better": False, "decode": d}
+
+
 def run_decode(args, dev, pg, peaks):
     import torch
     from sparse_moe_router_gb300 import abi, inputs
 
     wl = inputs.WORKLOADS["decode"]
-    shape, L = wl.shape, wl.n_layers
-    layers, x0 = inputs.make(wl, device=dev)
+    shape, L = wl.shape, (args.decode_layers or wl.n_layers)
+    layers, x0 = inputs.make(wl, device=dev, n_layers=L)
     cfg = abi.config_of(shape)
     wts = [abi.weights(l) for l in layers]
     s = torch.cuda.Stream(device=dev)
@@ -397,14 +419,16 @@ def run_decode(args, dev, pg, peaks):
         tT = _max_over_ranks(pg, statistics.median(graph_time(xT)[0]), dev)
         small.append({"T": T, "us_per_layer": round(1e3 * tT / L, 3),
                       "tokens_per_s": round(T * L / (tT * 1e-3), 1)})
-    return {"workload": "decode T=1, 40 distinct layers (64.7 GB of weights), CUDA graph",
+    return {"workload": "decode T=1, %d distinct layers (%.1f GB of weights), CUDA graph" % (
+                L, L * _decode_layer_bytes(shape) / 1e9),
             "us_per_layer": round(us_layer, 3), "graph_ms": round(t_med, 4), "reps": reps,
             "p10_p90_ms": [round(sorted(times)[len(times) // 10], 4),
                            round(sorted(times)[(9 * len(times)) // 10], 4)],
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
                          "frac_of_8000": round(gbs / 8000.0, 4), "bytes_per_layer": nbytes,
-                         "traffic": None, "peak_source": peaks["source"] + " hbm copy"},
+                         "traffic": DECODE_K2_DRAM_BYTES, "traffic_kernel": "decode_k2_kernel<1>",
+                         "peak_source": peaks["source"] + " hbm copy"},
             "eager_kernel_avg_us": split, "small_batch": small}
 
 
@@ -529,6 +553,10 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="prefill layers per step (default: the workload's 4); fewer only for profiler captures")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="run the decode measurement alone (for profiler captures)")
+    ap.add_argument("--decode-layers", type=int, default=0,
+                    help="decode layers (default: the workload's 40); fewer only for profiler captures")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=4.0)
     args = ap.parse_args()
@@ -537,6 +565,8 @@ def main():
     world, rank, local, pg = _dist_init()
     if args.impl == "reference":
         res = run_reference(args, world, rank)
+    elif args.decode_only:
+        res = run_decode_only(args, world, rank, local, pg)
     else:
         res = run_ours(args, world, rank, local, pg)
     if rank == 0 and res is not None:
