@@ -5,25 +5,34 @@
 // "MOE 内核优化": the MoE kernel bounds prefill) are, per expert e, products of the expert's
 // weight rows with the rows of the tokens routed to e.  The kernel computes them "swap-AB":
 //   D[f, j] = sum_k W[g*F + f, k] * B[row0 + j, k]
-// with 128 weight rows on the MMA's M side and up to 256 of the group's token rows on the N
-// side.  A group of c rows is cut into ceil(c/256) token tiles of equal size (rounded up to
-// 16), so an expert with 270 tokens costs two 144/126-wide tiles that each read the weight
-// tile once, not three tiles of 128/128/14.
-//   SwiGLU: the 128 weight rows of a tile are 64 gate rows and the same 64 features' up rows,
-//           so gate and up land in TMEM lanes i and 64 + i of one accumulator.
+// with weight rows on the MMA's M side and up to 256 of the group's token rows on the N side.
+// A group of c rows is cut into ceil(c/256) token tiles of equal size (rounded up to 16), so an
+// expert with 270 tokens costs two 144/126-wide tiles that each read the weight tile once, not
+// three tiles of 128/128/14.
 //
-// Roles (one CTA per SM):
+// CTA pairs (clusters of two, tcgen05 cta_group::2).  A pair computes a 256 x N tile with one
+// MMA stream issued by its even CTA: each CTA loads its own 128 weight rows and HALF of the N
+// token rows, the tensor cores of both SMs read both halves, and each CTA's TMEM receives its
+// own 128 rows of the accumulator.  Per SM that is 32 KB of operands per 64-wide K step instead
+// of 48 KB for a one-CTA 128 x 256 tile, which matters because the operand traffic of all SMs
+// together runs into the L2 -> SM limit (about 20 TB/s measured on this part).
+//   SwiGLU: each CTA's 128 weight rows are 64 gate rows and the same 64 features' up rows,
+//           so gate and up land in TMEM lanes i and 64 + i of its accumulator.
+//
+// Roles (one CTA per SM, two per pair):
 //   warps 0..P-1  epilogue (P = 16 for the weighted row scatter, else 8): warp w reads TMEM
 //               lanes 32*(w%4)..+31 (the hardware's lane quarters), and the P/4 warps of a
 //               quarter take every (P/4)-th 16-token chunk;
-//   warps P..P+3 producers: one thread issues the TMA loads of the weight tile and of the
-//               token tile (the other three warps idle);
-//   warp P+4    allocates TMEM; lane 0 issues tcgen05.mma (kind::f16, bf16 -> fp32) and
-//               tcgen05.commit.
-// Pipelines: 4 shared-memory stages (full/empty mbarriers) and two TMEM accumulators of 256
-// columns (acc_full/acc_empty), so the epilogue of one tile overlaps the next main loop.
-// Tiles are walked statically (tile = blockIdx.x + i*gridDim.x), ordered (group, weight tile,
-// token tile) with the token tile fastest, so CTAs sharing a weight tile run together.
+//   warps P..P+3 producers: one thread issues the TMA loads of its CTA's weight rows and token
+//               rows; both CTAs' loads complete on the even CTA's stage barrier;
+//   warp P+4    allocates TMEM (both CTAs, pair form); in the even CTA lane 0 issues
+//               tcgen05.mma (kind::f16, M = 256, bf16 -> fp32) and tcgen05.commit, whose
+//               arrivals go to both CTAs' barriers.
+// Pipelines: 6 shared-memory stages of 32 KB (full/empty mbarriers) and two TMEM accumulators
+// of 256 columns (acc_full/acc_empty; the odd CTA's epilogue releases an accumulator with a
+// remote arrive), so the epilogue of one tile overlaps the next main loop.
+// Pair tiles are walked statically (tile = pair + i*pairs), ordered (group, weight tile, token
+// tile) with the token tile fastest, so pairs sharing a weight tile run together.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -32,12 +41,13 @@
 namespace moe {
 namespace {
 
-constexpr int BM = kTileM;   // weight rows per tile (MMA M)
+constexpr int BM = kTileM;   // weight rows per CTA tile (the pair's MMA has M = 2 * BM)
 constexpr int BN = kTileN;   // token rows per tile (max MMA N)
 constexpr int BK = 64;       // K elements per stage: one 128-byte swizzle row
-constexpr int kStages = 4;
+constexpr int kStages = 6;
+constexpr int kBHalf = BN / 2;              // token rows each CTA of the pair holds
 constexpr int kABytes = BM * BK * 2;        // 16 KB
-constexpr int kBBytes = BN * BK * 2;        // 32 KB
+constexpr int kBBytes = kBHalf * BK * 2;    // 16 KB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kAccCols = BN;                // fp32 accumulator columns per TMEM buffer
 constexpr uint32_t kTmemCols = 2 * kAccCols;
@@ -50,18 +60,20 @@ struct Cfg {
     // epilogue warps: the weighted row scatter keeps many warps storing; the others need 8
     static constexpr int kEpiWarps = (EPI == EPI_COMBINE) ? 16 : 8;
     static constexpr int kProdWarp0 = kEpiWarps;    // 4 producer warps
-    static constexpr int kMmaWarp = kEpiWarps + 4;  // MMA + TMEM allocation warp
+    static constexpr int kMmaWarp = kEpiWarps + 4;  // TMEM allocation; lane 0 of the even CTA: MMA
     static constexpr int kThreads = (kEpiWarps + 5) * 32;
-    static constexpr int kFT = (EPI == EPI_SWIGLU) ? 64 : BM;    // output features per tile
+    static constexpr int kFT = (EPI == EPI_SWIGLU) ? 64 : BM;    // output features per CTA tile
     // SwiGLU: gate/up exchange, fp32 [2 sub-groups][16 rows][kStgStride];
     // combine: per-warp bf16 transpose buffers [warps][16 rows][32 features]
     static constexpr int kStagingBytes =
         (EPI == EPI_SWIGLU) ? 2 * 16 * kStgStride * 4 : (EPI == EPI_COMBINE ? kEpiWarps * 16 * 32 * 2 : 0);
     // combine: per-tile (output row, weight) of the BN tile rows, double-buffered
     static constexpr int kMetaBytes = (EPI == EPI_COMBINE) ? 2 * BN * 8 : 0;
+    // full, empty per stage; acc_full, acc_empty per accumulator; drain
     static constexpr int kBarBytes = (2 * kStages + 5) * 8;
     static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + kStagingBytes +
                                       kMetaBytes + kBarBytes + 32 + 2 * (kMaxGroups + 1) * 4;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory over the per-CTA limit");
 };
 
 struct TileInfo {
@@ -153,9 +165,11 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
-    const int cap = p.tile_cap > 0 ? p.tile_cap : BN;           // token tile cap
-    const uint32_t b_bytes = (uint32_t)cap * BK * 2;            // B box bytes per stage
     const int lane = tid & 31;
+    const int cap = p.tile_cap > 0 ? p.tile_cap : BN;  // token tile cap
+    // CTA pair: rank 0 issues the pair's MMAs (M = 256: its 128 weight rows, then the peer's);
+    // each CTA holds half of the tile's token rows and its own rows of the accumulator
+    const uint32_t rank = ptx::cluster_ctarank();
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -164,7 +178,7 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&acc_full[b], 1);
-            ptx::mbar_init(&acc_empty[b], kEpiWarps * 32);
+            ptx::mbar_init(&acc_empty[b], 2 * kEpiWarps);  // one arrival per epilogue warp of the pair
         }
         ptx::mbar_init(drain, 1);
         *abort_flag = 0;
@@ -190,15 +204,17 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
         }
     }
     __syncthreads();
-    const int nft = (p.F + C::kFT - 1) / C::kFT;
-    const int total = nft * g_tiles[G];
-    const int cid = (int)blockIdx.x, ncl = (int)gridDim.x;
-    if (cid >= total) return;  // CTA-uniform; nothing allocated yet
-    auto tile_of = [&](int u) { return decode_tile(u, nft, g_tiles, g_rows, G, cap, p.shared_last); };
+    const int nft = (p.F + C::kFT - 1) / C::kFT;  // CTA tiles along the features
+    const int nfp = (nft + 1) >> 1;               // pair tiles along the features
+    const int total = nfp * g_tiles[G];
+    const int pid = (int)(blockIdx.x >> 1), npair = (int)(gridDim.x >> 1);
+    if (pid >= total) return;  // the same for both CTAs of the pair; nothing allocated yet
+    auto tile_of = [&](int u) { return decode_tile(u, nfp, g_tiles, g_rows, G, cap, p.shared_last); };
 
-    if (warp == kMmaWarp) ptx::tmem_alloc(tmem_holder, kTmemCols);
+    if (warp == kMmaWarp) ptx::tmem_alloc_pair(tmem_holder, kTmemCols);
     ptx::tc_fence_before();
     __syncthreads();
+    ptx::cluster_sync();  // the peer's barriers are initialised before anyone signals them
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
     const int nkb = p.K / BK;
@@ -214,26 +230,34 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
                 ptx::tma_prefetch_desc(&tm_s0);
                 if (EPI == EPI_SWIGLU) ptx::tma_prefetch_desc(&tm_s1);
             }
-            int it = 0;
-            for (int tau = cid; tau < total && ok; tau += ncl) {
+            // stage s of both CTAs completes on the even CTA's full[s], which expects both
+            // CTAs' bytes; the odd CTA's loads signal it across the pair
+            const uint32_t full_even = ptx::mapa_shared(ptx::smem_u32(full), 0);
+            int it = 0, s = 0;
+            uint32_t ph = 0;
+            for (int tau = pid; tau < total && ok; tau += npair) {
                 const TileInfo t = tile_of(tau);
                 const bool shg = p.shared_last && t.g == G - 1;
-                const int arow = (shg ? 0 : t.g * p.F) + t.ftile * C::kFT;
+                const int ftile = 2 * t.ftile + (int)rank;
+                // a pair tile past the last feature tile (odd count) reads rows it never stores
+                const int arow = (shg ? 0 : t.g * p.F) + ftile * C::kFT;
                 const void *ma0 = shg ? (const void *)&tm_s0 : (const void *)&tm_a0;
                 const void *ma1 = shg ? (const void *)&tm_s1 : (const void *)&tm_a1;
+                // token rows: this CTA holds columns [rank * N/2, (rank + 1) * N/2) of the MMA
+                const int brow = t.row0 + (int)rank * (((t.nvalid + 15) & ~15) >> 1);
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
-                    const int s = it % kStages;
-                    const uint32_t ph = (uint32_t)(it / kStages) & 1u;
                     if (!ptx::mbar_wait(&empty[s], ph ^ 1u, kWaitLimitNs, abort_flag)) { ok = false; break; }
                     uint8_t *st = smem + s * kStageBytes;
-                    ptx::mbar_arrive_expect_tx(&full[s], kABytes + b_bytes);
+                    const uint32_t bar = full_even + (uint32_t)(s * 8);
+                    if (rank == 0) ptx::mbar_arrive_expect_tx(&full[s], 2 * kStageBytes);
                     if (EPI == EPI_SWIGLU) {
-                        ptx::tma_load_2d(st, ma0, kb * BK, arow, &full[s]);
-                        ptx::tma_load_2d(st + kABytes / 2, ma1, kb * BK, arow, &full[s]);
+                        ptx::tma_load_2d_pair(st, ma0, kb * BK, arow, bar);
+                        ptx::tma_load_2d_pair(st + kABytes / 2, ma1, kb * BK, arow, bar);
                     } else {
-                        ptx::tma_load_2d(st, ma0, kb * BK, arow, &full[s]);
+                        ptx::tma_load_2d_pair(st, ma0, kb * BK, arow, bar);
                     }
-                    ptx::tma_load_2d(st + kABytes, &tm_b, kb * BK, t.row0, &full[s]);
+                    ptx::tma_load_2d_pair(st + kABytes, &tm_b, kb * BK, brow, bar);
+                    if (++s == kStages) { s = 0; ph ^= 1u; }
                 }
             }
             fills[0] = it;
@@ -243,38 +267,45 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
             *abort_flag = 1;
         }
     } else if (warp == kMmaWarp) {
-        // ---------------------------------------------------------------- MMA --
-        if (lane == 0) {
-            int it = 0, tc = 0;
+        if (lane == 0 && rank == 0) {
+            // ------------------------------------------------- MMA (even CTA of the pair) --
+            // The tensor core runs only a few instructions ahead of this one thread, so the issue
+            // loop is kept to a handful of instructions per stage: stage and phase are counters,
+            // and the operand descriptors are stage 0's plus constant steps.
+            int it = 0, tc = 0, s = 0;
+            uint32_t ph = 0;
+            const uint64_t desc0 = ptx::sw128_desc(ptx::smem_u32(smem));
             bool ok = true;
-            for (int tau = cid; tau < total && ok; tau += ncl, ++tc) {
+            for (int tau = pid; tau < total && ok; tau += npair, ++tc) {
                 const TileInfo t = tile_of(tau);
                 const uint32_t nmma = (uint32_t)((t.nvalid + 15) & ~15);
                 const int buf = tc & 1;
                 const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
-                if (!ptx::mbar_wait(&acc_empty[buf], aph ^ 1u, kWaitLimitNs, abort_flag)) { ok = false; break; }
+                // both CTAs' epilogues have drained this accumulator
+                if (!ptx::mbar_wait_cluster(&acc_empty[buf], aph ^ 1u, kWaitLimitNs, abort_flag)) { ok = false; break; }
                 ptx::tc_fence_after();
                 const uint32_t d_base = tmem_base + (uint32_t)(buf * kAccCols);
-                const uint32_t idesc = ptx::idesc_bf16_f32(BM, nmma);
+                const uint32_t idesc = ptx::idesc_bf16_f32(2 * BM, nmma);
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
-                    const int s = it % kStages;
-                    const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-                    if (!ptx::mbar_wait(&full[s], ph, kWaitLimitNs, abort_flag)) { ok = false; break; }
+                    if (!ptx::mbar_wait_cluster(&full[s], ph, kWaitLimitNs, abort_flag)) { ok = false; break; }
                     ptx::tc_fence_after();
-                    const uint32_t a_addr = ptx::smem_u32(smem + s * kStageBytes);
-                    const uint32_t b_addr = a_addr + kABytes;
+                    // descriptors of stage s: the start-address field steps by bytes / 16, and
+                    // one K=16 slice is 32 bytes further along the swizzled 128-byte row
+                    const uint64_t da = desc0 + (uint64_t)(s * (kStageBytes >> 4));
+                    const uint64_t db = da + (uint64_t)(kABytes >> 4);
+                    ptx::mma_bf16_pair(d_base, da, db, idesc, kb != 0 ? 1u : 0u);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        ptx::mma_bf16(d_base, ptx::sw128_desc(a_addr + kk * 32), ptx::sw128_desc(b_addr + kk * 32),
-                                      idesc, (kb | kk) != 0 ? 1u : 0u);
-                    ptx::mma_commit(&empty[s]);
+                    for (int kk = 1; kk < BK / 16; ++kk)
+                        ptx::mma_bf16_pair(d_base, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), idesc, 1u);
+                    ptx::mma_commit_pair(&empty[s], (uint16_t)3);  // frees stage s in both CTAs
+                    if (++s == kStages) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
-                ptx::mma_commit(&acc_full[buf]);
+                ptx::mma_commit_pair(&acc_full[buf], (uint16_t)3);
             }
             fills[1] = it;
-            // Wait for every MMA of this CTA before TMEM is released.
-            ptx::mma_commit(drain);
+            // Wait for every MMA of the pair before TMEM is released.
+            ptx::mma_commit_pair(drain, (uint16_t)1);
             if (!ptx::mbar_wait(drain, 0, kWaitLimitNs, abort_flag)) ok = false;
             if (!ok) {
                 set_error(p.status, MOE_ERR_TIMEOUT);
@@ -288,12 +319,15 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
         const int sub = warp >> 2;     // this warp takes chunks cidx with cidx % kSubs == sub
         const int frow = quarter * 32 + lane;
         float *stg = staging + sub * 16 * kStgStride;  // SwiGLU exchange buffer of this sub-group
+        const uint32_t acc_empty_remote = ptx::mapa_shared(ptx::smem_u32(acc_empty), 0);
         int tc = 0;
         bool ok = true;
-        for (int tau = cid; tau < total; tau += ncl, ++tc) {
+        for (int tau = pid; tau < total; tau += npair, ++tc) {
             const TileInfo t = tile_of(tau);
             const int buf = tc & 1;
             const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
+            const int ftile = 2 * t.ftile + (int)rank;
+            const bool store = ftile < nft;  // false only for the odd half of a last pair tile
             // combine: the 16 warps fetch (output row, weight) of the tile's rows into shared
             // memory before the accumulator is ready (the loads overlap the main loop); the
             // vote barrier below publishes them to all epilogue warps
@@ -326,12 +360,12 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * kAccCols);
             float bias_f = 0.f;
             if (EPI == EPI_F32) {
-                const int f = t.ftile * BM + frow;
+                const int f = ftile * BM + frow;
                 if (p.bias != nullptr && f < p.F) bias_f = __ldg(&p.bias[f]);
             }
             // this warp's chunks are cidx = sub, sub + kSubs, ...; the TMEM load of the next
             // chunk is issued before the current one is processed, hiding its latency
-            const int n_chunks = (t.nvalid + 15) >> 4;
+            const int n_chunks = store ? (t.nvalid + 15) >> 4 : 0;
             uint32_t rn[16];
             if (sub < n_chunks) ptx::tmem_ld_16(taddr + (uint32_t)(16 * sub), rn);
             for (int cidx = sub; cidx < n_chunks; cidx += kSubs) {
@@ -361,12 +395,12 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
                             __float2bfloat16_rn(silu_mul(g1.x, u1.x)), __float2bfloat16_rn(silu_mul(g1.y, u1.y)),
                             __float2bfloat16_rn(silu_mul(g1.z, u1.z)), __float2bfloat16_rn(silu_mul(g1.w, u1.w))};
                         __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out);
-                        *reinterpret_cast<uint4 *>(&o[(size_t)(t.row0 + j0 + jj) * p.ld + t.ftile * 64 + fg]) =
+                        *reinterpret_cast<uint4 *>(&o[(size_t)(t.row0 + j0 + jj) * p.ld + ftile * 64 + fg]) =
                             *reinterpret_cast<const uint4 *>(h);
                     }
                     ptx::named_bar(2 + sub, 128);
                 } else if (EPI == EPI_F32) {
-                    const int f = t.ftile * BM + frow;
+                    const int f = ftile * BM + frow;
                     float *o = static_cast<float *>(p.out);
                     if (f < p.F) {
 #pragma unroll
@@ -395,14 +429,20 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
                         if (j0 + jj < t.nvalid) {
                             const uint4 v = *reinterpret_cast<const uint4 *>(&tb[jj * 32 + seg * 8]);
                             const int orow = meta_row[mb + jj];
-                            *reinterpret_cast<uint4 *>(&o[(size_t)orow * p.ld + t.ftile * BM + quarter * 32 + seg * 8]) = v;
+                            *reinterpret_cast<uint4 *>(&o[(size_t)orow * p.ld + ftile * BM + quarter * 32 + seg * 8]) = v;
                         }
                     }
                     __syncwarp();
                 }
             }
+            // release the accumulator to the even CTA's MMA: one arrival per warp, after the
+            // warp's TMEM loads are complete
             ptx::tc_fence_before();
-            ptx::mbar_arrive(&acc_empty[buf]);
+            __syncwarp();
+            if (lane == 0) {
+                if (rank == 0) ptx::mbar_arrive(&acc_empty[buf]);
+                else ptx::mbar_arrive_remote(acc_empty_remote + (uint32_t)(buf * 8));
+            }
         }
         if (!ok) {
             set_error(p.status, MOE_ERR_TIMEOUT);
@@ -414,15 +454,25 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
     __syncthreads();
     if (*abort_flag) {
         // a wait gave up: the stage fills issued but not consumed may still be landing in shared
-        // memory; let them finish (bounded) before the CTA's shared memory is released
-        if (tid == kProdWarp0 * 32)
-            for (int i = fills[1]; i < fills[0]; ++i)
-                ptx::mbar_wait(&full[i % kStages], (uint32_t)(i / kStages) & 1u, kWaitLimitNs, fills + 2);
+        // memory; let them finish (bounded) before the pair's shared memory is released.  The
+        // even CTA's full barriers count both CTAs' bytes; the odd CTA cannot wait on them and
+        // gives its own copies a fixed 100 us instead (a TMA load lands within microseconds).
+        if (tid == kProdWarp0 * 32) {
+            if (rank == 0) {
+                for (int i = fills[1]; i < fills[0]; ++i)
+                    ptx::mbar_wait(&full[i % kStages], (uint32_t)(i / kStages) & 1u, kWaitLimitNs, fills + 2);
+            } else {
+                const uint64_t t0 = ptx::globaltimer();
+                while (ptx::globaltimer() - t0 < 100000ull) {}
+            }
+        }
         __syncthreads();
     }
+    // neither CTA of the pair leaves (or frees TMEM) while the other may still signal it
+    ptx::cluster_sync();
     if (warp == kMmaWarp) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, kTmemCols);
+        ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
     }
 }
 
@@ -431,26 +481,44 @@ cudaError_t launch_impl(const GemmArgs &a, const CUtensorMap &m0, const CUtensor
                         const CUtensorMap &mb, const CUtensorMap &s0, const CUtensorMap &s1, int kc,
                         cudaStream_t s) {
     using C = Cfg<EPI>;
-    static bool attr_done[64] = {false};
+    // per device: the shared-memory opt-in and how many CTA pairs fit on the GPU at once
+    static int max_pairs[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 64 && !attr_done[dev]) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (dev >= 64) return cudaErrorInvalidDevice;
+    if (max_pairs[dev] == 0) {
         cudaError_t e = cudaFuncSetAttribute(gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemBytes);
         if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
+        cfg.gridDim = dim3(device_info().sm_count & ~1, 1, 1);
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<EPI>, &cfg);
+        if (e != cudaSuccess) return e;
+        if (n < 1) return cudaErrorInvalidConfiguration;
+        max_pairs[dev] = n;
     }
-    const DeviceInfo &di = device_info();
-    int grid = di.sm_count;
+    int pairs = max_pairs[dev];
     if (a.group_rows == nullptr) {
         const int nft = (a.F + C::kFT - 1) / C::kFT;
-        const int tiles = nft * token_tile_count(a.M_single, a.tile_cap > 0 ? a.tile_cap : BN);
-        if (tiles < grid) grid = tiles;
+        const int ptiles = ((nft + 1) / 2) * token_tile_count(a.M_single, a.tile_cap > 0 ? a.tile_cap : BN);
+        if (ptiles < pairs) pairs = ptiles;
     }
-    if (grid <= 0) return cudaSuccess;
+    if (pairs <= 0) return cudaSuccess;
+    cfg.gridDim = dim3(2 * pairs, 1, 1);
     LaunchScope scope(kc, s);
-    gemm_kernel<EPI><<<grid, C::kThreads, C::kSmemBytes, s>>>(a, m0, m1, mb, s0, s1);
-    return cudaGetLastError();
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_kernel<EPI>, a, m0, m1, mb, s0, s1);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

@@ -184,6 +184,8 @@ cudaError_t launch_decode_router(const DecodeArgs &a, cudaStream_t s);
 
 constexpr int kTileN = 256;   // tokens per GEMM tile (MMA N upper bound)
 constexpr int kTileM = 128;   // weight rows per GEMM tile (MMA M)
+// token rows per TMA box of a GEMM's token operand: each CTA of a pair holds half a tile
+constexpr int kTokenBoxRows = kTileN / 2;
 
 // Token tiles of a group of c rows: ceil(c / 256) tiles of equal size rounded up to 16 (the
 // MMA's N granularity); the last tile takes the remainder.  Shared by the permutation (tile

@@ -218,7 +218,7 @@ moe_status run_router_gemm(const moe_config &c, const moe_weights &w, const uint
                            float *logits, int *status, cudaStream_t s) {
     CUtensorMap tm, tb;
     if (!encode_tmap_2d_bf16(&tm, w.w_router, (uint64_t)c.n_experts, (uint64_t)c.hidden, kTileM, 64) ||
-        !encode_tmap_2d_bf16(&tb, x, (uint64_t)T, (uint64_t)c.hidden, kRouterTileN, 64))
+        !encode_tmap_2d_bf16(&tb, x, (uint64_t)T, (uint64_t)c.hidden, kTokenBoxRows, 64))
         return MOE_ERR_CUDA;
     GemmArgs a{};
     a.b_src = x;
@@ -244,8 +244,8 @@ moe_status run_shared(const moe_config &c, const moe_weights &w, const uint16_t 
     if (!encode_tmap_2d_bf16(&tg, w.ws_gate, c.shared_inter, c.hidden, kTileM / 2, 64) ||
         !encode_tmap_2d_bf16(&tu, w.ws_up, c.shared_inter, c.hidden, kTileM / 2, 64) ||
         !encode_tmap_2d_bf16(&td, w.ws_down, c.hidden, c.shared_inter, kTileM, 64) ||
-        !encode_tmap_2d_bf16(&tx, x, (uint64_t)T, c.hidden, kTileN, 64) ||
-        !encode_tmap_2d_bf16(&th, h_s, (uint64_t)T, c.shared_inter, kTileN, 64))
+        !encode_tmap_2d_bf16(&tx, x, (uint64_t)T, c.hidden, kTokenBoxRows, 64) ||
+        !encode_tmap_2d_bf16(&th, h_s, (uint64_t)T, c.shared_inter, kTokenBoxRows, 64))
         return MOE_ERR_CUDA;
     GemmArgs a{};
     a.b_src = x;
@@ -287,8 +287,8 @@ moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t 
     if (!encode_tmap_2d_bf16(&tg, w.w_gate, EI, c.hidden, kTileM / 2, 64) ||
         !encode_tmap_2d_bf16(&tu, w.w_up, EI, c.hidden, kTileM / 2, 64) ||
         !encode_tmap_2d_bf16(&td, w.w_down, (uint64_t)c.n_experts * c.hidden, c.inter, kTileM, 64) ||
-        !encode_tmap_2d_bf16(&tx, xp, rows, c.hidden, kTileN, 64) ||
-        !encode_tmap_2d_bf16(&th, h, rows, c.inter, kTileN, 64))
+        !encode_tmap_2d_bf16(&tx, xp, rows, c.hidden, kTokenBoxRows, 64) ||
+        !encode_tmap_2d_bf16(&th, h, rows, c.inter, kTokenBoxRows, 64))
         return MOE_ERR_CUDA;
     if (with_shared) {
         if (!encode_tmap_2d_bf16(&tsg, w.ws_gate, c.shared_inter, c.hidden, kTileM / 2, 64) ||
