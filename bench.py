@@ -155,10 +155,10 @@ class ClockSampler:
 # expert, T=8192, H=2048, E=256, k=8, I=I_s=512) from an ncu capture of the current kernel, or None
 # while the kernel has changed since the last capture: 1.4293 GB read + 72.34 MB written.
 GATEUP_DRAM_BYTES = 1_501_595_000
-# the same for the one-token decode kernel that streams the selected experts' and the shared
-# expert's weights (decode_k2_kernel<1>, H=2048, E=256, k=8, I=I_s=512): 56.71 MB read + 39 KB
-# written.  The router GEMV kernel before it reads the 1 MB router matrix and is not counted here.
-DECODE_K2_DRAM_BYTES = 56_752_000
+# the same per layer for the one-token decode chain (decode_chain_kernel, H=2048, E=256, k=8,
+# I=I_s=512), or None until captured for the current kernel: a 2-layer launch read 115.44 MB and
+# wrote 2.99 MB.
+DECODE_CHAIN_DRAM_BYTES_PER_LAYER = 59_211_648
 
 
 def _algorithmic(shape, T):
@@ -348,8 +348,9 @@ def run_decode(args, dev, pg, peaks):
     wts = [abi.weights(l) for l in layers]
     s = torch.cuda.Stream(device=dev)
 
-    def graph_time(x_start):
-        """Median time of the 40-layer chain for x_start's tokens, captured as one CUDA graph."""
+    def graph_time(x_start, one_launch=False):
+        """Median time of the 40-layer chain for x_start's tokens, captured as one CUDA graph:
+        one moe_forward call per layer, or (one_launch) one moe_decode_chain call for all."""
         T = x_start.shape[0]
         ws = abi.alloc_workspace(cfg, T)
         bufs = [x_start.clone(), torch.empty_like(x_start), torch.empty_like(x_start)]
@@ -357,6 +358,9 @@ def run_decode(args, dev, pg, peaks):
 
         def chain():
             # layer l+1 reads bf16(x_0 + out_l), fused into the layer's last kernel
+            if one_launch:
+                abi.moe_decode_chain(cfg, wts, bufs[0], out, bufs[1], ws, s, resid=bufs[0])
+                return
             x = bufs[0]
             for l in range(L):
                 nxt = bufs[1 + (l % 2)]
@@ -393,7 +397,11 @@ def run_decode(args, dev, pg, peaks):
         del g
         return times, chain
 
-    times, chain = graph_time(x0)
+    # the decode step: all layers in one cooperative launch (moe_decode_chain); the same stack as
+    # one moe_forward call per layer is reported beside it
+    times_calls, _ = graph_time(x0)
+    times, chain = graph_time(x0, one_launch=True)
+    us_calls = 1e3 * _max_over_ranks(pg, statistics.median(times_calls), dev) / L
     reps = len(times)
     t_med = statistics.median(times)
     t_med = _max_over_ranks(pg, t_med, dev)
@@ -407,7 +415,7 @@ def run_decode(args, dev, pg, peaks):
     torch.cuda.synchronize()
     abi.timing_enable(False)
     split = {}
-    for name in ("decode_router", "decode_experts"):
+    for name in ("decode_chain", "decode_router", "decode_experts"):
         n, ms = abi.timing_read(name)
         if n:
             split[name] = {"launches": n, "avg_us": round(1e3 * ms / n, 2)}
@@ -419,15 +427,16 @@ def run_decode(args, dev, pg, peaks):
         tT = _max_over_ranks(pg, statistics.median(graph_time(xT)[0]), dev)
         small.append({"T": T, "us_per_layer": round(1e3 * tT / L, 3),
                       "tokens_per_s": round(T * L / (tT * 1e-3), 1)})
-    return {"workload": "decode T=1, %d distinct layers (%.1f GB of weights), CUDA graph" % (
-                L, L * _decode_layer_bytes(shape) / 1e9),
+    return {"workload": "decode T=1, %d distinct layers (%.1f GB of weights), one moe_decode_chain launch "
+                        "in a CUDA graph" % (L, L * _decode_layer_bytes(shape) / 1e9),
             "us_per_layer": round(us_layer, 3), "graph_ms": round(t_med, 4), "reps": reps,
+            "us_per_layer_one_call_per_layer": round(us_calls, 3),
             "p10_p90_ms": [round(sorted(times)[len(times) // 10], 4),
                            round(sorted(times)[(9 * len(times)) // 10], 4)],
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
                          "frac_of_8000": round(gbs / 8000.0, 4), "bytes_per_layer": nbytes,
-                         "traffic": DECODE_K2_DRAM_BYTES, "traffic_kernel": "decode_k2_kernel<1>",
+                         "traffic": DECODE_CHAIN_DRAM_BYTES_PER_LAYER, "traffic_kernel": "decode_chain_kernel",
                          "peak_source": peaks["source"] + " hbm copy"},
             "eager_kernel_avg_us": split, "small_batch": small}
 

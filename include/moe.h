@@ -165,6 +165,24 @@ moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const moe_bf
                        moe_bf16 *out, const moe_bf16 *resid, moe_bf16 *x_next, void *ws,
                        size_t ws_bytes, void *stream);
 
+/* One token through a stack of n_layers MoE layers (1 <= n_layers <= 64), each with its own
+ * weights layers[l] (a host array of device pointers), in ONE cooperative kernel launch: the
+ * batch-1 greedy decode step the pages run ("AIMA AMD395 Qwen3.6 35B Windows Engine",
+ * "产品定位"), with the MoE layers back to back.  x_0 = x0 [H] bf16; for each layer
+ * out_l = the layer applied to x_l (as moe_forward with T = 1: same router rows, selection and
+ * rounding points) and x_{l+1} = bf16(r + out_l), r = resid [H] when given, else x_l (the
+ * residual stream).  out [H] receives the last layer's out; x_last [H] (may be NULL) receives
+ * x_{n_layers}.  The layers are separated by grid barriers instead of kernel boundaries; the
+ * fp32 atomics of the split-K down projection make the last bit run-dependent, as at T = 1.
+ * Requires T = 1 to fit the decode path (H <= 16384).  x0, resid, out, x_last 16-byte aligned;
+ * out and x_last must not alias x0 or resid.  ws: moe_workspace_size(cfg, 1) bytes; the call
+ * writes its barrier words there, so calls sharing a workspace must not overlap.  A barrier
+ * wait that runs out (2 s) records MOE_ERR_TIMEOUT in the workspace status word and every
+ * block returns.  MOE_ERR_UNSUPPORTED_SHAPE for more than 64 layers or a too-large H. */
+moe_status moe_decode_chain(const moe_config *cfg, const moe_weights *layers, int n_layers,
+                            const moe_bf16 *x0, const moe_bf16 *resid, moe_bf16 *out,
+                            moe_bf16 *x_last, void *ws, size_t ws_bytes, void *stream);
+
 /* Reads and clears the device status word in `ws` (synchronises `stream`).  *device_status
  * receives MOE_OK or the first error recorded by a kernel (MOE_ERR_TIMEOUT for a wait that
  * ran out, MOE_ERR_INVALID_ARG for an out-of-range expert id).  Returns MOE_ERR_CUDA if the

@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_WORKSPACE_TOO
 EXPORTS = ["moe_status_string", "moe_workspace_size", "moe_route", "moe_route_from_logits",
            "moe_permute", "moe_permute_noalloc", "moe_expert_ffn", "moe_combine", "moe_forward", "moe_check_status",
            "moe_plan_pieces", "moe_launch_count", "moe_timing_enable", "moe_timing_read",
-           "moe_timing_name", "moe_timing_classes", "moe_selftest_wait"]
+           "moe_timing_name", "moe_timing_classes", "moe_selftest_wait", "moe_decode_chain"]
 
 
 class MoeError(RuntimeError):
@@ -70,6 +70,7 @@ def load(path: str = LIB_PATH):
     L.moe_expert_ffn.argtypes = [C, W, _P, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]
     L.moe_combine.argtypes = [C, _P, _P, _P, _P, _I, _P, _P]
     L.moe_forward.argtypes = [C, W, _P, _I, _P, _P, _P, _P, _SZ, _P]
+    L.moe_decode_chain.argtypes = [C, W, _I, _P, _P, _P, _P, _P, _SZ, _P]
     L.moe_check_status.argtypes = [_P, _SZ, ctypes.POINTER(_I), _P]
     L.moe_selftest_wait.argtypes = [_P, _SZ, ctypes.c_ulonglong, _I, _P]
     L.moe_plan_pieces.argtypes = [_I, ctypes.POINTER(_I), _I]
@@ -83,7 +84,7 @@ def load(path: str = LIB_PATH):
     L.moe_timing_classes.argtypes = []
     for fn in ("moe_route", "moe_route_from_logits", "moe_permute", "moe_permute_noalloc", "moe_expert_ffn",
                "moe_combine", "moe_forward", "moe_check_status", "moe_timing_enable",
-               "moe_timing_read", "moe_timing_classes", "moe_selftest_wait"):
+               "moe_timing_read", "moe_timing_classes", "moe_selftest_wait", "moe_decode_chain"):
         getattr(L, fn).restype = _I
     _lib = L
     return L
@@ -192,6 +193,14 @@ def moe_forward(cfg, w: Weights, x, T, out, x_next, ws, stream=None, resid=None)
     st = lib().moe_forward(ctypes.byref(cfg), ctypes.byref(w), _ptr(x), int(T), _ptr(out),
                            _ptr(resid), _ptr(x_next), _ptr(ws), ws.numel(), _stream(stream))
     _check("moe_forward", st)
+
+
+def moe_decode_chain(cfg, layers, x0, out, x_last, ws, stream=None, resid=None):
+    """One token through len(layers) layers (a list of Weights) in one launch."""
+    arr = (Weights * len(layers))(*layers)
+    st = lib().moe_decode_chain(ctypes.byref(cfg), arr, len(layers), _ptr(x0), _ptr(resid), _ptr(out),
+                                _ptr(x_last), _ptr(ws), ws.numel(), _stream(stream))
+    _check("moe_decode_chain", st)
 
 
 def moe_forward_status(cfg, w: Weights, x, T, out, x_next, ws, stream=None, resid=None) -> int:

@@ -583,6 +583,342 @@ cudaError_t decode_attrs() {
     return e;
 }
 
+// ------------------------------------------------------------ chain of layers --
+// One token through L layers in one cooperative launch.  Each block keeps one work item of the
+// one-token layer (a 32-feature slice of a routed slot or of the shared expert, as in K2) and
+// the layers are separated by two grid barriers instead of kernel boundaries:
+//   A  every block: x_l into shared memory (from the previous layer's accumulator), up to
+//      ceil(E / blocks) router rows (one warp each, the same dot as K1, so the logits are the
+//      same bits), its share of clearing this layer's accumulator; then it arrives at B1.
+//      A shared-expert block goes straight on to stream its slice: it needs only x_l.
+//   B  after B1 a routed block selects the top-k from the logits and streams its expert slice;
+//      every block adds its split-K down partial into the accumulator, then B2.
+// The accumulators alternate between layers, so clearing one never races with reading the other.
+// Barriers count arrivals on one word (release by the arriving block, acquire by the waiting
+// one); every spin is bounded and a block that gives up raises a flag the others see.
+constexpr uint64_t kBarLimitNs = 2000000000ull;
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// All threads of the block: the block's earlier writes are visible GPU-wide before its arrival
+// (a release reduction: no round trip for the arriving thread).
+__device__ __forceinline__ void grid_arrive(unsigned *bar) {
+    __syncthreads();
+    if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(bar) : "memory");
+}
+
+// All threads of the block: true once `target` arrivals are counted; false (for the whole
+// block) when the wait runs out or another block gave up.
+__device__ __forceinline__ bool grid_wait(unsigned *bar, unsigned target, int *abort, int *status,
+                                          volatile int *s_flag) {
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        if (ld_acquire_u32(bar) < target) {
+            const uint64_t t0 = ptx::globaltimer();
+            for (uint32_t n = 1; ld_acquire_u32(bar) < target; ++n) {
+                if ((n & 31u) != 0u) continue;  // poll the count alone; the rest every 32 polls
+                if (*reinterpret_cast<volatile int *>(abort)) { ok = 0; break; }
+                if (ptx::globaltimer() - t0 > kBarLimitNs) {
+                    ok = 0;
+                    atomicExch(abort, 1);
+                    if (status) atomicCAS(status, 0, (int)MOE_ERR_TIMEOUT);
+                    break;
+                }
+            }
+        }
+        *s_flag = ok;
+    }
+    __syncthreads();
+    return *s_flag != 0;
+}
+
+// r = bf16 residual bits, a = fp32 accumulator: out = bf16(a), x = bf16(r + out) (the rounding
+// of the single-layer finish)
+__device__ __forceinline__ void finish4(const float4 &a, uint2 r, uint2 *o, uint2 *xn) {
+    const float vv[4] = {a.x, a.y, a.z, a.w};
+    const uint16_t rr[4] = {(uint16_t)(r.x & 0xffffu), (uint16_t)(r.x >> 16), (uint16_t)(r.y & 0xffffu),
+                            (uint16_t)(r.y >> 16)};
+    uint16_t ob[4], xb[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        ob[q] = bf16_bits(vv[q]);
+        xb[q] = bf16_bits(bf16_to_f(rr[q]) + bf16_to_f(ob[q]));
+    }
+    *o = make_uint2((uint32_t)ob[0] | ((uint32_t)ob[1] << 16), (uint32_t)ob[2] | ((uint32_t)ob[3] << 16));
+    *xn = make_uint2((uint32_t)xb[0] | ((uint32_t)xb[1] << 16), (uint32_t)xb[2] | ((uint32_t)xb[3] << 16));
+}
+
+// dot1_row_t<1> with the row already in shared memory: the same per-lane order, the same bits
+__device__ __forceinline__ float dot1_row_smem(const uint4 *w, const uint4 *xs, int n16, int lane) {
+    constexpr int U = 8;
+    float a = 0.f;
+    int c = lane;
+    for (; c + 32 * (U - 1) < n16; c += 32 * U) {
+        uint4 w0[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) w0[u] = w[c + 32 * u];
+#pragma unroll
+        for (int u = 0; u < U; ++u) a += dot8(w0[u], xs[c + 32 * u]);
+    }
+    for (; c < n16; c += 32) a += dot8(w[c], xs[c]);
+    return a;
+}
+
+// Rows of the router staged in shared memory a layer ahead: at most kStageRows rows a block, of
+// at most kStageH elements.
+constexpr int kStageRows = 2;
+constexpr int kStageH = 4096;
+
+__host__ __device__ __forceinline__ size_t chain_stage_off(int H, int E) {
+    return ((size_t)kChunkRows * kSlice * 2 + (size_t)H * 2 + (size_t)kSlice * 4 + (size_t)E * 4 + 15) & ~(size_t)15;
+}
+
+__global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __grid_constant__ ChainParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint16_t *wd = reinterpret_cast<uint16_t *>(smem);                           // [kChunkRows][kSlice]
+    uint4 *xs = reinterpret_cast<uint4 *>(smem + (size_t)kChunkRows * kSlice * 2);  // [H] bf16: x_l
+    float *hsl = reinterpret_cast<float *>(xs + p.H / 8);                          // [kSlice]
+    float *lg = hsl + kSlice;                                                      // [E] logits copy
+    uint4 *wr_s = reinterpret_cast<uint4 *>(smem + chain_stage_off(p.H, p.E));     // [kStageRows][H]
+    __shared__ int s_ids[32];
+    __shared__ float s_w[32];
+    __shared__ float s_lg[1024];
+    __shared__ unsigned s_chosen[32];
+    __shared__ __align__(8) uint64_t tbar;
+    __shared__ int s_ok, s_abort, s_flag;
+    __shared__ int s_zero[1];  // the token list of one token: token 0
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int H = p.H, E = p.E, n16 = H / 8;
+    const int slices = p.I / kSlice, n_shared = p.Is / kSlice;
+    const int n_items = n_shared + p.k * slices;
+    const int nb = (int)gridDim.x, b = (int)blockIdx.x;
+    const int rows0 = H < kChunkRows ? H : kChunkRows;
+    constexpr int kLoadWarp = kK2Warps - 1;
+    if (tid == 0) {
+        ptx::mbar_init(&tbar, 1);
+        s_ok = 1;
+        s_abort = 0;
+        s_zero[0] = 0;
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    // TMA of rows [r0, r0 + rows) of a slice's columns into shared memory (as in K2)
+    auto load_chunk = [&](const CUtensorMap *tm, int i0, int base_row, int r0, int rows) {
+        if (lane == 0) ptx::mbar_arrive_expect_tx(&tbar, (uint32_t)(rows * kSlice * 2));
+        __syncwarp();
+        if (lane < rows / kBoxRows)
+            ptx::tma_load_2d(wd + (size_t)lane * kBoxRows * kSlice, tm, i0, base_row + r0 + lane * kBoxRows, &tbar);
+    };
+    // the router rows of warps 0..1 (e = b + nb * warp) are staged in shared memory while the
+    // previous layer finishes, when every block has at most two rows of moderate length
+    const bool stage = E <= kStageRows * nb && H <= kStageH;
+    auto stage_rows = [&](int l) {
+        const int e = b + nb * warp;
+        if (warp < kStageRows && e < E) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(p.lay[l].w_router + (size_t)e * H);
+            uint4 *dst = wr_s + (size_t)warp * n16;
+            for (int c0 = lane; c0 < n16; c0 += 32 * 8) {
+                uint4 v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (c0 + 32 * u < n16) v[u] = ld_stream(src + c0 + 32 * u);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (c0 + 32 * u < n16) dst[c0 + 32 * u] = v[u];
+            }
+        }
+    };
+    if (stage) stage_rows(0);
+    uint32_t ph = 0;        // parity of the next chunk on tbar
+    bool pending = false;   // a chunk was issued and not yet waited for
+    unsigned nbar = 0;      // barriers passed
+    bool ok = true;
+    for (int l = 0; l < p.L && ok; ++l) {
+        const ChainLayer &ly = p.lay[l];
+        float *acc = (l & 1) ? p.acc1 : p.acc0;
+        const float *acc_prev = (l & 1) ? p.acc0 : p.acc1;
+        // ---------------------------------------------------------------- phase A --
+        if (l == 0) {
+            const uint4 *xg = reinterpret_cast<const uint4 *>(p.x0);
+            for (int i = tid; i < n16; i += kK2Threads) xs[i] = xg[i];
+        } else {
+            // x_l = bf16(r + bf16(acc_prev)), r = resid or x_{l-1} (in place: xs holds x_{l-1})
+            uint2 *x2 = reinterpret_cast<uint2 *>(xs);
+            for (int i = tid; i < H / 4; i += kK2Threads) {
+                const float4 a = __ldcg(reinterpret_cast<const float4 *>(acc_prev) + i);
+                const uint2 r = p.resid ? reinterpret_cast<const uint2 *>(p.resid)[i] : x2[i];
+                uint2 o, xn;
+                finish4(a, r, &o, &xn);
+                x2[i] = xn;
+            }
+        }
+        if (l == 0)  // the first layer's accumulator; later ones are cleared a layer ahead
+            for (int i = b * kK2Threads + tid; i < H / 4; i += nb * kK2Threads)
+                reinterpret_cast<float4 *>(acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        __syncthreads();
+        for (int e = b + nb * warp; e < E; e += nb * kK2Warps) {
+            float sc[1] = {0.f};
+            if (stage) sc[0] = dot1_row_smem(wr_s + (size_t)warp * n16, xs, n16, lane);
+            else dot1_row_t<1>(ly.w_router + (size_t)e * H, xs, n16, lane, 1, sc);
+            const float bias = ly.b_router ? ly.b_router[e] : 0.f;
+            const float v = warp_sum(sc[0]);
+            if (lane == 0) p.logits[e] = v + bias;
+        }
+        grid_arrive(p.bar);  // B1: the logits (and, at l = 0, the cleared accumulator)
+        const unsigned t_b1 = (++nbar) * (unsigned)nb;
+        if (l + 1 < p.L) {  // the next layer's router rows towards L2 while this layer streams
+            const char *wr = reinterpret_cast<const char *>(p.lay[l + 1].w_router);
+            for (int e = b + nb * warp; e < E; e += nb * kK2Warps)
+                for (int o = lane * 128; o < H * 2; o += 32 * 128) prefetch_l2(wr + (size_t)e * H * 2 + o);
+        }
+        // ---------------------------------------------------------------- phase B --
+        bool b1 = false, topk_done = false;
+        for (int w = b; w < n_items && ok; w += nb) {
+            const bool shared_task = w < n_shared;
+            const int i0 = shared_task ? w * kSlice : ((w - n_shared) % slices) * kSlice;
+            float wt = 1.f;
+            const CUtensorMap *tm = shared_task ? &p.tm_sdown[l] : &p.tm_down[l];
+            int base_row = 0;
+            const uint16_t *wg = ly.ws_gate, *wu = ly.ws_up;
+            if (!shared_task) {
+                if (!b1) {
+                    if (!grid_wait(p.bar, t_b1, p.abort, p.status, (volatile int *)&s_flag)) { ok = false; break; }
+                    b1 = true;
+                }
+                if (!topk_done) {
+                    if (warp == 0) {
+                        // the logits other blocks wrote, past L1, with eight loads in flight a lane
+                        for (int e0 = 0; e0 < E; e0 += 256) {
+                            float v[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const int e = e0 + lane + 32 * i;
+                                v[i] = e < E ? __ldcg(p.logits + e) : 0.f;
+                            }
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                if (e0 + lane + 32 * i < E) lg[e0 + lane + 32 * i] = v[i];
+                        }
+                        __syncwarp();
+                        warp_topk(lg, E, p.k, s_ids, s_w, s_lg, s_chosen);
+                    }
+                    __syncthreads();
+                    topk_done = true;
+                }
+                const int slot = (w - n_shared) / slices;
+                const int e = s_ids[slot];
+                wt = s_w[slot];
+                base_row = e * H;
+                wg = ly.w_gate + (size_t)e * p.I * H;
+                wu = ly.w_up + (size_t)e * p.I * H;
+            }
+            if (warp == kLoadWarp) load_chunk(tm, i0, base_row, 0, rows0);
+            pending = true;
+            // h for features i0 .. i0+31: 16 warps x 2 features
+            for (int f = warp; f < kSlice; f += kK2Warps) {
+                const size_t row = (size_t)(i0 + f);
+                float g[1] = {0.f}, u[1] = {0.f};
+                dot2_rows_t<1>(wg + row * H, wu + row * H, xs, n16, lane, s_zero, 1, g, u);
+                const float gs = warp_sum(g[0]), us = warp_sum(u[0]);
+                if (lane == 0) hsl[f] = __bfloat162float(__float2bfloat16_rn(silu_mul(gs, us)));
+            }
+            if (!b1) {  // a shared-expert block: the accumulator is cleared once B1 completes
+                if (!grid_wait(p.bar, t_b1, p.abort, p.status, (volatile int *)&s_flag)) { ok = false; break; }
+                b1 = true;
+            }
+            for (int r0 = 0; r0 < H; r0 += kChunkRows, ph ^= 1u) {
+                const int rows = (H - r0) < kChunkRows ? (H - r0) : kChunkRows;
+                if (tid == 0 && !ptx::mbar_wait(&tbar, ph, kWaitLimitNs, (volatile int *)&s_abort)) s_ok = 0;
+                __syncthreads();
+                if (!s_ok) {
+                    ok = false;
+                    break;
+                }
+                pending = false;
+                for (int n = tid; n < rows; n += kK2Threads) {
+                    const uint4 *rw = reinterpret_cast<const uint4 *>(wd + (size_t)n * kSlice);
+                    uint4 q[4];
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) q[cc] = rw[(cc + (n >> 1)) & 3];
+                    float a = 0.f;
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const int c = (cc + (n >> 1)) & 3;
+                        const __nv_bfloat162 *bq = reinterpret_cast<const __nv_bfloat162 *>(&q[cc]);
+                        const float *hf = hsl + c * 8;
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const float2 fv = __bfloat1622float2(bq[m]);
+                            a = fmaf(fv.x, hf[2 * m], a);
+                            a = fmaf(fv.y, hf[2 * m + 1], a);
+                        }
+                    }
+                    const float v1 = __shfl_down_sync(0xffffffffu, a, 1);
+                    const float v2 = __shfl_down_sync(0xffffffffu, a, 2);
+                    const float v3 = __shfl_down_sync(0xffffffffu, a, 3);
+                    if ((lane & 3) == 0) ptx::red_add_v4(&acc[r0 + n], wt * a, wt * v1, wt * v2, wt * v3);
+                }
+                __syncthreads();  // the chunk buffer and hsl are free again
+                if (r0 + kChunkRows < H && warp == kLoadWarp) {
+                    const int next = (H - r0 - kChunkRows) < kChunkRows ? (H - r0 - kChunkRows) : kChunkRows;
+                    load_chunk(tm, i0, base_row, r0 + kChunkRows, next);
+                }
+                if (r0 + kChunkRows < H) pending = true;
+            }
+        }
+        if (!ok) break;
+        if (!b1 && !grid_wait(p.bar, t_b1, p.abort, p.status, (volatile int *)&s_flag)) {  // a block with no item
+            ok = false;
+            break;
+        }
+        // the next layer's accumulator held layer l-1's sums, which every block read into x_l
+        // before B1 (passed by now): clear it here; it is added into only after the next B1
+        if (l + 1 < p.L) {
+            float *acc_next = ((l + 1) & 1) ? p.acc1 : p.acc0;
+            for (int i = b * kK2Threads + tid; i < H / 4; i += nb * kK2Threads)
+                reinterpret_cast<float4 *>(acc_next)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (stage && l + 1 < p.L) stage_rows(l + 1);  // lands while the barrier completes
+        grid_arrive(p.bar);  // B2: this layer's partials (and the next layer's cleared sums)
+        const unsigned t_b2 = (++nbar) * (unsigned)nb;
+        if (!grid_wait(p.bar, t_b2, p.abort, p.status, (volatile int *)&s_flag)) ok = false;
+    }
+    if (!ok || !s_ok) {
+        if (tid == 0) {
+            atomicExch(p.abort, 1);
+            if (p.status) atomicCAS(p.status, 0, (int)MOE_ERR_TIMEOUT);
+            // a chunk still landing in shared memory finishes before the block leaves (bounded)
+            if (pending) {
+                volatile int zero = 0;
+                ptx::mbar_wait(&tbar, ph, kWaitLimitNs, &zero);
+            }
+        }
+        return;
+    }
+    // after the last B2: out = bf16(acc), x_last = bf16(r + out); the first block writes them
+    if (b == 0) {
+        const float *acc = ((p.L - 1) & 1) ? p.acc1 : p.acc0;
+        const uint2 *x2 = reinterpret_cast<const uint2 *>(xs);
+        for (int i = tid; i < H / 4; i += kK2Threads) {
+            const float4 a = __ldcg(reinterpret_cast<const float4 *>(acc) + i);
+            const uint2 r = p.resid ? reinterpret_cast<const uint2 *>(p.resid)[i] : x2[i];
+            uint2 o, xn;
+            finish4(a, r, &o, &xn);
+            reinterpret_cast<uint2 *>(p.out)[i] = o;
+            if (p.x_last) reinterpret_cast<uint2 *>(p.x_last)[i] = xn;
+        }
+    }
+}
+
+size_t chain_smem(int H, int E) {
+    return 1024 + chain_stage_off(H, E) + (size_t)kStageRows * (H < kStageH ? H : kStageH) * 2;
+}
+
 }  // namespace
 
 int decode_slice() { return kSlice; }
@@ -630,6 +966,48 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &tm_down, const
                               : reinterpret_cast<const void *>(decode_k2_kernel<kMaxDecodeT>),
                           dim3(blocks), dim3(kK2Threads), k2_smem(a.T, a.H, one ? 1 : kMaxDecodeT), s, args);
     }
+}
+
+cudaError_t launch_decode_chain(const ChainParams &p, cudaStream_t s) {
+    if (p.L < 1 || p.L > kChainMaxLayers || p.H % kBoxRows != 0 || p.H > 16384 || p.E < 1 || p.E > 1024 ||
+        p.k < 1 || p.k > p.E || p.k > 32 || p.I % kSlice != 0 || p.Is % kSlice != 0)
+        return cudaErrorInvalidValue;
+    const size_t smem = chain_smem(p.H, p.E);
+    static int per_sm[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 64) return cudaErrorInvalidDevice;
+    if (per_sm[dev] == 0) {
+        cudaError_t e = cudaFuncSetAttribute(decode_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)chain_smem(16384, 1024));
+        if (e != cudaSuccess) return e;
+        int n = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_chain_kernel, kK2Threads, chain_smem(16384, 1024));
+        if (e != cudaSuccess) return e;
+        if (n < 1) return cudaErrorInvalidConfiguration;
+        per_sm[dev] = n;
+    }
+    // every block must be resident at once (the layers are separated by grid barriers): at most
+    // the blocks the GPU holds, each walking items blockIdx.x + i * gridDim.x
+    const int n_items = p.Is / kSlice + p.k * (p.I / kSlice);
+    int grid = per_sm[dev] * device_info().sm_count;
+    if (n_items < grid) grid = n_items;
+    cudaError_t e = cudaMemsetAsync(p.bar, 0, sizeof(unsigned), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p.abort, 0, sizeof(int), s);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kK2Threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    LaunchScope scope(KC_DECODE_CHAIN, s);
+    e = cudaLaunchKernelEx(&cfg, decode_chain_kernel, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace moe

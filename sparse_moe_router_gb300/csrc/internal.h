@@ -25,6 +25,7 @@ enum KernelClass {
     KC_DECODE_ROUTER,     // decode: router GEMV
     KC_DECODE_EXPERTS,    // decode: top-k, expert gate/up slices, split-K down, combine
     KC_GATHER_X,          // token rows copied into expert-sorted order
+    KC_DECODE_CHAIN,      // decode: a chain of layers in one cooperative launch
     KC_COUNT
 };
 
@@ -181,6 +182,31 @@ int decode_slice();
 int decode_box_rows();
 // Router logits of one token with the decode GEMV (the logits the decode path selects on).
 cudaError_t launch_decode_router(const DecodeArgs &a, cudaStream_t s);
+
+// One token through a chain of L layers in one cooperative launch (moe_decode_chain): per layer
+// out_l = layer_l(x_l), x_{l+1} = bf16(r + out_l) with r = resid, or x_l when resid is NULL.
+constexpr int kChainMaxLayers = 64;
+struct ChainLayer {
+    const uint16_t *w_router;
+    const float *b_router;
+    const uint16_t *w_gate, *w_up, *ws_gate, *ws_up;
+};
+struct ChainParams {
+    CUtensorMap tm_down[kChainMaxLayers];   // w_down as [E*H, I], decode box (see launch_decode)
+    CUtensorMap tm_sdown[kChainMaxLayers];  // ws_down as [H, Is]
+    ChainLayer lay[kChainMaxLayers];
+    int H, E, k, I, Is, L;
+    const uint16_t *x0;     // [H]
+    const uint16_t *resid;  // [H] or NULL
+    uint16_t *out;          // [H] the last layer's output
+    uint16_t *x_last;       // [H] or NULL: bf16(r + out) after the last layer
+    float *logits;          // [E]
+    float *acc0, *acc1;     // [H] each; layer l adds into acc0 (l even) or acc1 (l odd)
+    unsigned *bar;          // grid-barrier counter, zero at launch
+    int *abort;             // zero at launch; set by a block that gives up
+    int *status;            // device status word
+};
+cudaError_t launch_decode_chain(const ChainParams &p, cudaStream_t s);
 
 constexpr int kTileN = 256;   // tokens per GEMM tile (MMA N upper bound)
 constexpr int kTileM = 128;   // weight rows per GEMM tile (MMA M)

@@ -35,7 +35,8 @@ std::vector<TimedPair> g_timed[KC_COUNT];
 const char *const kClassNames[KC_COUNT] = {
     "router_gemm", "topk",          "permute",     "tile_prefix",   "gateup_gemm",
     "down_gemm",   "shared_gateup", "shared_down", "finalize",      "combine",
-    "zero",        "decode_router", "decode_experts", "gather_x"};
+    "zero",        "decode_router", "decode_experts", "gather_x",
+    "decode_chain"};
 }  // namespace
 
 const char *kernel_class_name(int kc) { return (kc >= 0 && kc < KC_COUNT) ? kClassNames[kc] : nullptr; }
@@ -594,6 +595,58 @@ moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const moe_bf
         }
         t0 += Tp;
     }
+    return MOE_OK;
+}
+
+moe_status moe_decode_chain(const moe_config *cfg, const moe_weights *layers, int n_layers, const moe_bf16 *x0,
+                            const moe_bf16 *resid, moe_bf16 *out, moe_bf16 *x_last, void *ws, size_t ws_bytes,
+                            void *stream) {
+    NvtxRange nvtx_range("moe_decode_chain");
+    MOE_TRY(check_config(cfg));
+    if (!layers || n_layers < 1) return MOE_ERR_INVALID_ARG;
+    if (n_layers > kChainMaxLayers) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!decode_fits(1, cfg->hidden)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!x0 || !out || !aligned16(x0) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+    if ((resid && !aligned16(resid)) || (x_last && !aligned16(x_last))) return MOE_ERR_INVALID_ARG;
+    for (int l = 0; l < n_layers; ++l) MOE_TRY(check_weights(cfg, &layers[l], true, true));
+    MOE_TRY(check_ws(cfg, ws, ws_bytes, 1));
+    const Layout L = layout(*cfg, 1);
+    const int H = cfg->hidden;
+    // about 20 KB: the per-layer pointers and down-projection tensor maps travel as the kernel's
+    // parameter block
+    static thread_local ChainParams p;
+    p.H = H;
+    p.E = cfg->n_experts;
+    p.k = cfg->top_k;
+    p.I = cfg->inter;
+    p.Is = cfg->shared_inter;
+    p.L = n_layers;
+    const uint32_t sl = (uint32_t)decode_slice(), br = (uint32_t)decode_box_rows();
+    for (int l = 0; l < n_layers; ++l) {
+        const moe_weights &w = layers[l];
+        p.lay[l] = ChainLayer{w.w_router, w.b_router, w.w_gate, w.w_up, w.ws_gate, w.ws_up};
+        if (!encode_tmap_2d_bf16(&p.tm_down[l], w.w_down, (uint64_t)cfg->n_experts * H, cfg->inter, br, sl, false))
+            return MOE_ERR_CUDA;
+        if (cfg->shared_inter > 0) {
+            if (!encode_tmap_2d_bf16(&p.tm_sdown[l], w.ws_down, H, cfg->shared_inter, br, sl, false))
+                return MOE_ERR_CUDA;
+        } else {
+            p.tm_sdown[l] = p.tm_down[l];
+        }
+    }
+    p.x0 = x0;
+    p.resid = resid;
+    p.out = out;
+    p.x_last = x_last;
+    p.logits = at<float>(ws, L.logits);
+    p.acc0 = at<float>(ws, L.acc);
+    p.acc1 = at<float>(ws, L.y);  // (k + 1) * H bf16 >= H fp32
+    int *st = at<int>(ws, L.status);
+    p.status = st;
+    // st[1] is the one-layer path's ticket counter; the chain's barrier count and abort flag follow
+    p.bar = reinterpret_cast<unsigned *>(st + 2);
+    p.abort = st + 3;
+    MOE_CUDA(launch_decode_chain(p, static_cast<cudaStream_t>(stream)));
     return MOE_OK;
 }
 
