@@ -54,6 +54,9 @@ constexpr uint32_t kTmemCols = 2 * kAccCols;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
 constexpr int kMaxGroups = 1026;                  // E <= 1024 experts, the shared expert, a spare
 constexpr int kStgStride = BM + 4;                // SwiGLU staging row (floats), padded for banks
+// combine transpose: a row of 32 words (features) per token pair, padded to 36 so that the
+// 16-byte reads of 8 lanes fall in distinct banks
+constexpr int kPairStride = 36;
 
 template <int EPI>
 struct Cfg {
@@ -64,9 +67,9 @@ struct Cfg {
     static constexpr int kThreads = (kEpiWarps + 5) * 32;
     static constexpr int kFT = (EPI == EPI_SWIGLU) ? 64 : BM;    // output features per CTA tile
     // SwiGLU: gate/up exchange, fp32 [2 sub-groups][16 rows][kStgStride];
-    // combine: per-warp bf16 transpose buffers [warps][16 rows][32 features]
+    // combine: per-warp transpose buffers [warps][8 token pairs][kPairStride words]
     static constexpr int kStagingBytes =
-        (EPI == EPI_SWIGLU) ? 2 * 16 * kStgStride * 4 : (EPI == EPI_COMBINE ? kEpiWarps * 16 * 32 * 2 : 0);
+        (EPI == EPI_SWIGLU) ? 2 * 16 * kStgStride * 4 : (EPI == EPI_COMBINE ? kEpiWarps * 8 * kPairStride * 4 : 0);
     // combine: per-tile (output row, weight) of the BN tile rows, double-buffered
     static constexpr int kMetaBytes = (EPI == EPI_COMBINE) ? 2 * BN * 8 : 0;
     // full, empty per stage; acc_full, acc_empty per accumulator; drain
@@ -131,6 +134,12 @@ __device__ __forceinline__ void set_error(int *status, int code) {
 // (a few fp32 ulp) is far below the bf16 rounding of h that follows.  g -> -inf gives
 // 1 / inf = 0, so the product stays 0.
 __device__ __forceinline__ float silu_mul(float g, float u) { return g * u * __frcp_rn(1.0f + __expf(-g)); }
+
+// bf16(a) in the low half, bf16(b) in the high half (round to nearest even)
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
 
 template <int EPI>
 __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
@@ -411,27 +420,36 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
                 } else {
                     // Weighted row scatter: tile row r is stored as bf16(w_r * D[:, r]) into
                     // output row meta_row[r] (the pair index, so the k rows of a token end up
-                    // adjacent).  The warp's 32 features x 16 rows go through its own 1 KB
-                    // buffer, transposed, and leave as 16-byte stores (8 features of a row).
-                    uint16_t *tb = reinterpret_cast<uint16_t *>(staging) + warp * (16 * 32);
+                    // adjacent).  The lane (one feature) packs tokens 2m and 2m+1 into one word;
+                    // the warp's 32 features x 16 tokens go through its own buffer, transposed,
+                    // and lane (m, seg) splits the words of features 8*seg.. into the two
+                    // tokens' 16-byte rows.
+                    uint32_t *tb = reinterpret_cast<uint32_t *>(staging) + warp * (8 * kPairStride);
                     const int mb = buf * BN + j0;
+                    const float4 *wv = reinterpret_cast<const float4 *>(meta_w + mb);
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const __nv_bfloat16 v = __float2bfloat16_rn(meta_w[mb + jj] * __uint_as_float(r[jj]));
-                        tb[jj * 32 + lane] = *reinterpret_cast<const uint16_t *>(&v);
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 w4 = wv[q];
+                        const uint32_t lo = pack_bf16x2(w4.x * __uint_as_float(r[4 * q]), w4.y * __uint_as_float(r[4 * q + 1]));
+                        const uint32_t hi = pack_bf16x2(w4.z * __uint_as_float(r[4 * q + 2]), w4.w * __uint_as_float(r[4 * q + 3]));
+                        tb[(2 * q) * kPairStride + lane] = lo;
+                        tb[(2 * q + 1) * kPairStride + lane] = hi;
                     }
                     __syncwarp();
                     uint16_t *o = static_cast<uint16_t *>(p.out);
-                    const int seg = lane & 3;
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        const int jj = (lane >> 2) + 8 * half;
-                        if (j0 + jj < t.nvalid) {
-                            const uint4 v = *reinterpret_cast<const uint4 *>(&tb[jj * 32 + seg * 8]);
-                            const int orow = meta_row[mb + jj];
-                            *reinterpret_cast<uint4 *>(&o[(size_t)orow * p.ld + ftile * BM + quarter * 32 + seg * 8]) = v;
-                        }
-                    }
+                    const int seg = lane & 3, m = lane >> 2;
+                    const uint4 a = *reinterpret_cast<const uint4 *>(&tb[m * kPairStride + seg * 8]);
+                    const uint4 c = *reinterpret_cast<const uint4 *>(&tb[m * kPairStride + seg * 8 + 4]);
+                    // words hold (token 2m in the low half, token 2m+1 in the high half)
+                    const uint4 e0 = make_uint4(__byte_perm(a.x, a.y, 0x5410), __byte_perm(a.z, a.w, 0x5410),
+                                                __byte_perm(c.x, c.y, 0x5410), __byte_perm(c.z, c.w, 0x5410));
+                    const uint4 e1 = make_uint4(__byte_perm(a.x, a.y, 0x7632), __byte_perm(a.z, a.w, 0x7632),
+                                                __byte_perm(c.x, c.y, 0x7632), __byte_perm(c.z, c.w, 0x7632));
+                    const size_t col = (size_t)ftile * BM + quarter * 32 + seg * 8;
+                    if (j0 + 2 * m < t.nvalid)
+                        *reinterpret_cast<uint4 *>(&o[(size_t)meta_row[mb + 2 * m] * p.ld + col]) = e0;
+                    if (j0 + 2 * m + 1 < t.nvalid)
+                        *reinterpret_cast<uint4 *>(&o[(size_t)meta_row[mb + 2 * m + 1] * p.ld + col]) = e1;
                     __syncwarp();
                 }
             }
