@@ -28,9 +28,10 @@
 //   warp P+4    allocates TMEM (both CTAs, pair form); in the even CTA lane 0 issues
 //               tcgen05.mma (kind::f16, M = 256, bf16 -> fp32) and tcgen05.commit, whose
 //               arrivals go to both CTAs' barriers.
-// Pipelines: 6 shared-memory stages of 32 KB (full/empty mbarriers) and two TMEM accumulators
-// of 256 columns (acc_full/acc_empty; the odd CTA's epilogue releases an accumulator with a
-// remote arrive), so the epilogue of one tile overlaps the next main loop.
+// Pipelines: 192 KB of shared-memory stages (full/empty mbarriers): 3 stages of two 64-wide K
+// blocks for the long-K GEMMs (router, gate/up), 6 stages of one block for the down GEMM; and two
+// TMEM accumulators of 256 columns (acc_full/acc_empty; the odd CTA's epilogue releases an
+// accumulator with a remote arrive), so the epilogue of one tile overlaps the next main loop.
 // Pair tiles are walked statically (tile = pair + i*pairs), ordered (group, weight tile, token
 // tile) with the token tile fastest, so pairs sharing a weight tile run together.
 #include <cuda_bf16.h>
@@ -43,12 +44,12 @@ namespace {
 
 constexpr int BM = kTileM;   // weight rows per CTA tile (the pair's MMA has M = 2 * BM)
 constexpr int BN = kTileN;   // token rows per tile (max MMA N)
-constexpr int BK = 64;       // K elements per stage: one 128-byte swizzle row
-constexpr int kStages = 6;
+constexpr int BK = 64;       // K elements per block: one 128-byte swizzle row
 constexpr int kBHalf = BN / 2;              // token rows each CTA of the pair holds
 constexpr int kABytes = BM * BK * 2;        // 16 KB
 constexpr int kBBytes = kBHalf * BK * 2;    // 16 KB
-constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kStepBytes = kABytes + kBBytes;  // one K block's operands in one CTA: 32 KB
+constexpr int kPipeBytes = 6 * kStepBytes;      // 192 KB of stages
 constexpr int kAccCols = BN;                // fp32 accumulator columns per TMEM buffer
 constexpr uint32_t kTmemCols = 2 * kAccCols;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
@@ -60,6 +61,12 @@ constexpr int kPairStride = 36;
 
 template <int EPI>
 struct Cfg {
+    // K blocks per pipeline stage.  The long-K GEMMs (router, gate/up: K = H) take two, so the MMA
+    // thread waits and commits once per 8 MMAs (each handshake costs the tensor pipe time it does
+    // not hide); the down GEMM (K = I, a few stages a tile) keeps one and the deeper ring.
+    static constexpr int kKB = (EPI == EPI_COMBINE) ? 1 : 2;
+    static constexpr int kStages = kPipeBytes / (kKB * kStepBytes);
+    static constexpr int kStageBytes = kKB * kStepBytes;
     // epilogue warps: the weighted row scatter keeps many warps storing; the others need 8
     static constexpr int kEpiWarps = (EPI == EPI_COMBINE) ? 16 : 8;
     static constexpr int kProdWarp0 = kEpiWarps;    // 4 producer warps
@@ -74,7 +81,7 @@ struct Cfg {
     static constexpr int kMetaBytes = (EPI == EPI_COMBINE) ? 2 * BN * 8 : 0;
     // full, empty per stage; acc_full, acc_empty per accumulator; drain
     static constexpr int kBarBytes = (2 * kStages + 5) * 8;
-    static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + kStagingBytes +
+    static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kPipeBytes + kStagingBytes +
                                       kMetaBytes + kBarBytes + 32 + 2 * (kMaxGroups + 1) * 4;
     static_assert(kSmemBytes <= 227 * 1024, "shared memory over the per-CTA limit");
 };
@@ -147,6 +154,9 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
                 const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_b,
                 const __grid_constant__ CUtensorMap tm_s0, const __grid_constant__ CUtensorMap tm_s1) {
     using C = Cfg<EPI>;
+    constexpr int kStages = C::kStages;
+    constexpr int kStageBytes = C::kStageBytes;
+    constexpr int kKB = C::kKB;
     constexpr int kEpiWarps = C::kEpiWarps;
     constexpr int kProdWarp0 = C::kProdWarp0;
     constexpr int kMmaWarp = C::kMmaWarp;
@@ -226,7 +236,7 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
     ptx::cluster_sync();  // the peer's barriers are initialised before anyone signals them
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
-    const int nkb = p.K / BK;
+    const int nks = p.K / (BK * kKB);  // stages per tile
 
     if (warp >= kProdWarp0 && warp < kMmaWarp) {
         // ------------------------------------------------------------ producers --
@@ -254,18 +264,22 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
                 const void *ma1 = shg ? (const void *)&tm_s1 : (const void *)&tm_a1;
                 // token rows: this CTA holds columns [rank * N/2, (rank + 1) * N/2) of the MMA
                 const int brow = t.row0 + (int)rank * (((t.nvalid + 15) & ~15) >> 1);
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                for (int ks = 0; ks < nks; ++ks, ++it) {
                     if (!ptx::mbar_wait(&empty[s], ph ^ 1u, kWaitLimitNs, abort_flag)) { ok = false; break; }
-                    uint8_t *st = smem + s * kStageBytes;
                     const uint32_t bar = full_even + (uint32_t)(s * 8);
                     if (rank == 0) ptx::mbar_arrive_expect_tx(&full[s], 2 * kStageBytes);
-                    if (EPI == EPI_SWIGLU) {
-                        ptx::tma_load_2d_pair(st, ma0, kb * BK, arow, bar);
-                        ptx::tma_load_2d_pair(st + kABytes / 2, ma1, kb * BK, arow, bar);
-                    } else {
-                        ptx::tma_load_2d_pair(st, ma0, kb * BK, arow, bar);
+#pragma unroll
+                    for (int j = 0; j < kKB; ++j) {
+                        uint8_t *st = smem + s * kStageBytes + j * kStepBytes;
+                        const int kc = (ks * kKB + j) * BK;
+                        if (EPI == EPI_SWIGLU) {
+                            ptx::tma_load_2d_pair(st, ma0, kc, arow, bar);
+                            ptx::tma_load_2d_pair(st + kABytes / 2, ma1, kc, arow, bar);
+                        } else {
+                            ptx::tma_load_2d_pair(st, ma0, kc, arow, bar);
+                        }
+                        ptx::tma_load_2d_pair(st + kABytes, &tm_b, kc, brow, bar);
                     }
-                    ptx::tma_load_2d_pair(st + kABytes, &tm_b, kb * BK, brow, bar);
                     if (++s == kStages) { s = 0; ph ^= 1u; }
                 }
             }
@@ -295,17 +309,20 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
                 ptx::tc_fence_after();
                 const uint32_t d_base = tmem_base + (uint32_t)(buf * kAccCols);
                 const uint32_t idesc = ptx::idesc_bf16_f32(2 * BM, nmma);
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                for (int ks = 0; ks < nks; ++ks, ++it) {
                     if (!ptx::mbar_wait_cluster(&full[s], ph, kWaitLimitNs, abort_flag)) { ok = false; break; }
                     ptx::tc_fence_after();
-                    // descriptors of stage s: the start-address field steps by bytes / 16, and
-                    // one K=16 slice is 32 bytes further along the swizzled 128-byte row
-                    const uint64_t da = desc0 + (uint64_t)(s * (kStageBytes >> 4));
-                    const uint64_t db = da + (uint64_t)(kABytes >> 4);
-                    ptx::mma_bf16_pair(d_base, da, db, idesc, kb != 0 ? 1u : 0u);
+                    // descriptors of stage s, block j: the start-address field steps by bytes / 16,
+                    // and one K=16 slice is 32 bytes further along the swizzled 128-byte row
 #pragma unroll
-                    for (int kk = 1; kk < BK / 16; ++kk)
-                        ptx::mma_bf16_pair(d_base, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), idesc, 1u);
+                    for (int j = 0; j < kKB; ++j) {
+                        const uint64_t da = desc0 + (uint64_t)((s * kStageBytes + j * kStepBytes) >> 4);
+                        const uint64_t db = da + (uint64_t)(kABytes >> 4);
+                        ptx::mma_bf16_pair(d_base, da, db, idesc, (ks | j) != 0 ? 1u : 0u);
+#pragma unroll
+                        for (int kk = 1; kk < BK / 16; ++kk)
+                            ptx::mma_bf16_pair(d_base, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), idesc, 1u);
+                    }
                     ptx::mma_commit_pair(&empty[s], (uint16_t)3);  // frees stage s in both CTAs
                     if (++s == kStages) { s = 0; ph ^= 1u; }
                 }
@@ -545,7 +562,7 @@ cudaError_t launch_gemm(GemmEpi epi, const GemmArgs &a, const CUtensorMap &tm_a0
                         const CUtensorMap &tm_b, const CUtensorMap &tm_s0, const CUtensorMap &tm_s1, int kc,
                         cudaStream_t s) {
     if (a.n_groups > kMaxGroups - 1) return cudaErrorInvalidValue;
-    if (a.K % BK != 0 || a.K <= 0) return cudaErrorInvalidValue;
+    if (a.K % (2 * BK) != 0 || a.K <= 0) return cudaErrorInvalidValue;
     if (a.tile_cap < 0 || a.tile_cap > BN || a.tile_cap % 16 != 0) return cudaErrorInvalidValue;
     if (a.tile_cap != 0 && a.group_rows != nullptr) return cudaErrorInvalidValue;  // groups use 256
     if (a.shared_last && (a.group_rows == nullptr || a.n_groups < 2))
