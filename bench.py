@@ -154,7 +154,7 @@ class ClockSampler:
 # dram__bytes_read.sum + dram__bytes_write.sum of one gate/up launch (routed experts + the shared
 # expert, T=8192, H=2048, E=256, k=8, I=I_s=512) from an ncu capture of the current kernel, or None
 # while the kernel has changed since the last capture: 1.4293 GB read + 72.34 MB written.
-GATEUP_DRAM_BYTES = 1_501_595_000
+GATEUP_DRAM_BYTES = None
 # the same per layer for the one-token decode chain (decode_chain_kernel, H=2048, E=256, k=8,
 # I=I_s=512), or None until captured for the current kernel: a 2-layer launch read 115.44 MB and
 # wrote 2.99 MB.
@@ -268,28 +268,30 @@ def run_ours(args, world, rank, local, pg):
 
     # ------------------------------------------------------------------------ e2e --
     # Every step copies its input from pinned host memory and its result back.  The copies run on
-    # a second stream with double-buffered device input and result, so step i's copies overlap
-    # the layers of steps i-1 and i+1; the timed region ends after the last copy back.
+    # their own streams (one per direction, so an input copy never queues behind a result copy
+    # that waits for its step), with double-buffered device input and result: step i's copies
+    # overlap the layers of steps i-1 and i+1.  The timed region ends after the last copy back.
     e2e = None
     if not args.skip_e2e:
         x_host = x0.cpu().pin_memory()
         out_host = [torch.empty_like(x_host).pin_memory() for _ in range(2)]
         xin = [torch.empty_like(x0) for _ in range(2)]
         res = [torch.empty_like(x0) for _ in range(2)]
-        copy_s = torch.cuda.Stream(device=dev)
+        h2d_s = torch.cuda.Stream(device=dev)
+        d2h_s = torch.cuda.Stream(device=dev)
         ev = lambda: torch.cuda.Event()
         in_ready, step_done, res_free = [ev(), ev()], [ev(), ev()], [ev(), ev()]
         for b in range(2):  # nothing to wait for before the first uses
             step_done[b].record(stream)
-            res_free[b].record(copy_s)
+            res_free[b].record(d2h_s)
 
         def e2e_steps(n):
             for i in range(n):
                 b = i & 1
-                with torch.cuda.stream(copy_s):
-                    copy_s.wait_event(step_done[b])  # step i-2 no longer reads xin[b]
+                with torch.cuda.stream(h2d_s):
+                    h2d_s.wait_event(step_done[b])  # step i-2 no longer reads xin[b]
                     xin[b].copy_(x_host, non_blocking=True)
-                    in_ready[b].record(copy_s)
+                    in_ready[b].record(h2d_s)
                 stream.wait_event(in_ready[b])
                 x = xin[b]
                 for l in range(L):
@@ -301,10 +303,10 @@ def run_ours(args, world, rank, local, pg):
                     abi.moe_forward(cfg, wts[l], x, T, out, nxt, ws, stream, resid=xin[b])
                     x = nxt
                 step_done[b].record(stream)
-                with torch.cuda.stream(copy_s):
-                    copy_s.wait_event(step_done[b])
+                with torch.cuda.stream(d2h_s):
+                    d2h_s.wait_event(step_done[b])
                     out_host[b].copy_(res[b], non_blocking=True)
-                    res_free[b].record(copy_s)
+                    res_free[b].record(d2h_s)
             for b in range(2):
                 stream.wait_event(res_free[b])
 
@@ -323,7 +325,7 @@ def run_ours(args, world, rank, local, pg):
                "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes,
                "ms_per_step": round(te / args.steps, 4),
                "path": "pinned host x -> moe_forward x4 layers (C-ABI) -> pinned host out; the copies on "
-                       "a second stream, double-buffered, overlapping the neighbouring steps' layers"}
+                       "their own streams (one per direction), double-buffered, overlapping the neighbouring steps' layers"}
 
     del layers, wts
     torch.cuda.empty_cache()
