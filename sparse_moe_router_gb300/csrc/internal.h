@@ -93,7 +93,8 @@ struct GemmArgs {
     const int32_t *epi_tok;
     const float *epi_w;
     int *status;
-    // token tile cap (a multiple of 16, <= 256; 0 = 256); the B tensor map's box has this many rows
+    // token tile cap (a multiple of 16, <= 256; 0 = 256).  The B tensor map's box is
+    // kTokenBoxRows rows: each CTA of a pair loads at most half a tile
     int tile_cap;
     // the last group is the shared expert: its weight rows come from the tm_s* maps (row
     // ftile*kFT of the shared matrix), its tiles are interleaved evenly among the routed ones,

@@ -1,5 +1,5 @@
-// ptx.cuh -- inline-PTX wrappers for sm_103a: mbarrier, TMA (cp.async.bulk.tensor),
-// cp.async, tcgen05 (MMA, TMEM alloc/ld, commit, fences).  Every wait is bounded: a wait
+// ptx.cuh -- inline-PTX wrappers for sm_103a: mbarrier, clusters, TMA (cp.async.bulk.tensor),
+// tcgen05 for CTA pairs (MMA, TMEM alloc/ld, commit, fences).  Every wait is bounded: a wait
 // that runs past its limit returns false and the caller records MOE_ERR_TIMEOUT and unwinds.
 #pragma once
 
@@ -153,14 +153,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const void *tma
         : "memory");
 }
 
-// Hint: bring the box at (c0, c1) into L2 ahead of its TMA load (no completion tracking).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const void *tmap, int c0, int c1) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(tmap)),
-                 "r"(c0), "r"(c1)
-                 : "memory");
-}
-
 // Fire-and-forget 16-byte vector add into global memory (no value returned, so the issuing
 // thread never waits on it).
 __device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
@@ -168,74 +160,12 @@ __device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float 
                  : "memory");
 }
 
-// Bulk (TMA) element-wise add of `bytes` (multiple of 16) from shared memory into global
-// memory, tracked by the issuing thread's bulk groups.
-__device__ __forceinline__ void bulk_reduce_add_f32(float *gdst, const void *ssrc, uint32_t bytes) {
-    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst),
-                 "r"(smem_u32(ssrc)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-// Wait until at most N bulk groups of this thread still read their shared-memory source.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-// Wait until all bulk groups of this thread have completed.
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 // Barrier among `count` threads on named barrier `id` (id 0 is __syncthreads).
 __device__ __forceinline__ void named_bar(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// ------------------------------------------------------------------------- cp.async --
-
-// 16-byte global -> shared copy; src_bytes == 0 fills the 16 bytes with zeros.
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Make this thread's generic-proxy shared-memory writes visible to the async proxy
-// (tcgen05.mma operand reads).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // -------------------------------------------------------------------------- tcgen05 --
-
-// Allocate `ncols` TMEM columns (power of two >= 32); the base address is written to
-// *dst_smem.  Executed by all 32 threads of one warp.
-__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(dst_smem)),
-                 "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
 
 // The same for a CTA pair (cta_group::2): one warp of each of the two CTAs executes it, and
 // the columns are allocated at the same address in both.
@@ -260,18 +190,6 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 x bf16 -> fp32, shapes from the instruction
-// descriptor.  Issued by one thread.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // The CTA-pair form, issued by the pair's even CTA: M = 256 rows, A's rows 0..127 from this
 // CTA's shared memory and 128..255 from the peer's (same address), B's first N/2 rows from this
 // CTA and the other N/2 from the peer; D rows 0..127 land in this CTA's TMEM, 128..255 in the
@@ -293,15 +211,6 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t *bar, uint16_t cta_mask
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
             smem_u32(bar)),
         "h"(cta_mask)
-        : "memory");
-}
-
-// Arrive (once) on `bar` when all previously issued tcgen05 async operations of this
-// thread have completed.
-__device__ __forceinline__ void mma_commit(uint64_t *bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
         : "memory");
 }
 
