@@ -315,3 +315,100 @@ void moe_ref_dense_masked(int H, int E, int k, int I, int Is, int T, const uint1
     free(hbuf);
     free(y);
 }
+
+/* ----------------------------------------------------- quantised expert weights -- */
+/* "AI MAX+ 395部署Qwen3大模型：GFX1151引擎实测优化解析", "两种权重格式：HGN 与 GGUF 的统一支持":
+ * one of the weight formats stores its large modules as 8-bit floats, with little precision
+ * lost; the page gives no layout.  Reading: E4M3 codes with one fp32 scale per output row of
+ * each expert matrix, weight = scale * code. */
+
+double moe_ref_e4m3_to_double(uint8_t q) {
+    int s = (q >> 7) & 1, e = (q >> 3) & 0xF, m = q & 7;
+    if (e == 0xF && m == 7) return NAN;
+    double v = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+uint8_t moe_ref_float_to_e4m3(float v) {
+    uint8_t sign = signbit(v) ? 0x80u : 0u;
+    double a = fabs((double)v);
+    if (isnan(v)) return 0x7Fu;
+    if (a >= 448.0) return (uint8_t)(sign | 0x7Eu);
+    if (a < 0x1p-6) {
+        /* subnormal step 2^-9; a rounded count of 8 is the smallest normal, code 0x08 */
+        double c = nearbyint(a * 512.0);
+        return (uint8_t)(sign | (uint8_t)c);
+    }
+    int e2;
+    (void)frexp(a, &e2);
+    int ex = e2 - 1;                           /* 2^ex <= a < 2^(ex+1), -6 <= ex <= 8 */
+    double c = nearbyint(a / ldexp(1.0, ex - 3)); /* 8 .. 16 steps of 2^(ex-3) */
+    if (c == 16.0) { ex += 1; c = 8.0; }
+    int code = ((ex + 7) << 3) | ((int)c - 8);
+    if (code > 0x7E) code = 0x7E;              /* 480 would be the NaN pattern: saturate */
+    return (uint8_t)(sign | code);
+}
+
+void moe_ref_quantize_e4m3_rows(int rows, int cols, const uint16_t *w, uint8_t *q, float *scale) {
+    for (int r = 0; r < rows; ++r) {
+        float amax = 0.0f;
+        for (int c = 0; c < cols; ++c) {
+            float a = (float)fabs(BF(w[(size_t)r * cols + c]));
+            if (a > amax) amax = a;
+        }
+        float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+        scale[r] = s;
+        for (int c = 0; c < cols; ++c) {
+            float v = (float)BF(w[(size_t)r * cols + c]) / s;
+            q[(size_t)r * cols + c] = moe_ref_float_to_e4m3(v);
+        }
+    }
+}
+
+/* h = bf16(silu(g) * u), y = Wd h with dequantised weights (fp64 sums); as swiglu_ffn. */
+static void swiglu_ffn_q8(int H, int I, const uint16_t *xrow, const uint8_t *qg, const float *sg,
+                          const uint8_t *qu, const float *su, const uint8_t *qd, const float *sd,
+                          double *hbuf, double *y) {
+    for (int i = 0; i < I; ++i) {
+        double g = 0.0, u = 0.0;
+        for (int h = 0; h < H; ++h) {
+            double xv = BF(xrow[h]);
+            g += (double)sg[i] * moe_ref_e4m3_to_double(qg[(size_t)i * H + h]) * xv;
+            u += (double)su[i] * moe_ref_e4m3_to_double(qu[(size_t)i * H + h]) * xv;
+        }
+        hbuf[i] = BF(moe_ref_double_to_bf16(moe_ref_silu(g) * u));
+    }
+    for (int n = 0; n < H; ++n) {
+        double acc = 0.0;
+        for (int i = 0; i < I; ++i) acc += (double)sd[n] * moe_ref_e4m3_to_double(qd[(size_t)n * I + i]) * hbuf[i];
+        y[n] = acc;
+    }
+}
+
+void moe_ref_forward_q8(int H, int E, int k, int I, int Is, int T, const uint16_t *x,
+                        const uint8_t *qg, const float *sg, const uint8_t *qu, const float *su,
+                        const uint8_t *qd, const float *sd, const uint8_t *qsg, const float *ssg,
+                        const uint8_t *qsu, const float *ssu, const uint8_t *qsd, const float *ssd,
+                        const int32_t *ids, const float *w, uint16_t *out) {
+    (void)E;
+    int maxI = I > Is ? I : Is;
+    double *hbuf = (double *)malloc(sizeof(double) * (size_t)(maxI > 0 ? maxI : 1));
+    double *y = (double *)malloc(sizeof(double) * (size_t)H);
+    double *acc = (double *)malloc(sizeof(double) * (size_t)H);
+    for (int t = 0; t < T; ++t) {
+        const uint16_t *xrow = x + (size_t)t * H;
+        for (int n = 0; n < H; ++n) acc[n] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            int e = ids[(size_t)t * k + j];
+            swiglu_ffn_q8(H, I, xrow, qg + (size_t)e * I * H, sg + (size_t)e * I, qu + (size_t)e * I * H,
+                          su + (size_t)e * I, qd + (size_t)e * H * I, sd + (size_t)e * H, hbuf, y);
+            for (int n = 0; n < H; ++n) acc[n] += (double)w[(size_t)t * k + j] * y[n];
+        }
+        if (Is > 0) {
+            swiglu_ffn_q8(H, Is, xrow, qsg, ssg, qsu, ssu, qsd, ssd, hbuf, y);
+            for (int n = 0; n < H; ++n) acc[n] += y[n];
+        }
+        for (int n = 0; n < H; ++n) out[(size_t)t * H + n] = moe_ref_double_to_bf16(acc[n]);
+    }
+    free(hbuf); free(y); free(acc);
+}

@@ -94,6 +94,26 @@ void moe_ref_dense_masked(int H, int E, int k, int I, int Is, int T, const uint1
 /* Number of threads the OpenMP loop of moe_ref_forward would use for n_threads. */
 int moe_ref_threads(int n_threads);
 
+/* ----------------------------------------------------- quantised expert weights -- */
+/* The 8-bit float E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 fraction bits, no infinities;
+ * exponent and fraction all ones is NaN.  Exponent e > 0: (-1)^s * 2^(e-7) * (1 + m/8);
+ * e = 0: (-1)^s * 2^-6 * (m/8).  Largest finite magnitude 448. */
+double moe_ref_e4m3_to_double(uint8_t q);
+/* float -> E4M3 pattern: round to nearest, ties to even; magnitudes past 448 saturate to 448. */
+uint8_t moe_ref_float_to_e4m3(float v);
+/* Row-wise quantisation of a bf16 matrix [rows, cols]: scale[r] = fp32(max_c |w[r,c]|) / 448
+ * in fp32 (1 for an all-zero row), q[r,c] = E4M3 of fp32(w[r,c]) / scale[r] (fp32 division). */
+void moe_ref_quantize_e4m3_rows(int rows, int cols, const uint16_t *w, uint8_t *q, float *scale);
+/* The layer for T tokens with quantised expert weights, weight[r,c] = scale[r] * e4m3(q[r,c])
+ * (exact in double), on a given routing ids/w [T,k]; the rounding points of moe_ref_forward
+ * (h to bf16 once, out to bf16 once).  Routed: qg, qu [E,I,H] with sg, su [E,I]; qd [E,H,I]
+ * with sd [E,H].  Shared (Is > 0): qsg, qsu [Is,H] with ssg, ssu [Is]; qsd [H,Is] with ssd [H]. */
+void moe_ref_forward_q8(int H, int E, int k, int I, int Is, int T, const uint16_t *x,
+                        const uint8_t *qg, const float *sg, const uint8_t *qu, const float *su,
+                        const uint8_t *qd, const float *sd, const uint8_t *qsg, const float *ssg,
+                        const uint8_t *qsu, const float *ssu, const uint8_t *qsd, const float *ssd,
+                        const int32_t *ids, const float *w, uint16_t *out);
+
 #ifdef __cplusplus
 }
 #endif

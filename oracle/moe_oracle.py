@@ -50,6 +50,14 @@ def _declare(L):
     L.moe_ref_dense_masked.restype = None
     L.moe_ref_threads.argtypes = [_I]
     L.moe_ref_threads.restype = _I
+    L.moe_ref_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    L.moe_ref_e4m3_to_double.restype = ctypes.c_double
+    L.moe_ref_float_to_e4m3.argtypes = [ctypes.c_float]
+    L.moe_ref_float_to_e4m3.restype = ctypes.c_uint8
+    L.moe_ref_quantize_e4m3_rows.argtypes = [_I, _I, _P, _P, _P]
+    L.moe_ref_quantize_e4m3_rows.restype = None
+    L.moe_ref_forward_q8.argtypes = [_I] * 6 + [_P] * 16
+    L.moe_ref_forward_q8.restype = None
 
 
 def _ptr(a):
@@ -210,3 +218,48 @@ def dense_masked(x, w, ids, topk_w, exact=False):
 
 def threads(n_threads=0):
     return lib().moe_ref_threads(int(n_threads))
+
+
+# ---------------------------------------------------------- quantised expert weights --
+
+def e4m3_to_f64(codes):
+    """E4M3 byte codes -> float64 values (the C oracle's decoder, element by element)."""
+    c = np.asarray(codes, dtype=np.uint8)
+    f = lib().moe_ref_e4m3_to_double
+    return np.array([f(int(v)) for v in c.ravel()], dtype=np.float64).reshape(c.shape)
+
+
+def float_to_e4m3(v):
+    return int(lib().moe_ref_float_to_e4m3(float(v)))
+
+
+def quantize_e4m3_rows(w):
+    """bf16 bits [rows, cols] -> (E4M3 codes uint8 [rows, cols], fp32 scales [rows])."""
+    w = _u16(w)
+    rows, cols = w.shape
+    q = np.empty((rows, cols), dtype=np.uint8)
+    s = np.empty(rows, dtype=np.float32)
+    lib().moe_ref_quantize_e4m3_rows(rows, cols, _ptr(w), _ptr(q), _ptr(s))
+    return q, s
+
+
+def forward_q8(x, wq, k, ids, topk_w):
+    """The layer with quantised expert weights on a given routing.  ``wq`` holds uint8 codes
+    q_gate, q_up [E,I,H], q_down [E,H,I] with float32 scales s_gate, s_up [E,I], s_down [E,H],
+    and optionally the shared expert's qs_gate, qs_up [Is,H], qs_down [H,Is] with ss_gate,
+    ss_up [Is], ss_down [H].  Returns out (u16 [T,H])."""
+    x = _u16(x)
+    T, H = x.shape
+    u8 = lambda a: None if a is None else np.ascontiguousarray(a, dtype=np.uint8)
+    qg, qu, qd = u8(wq["q_gate"]), u8(wq["q_up"]), u8(wq["q_down"])
+    E, I, _ = qg.shape
+    sg, su, sd = _f32(wq["s_gate"]), _f32(wq["s_up"]), _f32(wq["s_down"])
+    qsg, qsu, qsd = u8(wq.get("qs_gate")), u8(wq.get("qs_up")), u8(wq.get("qs_down"))
+    ssg, ssu, ssd = _f32(wq.get("ss_gate")), _f32(wq.get("ss_up")), _f32(wq.get("ss_down"))
+    Is = 0 if qsg is None else qsg.shape[0]
+    ids, topk_w = _i32(ids), _f32(topk_w)
+    out = np.empty((T, H), dtype=np.uint16)
+    lib().moe_ref_forward_q8(H, E, k, I, Is, T, _ptr(x), _ptr(qg), _ptr(sg), _ptr(qu), _ptr(su), _ptr(qd),
+                             _ptr(sd), _ptr(qsg), _ptr(ssg), _ptr(qsu), _ptr(ssu), _ptr(qsd), _ptr(ssd),
+                             _ptr(ids), _ptr(topk_w), _ptr(out))
+    return out

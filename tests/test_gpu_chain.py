@@ -48,7 +48,10 @@ def _layer_ref(shape, layer, x):
 
 @pytest.mark.parametrize("use_resid", [False, True])
 @pytest.mark.parametrize("shape,L", [(DECODE, 4), (TINY, 5), (inputs.Shape(256, 600, 8, 128, 128), 3),
-                                     (inputs.Shape(512, 32, 4, 256, 0), 3), (inputs.Shape(256, 64, 32, 128, 128), 3)])
+                                     (inputs.Shape(512, 32, 4, 256, 0), 3), (inputs.Shape(256, 64, 32, 128, 128), 3),
+                                     # 2 and 4 chunks of the down-projection slice; the widest also
+                                     # reads its router rows from global memory (no staging)
+                                     (inputs.Shape(4096, 16, 4, 128, 128), 3), (inputs.Shape(8192, 16, 4, 128, 128), 2)])
 def test_chain_layer_by_layer(shape, L, use_resid):
     layers, x0 = make(shape, 1, seed=500 + L + 7 * use_resid, n_layers=L)
     resid = x0.clone() if use_resid else None
