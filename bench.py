@@ -159,6 +159,8 @@ GATEUP_DRAM_BYTES = 1_494_038_000
 # I=I_s=512), or None until captured for the current kernel: a 2-layer launch read 115.44 MB and
 # wrote 2.99 MB.
 DECODE_CHAIN_DRAM_BYTES_PER_LAYER = 59_211_648
+# the same for the chain on E4M3 expert weights, or None until captured
+DECODE_CHAIN_Q8_DRAM_BYTES_PER_LAYER = None
 
 
 def _algorithmic(shape, T):
@@ -185,6 +187,13 @@ def _decode_layer_bytes(shape):
 def _decode_bytes(shape):
     H, E, k, I, Is = shape.hidden, shape.n_experts, shape.top_k, shape.inter, shape.shared_inter
     return E * H * 2 + k * 3 * H * I * 2 + 3 * H * Is * 2
+
+
+def _decode_bytes_q8(shape):
+    """The bytes one token reads with E4M3 expert weights: the bf16 router, one byte per expert
+    weight of the k routed and the shared expert, and their fp32 row scales."""
+    H, E, k, I, Is = shape.hidden, shape.n_experts, shape.top_k, shape.inter, shape.shared_inter
+    return E * H * 2 + k * 3 * H * I + 3 * H * Is + 4 * (k * (2 * I + H) + (2 * Is + H if Is else 0))
 
 
 def run_ours(args, world, rank, local, pg):
@@ -389,9 +398,10 @@ def run_decode(args, dev, pg, peaks):
     wts = [abi.weights(l) for l in layers]
     s = torch.cuda.Stream(device=dev)
 
-    def graph_time(x_start, one_launch=False):
+    def graph_time(x_start, one_launch=False, wts_q8=None):
         """Median time of the 40-layer chain for x_start's tokens, captured as one CUDA graph:
-        one moe_forward call per layer, or (one_launch) one moe_decode_chain call for all."""
+        one moe_forward call per layer, or (one_launch) one moe_decode_chain call for all, or
+        (wts_q8) one moe_decode_chain_q8 call on the E4M3 copies of the layers."""
         T = x_start.shape[0]
         ws = abi.alloc_workspace(cfg, T)
         bufs = [x_start.clone(), torch.empty_like(x_start), torch.empty_like(x_start)]
@@ -399,6 +409,9 @@ def run_decode(args, dev, pg, peaks):
 
         def chain():
             # layer l+1 reads bf16(x_0 + out_l), fused into the layer's last kernel
+            if wts_q8 is not None:
+                abi.moe_decode_chain_q8(cfg, wts_q8, bufs[0], out, bufs[1], ws, s, resid=bufs[0])
+                return
             if one_launch:
                 abi.moe_decode_chain(cfg, wts, bufs[0], out, bufs[1], ws, s, resid=bufs[0])
                 return
@@ -468,6 +481,23 @@ def run_decode(args, dev, pg, peaks):
         tT = _max_over_ranks(pg, statistics.median(graph_time(xT)[0]), dev)
         small.append({"T": T, "us_per_layer": round(1e3 * tT / L, 3),
                       "tokens_per_s": round(T * L / (tT * 1e-3), 1)})
+    # the same stack with E4M3 expert weights (row scales; the router stays bf16), quantised on the
+    # device from the bf16 layers, through moe_decode_chain_q8
+    q8 = None
+    if not args.skip_q8:
+        with torch.cuda.stream(s):
+            layers_q8 = [abi.quantize_layer(l, s) for l in layers]
+        torch.cuda.synchronize()
+        tq = _max_over_ranks(pg, statistics.median(graph_time(x0, wts_q8=[abi.weights_q8(l) for l in layers_q8])[0]),
+                             dev)
+        del layers_q8
+        us_q8 = 1e3 * tq / L
+        nq = _decode_bytes_q8(shape)
+        gq = nq / (us_q8 * 1e-6) / 1e9
+        q8 = {"us_per_layer": round(us_q8, 3), "bytes_per_layer": nq,
+              "roofline": {"bound": "hbm", "achieved": round(gq, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                           "frac": round(gq / peaks["hbm_gbs"], 4), "traffic": DECODE_CHAIN_Q8_DRAM_BYTES_PER_LAYER,
+                           "traffic_kernel": "decode_chain_kernel<true>"}}
     return {"workload": "decode T=1, %d distinct layers (%.1f GB of weights), one moe_decode_chain launch "
                         "in a CUDA graph" % (L, L * _decode_layer_bytes(shape) / 1e9),
             "us_per_layer": round(us_layer, 3), "graph_ms": round(t_med, 4), "reps": reps,
@@ -479,7 +509,7 @@ def run_decode(args, dev, pg, peaks):
                          "frac_of_8000": round(gbs / 8000.0, 4), "bytes_per_layer": nbytes,
                          "traffic": DECODE_CHAIN_DRAM_BYTES_PER_LAYER, "traffic_kernel": "decode_chain_kernel",
                          "peak_source": peaks["source"] + " hbm copy"},
-            "eager_kernel_avg_us": split, "small_batch": small}
+            "eager_kernel_avg_us": split, "small_batch": small, "e4m3_weights": q8}
 
 
 def cpu_baseline(wl, seconds=12.0):
@@ -599,6 +629,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-decode", action="store_true")
+    ap.add_argument("--skip-q8", action="store_true", help="skip the E4M3-weight decode measurement")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--layers", type=int, default=0,

@@ -79,6 +79,29 @@ typedef struct {
     const moe_bf16 *ws_down;  /* [H, Is]  (NULL when Is == 0) */
 } moe_weights;
 
+/* One layer with quantised expert weights: every expert matrix as E4M3 codes (1 sign, 4
+ * exponent bits with bias 7, 3 fraction bits; no infinities) with one fp32 scale per output row,
+ * weight[r, c] = scale[r] * code[r, c].  The router stays bf16.  ("AI MAX+ 395部署Qwen3大模型：
+ * GFX1151引擎实测优化解析", "两种权重格式：HGN 与 GGUF 的统一支持": 8-bit float weights for the large
+ * modules; the row scales are this library's reading, the page gives no layout.)  Code arrays
+ * 16-byte aligned; moe_quantize_e4m3 produces them from bf16 matrices. */
+typedef struct {
+    const moe_bf16 *w_router; /* [E, H] bf16 */
+    const float *b_router;    /* [E] fp32, or NULL */
+    const uint8_t *q_gate;    /* [E, I, H] codes */
+    const uint8_t *q_up;      /* [E, I, H] */
+    const uint8_t *q_down;    /* [E, H, I] */
+    const float *s_gate;      /* [E, I] row scales */
+    const float *s_up;        /* [E, I] */
+    const float *s_down;      /* [E, H] */
+    const uint8_t *qs_gate;   /* [Is, H] (NULL when Is == 0) */
+    const uint8_t *qs_up;     /* [Is, H] */
+    const uint8_t *qs_down;   /* [H, Is] */
+    const float *ss_gate;     /* [Is] */
+    const float *ss_up;       /* [Is] */
+    const float *ss_down;     /* [H] */
+} moe_weights_q8;
+
 /* Text for a status code (static storage). */
 const char *moe_status_string(moe_status s);
 
@@ -182,6 +205,22 @@ moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const moe_bf
 moe_status moe_decode_chain(const moe_config *cfg, const moe_weights *layers, int n_layers,
                             const moe_bf16 *x0, const moe_bf16 *resid, moe_bf16 *out,
                             moe_bf16 *x_last, void *ws, size_t ws_bytes, void *stream);
+
+/* moe_decode_chain for layers with quantised expert weights (moe_weights_q8): every expert
+ * row streamed as its E4M3 codes (half the bytes of bf16) and its scale, widened exactly and
+ * accumulated in fp32; otherwise the same steps, rounding points, barriers and errors. */
+moe_status moe_decode_chain_q8(const moe_config *cfg, const moe_weights_q8 *layers, int n_layers,
+                               const moe_bf16 *x0, const moe_bf16 *resid, moe_bf16 *out,
+                               moe_bf16 *x_last, void *ws, size_t ws_bytes, void *stream);
+
+/* Row-wise E4M3 quantisation of a bf16 matrix w [rows, cols] (device pointers): scale[r] =
+ * max_c |w[r,c]| / 448 (1 for an all-zero row) and q[r,c] = the E4M3 code nearest to
+ * w[r,c] / scale[r] (ties to even; magnitudes past 448 saturate), in fp32 with IEEE division,
+ * so the result is a function of the row alone.  q [rows, cols] bytes, scale [rows] fp32.
+ * Rows holding an infinity or a NaN give unspecified codes.  Asynchronous on `stream`; rows or
+ * cols of 0 do nothing; a negative size or a NULL pointer is MOE_ERR_INVALID_ARG. */
+moe_status moe_quantize_e4m3(const moe_bf16 *w, int rows, int cols, uint8_t *q, float *scale,
+                             void *stream);
 
 /* Reads and clears the device status word in `ws` (synchronises `stream`).  *device_status
  * receives MOE_OK or the first error recorded by a kernel (MOE_ERR_TIMEOUT for a wait that

@@ -24,7 +24,8 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_WORKSPACE_TOO
 EXPORTS = ["moe_status_string", "moe_workspace_size", "moe_route", "moe_route_from_logits",
            "moe_permute", "moe_permute_noalloc", "moe_expert_ffn", "moe_combine", "moe_forward", "moe_check_status",
            "moe_plan_pieces", "moe_launch_count", "moe_timing_enable", "moe_timing_read",
-           "moe_timing_name", "moe_timing_classes", "moe_selftest_wait", "moe_decode_chain"]
+           "moe_timing_name", "moe_timing_classes", "moe_selftest_wait", "moe_decode_chain",
+           "moe_decode_chain_q8", "moe_quantize_e4m3"]
 
 
 class MoeError(RuntimeError):
@@ -41,6 +42,12 @@ class Config(ctypes.Structure):
 class Weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("w_router", "b_router", "w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down")]
+
+
+class WeightsQ8(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("w_router", "b_router", "q_gate", "q_up", "q_down", "s_gate", "s_up", "s_down",
+                 "qs_gate", "qs_up", "qs_down", "ss_gate", "ss_up", "ss_down")]
 
 
 _P = ctypes.c_void_p
@@ -71,6 +78,8 @@ def load(path: str = LIB_PATH):
     L.moe_combine.argtypes = [C, _P, _P, _P, _P, _I, _P, _P]
     L.moe_forward.argtypes = [C, W, _P, _I, _P, _P, _P, _P, _SZ, _P]
     L.moe_decode_chain.argtypes = [C, W, _I, _P, _P, _P, _P, _P, _SZ, _P]
+    L.moe_decode_chain_q8.argtypes = [C, ctypes.POINTER(WeightsQ8), _I, _P, _P, _P, _P, _P, _SZ, _P]
+    L.moe_quantize_e4m3.argtypes = [_P, _I, _I, _P, _P, _P]
     L.moe_check_status.argtypes = [_P, _SZ, ctypes.POINTER(_I), _P]
     L.moe_selftest_wait.argtypes = [_P, _SZ, ctypes.c_ulonglong, _I, _P]
     L.moe_plan_pieces.argtypes = [_I, ctypes.POINTER(_I), _I]
@@ -84,7 +93,8 @@ def load(path: str = LIB_PATH):
     L.moe_timing_classes.argtypes = []
     for fn in ("moe_route", "moe_route_from_logits", "moe_permute", "moe_permute_noalloc", "moe_expert_ffn",
                "moe_combine", "moe_forward", "moe_check_status", "moe_timing_enable",
-               "moe_timing_read", "moe_timing_classes", "moe_selftest_wait", "moe_decode_chain"):
+               "moe_timing_read", "moe_timing_classes", "moe_selftest_wait", "moe_decode_chain",
+               "moe_decode_chain_q8", "moe_quantize_e4m3"):
         getattr(L, fn).restype = _I
     _lib = L
     return L
@@ -119,6 +129,17 @@ def weights(layer: dict) -> Weights:
     """Weights struct from a dict of device tensors (keys as in include/moe.h)."""
     w = Weights()
     for name, _ in Weights._fields_:
+        t = layer.get(name)
+        setattr(w, name, None if t is None else t.data_ptr())
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("weight %s must be a contiguous CUDA tensor" % name)
+    return w
+
+
+def weights_q8(layer: dict) -> WeightsQ8:
+    """WeightsQ8 struct from a dict of device tensors (keys as in include/moe.h)."""
+    w = WeightsQ8()
+    for name, _ in WeightsQ8._fields_:
         t = layer.get(name)
         setattr(w, name, None if t is None else t.data_ptr())
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
@@ -201,6 +222,38 @@ def moe_decode_chain(cfg, layers, x0, out, x_last, ws, stream=None, resid=None):
     st = lib().moe_decode_chain(ctypes.byref(cfg), arr, len(layers), _ptr(x0), _ptr(resid), _ptr(out),
                                 _ptr(x_last), _ptr(ws), ws.numel(), _stream(stream))
     _check("moe_decode_chain", st)
+
+
+def moe_decode_chain_q8(cfg, layers_q8, x0, out, x_last, ws, stream=None, resid=None):
+    """One token through len(layers_q8) layers with E4M3 expert weights (WeightsQ8 list)."""
+    arr = (WeightsQ8 * len(layers_q8))(*layers_q8)
+    st = lib().moe_decode_chain_q8(ctypes.byref(cfg), arr, len(layers_q8), _ptr(x0), _ptr(resid), _ptr(out),
+                                   _ptr(x_last), _ptr(ws), ws.numel(), _stream(stream))
+    _check("moe_decode_chain_q8", st)
+
+
+def moe_quantize_e4m3(w, q, scale, stream=None):
+    """Row-wise E4M3 codes q (uint8, w's shape) and fp32 scales (one per row) of a bf16 w whose
+    last dimension is the row."""
+    rows, cols = (w.numel() // w.shape[-1]) if w.dim() > 1 else 1, w.shape[-1]
+    st = lib().moe_quantize_e4m3(_ptr(w), int(rows), int(cols), _ptr(q), _ptr(scale), _stream(stream))
+    _check("moe_quantize_e4m3", st)
+
+
+def quantize_layer(layer: dict, stream=None) -> dict:
+    """A layer's expert matrices as E4M3 codes and row scales (the router kept as it is), on the
+    device, through moe_quantize_e4m3."""
+    out = {"w_router": layer["w_router"], "b_router": layer.get("b_router")}
+    for src, q, sc in (("w_gate", "q_gate", "s_gate"), ("w_up", "q_up", "s_up"), ("w_down", "q_down", "s_down"),
+                       ("ws_gate", "qs_gate", "ss_gate"), ("ws_up", "qs_up", "ss_up"),
+                       ("ws_down", "qs_down", "ss_down")):
+        w = layer.get(src)
+        if w is None:
+            continue
+        out[q] = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+        out[sc] = torch.empty(w.shape[:-1], dtype=torch.float32, device=w.device)
+        moe_quantize_e4m3(w, out[q], out[sc], stream)
+    return out
 
 
 def moe_forward_status(cfg, w: Weights, x, T, out, x_next, ws, stream=None, resid=None) -> int:

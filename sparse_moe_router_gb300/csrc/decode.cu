@@ -24,6 +24,8 @@
 // The accumulator adds are fp32 atomics: the summation order, hence the last bit of out,
 // can differ from run to run at T = 1.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -652,6 +654,55 @@ __device__ __forceinline__ void finish4(const float4 &a, uint2 r, uint2 *o, uint
     *xn = make_uint2((uint32_t)xb[0] | ((uint32_t)xb[1] << 16), (uint32_t)xb[2] | ((uint32_t)xb[3] << 16));
 }
 
+// 16 E4M3 codes (one 16-byte load) against 16 bf16 values of x (two 16-byte chunks): each code
+// pair is widened exactly to two halves, then to fp32
+__device__ __forceinline__ float dot16_q8(const uint4 &w, const uint4 &xa, const uint4 &xb) {
+    const __nv_fp8x2_storage_t *wp = reinterpret_cast<const __nv_fp8x2_storage_t *>(&w);
+    const __nv_bfloat162 *x0 = reinterpret_cast<const __nv_bfloat162 *>(&xa);
+    const __nv_bfloat162 *x1 = reinterpret_cast<const __nv_bfloat162 *>(&xb);
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(wp[i], __NV_E4M3);
+        const float2 wf = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
+        const float2 xf = __bfloat1622float2(i < 4 ? x0[i] : x1[i - 4]);
+        acc = fmaf(wf.x, xf.x, acc);
+        acc = fmaf(wf.y, xf.y, acc);
+    }
+    return acc;
+}
+
+// Two rows of H E4M3 codes (gate and up of one feature) against x in shared memory (bf16, n16
+// chunks of 8): 16 codes per load, four loads a row in flight per lane.
+__device__ __forceinline__ void dot2_rows_q8(const uint8_t *r0, const uint8_t *r1, const uint4 *xs, int n16,
+                                             int lane, float &a0, float &a1) {
+    constexpr int U = 4;
+    const int nq = n16 >> 1;  // 16-byte chunks of a code row
+    const uint4 *p0 = reinterpret_cast<const uint4 *>(r0);
+    const uint4 *p1 = reinterpret_cast<const uint4 *>(r1);
+    int c = lane;
+    for (; c + 32 * (U - 1) < nq; c += 32 * U) {
+        uint4 w0[U], w1[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            w0[u] = ld_stream(p0 + c + 32 * u);
+            w1[u] = ld_stream(p1 + c + 32 * u);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint4 xa = xs[2 * (c + 32 * u)], xb = xs[2 * (c + 32 * u) + 1];
+            a0 += dot16_q8(w0[u], xa, xb);
+            a1 += dot16_q8(w1[u], xa, xb);
+        }
+    }
+    for (; c < nq; c += 32) {
+        const uint4 w0 = ld_stream(p0 + c), w1 = ld_stream(p1 + c);
+        const uint4 xa = xs[2 * c], xb = xs[2 * c + 1];
+        a0 += dot16_q8(w0, xa, xb);
+        a1 += dot16_q8(w1, xa, xb);
+    }
+}
+
 // dot1_row_t<1> with the row already in shared memory: the same per-lane order, the same bits
 __device__ __forceinline__ float dot1_row_smem(const uint4 *w, const uint4 *xs, int n16, int lane) {
     constexpr int U = 8;
@@ -677,10 +728,14 @@ __host__ __device__ __forceinline__ size_t chain_stage_off(int H, int E) {
     return ((size_t)kChunkRows * kSlice * 2 + (size_t)H * 2 + (size_t)kSlice * 4 + (size_t)E * 4 + 15) & ~(size_t)15;
 }
 
+// Q8: the expert weights are E4M3 codes with fp32 scales per output row (gate/up rows of H
+// bytes, the down slice 32 bytes a row); the router stays bf16.
+template <bool Q8>
 __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __grid_constant__ ChainParams p) {
+    constexpr int kWB = Q8 ? 1 : 2;  // bytes per expert weight
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint16_t *wd = reinterpret_cast<uint16_t *>(smem);                           // [kChunkRows][kSlice]
+    uint8_t *wd = smem;                                                          // [kChunkRows][kSlice] weights
     uint4 *xs = reinterpret_cast<uint4 *>(smem + (size_t)kChunkRows * kSlice * 2);  // [H] bf16: x_l
     float *hsl = reinterpret_cast<float *>(xs + p.H / 8);                          // [kSlice]
     float *lg = hsl + kSlice;                                                      // [E] logits copy
@@ -709,10 +764,11 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
     __syncthreads();
     // TMA of rows [r0, r0 + rows) of a slice's columns into shared memory (as in K2)
     auto load_chunk = [&](const CUtensorMap *tm, int i0, int base_row, int r0, int rows) {
-        if (lane == 0) ptx::mbar_arrive_expect_tx(&tbar, (uint32_t)(rows * kSlice * 2));
+        if (lane == 0) ptx::mbar_arrive_expect_tx(&tbar, (uint32_t)(rows * kSlice * kWB));
         __syncwarp();
         if (lane < rows / kBoxRows)
-            ptx::tma_load_2d(wd + (size_t)lane * kBoxRows * kSlice, tm, i0, base_row + r0 + lane * kBoxRows, &tbar);
+            ptx::tma_load_2d(wd + (size_t)lane * kBoxRows * kSlice * kWB, tm, i0, base_row + r0 + lane * kBoxRows,
+                             &tbar);
     };
     // the router rows of warps 0..1 (e = b + nb * warp) are staged in shared memory while the
     // previous layer finishes, when every block has at most two rows of moderate length
@@ -784,7 +840,9 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
             float wt = 1.f;
             const CUtensorMap *tm = shared_task ? &p.tm_sdown[l] : &p.tm_down[l];
             int base_row = 0;
-            const uint16_t *wg = ly.ws_gate, *wu = ly.ws_up;
+            const uint8_t *wg = static_cast<const uint8_t *>(ly.ws_gate), *wu = static_cast<const uint8_t *>(ly.ws_up);
+            // Q8: the row scales of this item's gate/up rows and down rows
+            const float *sgr = ly.ss_gate, *sur = ly.ss_up, *sdr = ly.ss_down;
             if (!shared_task) {
                 if (!b1) {
                     if (!grid_wait(p.bar, t_b1, p.abort, p.status, (volatile int *)&s_flag)) { ok = false; break; }
@@ -814,17 +872,33 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
                 const int e = s_ids[slot];
                 wt = s_w[slot];
                 base_row = e * H;
-                wg = ly.w_gate + (size_t)e * p.I * H;
-                wu = ly.w_up + (size_t)e * p.I * H;
+                wg = static_cast<const uint8_t *>(ly.w_gate) + (size_t)e * p.I * H * kWB;
+                wu = static_cast<const uint8_t *>(ly.w_up) + (size_t)e * p.I * H * kWB;
+                if (Q8) {
+                    sgr = ly.s_gate + (size_t)e * p.I;
+                    sur = ly.s_up + (size_t)e * p.I;
+                    sdr = ly.s_down + (size_t)e * H;
+                }
             }
             if (warp == kLoadWarp) load_chunk(tm, i0, base_row, 0, rows0);
             pending = true;
             // h for features i0 .. i0+31: 16 warps x 2 features
             for (int f = warp; f < kSlice; f += kK2Warps) {
                 const size_t row = (size_t)(i0 + f);
-                float g[1] = {0.f}, u[1] = {0.f};
-                dot2_rows_t<1>(wg + row * H, wu + row * H, xs, n16, lane, s_zero, 1, g, u);
-                const float gs = warp_sum(g[0]), us = warp_sum(u[0]);
+                float gs, us;
+                if constexpr (Q8) {
+                    const float sg = __ldg(sgr + row), su = __ldg(sur + row);  // in flight with the rows
+                    float g = 0.f, u = 0.f;
+                    dot2_rows_q8(wg + row * H, wu + row * H, xs, n16, lane, g, u);
+                    gs = sg * warp_sum(g);
+                    us = su * warp_sum(u);
+                } else {
+                    float g[1] = {0.f}, u[1] = {0.f};
+                    dot2_rows_t<1>(reinterpret_cast<const uint16_t *>(wg) + row * H,
+                                   reinterpret_cast<const uint16_t *>(wu) + row * H, xs, n16, lane, s_zero, 1, g, u);
+                    gs = warp_sum(g[0]);
+                    us = warp_sum(u[0]);
+                }
                 if (lane == 0) hsl[f] = __bfloat162float(__float2bfloat16_rn(silu_mul(gs, us)));
             }
             if (!b1) {  // a shared-expert block: the accumulator is cleared once B1 completes
@@ -833,6 +907,15 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
             }
             for (int r0 = 0; r0 < H; r0 += kChunkRows, ph ^= 1u) {
                 const int rows = (H - r0) < kChunkRows ? (H - r0) : kChunkRows;
+                // Q8: this thread's down-row scales (rows tid + 512 i), in flight across the wait
+                float sdn[kChunkRows / kK2Threads];
+                if constexpr (Q8) {
+#pragma unroll
+                    for (int i = 0; i < kChunkRows / kK2Threads; ++i) {
+                        const int n = tid + i * kK2Threads;
+                        sdn[i] = n < rows ? __ldg(sdr + r0 + n) : 0.f;
+                    }
+                }
                 if (tid == 0 && !ptx::mbar_wait(&tbar, ph, kWaitLimitNs, (volatile int *)&s_abort)) s_ok = 0;
                 __syncthreads();
                 if (!s_ok) {
@@ -840,8 +923,40 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
                     break;
                 }
                 pending = false;
+                if constexpr (Q8) {
+#pragma unroll
+                    for (int i = 0; i < kChunkRows / kK2Threads; ++i) {
+                        const int n = tid + i * kK2Threads;
+                        if (n >= rows) break;  // rows is a multiple of 128: whole warps leave together
+                        const uint4 *rw = reinterpret_cast<const uint4 *>(wd + (size_t)n * kSlice);
+                        const uint4 q0 = rw[n & 1], q1 = rw[(n & 1) ^ 1];  // alternate halves against bank conflicts
+                        const float *h0 = hsl + (n & 1) * 16, *h1 = hsl + ((n & 1) ^ 1) * 16;
+                        const __nv_fp8x2_storage_t *c0 = reinterpret_cast<const __nv_fp8x2_storage_t *>(&q0);
+                        const __nv_fp8x2_storage_t *c1 = reinterpret_cast<const __nv_fp8x2_storage_t *>(&q1);
+                        float a = 0.f;
+#pragma unroll
+                        for (int m = 0; m < 8; ++m) {
+                            const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(c0[m], __NV_E4M3);
+                            const float2 fv = __half22float2(*reinterpret_cast<const __half2 *>(&r));
+                            a = fmaf(fv.x, h0[2 * m], a);
+                            a = fmaf(fv.y, h0[2 * m + 1], a);
+                        }
+#pragma unroll
+                        for (int m = 0; m < 8; ++m) {
+                            const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(c1[m], __NV_E4M3);
+                            const float2 fv = __half22float2(*reinterpret_cast<const __half2 *>(&r));
+                            a = fmaf(fv.x, h1[2 * m], a);
+                            a = fmaf(fv.y, h1[2 * m + 1], a);
+                        }
+                        a *= sdn[i];
+                        const float v1 = __shfl_down_sync(0xffffffffu, a, 1);
+                        const float v2 = __shfl_down_sync(0xffffffffu, a, 2);
+                        const float v3 = __shfl_down_sync(0xffffffffu, a, 3);
+                        if ((lane & 3) == 0) ptx::red_add_v4(&acc[r0 + n], wt * a, wt * v1, wt * v2, wt * v3);
+                    }
+                } else
                 for (int n = tid; n < rows; n += kK2Threads) {
-                    const uint4 *rw = reinterpret_cast<const uint4 *>(wd + (size_t)n * kSlice);
+                    const uint4 *rw = reinterpret_cast<const uint4 *>(wd + (size_t)n * kSlice * 2);
                     uint4 q[4];
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) q[cc] = rw[(cc + (n >> 1)) & 3];
@@ -968,29 +1083,30 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &tm_down, const
     }
 }
 
-cudaError_t launch_decode_chain(const ChainParams &p, cudaStream_t s) {
+cudaError_t launch_decode_chain(const ChainParams &p, bool q8, cudaStream_t s) {
     if (p.L < 1 || p.L > kChainMaxLayers || p.H % kBoxRows != 0 || p.H > 16384 || p.E < 1 || p.E > 1024 ||
         p.k < 1 || p.k > p.E || p.k > 32 || p.I % kSlice != 0 || p.Is % kSlice != 0)
         return cudaErrorInvalidValue;
+    const void *fn = q8 ? reinterpret_cast<const void *>(decode_chain_kernel<true>)
+                        : reinterpret_cast<const void *>(decode_chain_kernel<false>);
     const size_t smem = chain_smem(p.H, p.E);
-    static int per_sm[64] = {0};
+    static int per_sm[2][64] = {{0}};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 64) return cudaErrorInvalidDevice;
-    if (per_sm[dev] == 0) {
-        cudaError_t e = cudaFuncSetAttribute(decode_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)chain_smem(16384, 1024));
+    if (per_sm[q8][dev] == 0) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)chain_smem(16384, 1024));
         if (e != cudaSuccess) return e;
         int n = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_chain_kernel, kK2Threads, chain_smem(16384, 1024));
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kK2Threads, chain_smem(16384, 1024));
         if (e != cudaSuccess) return e;
         if (n < 1) return cudaErrorInvalidConfiguration;
-        per_sm[dev] = n;
+        per_sm[q8][dev] = n;
     }
     // every block must be resident at once (the layers are separated by grid barriers): at most
     // the blocks the GPU holds, each walking items blockIdx.x + i * gridDim.x
     const int n_items = p.Is / kSlice + p.k * (p.I / kSlice);
-    int grid = per_sm[dev] * device_info().sm_count;
+    int grid = per_sm[q8][dev] * device_info().sm_count;
     if (n_items < grid) grid = n_items;
     cudaError_t e = cudaMemsetAsync(p.bar, 0, sizeof(unsigned), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(p.abort, 0, sizeof(int), s);
@@ -1006,8 +1122,47 @@ cudaError_t launch_decode_chain(const ChainParams &p, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     LaunchScope scope(KC_DECODE_CHAIN, s);
-    e = cudaLaunchKernelEx(&cfg, decode_chain_kernel, p);
+    ChainParams pc = p;
+    void *args[] = {&pc};
+    e = cudaLaunchKernelExC(&cfg, fn, args);
     return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+namespace {
+// One block per row: the row's largest magnitude, then its codes.  fp32 arithmetic with IEEE
+// division, so that the scale and every code follow from the row's values alone.
+__global__ void __launch_bounds__(256) quantize_e4m3_kernel(const uint16_t *__restrict__ w, int cols,
+                                                            uint8_t *__restrict__ q, float *__restrict__ scale) {
+    __shared__ float red[8];
+    __shared__ float s_scale;
+    const int r = blockIdx.x, tid = threadIdx.x;
+    const uint16_t *row = w + (size_t)r * cols;
+    float amax = 0.f;
+    for (int c = tid; c < cols; c += 256) amax = fmaxf(amax, fabsf(bf16_to_f(row[c])));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if ((tid & 31) == 0) red[tid >> 5] = amax;
+    __syncthreads();
+    if (tid == 0) {
+        float m = red[0];
+        for (int i = 1; i < 8; ++i) m = fmaxf(m, red[i]);
+        const float sc = m > 0.f ? __fdiv_rn(m, 448.0f) : 1.0f;
+        s_scale = sc;
+        scale[r] = sc;
+    }
+    __syncthreads();
+    const float sc = s_scale;
+    for (int c = tid; c < cols; c += 256)
+        q[(size_t)r * cols + c] =
+            (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(bf16_to_f(row[c]), sc), __NV_SATFINITE, __NV_E4M3);
+}
+}  // namespace
+
+cudaError_t launch_quantize_e4m3(const uint16_t *w, int rows, int cols, uint8_t *q, float *scale, cudaStream_t s) {
+    if (rows <= 0 || cols <= 0) return cudaSuccess;
+    LaunchScope scope(KC_QUANTIZE, s);
+    quantize_e4m3_kernel<<<rows, 256, 0, s>>>(w, cols, q, scale);
+    return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -26,6 +26,7 @@ enum KernelClass {
     KC_DECODE_EXPERTS,    // decode: top-k, expert gate/up slices, split-K down, combine
     KC_GATHER_X,          // token rows copied into expert-sorted order
     KC_DECODE_CHAIN,      // decode: a chain of layers in one cooperative launch
+    KC_QUANTIZE,          // row-wise E4M3 quantisation of weights
     KC_COUNT
 };
 
@@ -190,10 +191,13 @@ constexpr int kChainMaxLayers = 64;
 struct ChainLayer {
     const uint16_t *w_router;
     const float *b_router;
-    const uint16_t *w_gate, *w_up, *ws_gate, *ws_up;
+    // bf16 expert rows, or (the E4M3 chain) their byte codes
+    const void *w_gate, *w_up, *ws_gate, *ws_up;
+    // E4M3 chain only: fp32 scales per output row (gate/up [E, I], down [E, H]; shared [Is], [H])
+    const float *s_gate, *s_up, *s_down, *ss_gate, *ss_up, *ss_down;
 };
 struct ChainParams {
-    CUtensorMap tm_down[kChainMaxLayers];   // w_down as [E*H, I], decode box (see launch_decode)
+    CUtensorMap tm_down[kChainMaxLayers];   // w_down as [E*H, I] (bf16 or bytes), decode box
     CUtensorMap tm_sdown[kChainMaxLayers];  // ws_down as [H, Is]
     ChainLayer lay[kChainMaxLayers];
     int H, E, k, I, Is, L;
@@ -207,7 +211,12 @@ struct ChainParams {
     int *abort;             // zero at launch; set by a block that gives up
     int *status;            // device status word
 };
-cudaError_t launch_decode_chain(const ChainParams &p, cudaStream_t s);
+// q8: expert weights as E4M3 codes with fp32 row scales (ChainLayer's s_*), W_d maps over bytes
+cudaError_t launch_decode_chain(const ChainParams &p, bool q8, cudaStream_t s);
+// Row-wise E4M3 quantisation: scale[r] = max_c |w[r,c]| / 448 (1 for a zero row),
+// q[r,c] = E4M3(w[r,c] / scale[r]), fp32 arithmetic, round to nearest even, saturating.
+cudaError_t launch_quantize_e4m3(const uint16_t *w, int rows, int cols, uint8_t *q, float *scale,
+                                 cudaStream_t s);
 
 constexpr int kTileN = 256;   // tokens per GEMM tile (MMA N upper bound)
 constexpr int kTileM = 128;   // weight rows per GEMM tile (MMA M)

@@ -36,7 +36,7 @@ const char *const kClassNames[KC_COUNT] = {
     "router_gemm", "topk",          "permute",     "tile_prefix",   "gateup_gemm",
     "down_gemm",   "shared_gateup", "shared_down", "finalize",      "combine",
     "zero",        "decode_router", "decode_experts", "gather_x",
-    "decode_chain"};
+    "decode_chain", "quantize"};
 }  // namespace
 
 const char *kernel_class_name(int kc) { return (kc >= 0 && kc < KC_COUNT) ? kClassNames[kc] : nullptr; }
@@ -95,19 +95,26 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 }  // namespace
 
-bool encode_tmap_2d_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
-                         uint32_t box_rows, uint32_t box_cols, bool swizzle128) {
+namespace {
+bool encode_tmap_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                    uint32_t box_cols, bool swizzle128, CUtensorMapDataType dtype, uint64_t esize) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
     if (!enc) return false;
     cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
+    cuuint64_t strides[1] = {cols * esize};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+    CUresult r = enc(map, dtype, 2, const_cast<void *>(base), dims, strides, box,
                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+}  // namespace
+
+bool encode_tmap_2d_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                         uint32_t box_rows, uint32_t box_cols, bool swizzle128) {
+    return encode_tmap_2d(map, base, rows, cols, box_rows, box_cols, swizzle128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2);
 }
 
 // -------------------------------------------------------------- workspace layout --
@@ -598,29 +605,51 @@ moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const moe_bf
     return MOE_OK;
 }
 
-moe_status moe_decode_chain(const moe_config *cfg, const moe_weights *layers, int n_layers, const moe_bf16 *x0,
-                            const moe_bf16 *resid, moe_bf16 *out, moe_bf16 *x_last, void *ws, size_t ws_bytes,
-                            void *stream) {
-    NvtxRange nvtx_range("moe_decode_chain");
+namespace {
+// The part of a chain launch both weight formats share: shape, token and workspace pointers.
+moe_status chain_common(const moe_config *cfg, int n_layers, const moe_bf16 *x0, const moe_bf16 *resid,
+                        moe_bf16 *out, moe_bf16 *x_last, void *ws, size_t ws_bytes, ChainParams &p) {
     MOE_TRY(check_config(cfg));
-    if (!layers || n_layers < 1) return MOE_ERR_INVALID_ARG;
+    if (n_layers < 1) return MOE_ERR_INVALID_ARG;
     if (n_layers > kChainMaxLayers) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (!decode_fits(1, cfg->hidden)) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (!x0 || !out || !aligned16(x0) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
     if ((resid && !aligned16(resid)) || (x_last && !aligned16(x_last))) return MOE_ERR_INVALID_ARG;
-    for (int l = 0; l < n_layers; ++l) MOE_TRY(check_weights(cfg, &layers[l], true, true));
     MOE_TRY(check_ws(cfg, ws, ws_bytes, 1));
     const Layout L = layout(*cfg, 1);
-    const int H = cfg->hidden;
-    // about 20 KB: the per-layer pointers and down-projection tensor maps travel as the kernel's
-    // parameter block
-    static thread_local ChainParams p;
-    p.H = H;
+    p.H = cfg->hidden;
     p.E = cfg->n_experts;
     p.k = cfg->top_k;
     p.I = cfg->inter;
     p.Is = cfg->shared_inter;
     p.L = n_layers;
+    p.x0 = x0;
+    p.resid = resid;
+    p.out = out;
+    p.x_last = x_last;
+    p.logits = at<float>(ws, L.logits);
+    p.acc0 = at<float>(ws, L.acc);
+    p.acc1 = at<float>(ws, L.y);  // (k + 1) * H bf16 >= H fp32
+    int *st = at<int>(ws, L.status);
+    p.status = st;
+    // st[1] is the one-layer path's ticket counter; the chain's barrier count and abort flag follow
+    p.bar = reinterpret_cast<unsigned *>(st + 2);
+    p.abort = st + 3;
+    return MOE_OK;
+}
+}  // namespace
+
+moe_status moe_decode_chain(const moe_config *cfg, const moe_weights *layers, int n_layers, const moe_bf16 *x0,
+                            const moe_bf16 *resid, moe_bf16 *out, moe_bf16 *x_last, void *ws, size_t ws_bytes,
+                            void *stream) {
+    NvtxRange nvtx_range("moe_decode_chain");
+    if (!layers) return MOE_ERR_INVALID_ARG;
+    // about 20 KB: the per-layer pointers and down-projection tensor maps travel as the kernel's
+    // parameter block
+    static thread_local ChainParams p;
+    MOE_TRY(chain_common(cfg, n_layers, x0, resid, out, x_last, ws, ws_bytes, p));
+    for (int l = 0; l < n_layers; ++l) MOE_TRY(check_weights(cfg, &layers[l], true, true));
+    const int H = cfg->hidden;
     const uint32_t sl = (uint32_t)decode_slice(), br = (uint32_t)decode_box_rows();
     for (int l = 0; l < n_layers; ++l) {
         const moe_weights &w = layers[l];
@@ -634,19 +663,54 @@ moe_status moe_decode_chain(const moe_config *cfg, const moe_weights *layers, in
             p.tm_sdown[l] = p.tm_down[l];
         }
     }
-    p.x0 = x0;
-    p.resid = resid;
-    p.out = out;
-    p.x_last = x_last;
-    p.logits = at<float>(ws, L.logits);
-    p.acc0 = at<float>(ws, L.acc);
-    p.acc1 = at<float>(ws, L.y);  // (k + 1) * H bf16 >= H fp32
-    int *st = at<int>(ws, L.status);
-    p.status = st;
-    // st[1] is the one-layer path's ticket counter; the chain's barrier count and abort flag follow
-    p.bar = reinterpret_cast<unsigned *>(st + 2);
-    p.abort = st + 3;
-    MOE_CUDA(launch_decode_chain(p, static_cast<cudaStream_t>(stream)));
+    MOE_CUDA(launch_decode_chain(p, false, static_cast<cudaStream_t>(stream)));
+    return MOE_OK;
+}
+
+moe_status moe_decode_chain_q8(const moe_config *cfg, const moe_weights_q8 *layers, int n_layers,
+                               const moe_bf16 *x0, const moe_bf16 *resid, moe_bf16 *out, moe_bf16 *x_last,
+                               void *ws, size_t ws_bytes, void *stream) {
+    NvtxRange nvtx_range("moe_decode_chain_q8");
+    if (!layers) return MOE_ERR_INVALID_ARG;
+    static thread_local ChainParams p;
+    MOE_TRY(chain_common(cfg, n_layers, x0, resid, out, x_last, ws, ws_bytes, p));
+    const bool shared = cfg->shared_inter > 0;
+    for (int l = 0; l < n_layers; ++l) {
+        const moe_weights_q8 &w = layers[l];
+        if (!w.w_router || !aligned16(w.w_router) || !w.q_gate || !w.q_up || !w.q_down || !w.s_gate ||
+            !w.s_up || !w.s_down || !aligned16(w.q_gate) || !aligned16(w.q_up) || !aligned16(w.q_down))
+            return MOE_ERR_INVALID_ARG;
+        if (shared && (!w.qs_gate || !w.qs_up || !w.qs_down || !w.ss_gate || !w.ss_up || !w.ss_down ||
+                       !aligned16(w.qs_gate) || !aligned16(w.qs_up) || !aligned16(w.qs_down)))
+            return MOE_ERR_INVALID_ARG;
+    }
+    const int H = cfg->hidden;
+    const uint32_t sl = (uint32_t)decode_slice(), br = (uint32_t)decode_box_rows();
+    for (int l = 0; l < n_layers; ++l) {
+        const moe_weights_q8 &w = layers[l];
+        p.lay[l] = ChainLayer{w.w_router, w.b_router, w.q_gate, w.q_up, w.qs_gate, w.qs_up,
+                              w.s_gate, w.s_up, w.s_down, w.ss_gate, w.ss_up, w.ss_down};
+        if (!encode_tmap_2d(&p.tm_down[l], w.q_down, (uint64_t)cfg->n_experts * H, cfg->inter, br, sl, false,
+                            CU_TENSOR_MAP_DATA_TYPE_UINT8, 1))
+            return MOE_ERR_CUDA;
+        if (shared) {
+            if (!encode_tmap_2d(&p.tm_sdown[l], w.qs_down, H, cfg->shared_inter, br, sl, false,
+                                CU_TENSOR_MAP_DATA_TYPE_UINT8, 1))
+                return MOE_ERR_CUDA;
+        } else {
+            p.tm_sdown[l] = p.tm_down[l];
+        }
+    }
+    MOE_CUDA(launch_decode_chain(p, true, static_cast<cudaStream_t>(stream)));
+    return MOE_OK;
+}
+
+moe_status moe_quantize_e4m3(const moe_bf16 *w, int rows, int cols, uint8_t *q, float *scale, void *stream) {
+    NvtxRange nvtx_range("moe_quantize_e4m3");
+    if (rows < 0 || cols < 0) return MOE_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return MOE_OK;
+    if (!w || !q || !scale) return MOE_ERR_INVALID_ARG;
+    MOE_CUDA(launch_quantize_e4m3(w, rows, cols, q, scale, static_cast<cudaStream_t>(stream)));
     return MOE_OK;
 }
 

@@ -78,10 +78,8 @@ def _normal_bf16(gen, shape, std, device):
     return t.to(torch.bfloat16)
 
 
-def make_layer(w: Workload, gen: torch.Generator, device) -> dict:
-    """Draw one layer's weights (see the module docstring for the order)."""
-    s = w.shape
-    H, E, I, Is = s.hidden, s.n_experts, s.inter, s.shared_inter
+def _make_router(w: Workload, gen: torch.Generator, device) -> dict:
+    E, H = w.shape.n_experts, w.shape.hidden
     layer = {"w_router": _normal_bf16(gen, (E, H), w.router_std, device)}
     if w.zipf_s is not None:
         rank = torch.randperm(E, generator=gen, device=device).to(torch.float64) + 1.0
@@ -91,6 +89,14 @@ def make_layer(w: Workload, gen: torch.Generator, device) -> dict:
         layer["b_router"] = b.to(torch.float32)
     else:
         layer["b_router"] = None
+    return layer
+
+
+def make_layer(w: Workload, gen: torch.Generator, device) -> dict:
+    """Draw one layer's weights (see the module docstring for the order)."""
+    s = w.shape
+    H, E, I, Is = s.hidden, s.n_experts, s.inter, s.shared_inter
+    layer = _make_router(w, gen, device)
     layer["w_gate"] = _normal_bf16(gen, (E, I, H), w.w_std, device)
     layer["w_up"] = _normal_bf16(gen, (E, I, H), w.w_std, device)
     layer["w_down"] = _normal_bf16(gen, (E, H, I), w.w_std, device)
@@ -112,6 +118,50 @@ def make(w: Workload, device="cpu", n_layers: Optional[int] = None, T: Optional[
     gen.manual_seed(w.seed)
     L = w.n_layers if n_layers is None else n_layers
     layers = [make_layer(w, gen, device) for _ in range(L)]
+    TT = w.T if T is None else T
+    x = _normal_bf16(gen, (TT, w.shape.hidden), w.x_std, device)
+    return layers, x
+
+
+def _e4m3_codes(gen, shape, device):
+    """Uniform draws over the 254 finite E4M3 bit patterns (0x7F and 0xFF, the NaNs, excluded).
+    Bit patterns only: nothing here decodes them."""
+    c = torch.randint(0, 254, shape, generator=gen, device=device, dtype=torch.int32)
+    c = c + (c >= 0x7F).to(torch.int32)                # skip 0x7F
+    return c.to(torch.uint8)
+
+
+def _scales(gen, shape, base, device):
+    s = torch.empty(shape, dtype=torch.float32, device=device)
+    s.uniform_(0.5 * base, 1.5 * base, generator=gen)
+    return s
+
+
+def make_q8(w: Workload, device="cpu", n_layers: Optional[int] = None, T: Optional[int] = None,
+            scale_base: float = 2e-4):
+    """Layers with E4M3 expert weights and the input x, for the quantised-weight path.
+
+    Per layer, in this order: W_r and b as in ``make_layer``; then for W_g, W_u, W_d and the shared
+    expert's three matrices, the codes (uniform over the finite bit patterns) followed by one fp32
+    scale per row, uniform in [0.5, 1.5] * scale_base.  Uniform codes have an RMS value near 100, so
+    the default base puts the dequantised weights near the bf16 workloads' 0.02.  Then x ~ N(0, 1).
+    Keys: w_router, b_router, q_gate/q_up/q_down with s_gate/s_up/s_down, and qs_*/ss_* for the
+    shared expert (absent when I_s = 0).
+    """
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed)
+    s = w.shape
+    H, E, I, Is = s.hidden, s.n_experts, s.inter, s.shared_inter
+    layers = []
+    for _ in range(w.n_layers if n_layers is None else n_layers):
+        layer = _make_router(w, gen, device)
+        mats = [("q_gate", "s_gate", (E, I, H)), ("q_up", "s_up", (E, I, H)), ("q_down", "s_down", (E, H, I))]
+        if Is > 0:
+            mats += [("qs_gate", "ss_gate", (Is, H)), ("qs_up", "ss_up", (Is, H)), ("qs_down", "ss_down", (H, Is))]
+        for qn, sn, shp in mats:
+            layer[qn] = _e4m3_codes(gen, shp, device)
+            layer[sn] = _scales(gen, shp[:-1], scale_base, device)
+        layers.append(layer)
     TT = w.T if T is None else T
     x = _normal_bf16(gen, (TT, w.shape.hidden), w.x_std, device)
     return layers, x

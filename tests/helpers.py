@@ -37,6 +37,13 @@ def bf16_f64(bits):
     return orc.bf16_to_f64(bits)
 
 
+def residual_step(r_u16, out_u16):
+    """bf16(r + out) of bf16 bit patterns: the exact sum rounded to bf16 once (for two bf16
+    operands the kernel's fp32 sum is exact, or its error is far below half a bf16 step)."""
+    v = orc.bf16_to_f64(r_u16) + orc.bf16_to_f64(out_u16)
+    return np.array([orc.double_to_bf16(t) for t in v.ravel()], dtype=np.uint16).reshape(v.shape)
+
+
 def abs_bound(ref_f64):
     """Per-element absolute bound: 2e-2, or two bf16 spacings at |ref| where that is larger.
 

@@ -12,7 +12,7 @@ import torch
 from oracle import moe_oracle as orc
 from sparse_moe_router_gb300 import abi, inputs
 
-from helpers import cfg_of, check_layer, compare_out, forward_gpu, host, make, route_gpu, u16
+from helpers import cfg_of, check_layer, compare_out, forward_gpu, host, make, residual_step, route_gpu, u16
 
 pytestmark = pytest.mark.gpu
 
@@ -29,13 +29,6 @@ def _chain(shape, layers, x0, n, resid=None, ws=None):
     torch.cuda.synchronize()
     assert abi.moe_check_status(ws) == 0
     return out, x_last
-
-
-def _residual_step(r_u16, out_u16):
-    """bf16(r + out) of bf16 bit patterns: the exact sum rounded to bf16 once (for two bf16
-    operands the kernel's fp32 sum is exact, or its error is far below half a bf16 step)."""
-    v = orc.bf16_to_f64(r_u16) + orc.bf16_to_f64(out_u16)
-    return np.array([orc.double_to_bf16(t) for t in v.ravel()], dtype=np.uint16).reshape(v.shape)
 
 
 def _layer_ref(shape, layer, x):
@@ -61,7 +54,7 @@ def test_chain_layer_by_layer(shape, L, use_resid):
         ref = _layer_ref(shape, layers[n - 1], x_in)
         compare_out(u16(out), ref, what="chain layer %d out" % (n - 1))
         r = u16(resid) if use_resid else u16(x_in)
-        np.testing.assert_array_equal(u16(x_last), _residual_step(r, u16(out)))
+        np.testing.assert_array_equal(u16(x_last), residual_step(r, u16(out)))
         x_in = x_last
 
 
