@@ -151,7 +151,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 template <int EPI>
 __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
     gemm_kernel(const GemmArgs p, const __grid_constant__ CUtensorMap tm_a0,
-                const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_b,
+                const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ TokenMaps tm_b,
                 const __grid_constant__ CUtensorMap tm_s0, const __grid_constant__ CUtensorMap tm_s1) {
     using C = Cfg<EPI>;
     constexpr int kStages = C::kStages;
@@ -244,7 +244,9 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
         if (tid == kProdWarp0 * 32) {
             ptx::tma_prefetch_desc(&tm_a0);
             if (EPI == EPI_SWIGLU) ptx::tma_prefetch_desc(&tm_a1);
-            ptx::tma_prefetch_desc(&tm_b);
+#pragma unroll
+            for (int i = 0; i < kTokenBoxes; ++i) ptx::tma_prefetch_desc(&tm_b.m[i]);
+            if (p.shared_b_own) ptx::tma_prefetch_desc(&tm_b.shared);
             if (p.shared_last) {
                 ptx::tma_prefetch_desc(&tm_s0);
                 if (EPI == EPI_SWIGLU) ptx::tma_prefetch_desc(&tm_s1);
@@ -262,12 +264,18 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
                 const int arow = (shg ? 0 : t.g * p.F) + ftile * C::kFT;
                 const void *ma0 = shg ? (const void *)&tm_s0 : (const void *)&tm_a0;
                 const void *ma1 = shg ? (const void *)&tm_s1 : (const void *)&tm_a1;
-                // token rows: this CTA holds columns [rank * N/2, (rank + 1) * N/2) of the MMA
-                const int brow = t.row0 + (int)rank * (((t.nvalid + 15) & ~15) >> 1);
+                // token rows: this CTA holds columns [rank * N/2, (rank + 1) * N/2) of the MMA, loaded
+                // with the smallest box that holds N/2 rows (both CTAs use the same box)
+                const int half = ((t.nvalid + 15) & ~15) >> 1;
+                const bool own = shg && p.shared_b_own;
+                const int nbox = own ? kTokenBoxes : (half + 15) >> 4;  // box rows / 16, 1..kTokenBoxes
+                const void *mb = own ? (const void *)&tm_b.shared : (const void *)&tm_b.m[nbox - 1];
+                const int brow = (own ? t.row0 - g_rows[G - 1] : t.row0) + (int)rank * half;
+                const uint32_t stage_tx = 2u * (uint32_t)kKB * (uint32_t)(kABytes + nbox * 16 * BK * 2);
                 for (int ks = 0; ks < nks; ++ks, ++it) {
                     if (!ptx::mbar_wait(&empty[s], ph ^ 1u, kWaitLimitNs, abort_flag)) { ok = false; break; }
                     const uint32_t bar = full_even + (uint32_t)(s * 8);
-                    if (rank == 0) ptx::mbar_arrive_expect_tx(&full[s], 2 * kStageBytes);
+                    if (rank == 0) ptx::mbar_arrive_expect_tx(&full[s], stage_tx);
 #pragma unroll
                     for (int j = 0; j < kKB; ++j) {
                         uint8_t *st = smem + s * kStageBytes + j * kStepBytes;
@@ -278,7 +286,7 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
                         } else {
                             ptx::tma_load_2d_pair(st, ma0, kc, arow, bar);
                         }
-                        ptx::tma_load_2d_pair(st + kABytes, &tm_b, kc, brow, bar);
+                        ptx::tma_load_2d_pair(st + kABytes, mb, kc, brow, bar);
                     }
                     if (++s == kStages) { s = 0; ph ^= 1u; }
                 }
@@ -513,7 +521,7 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
 
 template <int EPI>
 cudaError_t launch_impl(const GemmArgs &a, const CUtensorMap &m0, const CUtensorMap &m1,
-                        const CUtensorMap &mb, const CUtensorMap &s0, const CUtensorMap &s1, int kc,
+                        const TokenMaps &mb, const CUtensorMap &s0, const CUtensorMap &s1, int kc,
                         cudaStream_t s) {
     using C = Cfg<EPI>;
     // per device: the shared-memory opt-in and how many CTA pairs fit on the GPU at once
@@ -559,7 +567,7 @@ cudaError_t launch_impl(const GemmArgs &a, const CUtensorMap &m0, const CUtensor
 }  // namespace
 
 cudaError_t launch_gemm(GemmEpi epi, const GemmArgs &a, const CUtensorMap &tm_a0, const CUtensorMap &tm_a1,
-                        const CUtensorMap &tm_b, const CUtensorMap &tm_s0, const CUtensorMap &tm_s1, int kc,
+                        const TokenMaps &tm_b, const CUtensorMap &tm_s0, const CUtensorMap &tm_s1, int kc,
                         cudaStream_t s) {
     if (a.n_groups > kMaxGroups - 1) return cudaErrorInvalidValue;
     if (a.K % (2 * BK) != 0 || a.K <= 0) return cudaErrorInvalidValue;
@@ -567,6 +575,7 @@ cudaError_t launch_gemm(GemmEpi epi, const GemmArgs &a, const CUtensorMap &tm_a0
     if (a.tile_cap != 0 && a.group_rows != nullptr) return cudaErrorInvalidValue;  // groups use 256
     if (a.shared_last && (a.group_rows == nullptr || a.n_groups < 2))
         return cudaErrorInvalidValue;
+    if (a.shared_b_own && !a.shared_last) return cudaErrorInvalidValue;
     if (epi == EPI_SWIGLU && (a.F % 64 != 0 || a.ld % 8 != 0)) return cudaErrorInvalidValue;
     if (epi == EPI_COMBINE && (a.F % BM != 0 || a.ld % 8 != 0)) return cudaErrorInvalidValue;
     switch (epi) {

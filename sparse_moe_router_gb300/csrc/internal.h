@@ -55,6 +55,22 @@ bool encode_tmap_2d_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint
 
 // ---- GEMM (tcgen05, swap-AB: weight rows on M, tokens on N) ---------------------------
 
+constexpr int kTileN = 256;   // tokens per GEMM tile (MMA N upper bound)
+constexpr int kTileM = 128;   // weight rows per GEMM tile (MMA M)
+// token rows per TMA box of a GEMM's token operand: each CTA of a pair holds half a tile
+constexpr int kTokenBoxRows = kTileN / 2;
+// The token operand's maps: m[i] has a box of 16 (i + 1) rows x 64 columns, so that each CTA
+// loads, in one TMA instruction a K block, the smallest box that holds its half of a tile.
+// `shared` (box kTokenBoxRows rows) is the shared expert's token rows when they live in a
+// buffer of their own (GemmArgs::shared_b_own).
+constexpr int kTokenBoxes = kTokenBoxRows / 16;
+struct TokenMaps {
+    CUtensorMap m[kTokenBoxes];
+    CUtensorMap shared;
+};
+// m[] over [rows, cols] bf16 at base; `shared` set to m[kTokenBoxes - 1]
+bool encode_token_maps(TokenMaps *tm, const void *base, uint64_t rows, uint64_t cols);
+
 // EPI_F32: out[r, f] = D + bias[f] (fp32).  EPI_SWIGLU: h = bf16(silu(gate) * up).
 // EPI_COMBINE: out[epi_tok[r], f] = bf16(epi_w[r] * D) -- the weighted expert rows, stored in
 // pair order for the combine that follows.
@@ -94,21 +110,24 @@ struct GemmArgs {
     const int32_t *epi_tok;
     const float *epi_w;
     int *status;
-    // token tile cap (a multiple of 16, <= 256; 0 = 256).  The B tensor map's box is
-    // kTokenBoxRows rows: each CTA of a pair loads at most half a tile
+    // token tile cap (a multiple of 16, <= 256; 0 = 256).  Each CTA of a pair loads half a
+    // tile: N/2 rows, N = the tile's rows rounded up to 16
     int tile_cap;
     // the last group is the shared expert: its weight rows come from the tm_s* maps (row
     // ftile*kFT of the shared matrix), its tiles are interleaved evenly among the routed ones,
     // and the combine epilogue stores its rows in place with weight 1
     bool shared_last;
+    // with shared_last: the last group's token rows are rows 0.. of the TokenMaps' `shared` map
+    // (the tokens in order, e.g. x itself) instead of rows group_rows[G-1].. of the m[] maps
+    bool shared_b_own;
 };
 
 // Launch the persistent grouped GEMM.  tm_a0 (and tm_a1 for EPI_SWIGLU: the up projection)
-// are 2-D tensor maps over the weight rows (64- or 128-row box, 64 columns); tm_b is a map over
-// the B rows ([rows, K], box of tile_cap rows x 64).  tm_s0 / tm_s1 are the shared expert's
+// are 2-D tensor maps over the weight rows (64- or 128-row box, 64 columns); tm_b holds the maps
+// over the B rows ([rows, K], see TokenMaps).  tm_s0 / tm_s1 are the shared expert's
 // weight maps, read for the last group when a.shared_last (pass any map otherwise).
 cudaError_t launch_gemm(GemmEpi epi, const GemmArgs &a, const CUtensorMap &tm_a0, const CUtensorMap &tm_a1,
-                        const CUtensorMap &tm_b, const CUtensorMap &tm_s0, const CUtensorMap &tm_s1, int kc,
+                        const TokenMaps &tm_b, const CUtensorMap &tm_s0, const CUtensorMap &tm_s1, int kc,
                         cudaStream_t s);
 
 // ---- routing / permutation / elementwise ---------------------------------------------
@@ -217,11 +236,6 @@ cudaError_t launch_decode_chain(const ChainParams &p, bool q8, cudaStream_t s);
 // q[r,c] = E4M3(w[r,c] / scale[r]), fp32 arithmetic, round to nearest even, saturating.
 cudaError_t launch_quantize_e4m3(const uint16_t *w, int rows, int cols, uint8_t *q, float *scale,
                                  cudaStream_t s);
-
-constexpr int kTileN = 256;   // tokens per GEMM tile (MMA N upper bound)
-constexpr int kTileM = 128;   // weight rows per GEMM tile (MMA M)
-// token rows per TMA box of a GEMM's token operand: each CTA of a pair holds half a tile
-constexpr int kTokenBoxRows = kTileN / 2;
 
 // Token tiles of a group of c rows: ceil(c / 256) tiles of equal size rounded up to 16 (the
 // MMA's N granularity); the last tile takes the remainder.  Shared by the permutation (tile

@@ -117,6 +117,13 @@ bool encode_tmap_2d_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint
     return encode_tmap_2d(map, base, rows, cols, box_rows, box_cols, swizzle128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2);
 }
 
+bool encode_token_maps(TokenMaps *tm, const void *base, uint64_t rows, uint64_t cols) {
+    for (int i = 0; i < kTokenBoxes; ++i)
+        if (!encode_tmap_2d_bf16(&tm->m[i], base, rows, cols, (uint32_t)(16 * (i + 1)), 64)) return false;
+    tm->shared = tm->m[kTokenBoxes - 1];
+    return true;
+}
+
 // -------------------------------------------------------------- workspace layout --
 
 namespace {
@@ -224,9 +231,10 @@ moe_status cuda_status(cudaError_t e) {
 constexpr int kRouterTileN = MOE_ROUTER_TILE_N;
 moe_status run_router_gemm(const moe_config &c, const moe_weights &w, const uint16_t *x, int T,
                            float *logits, int *status, cudaStream_t s) {
-    CUtensorMap tm, tb;
+    CUtensorMap tm;
+    TokenMaps tb;
     if (!encode_tmap_2d_bf16(&tm, w.w_router, (uint64_t)c.n_experts, (uint64_t)c.hidden, kTileM, 64) ||
-        !encode_tmap_2d_bf16(&tb, x, (uint64_t)T, (uint64_t)c.hidden, kTokenBoxRows, 64))
+        !encode_token_maps(&tb, x, (uint64_t)T, (uint64_t)c.hidden))
         return MOE_ERR_CUDA;
     GemmArgs a{};
     a.b_src = x;
@@ -248,12 +256,13 @@ moe_status run_router_gemm(const moe_config &c, const moe_weights &w, const uint
 // rows and the same features' up rows.
 moe_status run_shared(const moe_config &c, const moe_weights &w, const uint16_t *x, int T,
                       uint16_t *h_s, float *out, int *status, cudaStream_t s) {
-    CUtensorMap tg, tu, td, tx, th;
+    CUtensorMap tg, tu, td;
+    TokenMaps tx, th;
     if (!encode_tmap_2d_bf16(&tg, w.ws_gate, c.shared_inter, c.hidden, kTileM / 2, 64) ||
         !encode_tmap_2d_bf16(&tu, w.ws_up, c.shared_inter, c.hidden, kTileM / 2, 64) ||
         !encode_tmap_2d_bf16(&td, w.ws_down, c.hidden, c.shared_inter, kTileM, 64) ||
-        !encode_tmap_2d_bf16(&tx, x, (uint64_t)T, c.hidden, kTokenBoxRows, 64) ||
-        !encode_tmap_2d_bf16(&th, h_s, (uint64_t)T, c.shared_inter, kTokenBoxRows, 64))
+        !encode_token_maps(&tx, x, (uint64_t)T, c.hidden) ||
+        !encode_token_maps(&th, h_s, (uint64_t)T, c.shared_inter))
         return MOE_ERR_CUDA;
     GemmArgs a{};
     a.b_src = x;
@@ -282,8 +291,8 @@ moe_status run_shared(const moe_config &c, const moe_weights &w, const uint16_t 
 // (xp), then the down projection either stored per row in fp32 (y_rows, unfused) or weighted
 // and stored as bf16 rows in pair order (y_pairs[perm[r]] = bf16(row_w[r] * y)) for the
 // combine.  with_shared: the shared expert (I_s == I) runs as one more group of the T tokens
-// in order: rows P .. P+T-1 of xp, h and y_pairs (weight 1); offsets/tiles then hold E + 2
-// entries.
+// in order, read straight from x, into rows P .. P+T-1 of h and y_pairs (weight 1);
+// offsets/tiles then hold E + 2 entries.
 moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t *x, int T,
                       const int32_t *offsets, const int32_t *tiles, const int32_t *row_tok,
                       const int32_t *perm, const float *row_w, uint16_t *xp, uint16_t *h, float *y_rows,
@@ -291,12 +300,15 @@ moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t 
     const uint64_t EI = (uint64_t)c.n_experts * c.inter;
     const uint64_t P = (uint64_t)T * c.top_k;
     const uint64_t rows = P + (with_shared ? (uint64_t)T : 0);
-    CUtensorMap tg, tu, td, tx, th, tsg, tsu, tsd;
+    CUtensorMap tg, tu, td, tsg, tsu, tsd;
+    TokenMaps tx, th;
     if (!encode_tmap_2d_bf16(&tg, w.w_gate, EI, c.hidden, kTileM / 2, 64) ||
         !encode_tmap_2d_bf16(&tu, w.w_up, EI, c.hidden, kTileM / 2, 64) ||
         !encode_tmap_2d_bf16(&td, w.w_down, (uint64_t)c.n_experts * c.hidden, c.inter, kTileM, 64) ||
-        !encode_tmap_2d_bf16(&tx, xp, rows, c.hidden, kTokenBoxRows, 64) ||
-        !encode_tmap_2d_bf16(&th, h, rows, c.inter, kTokenBoxRows, 64))
+        !encode_token_maps(&tx, xp, P, c.hidden) || !encode_token_maps(&th, h, rows, c.inter))
+        return MOE_ERR_CUDA;
+    // the shared expert's token rows are x itself, in order
+    if (with_shared && !encode_tmap_2d_bf16(&tx.shared, x, (uint64_t)T, c.hidden, kTokenBoxRows, 64))
         return MOE_ERR_CUDA;
     if (with_shared) {
         if (!encode_tmap_2d_bf16(&tsg, w.ws_gate, c.shared_inter, c.hidden, kTileM / 2, 64) ||
@@ -308,9 +320,8 @@ moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t 
         tsu = tu;
         tsd = td;
     }
-    // the token rows in expert-sorted order (then x itself for the shared expert), so that both
-    // GEMM operands load as TMA tiles
-    MOE_CUDA(launch_gather_rows(x, T, c.hidden, row_tok, (int)P, xp, s, with_shared ? T : 0));
+    // the token rows in expert-sorted order, so that both GEMM operands load as TMA tiles
+    MOE_CUDA(launch_gather_rows(x, T, c.hidden, row_tok, (int)P, xp, s, 0));
     GemmArgs a{};
     a.b_src = xp;
     a.K = c.hidden;
@@ -322,6 +333,7 @@ moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t 
     a.ld = c.inter;
     a.status = status;
     a.shared_last = with_shared;
+    a.shared_b_own = with_shared;
     MOE_CUDA(launch_gemm(EPI_SWIGLU, a, tg, tu, tx, tsg, tsu, KC_GATEUP_GEMM, s));
     GemmArgs d{};
     d.b_src = h;

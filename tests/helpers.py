@@ -44,6 +44,20 @@ def residual_step(r_u16, out_u16):
     return np.array([orc.double_to_bf16(t) for t in v.ravel()], dtype=np.uint16).reshape(v.shape)
 
 
+def check_x_last(x_last_u16, r_u16, out_u16, fixed_resid):
+    """x_last = bf16(r + out).  With a fixed residual r the chain adds exactly that r: bit-exact.
+    Without one, r is the chain's own x_l, rebuilt inside the launch from the previous layer's
+    split-K sum, whose fp32 atomics may land one bf16 step away from the x_l the caller holds
+    (from a shorter run): then x_last may differ by one bf16 step at |x_last|."""
+    want = residual_step(r_u16, out_u16)
+    if fixed_resid:
+        np.testing.assert_array_equal(x_last_u16, want)
+        return
+    a, b = orc.bf16_to_f64(x_last_u16), orc.bf16_to_f64(want)
+    step = np.ldexp(1.0, np.frexp(np.maximum(np.maximum(np.abs(a), np.abs(b)), 2.0 ** -126))[1] - 8)
+    assert np.all(np.abs(a - b) <= step), "x_last: %d elements beyond one bf16 step" % int((np.abs(a - b) > step).sum())
+
+
 def abs_bound(ref_f64):
     """Per-element absolute bound: 2e-2, or two bf16 spacings at |ref| where that is larger.
 

@@ -12,7 +12,7 @@ import torch
 from oracle import moe_oracle as orc
 from sparse_moe_router_gb300 import abi, inputs
 
-from helpers import cfg_of, check_layer, compare_out, forward_gpu, host, make, residual_step, route_gpu, u16
+from helpers import cfg_of, check_layer, compare_out, forward_gpu, host, make, check_x_last, route_gpu, u16
 
 pytestmark = pytest.mark.gpu
 
@@ -54,7 +54,7 @@ def test_chain_layer_by_layer(shape, L, use_resid):
         ref = _layer_ref(shape, layers[n - 1], x_in)
         compare_out(u16(out), ref, what="chain layer %d out" % (n - 1))
         r = u16(resid) if use_resid else u16(x_in)
-        np.testing.assert_array_equal(u16(x_last), residual_step(r, u16(out)))
+        check_x_last(u16(x_last), r, u16(out), use_resid)
         x_in = x_last
 
 

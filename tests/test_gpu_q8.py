@@ -14,7 +14,7 @@ import torch
 from oracle import moe_oracle as orc
 from sparse_moe_router_gb300 import abi, inputs
 
-from helpers import cfg_of, compare_out, residual_step, route_gpu, u16
+from helpers import cfg_of, compare_out, check_x_last, route_gpu, u16
 
 pytestmark = pytest.mark.gpu
 
@@ -116,7 +116,7 @@ def test_chain_q8_layer_by_layer(shape, L, use_resid):
         out, x_last = _chain_q8(shape, layers, x0, n, resid)
         compare_out(u16(out), _layer_ref_q8(shape, layers[n - 1], x_in), what="q8 chain layer %d" % (n - 1))
         r = u16(resid) if use_resid else u16(x_in)
-        np.testing.assert_array_equal(u16(x_last), residual_step(r, u16(out)))
+        check_x_last(u16(x_last), r, u16(out), use_resid)
         x_in = x_last
 
 
