@@ -188,6 +188,30 @@ moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const moe_bf
                        moe_bf16 *out, const moe_bf16 *resid, moe_bf16 *x_next, void *ws,
                        size_t ws_bytes, void *stream);
 
+/* A layer stack captured once as a CUDA graph and replayed (the resident prefill buckets of
+ * "AIMA AMD395 Qwen3.6 35B Linux Engine", release boundary v1.5.0: one graph per bucket size,
+ * kept resident with its workspace).  The graph holds n_layers (1..64) moe_forward calls on T
+ * tokens with these exact pointers: layer 0 reads x0; layer l writes out and
+ * x_{l+1} = bf16(r + out_l), r = resid when given, else x_l; layer l+1 reads x_{l+1}.  The
+ * intermediate x_l alternate between x_last and scratch so that x_last receives x_{n_layers};
+ * both [T,H] bf16, required when n_layers > 1 (x_last may be NULL for one layer; scratch is
+ * then unused), distinct from x0, resid and out.  Every buffer, the weights and ws must stay
+ * allocated and unchanged in place while the graph lives; their contents may change between
+ * launches (a new x0 is simply copied into x0's buffer).
+ * moe_graph_create validates as moe_forward does, runs the stack once on `stream` (this
+ * warms the library's per-device launch caches and writes the outputs), then captures it on a
+ * private stream and instantiates it.  moe_graph_launch replays it on `stream`, asynchronously;
+ * moe_launch_count() advances by the graph's kernel count.  Calls sharing ws must not overlap.
+ * moe_graph_destroy frees the graph (NULL is a no-op). */
+typedef struct moe_graph_s *moe_graph;
+moe_status moe_graph_create(const moe_config *cfg, const moe_weights *layers, int n_layers, int T,
+                            const moe_bf16 *x0, const moe_bf16 *resid, moe_bf16 *out, moe_bf16 *x_last,
+                            moe_bf16 *scratch, void *ws, size_t ws_bytes, void *stream, moe_graph *graph);
+moe_status moe_graph_launch(moe_graph graph, void *stream);
+/* Kernel nodes in the graph (-1 for NULL). */
+int moe_graph_kernel_count(moe_graph graph);
+moe_status moe_graph_destroy(moe_graph graph);
+
 /* One token through a stack of n_layers MoE layers (1 <= n_layers <= 64), each with its own
  * weights layers[l] (a host array of device pointers), in ONE cooperative kernel launch: the
  * batch-1 greedy decode step the pages run ("AIMA AMD395 Qwen3.6 35B Windows Engine",

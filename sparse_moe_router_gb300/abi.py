@@ -25,7 +25,8 @@ EXPORTS = ["moe_status_string", "moe_workspace_size", "moe_route", "moe_route_fr
            "moe_permute", "moe_permute_noalloc", "moe_expert_ffn", "moe_combine", "moe_forward", "moe_check_status",
            "moe_plan_pieces", "moe_launch_count", "moe_timing_enable", "moe_timing_read",
            "moe_timing_name", "moe_timing_classes", "moe_selftest_wait", "moe_decode_chain",
-           "moe_decode_chain_q8", "moe_quantize_e4m3"]
+           "moe_decode_chain_q8", "moe_quantize_e4m3", "moe_graph_create", "moe_graph_launch",
+           "moe_graph_kernel_count", "moe_graph_destroy"]
 
 
 class MoeError(RuntimeError):
@@ -82,6 +83,11 @@ def load(path: str = LIB_PATH):
     L.moe_quantize_e4m3.argtypes = [_P, _I, _I, _P, _P, _P]
     L.moe_check_status.argtypes = [_P, _SZ, ctypes.POINTER(_I), _P]
     L.moe_selftest_wait.argtypes = [_P, _SZ, ctypes.c_ulonglong, _I, _P]
+    L.moe_graph_create.argtypes = [C, W, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P, ctypes.POINTER(_P)]
+    L.moe_graph_launch.argtypes = [_P, _P]
+    L.moe_graph_kernel_count.argtypes = [_P]
+    L.moe_graph_kernel_count.restype = _I
+    L.moe_graph_destroy.argtypes = [_P]
     L.moe_plan_pieces.argtypes = [_I, ctypes.POINTER(_I), _I]
     L.moe_plan_pieces.restype = _I
     L.moe_launch_count.argtypes = []
@@ -94,7 +100,8 @@ def load(path: str = LIB_PATH):
     for fn in ("moe_route", "moe_route_from_logits", "moe_permute", "moe_permute_noalloc", "moe_expert_ffn",
                "moe_combine", "moe_forward", "moe_check_status", "moe_timing_enable",
                "moe_timing_read", "moe_timing_classes", "moe_selftest_wait", "moe_decode_chain",
-               "moe_decode_chain_q8", "moe_quantize_e4m3"):
+               "moe_decode_chain_q8", "moe_quantize_e4m3", "moe_graph_create", "moe_graph_launch",
+               "moe_graph_destroy"):
         getattr(L, fn).restype = _I
     _lib = L
     return L
@@ -214,6 +221,39 @@ def moe_forward(cfg, w: Weights, x, T, out, x_next, ws, stream=None, resid=None)
     st = lib().moe_forward(ctypes.byref(cfg), ctypes.byref(w), _ptr(x), int(T), _ptr(out),
                            _ptr(resid), _ptr(x_next), _ptr(ws), ws.numel(), _stream(stream))
     _check("moe_forward", st)
+
+
+class Graph:
+    """A layer stack captured by moe_graph_create; launch() replays it.  Holds references to
+    every tensor the graph reads or writes, so none is freed while the graph lives."""
+
+    def __init__(self, cfg, layers, T, x0, out, x_last, scratch, ws, stream=None, resid=None, keep=()):
+        arr = (Weights * len(layers))(*layers)
+        h = ctypes.c_void_p()
+        st = lib().moe_graph_create(ctypes.byref(cfg), arr, len(layers), int(T), _ptr(x0), _ptr(resid), _ptr(out),
+                                    _ptr(x_last), _ptr(scratch), _ptr(ws), ws.numel(), _stream(stream),
+                                    ctypes.byref(h))
+        _check("moe_graph_create", st)
+        self._h = h
+        self._keep = (x0, out, x_last, scratch, ws, resid, tuple(keep))
+
+    @property
+    def kernels(self) -> int:
+        return int(lib().moe_graph_kernel_count(self._h))
+
+    def launch(self, stream=None):
+        _check("moe_graph_launch", lib().moe_graph_launch(self._h, _stream(stream)))
+
+    def destroy(self):
+        if self._h is not None and self._h.value:
+            lib().moe_graph_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
 
 
 def moe_decode_chain(cfg, layers, x0, out, x_last, ws, stream=None, resid=None):

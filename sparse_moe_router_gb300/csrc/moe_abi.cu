@@ -41,7 +41,12 @@ const char *const kClassNames[KC_COUNT] = {
 
 const char *kernel_class_name(int kc) { return (kc >= 0 && kc < KC_COUNT) ? kClassNames[kc] : nullptr; }
 
+// set while this thread captures a graph: launches are counted when the graph is replayed,
+// and no timing events are recorded into it
+thread_local bool t_capturing = false;
+
 LaunchScope::LaunchScope(int kc_, cudaStream_t s) : kc(kc_), stream(s), ev0(nullptr), ev1(nullptr), timed(false) {
+    if (t_capturing) return;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (g_timing.load(std::memory_order_relaxed)) {
         if (cudaEventCreate(&ev0) == cudaSuccess && cudaEventCreate(&ev1) == cudaSuccess) {
@@ -735,6 +740,97 @@ moe_status moe_check_status(void *ws, size_t ws_bytes, int *device_status, void 
     *device_status = v;
     if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+struct moe_graph_s {
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    int kernels = 0;
+};
+
+namespace {
+// The stack of moe_graph_create: layer l reads x_l and writes x_{l+1} into x_last or scratch,
+// alternating so that the last layer writes x_last.
+moe_status run_stack(const moe_config *cfg, const moe_weights *layers, int n, int T, const moe_bf16 *x0,
+                     const moe_bf16 *resid, moe_bf16 *out, moe_bf16 *x_last, moe_bf16 *scratch, void *ws,
+                     size_t ws_bytes, void *stream) {
+    const moe_bf16 *x = x0;
+    for (int l = 0; l < n; ++l) {
+        moe_bf16 *nxt = ((n - 1 - l) & 1) ? scratch : x_last;
+        MOE_TRY(moe_forward(cfg, &layers[l], x, T, out, resid, nxt, ws, ws_bytes, stream));
+        x = nxt;
+    }
+    return MOE_OK;
+}
+}  // namespace
+
+moe_status moe_graph_create(const moe_config *cfg, const moe_weights *layers, int n_layers, int T,
+                            const moe_bf16 *x0, const moe_bf16 *resid, moe_bf16 *out, moe_bf16 *x_last,
+                            moe_bf16 *scratch, void *ws, size_t ws_bytes, void *stream, moe_graph *graph) {
+    NvtxRange nvtx_range("moe_graph_create");
+    if (!graph) return MOE_ERR_INVALID_ARG;
+    *graph = nullptr;
+    if (!layers || n_layers < 1 || T < 1) return MOE_ERR_INVALID_ARG;
+    if (n_layers > kChainMaxLayers) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (n_layers > 1) {
+        if (!x_last || !scratch || x_last == scratch) return MOE_ERR_INVALID_ARG;
+        for (const moe_bf16 *b : {(const moe_bf16 *)x_last, (const moe_bf16 *)scratch})
+            if (b == x0 || b == resid || b == out) return MOE_ERR_INVALID_ARG;
+    }
+    // one eager run: validates every argument and fills the per-device launch caches (function
+    // attributes, occupancy), which must not be queried inside the capture
+    MOE_TRY(run_stack(cfg, layers, n_layers, T, x0, resid, out, x_last, scratch, ws, ws_bytes, stream));
+    // captured on a private stream: nothing runs until a launch, which the caller orders on
+    // its own stream
+    cudaStream_t cs = nullptr;
+    MOE_CUDA(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking));
+    moe_graph g = new moe_graph_s();
+    moe_status st = MOE_OK;
+    cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+    if (e == cudaSuccess) {
+        t_capturing = true;
+        st = run_stack(cfg, layers, n_layers, T, x0, resid, out, x_last, scratch, ws, ws_bytes, cs);
+        t_capturing = false;
+        const cudaError_t e2 = cudaStreamEndCapture(cs, &g->graph);
+        if (st == MOE_OK && e2 != cudaSuccess) st = MOE_ERR_CUDA;
+    } else {
+        st = MOE_ERR_CUDA;
+    }
+    if (st == MOE_OK && cudaGraphInstantiate(&g->exec, g->graph, 0) != cudaSuccess) st = MOE_ERR_CUDA;
+    if (st == MOE_OK) {
+        size_t n = 0;
+        if (cudaGraphGetNodes(g->graph, nullptr, &n) != cudaSuccess) st = MOE_ERR_CUDA;
+        std::vector<cudaGraphNode_t> nodes(n);
+        if (st == MOE_OK && n > 0 && cudaGraphGetNodes(g->graph, nodes.data(), &n) != cudaSuccess) st = MOE_ERR_CUDA;
+        for (size_t i = 0; st == MOE_OK && i < n; ++i) {
+            cudaGraphNodeType ty;
+            if (cudaGraphNodeGetType(nodes[i], &ty) == cudaSuccess && ty == cudaGraphNodeTypeKernel) ++g->kernels;
+        }
+    }
+    cudaStreamDestroy(cs);
+    if (st != MOE_OK) {
+        moe_graph_destroy(g);
+        return st;
+    }
+    *graph = g;
+    return MOE_OK;
+}
+
+moe_status moe_graph_launch(moe_graph graph, void *stream) {
+    if (!graph || !graph->exec) return MOE_ERR_INVALID_ARG;
+    MOE_CUDA(cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)));
+    g_launches.fetch_add((uint64_t)graph->kernels, std::memory_order_relaxed);
+    return MOE_OK;
+}
+
+int moe_graph_kernel_count(moe_graph graph) { return graph ? graph->kernels : -1; }
+
+moe_status moe_graph_destroy(moe_graph graph) {
+    if (!graph) return MOE_OK;
+    if (graph->exec) cudaGraphExecDestroy(graph->exec);
+    if (graph->graph) cudaGraphDestroy(graph->graph);
+    delete graph;
     return MOE_OK;
 }
 

@@ -109,3 +109,28 @@ def test_status_strings_and_timing_names():
     assert "gateup_gemm" in names and "decode_experts" in names
     with pytest.raises(abi.MoeError):
         abi.timing_read("no_such_kernel")
+
+
+def test_graph_entry_points_validate_on_the_host():
+    """moe_graph_*: argument errors are returned before any device work."""
+    L = abi.load()
+    cfg = _cfg()
+    w = (abi.Weights * 2)()
+    h = ctypes.c_void_p()
+    fake = ctypes.c_void_p(0x1000)
+    # no handle pointer, no layers, no layers counted, no tokens
+    assert L.moe_graph_create(cfg, w, 1, 8, fake, None, fake, None, None, fake, 1 << 20, None, None) == 1
+    assert L.moe_graph_create(cfg, None, 1, 8, fake, None, fake, None, None, fake, 1 << 20, None, ctypes.byref(h)) == 1
+    assert L.moe_graph_create(cfg, w, 0, 8, fake, None, fake, None, None, fake, 1 << 20, None, ctypes.byref(h)) == 1
+    assert L.moe_graph_create(cfg, w, 1, 0, fake, None, fake, None, None, fake, 1 << 20, None, ctypes.byref(h)) == 1
+    # a stack needs x_last and scratch, distinct from each other and from x0 / out
+    assert L.moe_graph_create(cfg, w, 2, 8, fake, None, fake, None, fake, fake, 1 << 20, None, ctypes.byref(h)) == 1
+    a, b = ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000)
+    assert L.moe_graph_create(cfg, w, 2, 8, fake, None, b, a, a, fake, 1 << 20, None, ctypes.byref(h)) == 1
+    assert L.moe_graph_create(cfg, w, 2, 8, fake, None, b, fake, a, fake, 1 << 20, None, ctypes.byref(h)) == 1
+    assert L.moe_graph_create(cfg, w, 65, 8, fake, None, b, a, ctypes.c_void_p(0x4000), fake, 1 << 20, None,
+                              ctypes.byref(h)) == 3
+    assert not h.value
+    assert L.moe_graph_launch(None, None) == 1
+    assert L.moe_graph_kernel_count(None) == -1
+    assert L.moe_graph_destroy(None) == 0
