@@ -119,3 +119,92 @@ def test_prompt_13337_composed_skewed():
         assert np.array_equal(offs.cpu().numpy(), o) and np.array_equal(perm.cpu().numpy(), pm)
         assert np.array_equal(inv.cpu().numpy(), iv)
         t0 += p
+
+
+def test_prefill_8k_graph_step_equals_eager():
+    """The benchmark's step: the four prefill layers captured by moe_graph_create and replayed;
+    bit-identical to the same moe_forward calls made eagerly (checked against the oracle above)."""
+    wl = inputs.WORKLOADS["prefill8k"]
+    layers, x0 = inputs.make(wl, device="cuda")
+    cfg = cfg_of(wl.shape)
+    T = wl.T
+    ws = abi.alloc_workspace(cfg, T)
+    wts = [abi.weights(l) for l in layers]
+    x = x0
+    out_e = torch.empty_like(x0)
+    for w in wts:
+        nxt = torch.empty_like(x0)
+        abi.moe_forward(cfg, w, x, T, out_e, nxt, ws, resid=x0)
+        x = nxt
+    torch.cuda.synchronize()
+    out, xl, sc = torch.empty_like(x0), torch.empty_like(x0), torch.empty_like(x0)
+    g = abi.Graph(cfg, wts, T, x0, out, xl, sc, ws, resid=x0, keep=layers)
+    out.zero_()
+    xl.zero_()
+    g.launch()
+    g.launch()
+    torch.cuda.synchronize()
+    assert abi.moe_check_status(ws) == 0
+    assert torch.equal(out, out_e) and torch.equal(xl, x)
+
+
+def _decode_chain_last_layer(layers_dev, wts, x0, launch, ref_fn):
+    """The 40-layer one-token chain as the benchmark launches it (x_{l+1} = bf16(x_0 + out_l)):
+    its last layer's out against the oracle on x_39, which a 39-layer chain leaves in x_last."""
+    L = len(wts)
+    out, x39, dummy = torch.empty_like(x0), torch.empty_like(x0), torch.empty_like(x0)
+    launch(wts, out, dummy)
+    out_last = out.clone()
+    launch(wts[:L - 1], out, x39)
+    torch.cuda.synchronize()
+    compare_out(u16(out_last), ref_fn(x39), what="layer %d of the chain" % (L - 1))
+
+
+def test_decode_chain_40_layers_full_size():
+    wl = inputs.WORKLOADS["decode"]
+    layers, x0 = inputs.make(wl, device="cuda")
+    shape, cfg = wl.shape, cfg_of(wl.shape)
+    ws = abi.alloc_workspace(cfg, 1)
+
+    def launch(wts, out, x_last):
+        abi.moe_decode_chain(cfg, wts, x0, out, x_last, ws, resid=x0)
+        torch.cuda.synchronize()
+        assert abi.moe_check_status(ws) == 0
+
+    def ref(x):
+        logits, ids, w = route_gpu(shape, layers[-1], x)
+        hl = _subset_layer(layers[-1], ids[0])
+        sub = np.arange(shape.top_k, dtype=np.int32)[None, :]
+        return orc.forward(u16(x), hl, shape.top_k, ids=sub, topk_w=w)["out"]
+
+    _decode_chain_last_layer(layers, [abi.weights(l) for l in layers], x0, launch, ref)
+
+
+def test_decode_chain_q8_40_layers_full_size():
+    wl = inputs.WORKLOADS["decode"]
+    layers, x0 = inputs.make(wl, device="cuda")
+    shape, cfg = wl.shape, cfg_of(wl.shape)
+    ws = abi.alloc_workspace(cfg, 1)
+    lq = [abi.quantize_layer(l) for l in layers]
+    del layers
+    torch.cuda.synchronize()
+
+    def launch(wts, out, x_last):
+        abi.moe_decode_chain_q8(cfg, wts, x0, out, x_last, ws, resid=x0)
+        torch.cuda.synchronize()
+        assert abi.moe_check_status(ws) == 0
+
+    def ref(x):
+        last = lq[-1]
+        logits, ids, w = route_gpu(shape, last, x)
+        sel = torch.as_tensor(ids[0].astype(np.int64), device="cuda")
+        sub = {"q_gate": last["q_gate"].index_select(0, sel), "q_up": last["q_up"].index_select(0, sel),
+               "q_down": last["q_down"].index_select(0, sel), "s_gate": last["s_gate"].index_select(0, sel),
+               "s_up": last["s_up"].index_select(0, sel), "s_down": last["s_down"].index_select(0, sel)}
+        for k in ("qs_gate", "qs_up", "qs_down", "ss_gate", "ss_up", "ss_down"):
+            sub[k] = last[k]
+        hq = {k: v.cpu().numpy() for k, v in sub.items()}
+        ids_sub = np.arange(shape.top_k, dtype=np.int32)[None, :]
+        return orc.forward_q8(u16(x), hq, shape.top_k, ids_sub, w)
+
+    _decode_chain_last_layer(None, [abi.weights_q8(l) for l in lq], x0, launch, ref)
