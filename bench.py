@@ -602,9 +602,13 @@ def run_reference(args, world, rank):
     t0 = time.perf_counter()
     orc.forward(np.ascontiguousarray(xs[:n0]), hl, k)
     per_tok = (time.perf_counter() - t0) / n0
-    # each step: about args.ref_step_seconds of oracle work
-    n = int(max(threads, min(wl.T, args.ref_step_seconds / max(per_tok, 1e-9))))
-    n = max(threads, (n // threads) * threads)
+    # each step: about args.ref_step_seconds of oracle work, less when the whole run (warm-up and
+    # timed steps) would otherwise exceed args.ref_total_seconds
+    step_s = min(args.ref_step_seconds, args.ref_total_seconds / max(1, args.steps + args.warmup))
+    n = int(max(1, min(wl.T, step_s / max(per_tok, 1e-9))))
+    if n >= threads:
+        n = (n // threads) * threads
+    threads = min(threads, n)
     sample = np.ascontiguousarray(xs[:n])
     for _ in range(args.warmup):
         orc.forward(sample, hl, k)
@@ -643,6 +647,8 @@ def main():
                     help="decode layers (default: the workload's 40); fewer only for profiler captures")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=4.0)
+    ap.add_argument("--ref-total-seconds", type=float, default=120.0,
+                    help="bound on the reference arm's oracle work over all its warm-up and timed steps")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
