@@ -24,7 +24,9 @@
 //               lanes 32*(w%4)..+31 (the hardware's lane quarters), and the P/4 warps of a
 //               quarter take every (P/4)-th 16-token chunk;
 //   warps P..P+3 producers: one thread issues the TMA loads of its CTA's weight rows and token
-//               rows; both CTAs' loads complete on the even CTA's stage barrier;
+//               rows (the token rows with the smallest of eight boxes, 16..128 rows, that holds
+//               the CTA's half of the tile); both CTAs' loads complete on the even CTA's stage
+//               barrier;
 //   warp P+4    allocates TMEM (both CTAs, pair form); in the even CTA lane 0 issues
 //               tcgen05.mma (kind::f16, M = 256, bf16 -> fp32) and tcgen05.commit, whose
 //               arrivals go to both CTAs' barriers.
@@ -33,7 +35,8 @@
 // TMEM accumulators of 256 columns (acc_full/acc_empty; the odd CTA's epilogue releases an
 // accumulator with a remote arrive), so the epilogue of one tile overlaps the next main loop.
 // Pair tiles are walked statically (tile = pair + i*pairs), ordered (group, weight tile, token
-// tile) with the token tile fastest, so pairs sharing a weight tile run together.
+// tile) with the token tile fastest, so pairs sharing a weight tile run together; a shared-expert
+// group's tiles are spread evenly among the routed ones.
 #include <cuda_bf16.h>
 
 #include "internal.h"
