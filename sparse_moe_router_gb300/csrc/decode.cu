@@ -302,7 +302,7 @@ __device__ __forceinline__ void warp_topk(const float *logits, int E, int k, int
 // layer on the same SM, so the router spreads over the GPU instead of the few SMs K2 leaves idle
 // (with several tokens the gate/up accumulators need 128).
 //
-// T tokens (NT = 1, or 8 for 2 <= T <= 8).  Work items: the shared expert's 32-feature slices
+// T tokens (NT = 1, or kMaxDecodeT = 4 for 2 <= T <= 4).  Work items: the shared expert's 32-feature slices
 // first (a block whose first item is one starts its loads before K1 finishes), then one item per
 // (token t, slot j, slice).  A routed item works only for the first (token, slot) in token order
 // that selected its expert e, and then serves every token that selected e: the expert's
