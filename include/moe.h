@@ -113,7 +113,10 @@ const char *moe_status_string(moe_status s);
  * is scratch that every call overwrites. */
 size_t moe_workspace_size(const moe_config *cfg, int max_T);
 
-/* Router: logits, softmax, top-k and renormalisation.
+/* Router: logits, softmax, top-k and renormalisation.  Passage: each token activates only a few
+ * of many experts ("AI MAX+ 395部署Qwen3大模型：GFX1151引擎实测优化解析", explanatory MoE
+ * paragraph under "MOE 内核优化"); the selection rule (largest logits, lower index on ties,
+ * weights renormalised over the k) is this library's reading, the pages give no formula.
  * x [T,H] bf16 -> topk_ids [T,k] int32 and topk_w [T,k] fp32, slots in descending logit
  * order.  logits_out [T,E] fp32 may be NULL; when given it receives the exact fp32 logits the
  * selection used.  ws: workspace of moe_workspace_size(cfg, T) bytes (holds the logits when
@@ -124,12 +127,16 @@ moe_status moe_route(const moe_config *cfg, const moe_weights *w, const moe_bf16
                      float *logits_out, int32_t *topk_ids, float *topk_w, void *ws,
                      size_t ws_bytes, void *stream);
 
-/* Softmax + top-k + renormalisation only, from given fp32 logits [T,E].  Bit-exact ids for
+/* Softmax + top-k + renormalisation only, from given fp32 logits [T,E] (the routing step of
+ * the same passage as moe_route).  Bit-exact ids for
  * identical logits (the selection compares fp32 values exactly, lower index first on ties). */
 moe_status moe_route_from_logits(const moe_config *cfg, const float *logits, int T,
                                  int32_t *topk_ids, float *topk_w, void *stream);
 
-/* Permutation of the T*k (token, slot) pairs by expert: a stable counting sort.
+/* Permutation of the T*k (token, slot) pairs by expert: a stable counting sort.  Passage: the
+ * "selected-MoE" kernel runs only the experts each token selected ("AIMA AMD395 Qwen3.6 35B
+ * Windows Engine", "性能优化做了什么"), which needs each expert's tokens gathered together; the
+ * page does not describe how, so the grouping is this library's (a textbook stable sort).
  * topk_ids [T,k] -> expert_offsets [E+1] (exclusive prefix sum of the per-expert counts,
  * offsets[E] == T*k), perm [T*k] (row of the expert-sorted order -> pair index t*k+j),
  * inv [T*k] (pair index -> row).  Pairs of one expert keep increasing pair order.  Bit-exact.
@@ -156,7 +163,10 @@ moe_status moe_permute_noalloc(const moe_config *cfg, const int32_t *topk_ids, i
                                int32_t *expert_offsets, int32_t *perm, int32_t *inv,
                                void *stream);
 
-/* Expert FFNs, unfused (for step-by-step checking).  Routed rows in the permuted order:
+/* Expert FFNs, unfused (for step-by-step checking).  Passage: the selected experts' own
+ * sub-networks ("AI MAX+ 395部署Qwen3大模型：GFX1151引擎实测优化解析", "MOE 内核优化": the MoE
+ * kernel that bounds prefill), read as SwiGLU experts plus an always-on shared expert.
+ * Routed rows in the permuted order:
  * h_rows [T*k, I] bf16 = bf16(silu(Wg[e] x_t) * (Wu[e] x_t)) and y_rows [T*k, H] fp32 =
  * Wd[e] h, for row r of expert e holding pair perm[r] of token perm[r]/k.  When shared_y is not
  * NULL and Is > 0, also shared_y [T,H] fp32 = the shared expert applied to every token.
@@ -166,7 +176,9 @@ moe_status moe_expert_ffn(const moe_config *cfg, const moe_weights *w, const moe
                           float *y_rows, float *shared_y, void *ws, size_t ws_bytes,
                           void *stream);
 
-/* Weighted combine: out[t] = bf16( sum_j topk_w[t,j] * y_rows[inv[t*k+j]] + shared_y[t] ).
+/* Weighted combine (the last step of the selected-MoE layer, "AIMA AMD395 Qwen3.6 35B Windows
+ * Engine", "性能优化做了什么"; the weighting by the renormalised routing weights is this
+ * library's reading): out[t] = bf16( sum_j topk_w[t,j] * y_rows[inv[t*k+j]] + shared_y[t] ).
  * shared_y may be NULL (no shared term).  Deterministic (fixed slot order, fp32). */
 moe_status moe_combine(const moe_config *cfg, const float *y_rows, const int32_t *inv,
                        const float *topk_w, const float *shared_y, int T, moe_bf16 *out,
@@ -183,7 +195,9 @@ moe_status moe_combine(const moe_config *cfg, const float *y_rows, const int32_t
  * resid (not x, when they differ).  ws: moe_workspace_size(cfg, T) bytes.  Rounding on the
  * prefill path: h is rounded to bf16 once, each weighted expert row w*y (and the shared
  * expert's row) is stored as bf16, the k+1 rows of a token are summed in fp32 in slot order,
- * and the sum is rounded to bf16 once.  No atomics there: the result is bit-reproducible. */
+ * and the sum is rounded to bf16 once.  No atomics there: the result is bit-reproducible.
+ * Any T >= 0 (int) is accepted: the pieces are walked one after another, so there is no limit
+ * on their number. */
 moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const moe_bf16 *x, int T,
                        moe_bf16 *out, const moe_bf16 *resid, moe_bf16 *x_next, void *ws,
                        size_t ws_bytes, void *stream);

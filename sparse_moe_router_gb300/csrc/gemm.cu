@@ -39,6 +39,8 @@
 // group's tiles are spread evenly among the routed ones.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -527,8 +529,10 @@ cudaError_t launch_impl(const GemmArgs &a, const CUtensorMap &m0, const CUtensor
                         const TokenMaps &mb, const CUtensorMap &s0, const CUtensorMap &s1, int kc,
                         cudaStream_t s) {
     using C = Cfg<EPI>;
-    // per device: the shared-memory opt-in and how many CTA pairs fit on the GPU at once
+    // per device: the shared-memory opt-in and how many CTA pairs fit on the GPU at once (set
+    // once under a lock, so that two host threads' first launches do not race)
     static int max_pairs[64] = {0};
+    static std::mutex mu;
     int dev = 0;
     cudaGetDevice(&dev);
     cudaLaunchConfig_t cfg = {};
@@ -542,7 +546,8 @@ cudaError_t launch_impl(const GemmArgs &a, const CUtensorMap &m0, const CUtensor
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (dev >= 64) return cudaErrorInvalidDevice;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::unique_lock<std::mutex> lk(mu);
     if (max_pairs[dev] == 0) {
         cudaError_t e = cudaFuncSetAttribute(gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemBytes);
@@ -555,6 +560,7 @@ cudaError_t launch_impl(const GemmArgs &a, const CUtensorMap &m0, const CUtensor
         max_pairs[dev] = n;
     }
     int pairs = max_pairs[dev];
+    lk.unlock();
     if (a.group_rows == nullptr) {
         const int nft = (a.F + C::kFT - 1) / C::kFT;
         const int ptiles = ((nft + 1) / 2) * token_tile_count(a.M_single, a.tile_cap > 0 ? a.tile_cap : BN);

@@ -139,6 +139,9 @@ cudaError_t launch_topk(const float *logits, int T, int E, int k, int32_t *ids, 
 // routing weight topk_w[pair] (what the expert GEMMs read per row).  extra_rows > 0 appends one
 // more group of that many rows after the experts (offsets[E+1], tile_prefix[E+1]): the shared
 // expert's rows when it runs inside the routed GEMMs.
+// Pairs per block of the permutation kernels: the chunk table holds one row of E counts per
+// chunk of this many consecutive pairs.
+constexpr int kPermChunk = 2048;
 size_t permute_scratch_ints(int T, int E, int k);
 cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int32_t *offsets,
                            int32_t *perm, int32_t *inv, int32_t *tile_prefix, int tile_n,

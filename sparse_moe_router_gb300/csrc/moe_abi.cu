@@ -603,12 +603,17 @@ moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const moe_bf
         MOE_CUDA(launch_decode(a, td, tsd, s));
         return MOE_OK;
     }
-    int pieces[64];
-    const int n = moe_plan_pieces(T, pieces, 64);
-    if (n > 64) return MOE_ERR_UNSUPPORTED_SHAPE;
+    // the pieces in moe_plan_pieces order: the largest bucket that fits, then the exact tail
+    static const int kBuckets[4] = {8192, 4096, 2048, 1024};
     size_t t0 = 0;
-    for (int i = 0; i < n; ++i) {
-        const int Tp = pieces[i];
+    for (int rem = T; rem > 0;) {
+        int Tp = rem;
+        for (int b = 0; b < 4; ++b)
+            if (rem >= kBuckets[b]) {
+                Tp = kBuckets[b];
+                break;
+            }
+        rem -= Tp;
         uint16_t *xn = x_next ? x_next + t0 * H : nullptr;
         if (decode_fits(Tp, H)) {
             // a tail of a few tokens takes the decode path of the same layer

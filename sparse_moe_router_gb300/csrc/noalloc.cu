@@ -23,11 +23,12 @@ namespace {
 // Largest problem the fixed table serves: T*k <= 65536 pairs and E <= 1024 experts.
 constexpr int kNoAllocMaxPairs = 65536;
 constexpr int kNoAllocMaxExperts = 1024;
-constexpr int kNoAllocChunks = (kNoAllocMaxPairs + 2047) / 2048;  // pairs per chunk: 2048
+constexpr int kNoAllocChunks = (kNoAllocMaxPairs + kPermChunk - 1) / kPermChunk;
+constexpr size_t kNoAllocTableInts = (size_t)kNoAllocChunks * kNoAllocMaxExperts;
 
 // The chunk count table: every entry a call reads is first written by that same call, so
 // nothing in it has to start at zero.
-static __device__ __align__(256) int32_t g_noalloc_chunk_tab[kNoAllocChunks * kNoAllocMaxExperts];
+static __device__ __align__(256) int32_t g_noalloc_chunk_tab[kNoAllocTableInts];
 
 std::mutex g_noalloc_mu;
 void *g_noalloc_addr[64] = {nullptr};
@@ -63,6 +64,8 @@ extern "C" moe_status moe_permute_noalloc(const moe_config *cfg, const int32_t *
     if (!topk_ids || !expert_offsets || !perm || !inv) return MOE_ERR_INVALID_ARG;
     if (cfg->n_experts > kNoAllocMaxExperts || cfg->top_k > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
     if ((long long)T * cfg->top_k > kNoAllocMaxPairs) return MOE_ERR_UNSUPPORTED_SHAPE;
+    // the table the permutation will index: one row of E counts per chunk of pairs
+    if (permute_scratch_ints(T, cfg->n_experts, cfg->top_k) > kNoAllocTableInts) return MOE_ERR_UNSUPPORTED_SHAPE;
     int32_t *table = nullptr;
     if (noalloc_table(&table) != cudaSuccess) return MOE_ERR_CUDA;
     // No tile prefix, per-row token/weight arrays or status word: outputs only.

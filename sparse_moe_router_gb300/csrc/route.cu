@@ -9,6 +9,8 @@
 #include <cuda_bf16.h>
 #include <float.h>
 
+#include <mutex>
+
 #include "internal.h"
 
 namespace moe {
@@ -108,7 +110,8 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ log
 // Pairs of one expert therefore keep increasing pair order: the result is bit-exact.
 constexpr int kPermThreads = 1024;
 constexpr int kPermWarps = kPermThreads / 32;
-constexpr int kChunk = 2048;                 // pairs per block (64 per warp)
+constexpr int kChunk = kPermChunk;           // pairs per block (64 per warp)
+static_assert(kChunk == 64 * kPermWarps, "the scatter gives each warp two 32-pair batches");
 
 __device__ __forceinline__ int block_excl_scan(int v, int *sh_warp, int *total) {
     // exclusive scan of one value per thread across the 1024-thread block
@@ -431,14 +434,21 @@ cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int32_t *off
                            float *row_w, int *status, cudaStream_t s, int extra_rows) {
     const int P = T * k;
     const int n_chunks = (P + kChunk - 1) / kChunk;
+    // the scatter's shared-memory opt-in, once per device (under a lock: two host threads' first
+    // calls would otherwise race on the flag)
     static bool attr_done[64] = {false};
+    static std::mutex mu;
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(perm_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)(kPermWarps * 1024 * sizeof(int)));
-        if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!attr_done[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(perm_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)(kPermWarps * 1024 * sizeof(int)));
+            if (e != cudaSuccess) return e;
+            attr_done[dev] = true;
+        }
     }
     {
         LaunchScope scope(KC_PERMUTE, s);

@@ -58,31 +58,50 @@ def check_x_last(x_last_u16, r_u16, out_u16, fixed_resid):
     assert np.all(np.abs(a - b) <= step), "x_last: %d elements beyond one bf16 step" % int((np.abs(a - b) > step).sum())
 
 
-def abs_bound(ref_f64):
-    """Per-element absolute bound: 2e-2, or two bf16 spacings at |ref| where that is larger.
+def bf16_spacing(v_f64):
+    """The distance between adjacent bf16 values at |v| (2^(e-7) in binade [2^e, 2^(e+1)))."""
+    return np.ldexp(1.0, np.frexp(np.maximum(np.abs(v_f64), 2.0 ** -126))[1] - 8)
 
-    Both sides round the same sum (fp32 on the GPU, fp64 in the oracle) to bf16 once, so a
-    one-step difference is always possible; one bf16 step exceeds 2e-2 only for |ref| > 2.56,
-    which the chained multi-layer workloads reach (the residual stream grows layer by layer).
-    For unit-scale outputs the bound is exactly 2e-2."""
-    spacing = np.ldexp(1.0, np.frexp(np.maximum(np.abs(ref_f64), 2.0 ** -126))[1] - 8)
-    return np.maximum(MAX_ABS, 2.0 * spacing)
+
+def abs_bound(ref_f64):
+    """Per-element absolute bound: 2e-2, or ONE bf16 spacing at |ref| where that is larger.
+
+    Both sides round a sum of the same terms to bf16 once (the oracle its fp64 sum, the GPU its
+    fp32 sum), so when the two sums straddle a rounding boundary their outputs differ by one
+    bf16 spacing however close the sums are.  One spacing exceeds 2e-2 only for |ref| >= 4
+    (spacing 2^-5); below that the bound is exactly 2e-2."""
+    return np.maximum(MAX_ABS, bf16_spacing(ref_f64))
+
+
+class Comparison(tuple):
+    """(max |diff|, rel L2) with the count of elements whose |diff| exceeds the fixed 2e-2
+    (allowed only where one bf16 spacing at |ref| is larger) as `n_over_fixed`."""
+
+    def __new__(cls, max_abs, rel, n_over_fixed, n):
+        c = super().__new__(cls, (max_abs, rel))
+        c.n_over_fixed = n_over_fixed
+        c.n = n
+        return c
 
 
 def compare_out(got_u16, ref_u16, what="out"):
     """Layer-output check against the oracle's bf16 output: every |diff| within abs_bound
-    (2e-2 at unit scale) and relative L2 error <= 5e-3.  Returns (max |diff|, rel L2)."""
+    (2e-2, or one bf16 spacing where |ref| >= 4) and relative L2 error <= 5e-3.
+
+    Returns (max |diff|, rel L2); the result's `n_over_fixed` counts the elements beyond the
+    fixed 2e-2, and the assertion message reports it."""
     g = bf16_f64(got_u16)
     r = bf16_f64(ref_u16)
     assert np.all(np.isfinite(g)), what + ": non-finite values"
     d = np.abs(g - r)
     max_abs = float(d.max()) if d.size else 0.0
     rel = float(np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-30)) if d.size else 0.0
+    n_over = int((d > MAX_ABS).sum())
     bad = d > abs_bound(r)
-    assert not bad.any(), "%s: %d elements beyond the abs bound (max diff %.3g at |ref| %.3g)" % (
-        what, int(bad.sum()), float(d[bad].max()), float(np.abs(r[bad]).max()))
+    assert not bad.any(), "%s: %d elements beyond the abs bound (max diff %.3g at |ref| %.3g; %d beyond 2e-2)" % (
+        what, int(bad.sum()), float(d[bad].max()), float(np.abs(r[bad]).max()), n_over)
     assert rel <= REL_L2, "%s: rel L2 %.3g > %.3g" % (what, rel, REL_L2)
-    return max_abs, rel
+    return Comparison(max_abs, rel, n_over, int(d.size))
 
 
 def cfg_of(shape):

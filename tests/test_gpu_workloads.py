@@ -121,6 +121,34 @@ def test_prompt_13337_composed_skewed():
         t0 += p
 
 
+@pytest.mark.parametrize("T", [4095, 4097, 8191, 8193])
+def test_near_bucket_lengths_layer_shape(T):
+    """Prompt lengths one token either side of a bucket (the near-bucket lesson of "AIMA Intel
+    PTL Qwen3.6 35B U4 Engine", "当前发布边界": lengths just short of a bucket broke a
+    physical/logical buffer layout there), through moe_forward at the 2048-wide, 256-expert
+    top-8 layer shape.  4095 = 2048+1024+1023, 4097 = 4096+1 (a one-token tail on the decode
+    path), 8191 = 4096+2048+1024+1023, 8193 = 8192+1.  Sampled rows include every piece's
+    first and last rows."""
+    shape = inputs.WORKLOADS["prefill8k"].shape
+    wl = inputs.custom(shape, T=T, seed=500 + T % 1000, router_std=1.0 / np.sqrt(shape.hidden))
+    layers, x = inputs.make(wl, device="cuda")
+    cfg = cfg_of(shape)
+    ws = abi.alloc_workspace(cfg, min(T, 8192))
+    out = torch.empty_like(x)
+    xn = torch.empty_like(x)
+    abi.moe_forward(cfg, abi.weights(layers[0]), x, T, out, xn, ws)
+    torch.cuda.synchronize()
+    assert abi.moe_check_status(ws) == 0
+    assert torch.equal(xn, (x.float() + out.float()).to(torch.bfloat16))
+    edges, t0 = [], 0
+    for p in abi.moe_plan_pieces(T):
+        edges += [t0, t0 + 1, t0 + p - 2, t0 + p - 1]
+        t0 += p
+    rng = np.random.default_rng(T)
+    rows = np.unique(np.clip(np.concatenate([edges, rng.choice(T, size=96, replace=False)]), 0, T - 1))
+    _check_rows(shape, layers[0], x, out, rows)
+
+
 def test_prefill_8k_graph_step_equals_eager():
     """The benchmark's step: the four prefill layers captured by moe_graph_create and replayed;
     bit-identical to the same moe_forward calls made eagerly (checked against the oracle above)."""

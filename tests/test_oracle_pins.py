@@ -299,6 +299,35 @@ def test_unfused_pieces_match_whole_layer():
     assert np.mean(out == res["out"]) > 0.99
 
 
+def test_expert_ffn_given_h_rows():
+    """The h_in path of expert_ffn (the GPU down-projection check feeds it the GPU's h rows):
+    (a) fed its own h rows it reproduces its own y rows, which equal the whole layer's per-pair
+    y (the combine of those rows gives forward's output); (b) fed arbitrary bf16 rows in a
+    shuffled row order, row r's y is W_d[e(r)] @ h_in[r] (torch float64 matmul), so a slip of
+    the row index, a transposed W_d or a wrong expert base fails."""
+    w, x, s = _tiny(seed=14, T=23)
+    logits = orc.router_logits(x, w["w_router"])
+    ids, wt = orc.route_from_logits(logits, s.top_k)
+    offs, perm, inv = orc.permute(ids, s.n_experts)
+    h_rows, y_rows, shared_y = orc.expert_ffn(x, offs, perm, s.top_k, w)
+    _, y_again, _ = orc.expert_ffn(x, offs, perm, s.top_k, w, h_in=h_rows)
+    assert np.array_equal(y_again, y_rows)
+    out = orc.combine(y_again, inv, wt, shared_y)
+    ref = orc.forward(x, w, s.top_k)["out"]
+    a, b = orc.bf16_to_f64(out), orc.bf16_to_f64(ref)
+    assert np.all(np.abs(a - b) <= np.abs(b) * 2 ** -7 + 1e-30)
+    # (b) shuffled, arbitrary h rows
+    rng = np.random.default_rng(3)
+    h_any = _bf16_bits(rng.standard_normal(h_rows.shape))
+    h_any = np.ascontiguousarray(h_any[rng.permutation(h_any.shape[0])])
+    _, y_any, _ = orc.expert_ffn(x, offs, perm, s.top_k, w, h_in=h_any)
+    wd = torch.as_tensor(orc.bf16_to_f64(w["w_down"]))
+    hv = torch.as_tensor(orc.bf16_to_f64(h_any))
+    expert_of_row = np.repeat(np.arange(s.n_experts), np.diff(offs))
+    want = torch.stack([wd[int(e)] @ hv[r] for r, e in enumerate(expert_of_row)])
+    np.testing.assert_allclose(y_any, want.to(torch.float32).numpy(), rtol=1e-6, atol=1e-7)
+
+
 def test_x_next_is_rounded_residual():
     w, x, s = _tiny(seed=10, T=9)
     res = orc.forward(x, w, s.top_k, want_x_next=True)

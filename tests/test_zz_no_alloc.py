@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 import torch
 
+from oracle import moe_oracle as orc
 from sparse_moe_router_gb300 import abi
 
 pytestmark = pytest.mark.gpu
@@ -45,7 +46,8 @@ def _no_alloc(cfg, ids):
 @pytest.mark.parametrize("T,E,k", [(8192, 256, 8), (1000, 64, 6), (3, 16, 4)])
 def test_no_alloc_permute_matches_workspace_permute_twice(T, E, k):
     """Two calls in a row (different inputs, so the second reuses the table the first left
-    behind) each match moe_permute exactly (integer outputs: the tolerance is zero)."""
+    behind) each match moe_permute and the oracle's permutation exactly (integer outputs: the
+    tolerance is zero)."""
     cfg = abi.config(2048, E, k, 512, 512)
     for seed in (1, 2):
         ids = _ids(T, E, k, seed + T)
@@ -53,6 +55,9 @@ def test_no_alloc_permute_matches_workspace_permute_twice(T, E, k):
         got = _no_alloc(cfg, ids)
         for g, w in zip(got, want):
             assert np.array_equal(g, w)
+        # and against the CPU oracle's stable counting sort
+        for g, o in zip(got, orc.permute(ids, E)):
+            assert np.array_equal(g, o)
 
 
 def test_no_alloc_permute_rejects_oversize_problems():
