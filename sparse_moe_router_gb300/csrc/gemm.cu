@@ -63,6 +63,9 @@ constexpr int kStgStride = BM + 4;                // SwiGLU staging row (floats)
 // combine transpose: a row of 32 words (features) per token pair, padded to 36 so that the
 // 16-byte reads of 8 lanes fall in distinct banks
 constexpr int kPairStride = 36;
+// Dynamic schedule: slots of the ring through which the even CTA's producer hands each claimed
+// pair tile to the other roles of both CTAs (more than the tiles any role can run ahead).
+constexpr int kSchedDepth = 8;
 
 template <int EPI>
 struct Cfg {
@@ -84,10 +87,12 @@ struct Cfg {
         (EPI == EPI_SWIGLU) ? 2 * 16 * kStgStride * 4 : (EPI == EPI_COMBINE ? kEpiWarps * 8 * kPairStride * 4 : 0);
     // combine: per-tile (output row, weight) of the BN tile rows, double-buffered
     static constexpr int kMetaBytes = (EPI == EPI_COMBINE) ? 2 * BN * 8 : 0;
-    // full, empty per stage; acc_full, acc_empty per accumulator; drain
-    static constexpr int kBarBytes = (2 * kStages + 5) * 8;
+    // full, empty per stage; acc_full, acc_empty per accumulator; drain; sched_full, sched_empty
+    // per slot of the tile ring
+    static constexpr int kBarBytes = (2 * kStages + 5 + 2 * kSchedDepth) * 8;
     static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kPipeBytes + kStagingBytes +
-                                      kMetaBytes + kBarBytes + 32 + 2 * (kMaxGroups + 1) * 4;
+                                      kMetaBytes + kBarBytes + 32 + 2 * (kMaxGroups + 1) * 4 +
+                                      kSchedDepth * 4;
     static_assert(kSmemBytes <= 227 * 1024, "shared memory over the per-CTA limit");
 };
 
@@ -179,13 +184,16 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
     uint64_t *acc_full = bars + 2 * kStages;
     uint64_t *acc_empty = acc_full + 2;
     uint64_t *drain = acc_empty + 2;
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
+    uint64_t *sched_full = drain + 1;                // [kSchedDepth], one arrival (the claimer)
+    uint64_t *sched_empty = sched_full + kSchedDepth;  // [kSchedDepth], even CTA: every reader
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sched_empty + kSchedDepth);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     volatile int *epi_vote = reinterpret_cast<volatile int *>(tmem_holder + 2);  // 2 slots
     // stage fills issued by the producer / consumed by the MMA (read on abort), a zero flag
     volatile int *fills = reinterpret_cast<volatile int *>(tmem_holder + 4);
     int *g_tiles = reinterpret_cast<int *>(tmem_holder + 8);
     int *g_rows = g_tiles + (kMaxGroups + 1);
+    volatile int *sched_tile = g_rows + (kMaxGroups + 1);  // [kSchedDepth] claimed tile ids
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -205,6 +213,12 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
             ptx::mbar_init(&acc_empty[b], 2 * kEpiWarps);  // one arrival per epilogue warp of the pair
         }
         ptx::mbar_init(drain, 1);
+        for (int i = 0; i < kSchedDepth; ++i) {
+            ptx::mbar_init(&sched_full[i], 1);
+            // readers of a slot: the even CTA's MMA thread, the odd CTA's producer, and every
+            // epilogue warp of both CTAs
+            ptx::mbar_init(&sched_empty[i], 2 + 2 * kEpiWarps);
+        }
         *abort_flag = 0;
         epi_vote[0] = 0;
         epi_vote[1] = 0;
@@ -235,6 +249,34 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
     if (pid >= total) return;  // the same for both CTAs of the pair; nothing allocated yet
     auto tile_of = [&](int u) { return decode_tile(u, nfp, g_tiles, g_rows, G, cap, p.shared_last); };
 
+    // The pair's n-th tile.  The first S = max(npair, total - dyn_tail) tiles are walked
+    // round-robin (pair p takes p, p + npair, ...: its first ns of them), which keeps the pairs in
+    // step over neighbouring tiles, so that pairs sharing a weight tile stream it together.  The
+    // last tiles go to whichever pair is free: the even CTA's producer claims each (S + the launch
+    // counter's next value; `total` once all are handed out) and publishes it through ring slot
+    // (n - ns) % kSchedDepth of both CTAs, which every other role reads in the same order and
+    // then releases on the even CTA's sched_empty.
+    const bool dyn = p.tile_counter != nullptr && p.dyn_tail > 0;
+    const int S = dyn ? max(npair, total - p.dyn_tail) : total;
+    const int ns = (S - pid + npair - 1) / npair;  // >= 1: pid < npair <= S
+    auto ring_get = [&](int n, int &tau) -> bool {
+        if (!dyn || n < ns) {
+            tau = pid + n * npair;
+            return true;
+        }
+        const int u = n - ns, slot = u % kSchedDepth;
+        if (!ptx::mbar_wait_cluster(&sched_full[slot], (uint32_t)(u / kSchedDepth) & 1u, kWaitLimitNs, abort_flag))
+            return false;
+        tau = sched_tile[slot];
+        return true;
+    };
+    auto ring_release = [&](int n) {
+        if (!dyn || n < ns) return;
+        const int slot = (n - ns) % kSchedDepth;
+        if (rank == 0) ptx::mbar_arrive(&sched_empty[slot]);
+        else ptx::mbar_arrive_remote(ptx::mapa_shared(ptx::smem_u32(&sched_empty[slot]), 0));
+    };
+
     if (warp == kMmaWarp) ptx::tmem_alloc_pair(tmem_holder, kTmemCols);
     ptx::tc_fence_before();
     __syncthreads();
@@ -261,7 +303,41 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
             const uint32_t full_even = ptx::mapa_shared(ptx::smem_u32(full), 0);
             int it = 0, s = 0;
             uint32_t ph = 0;
-            for (int tau = pid; tau < total && ok; tau += npair) {
+            // dynamic tail, even CTA: tile n + 1 is published when tile n starts (so no role ever
+            // waits on the claim), and it was claimed one tile before that (so the atomic's round
+            // trip never stalls this thread)
+            const bool claimer = dyn && rank == 0;
+            int pend = (claimer && ns <= 1) ? atomicAdd(p.tile_counter, 1) : 0;
+            bool more = true;  // the counter may still hand out tiles
+            int tau = pid;
+            for (int n = 0;; ++n) {
+                if (n > 0 && !claimer) {
+                    if (!ring_get(n, tau)) {
+                        ok = false;
+                        break;
+                    }
+                    ring_release(n);
+                }
+                if (tau >= total) break;
+                int tau_next = pid + (n + 1) * npair;
+                if (claimer && n + 1 >= ns) {
+                    // publish tile n + 1 in both CTAs' ring slot (n + 1 - ns) % kSchedDepth
+                    const int u = n + 1 - ns, slot = u % kSchedDepth;
+                    if (u >= kSchedDepth &&
+                        !ptx::mbar_wait_cluster(&sched_empty[slot], (uint32_t)(u / kSchedDepth - 1) & 1u, kWaitLimitNs,
+                                                abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tau_next = S + pend < total ? S + pend : total;
+                    more = tau_next < total;
+                    sched_tile[slot] = tau_next;
+                    ptx::st_cluster_u32(ptx::mapa_shared(ptx::smem_u32((const void *)&sched_tile[slot]), 1),
+                                        (uint32_t)tau_next);
+                    ptx::mbar_arrive(&sched_full[slot]);
+                    ptx::mbar_arrive_remote(ptx::mapa_shared(ptx::smem_u32(&sched_full[slot]), 1));
+                }
+                if (claimer && more && n + 2 >= ns) pend = atomicAdd(p.tile_counter, 1);  // tile n + 2
                 const TileInfo t = tile_of(tau);
                 const bool shg = p.shared_last && t.g == G - 1;
                 const int ftile = 2 * t.ftile + (int)rank;
@@ -295,6 +371,8 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
                     }
                     if (++s == kStages) { s = 0; ph ^= 1u; }
                 }
+                if (!ok) break;
+                if (claimer) tau = tau_next;
             }
             fills[0] = it;
         }
@@ -312,7 +390,14 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
             uint32_t ph = 0;
             const uint64_t desc0 = ptx::sw128_desc(ptx::smem_u32(smem));
             bool ok = true;
-            for (int tau = pid; tau < total && ok; tau += npair, ++tc) {
+            for (int n = 0;; ++n, ++tc) {
+                int tau;
+                if (!ring_get(n, tau)) {
+                    ok = false;
+                    break;
+                }
+                ring_release(n);
+                if (tau >= total) break;
                 const TileInfo t = tile_of(tau);
                 const uint32_t nmma = (uint32_t)((t.nvalid + 15) & ~15);
                 const int buf = tc & 1;
@@ -361,8 +446,20 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
         const uint32_t acc_empty_remote = ptx::mapa_shared(ptx::smem_u32(acc_empty), 0);
         int tc = 0;
         bool ok = true;
-        for (int tau = pid; tau < total; tau += npair, ++tc) {
-            const TileInfo t = tile_of(tau);
+        for (int n = 0;; ++n, ++tc) {
+            // lane 0 takes the tile from the ring and hands it to the warp; every warp then
+            // passes the vote below even on the last (end) round, so they leave together
+            int tau = total;
+            int ok_t = 1;
+            if (lane == 0) {
+                ok_t = ring_get(n, tau) ? 1 : 0;
+                if (ok_t) ring_release(n);
+            }
+            ok_t = __shfl_sync(0xffffffffu, ok_t, 0);
+            tau = __shfl_sync(0xffffffffu, tau, 0);
+            const bool end = ok_t && tau >= total;
+            const bool live = ok_t && !end;
+            const TileInfo t = live ? tile_of(tau) : TileInfo{0, 0, 0, 0};
             const int buf = tc & 1;
             const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
             const int ftile = 2 * t.ftile + (int)rank;
@@ -370,7 +467,7 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
             // combine: the 16 warps fetch (output row, weight) of the tile's rows into shared
             // memory before the accumulator is ready (the loads overlap the main loop); the
             // vote barrier below publishes them to all epilogue warps
-            if (EPI == EPI_COMBINE && lane < BN / kEpiWarps) {
+            if (EPI == EPI_COMBINE && live && lane < BN / kEpiWarps) {
                 const int j = warp * (BN / kEpiWarps) + lane;
                 int orow = 0;
                 float w = 0.f;
@@ -389,12 +486,13 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
             }
             // The epilogue warps share named barriers, so they give up together: lane 0 of
             // each warp votes, and the vote is read by all after the barrier.
-            const bool got = ptx::mbar_wait(&acc_full[buf], aph, kWaitLimitNs, abort_flag);
-            if (lane == 0 && !got) epi_vote[tc & 1] = 1;
+            const bool got = live ? ptx::mbar_wait(&acc_full[buf], aph, kWaitLimitNs, abort_flag) : true;
+            if (lane == 0 && (!ok_t || !got)) epi_vote[tc & 1] = 1;
             ptx::named_bar(1, kEpiWarps * 32);
             const bool fail = epi_vote[tc & 1] != 0;
             ptx::named_bar(1, kEpiWarps * 32);
             if (fail) { ok = false; break; }
+            if (end) break;
             ptx::tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * kAccCols);
             float bias_f = 0.f;

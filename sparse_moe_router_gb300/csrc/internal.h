@@ -120,6 +120,11 @@ struct GemmArgs {
     // with shared_last: the last group's token rows are rows 0.. of the TokenMaps' `shared` map
     // (the tokens in order, e.g. x itself) instead of rows group_rows[G-1].. of the m[] maps
     bool shared_b_own;
+    // tile schedule: pair p takes tiles p, p + pairs, ... except the last dyn_tail tiles, which
+    // pairs claim from tile_counter (a device counter, zero at launch) as they come free.
+    // tile_counter NULL or dyn_tail 0: every tile round-robin.
+    int *tile_counter;
+    int dyn_tail;
 };
 
 // Launch the persistent grouped GEMM.  tm_a0 (and tm_a1 for EPI_SWIGLU: the up projection)
@@ -142,15 +147,20 @@ cudaError_t launch_topk(const float *logits, int T, int E, int k, int32_t *ids, 
 // Pairs per block of the permutation kernels: the chunk table holds one row of E counts per
 // chunk of this many consecutive pairs.
 constexpr int kPermChunk = 2048;
+// Tile counters of the grouped GEMMs that follow a permutation (gate/up, down): `sched` (or
+// NULL) receives kSchedCounters zeros from the permutation's scan kernel.
+constexpr int kSchedCounters = 2;
 size_t permute_scratch_ints(int T, int E, int k);
 cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int32_t *offsets,
                            int32_t *perm, int32_t *inv, int32_t *tile_prefix, int tile_n,
                            int32_t *chunk_tab, const float *topk_w, int32_t *row_tok,
-                           float *row_w, int *status, cudaStream_t s, int extra_rows = 0);
-// Token-tile prefix from given offsets, and row_tok[r] = perm[r] / k for the P rows.
+                           float *row_w, int *status, cudaStream_t s, int extra_rows = 0,
+                           int *sched = nullptr);
+// Token-tile prefix from given offsets, and row_tok[r] = perm[r] / k for the P rows (and the
+// zeroed tile counters, as launch_permute).
 cudaError_t launch_tile_prefix(const int32_t *offsets, int E, int32_t *tile_prefix, int tile_n,
                                const int32_t *perm, int P, int k, int32_t *row_tok,
-                               cudaStream_t s);
+                               cudaStream_t s, int *sched = nullptr);
 // out[t] = bf16( sum_j y[t*k + j] + acc[t] ) with y bf16 [T*k, H] (the weighted expert rows in
 // pair order) and acc fp32 [T, H] (the shared expert, or NULL); when x_next != NULL also
 // x_next = bf16(resid + out).  The sum runs in fp32, slots in order, then the shared term.

@@ -144,7 +144,7 @@ constexpr int kMaxPiece = 8192;
 size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
 struct Layout {
-    size_t status, logits, ids, topw, offsets, tiles, chunks, perm, inv, row_tok, row_w, h, h_s, acc, y, total;
+    size_t status, sched, logits, ids, topw, offsets, tiles, chunks, perm, inv, row_tok, row_w, h, h_s, acc, y, total;
 };
 
 Layout layout(const moe_config &c, int T) {
@@ -157,6 +157,7 @@ Layout layout(const moe_config &c, int T) {
     };
     const size_t Tt = (size_t)(T > 0 ? T : 1);
     L.status = take(256);
+    L.sched = take(256);  // the grouped GEMMs' tile counters
     L.logits = take(Tt * c.n_experts * 4);
     L.ids = take(Tt * c.top_k * 4);
     L.topw = take(Tt * c.top_k * 4);
@@ -292,6 +293,13 @@ moe_status run_shared(const moe_config &c, const moe_weights &w, const uint16_t 
     return MOE_OK;
 }
 
+// Tiles at the end of a grouped GEMM that CTA pairs claim dynamically, in waves of one tile
+// per pair (the rest run round-robin).
+#ifndef MOE_DYN_TAIL_WAVES
+#define MOE_DYN_TAIL_WAVES 1
+#endif
+int dyn_tail_tiles() { return MOE_DYN_TAIL_WAVES * (device_info().sm_count / 2); }
+
 // Routed experts, grouped: h rows (expert-sorted order) from the expert-sorted copy of x
 // (xp), then the down projection either stored per row in fp32 (y_rows, unfused) or weighted
 // and stored as bf16 rows in pair order (y_pairs[perm[r]] = bf16(row_w[r] * y)) for the
@@ -301,7 +309,7 @@ moe_status run_shared(const moe_config &c, const moe_weights &w, const uint16_t 
 moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t *x, int T,
                       const int32_t *offsets, const int32_t *tiles, const int32_t *row_tok,
                       const int32_t *perm, const float *row_w, uint16_t *xp, uint16_t *h, float *y_rows,
-                      uint16_t *y_pairs, int *status, cudaStream_t s, bool with_shared = false) {
+                      uint16_t *y_pairs, int *status, int *sched, cudaStream_t s, bool with_shared = false) {
     const uint64_t EI = (uint64_t)c.n_experts * c.inter;
     const uint64_t P = (uint64_t)T * c.top_k;
     const uint64_t rows = P + (with_shared ? (uint64_t)T : 0);
@@ -339,6 +347,8 @@ moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t 
     a.status = status;
     a.shared_last = with_shared;
     a.shared_b_own = with_shared;
+    a.tile_counter = sched;
+    a.dyn_tail = dyn_tail_tiles();
     MOE_CUDA(launch_gemm(EPI_SWIGLU, a, tg, tu, tx, tsg, tsu, KC_GATEUP_GEMM, s));
     GemmArgs d{};
     d.b_src = h;
@@ -350,6 +360,8 @@ moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t 
     d.ld = c.hidden;
     d.status = status;
     d.shared_last = with_shared;
+    d.tile_counter = sched ? sched + 1 : nullptr;
+    d.dyn_tail = dyn_tail_tiles();
     if (y_rows) {
         if (with_shared) return MOE_ERR_INVALID_ARG;
         d.out = y_rows;
@@ -385,13 +397,14 @@ moe_status forward_piece(const moe_config &c, const moe_weights &w, const uint16
     float *row_w = at<float>(ws, L.row_w);
     // a shared expert as wide as the routed ones runs inside the routed GEMMs, as group E
     const bool merged = c.shared_inter > 0 && c.shared_inter == c.inter;
+    int *sched = at<int>(ws, L.sched);
     MOE_CUDA(launch_permute(ids, T, c.n_experts, c.top_k, offsets, perm, inv, tiles, kTileN,
-                            at<int32_t>(ws, L.chunks), topw, row_tok, row_w, status, s, merged ? T : 0));
+                            at<int32_t>(ws, L.chunks), topw, row_tok, row_w, status, s, merged ? T : 0, sched));
     uint16_t *y = at<uint16_t>(ws, L.y);
     if (c.shared_inter > 0 && !merged) MOE_TRY(run_shared(c, w, x, T, h_s, acc, status, s));
     // y doubles as the expert-sorted copy of x: the gate/up GEMM is done reading it before the
     // down GEMM writes y (same stream)
-    MOE_TRY(run_routed(c, w, x, T, offsets, tiles, row_tok, perm, row_w, y, h, nullptr, y, status, s, merged));
+    MOE_TRY(run_routed(c, w, x, T, offsets, tiles, row_tok, perm, row_w, y, h, nullptr, y, status, sched, s, merged));
     const size_t P = (size_t)T * c.top_k;
     MOE_CUDA(launch_finalize(y, c.top_k, (c.shared_inter > 0 && !merged) ? acc : nullptr, resid, T, c.hidden, out,
                              x_next, s, merged ? y + P * c.hidden : nullptr));
@@ -503,10 +516,11 @@ moe_status moe_expert_ffn(const moe_config *cfg, const moe_weights *w, const moe
     int *status = at<int>(ws, L.status);
     int32_t *tiles = at<int32_t>(ws, L.tiles);
     int32_t *row_tok = at<int32_t>(ws, L.row_tok);
+    int *sched = at<int>(ws, L.sched);
     MOE_CUDA(launch_tile_prefix(expert_offsets, cfg->n_experts, tiles, kTileN, perm, T * cfg->top_k,
-                                cfg->top_k, row_tok, s));
+                                cfg->top_k, row_tok, s, sched));
     MOE_TRY(run_routed(*cfg, *w, x, T, expert_offsets, tiles, row_tok, perm, nullptr, at<uint16_t>(ws, L.y), h_rows,
-                       y_rows, nullptr, status, s));
+                       y_rows, nullptr, status, sched, s));
     if (shared_y && cfg->shared_inter > 0)
         MOE_TRY(run_shared(*cfg, *w, x, T, at<uint16_t>(ws, L.h_s), shared_y, status, s));
     return MOE_OK;

@@ -160,9 +160,11 @@ __global__ void __launch_bounds__(kPermThreads) perm_hist_kernel(const int32_t *
 
 __global__ void __launch_bounds__(kPermThreads, 1)
     perm_scan_kernel(int32_t *__restrict__ chunk_tab, int n_chunks, int E, int32_t *__restrict__ offsets,
-                     int32_t *__restrict__ tile_prefix, int tile_n, int extra_rows) {
+                     int32_t *__restrict__ tile_prefix, int tile_n, int extra_rows, int *__restrict__ sched) {
     __shared__ int sh_warp[32];
     const int tid = threadIdx.x;
+    // the grouped GEMMs' tile counters (gate/up, down) start at zero for the launches that follow
+    if (sched && tid < kSchedCounters) sched[tid] = 0;
     // tpe adjacent lanes per expert (a power of two <= 32 with E * tpe <= 1024); lane `sub` of
     // expert e owns chunks [c0, c1) of e's column of the table
     int tpe = 1;
@@ -289,9 +291,10 @@ __global__ void __launch_bounds__(kPermThreads) perm_scatter_kernel(const int32_
 __global__ void __launch_bounds__(kPermThreads, 1)
     tile_prefix_kernel(const int32_t *__restrict__ offsets, int E, int32_t *__restrict__ tile_prefix,
                        int tile_n, const int32_t *__restrict__ perm, int P, int k,
-                       int32_t *__restrict__ row_tok) {
+                       int32_t *__restrict__ row_tok, int *__restrict__ sched) {
     __shared__ int sh_warp[32];
     const int tid = threadIdx.x;
+    if (sched && tid < kSchedCounters) sched[tid] = 0;
     for (int r = tid; r < P; r += kPermThreads) row_tok[r] = perm[r] / k;
     const int cnt = tid < E ? offsets[tid + 1] - offsets[tid] : 0;
     const int tiles = tid < E ? token_tile_count(cnt) : 0;
@@ -431,7 +434,7 @@ size_t permute_scratch_ints(int T, int E, int k) {
 cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int32_t *offsets,
                            int32_t *perm, int32_t *inv, int32_t *tile_prefix, int tile_n,
                            int32_t *chunk_tab, const float *topk_w, int32_t *row_tok,
-                           float *row_w, int *status, cudaStream_t s, int extra_rows) {
+                           float *row_w, int *status, cudaStream_t s, int extra_rows, int *sched) {
     const int P = T * k;
     const int n_chunks = (P + kChunk - 1) / kChunk;
     // the scatter's shared-memory opt-in, once per device (under a lock: two host threads' first
@@ -457,7 +460,7 @@ cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int32_t *off
     {
         LaunchScope scope(KC_PERMUTE, s);
         perm_scan_kernel<<<1, kPermThreads, 0, s>>>(chunk_tab, n_chunks, E, offsets, tile_prefix, tile_n,
-                                                    extra_rows);
+                                                    extra_rows, sched);
     }
     LaunchScope scope(KC_PERMUTE, s);
     perm_scatter_kernel<<<n_chunks, kPermThreads, kPermWarps * E * sizeof(int), s>>>(
@@ -467,9 +470,9 @@ cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int32_t *off
 
 cudaError_t launch_tile_prefix(const int32_t *offsets, int E, int32_t *tile_prefix, int tile_n,
                                const int32_t *perm, int P, int k, int32_t *row_tok,
-                               cudaStream_t s) {
+                               cudaStream_t s, int *sched) {
     LaunchScope scope(KC_TILE_PREFIX, s);
-    tile_prefix_kernel<<<1, kPermThreads, 0, s>>>(offsets, E, tile_prefix, tile_n, perm, P, k, row_tok);
+    tile_prefix_kernel<<<1, kPermThreads, 0, s>>>(offsets, E, tile_prefix, tile_n, perm, P, k, row_tok, sched);
     return cudaGetLastError();
 }
 
