@@ -371,6 +371,11 @@ def run_ours(args, world, rank, local, pg):
     del layers, wts
     torch.cuda.empty_cache()
 
+    # -------------------------------------------------- the other prefill workloads --
+    workloads = None
+    if not args.skip_workloads:
+        workloads = run_workloads(args, dev, pg, peaks)
+
     # --------------------------------------------------------------------- decode --
     decode = None
     if not args.skip_decode:
@@ -394,8 +399,106 @@ def run_ours(args, world, rank, local, pg):
                                 "moe_graph_create"},
            "layer_tflops": round(layer_tflops, 1),
            "roofline": roofline, "per_kernel": per_kernel, "gpu_launches": int(launches),
-           "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "decode": decode,
+           "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "decode": decode, "workloads": workloads,
            "peaks": peaks}
+    return res
+
+
+def _graph_ms(abi, cfg, wts, T, x, ws, stream, steps, warmup, keep):
+    """Median-free mean time of one replay of the layer stack `wts` on x's T tokens, captured by
+    moe_graph_create (each layer l+1 reads bf16(x + out_l)); CUDA events on the launching stream."""
+    import torch
+    out, xb, xc = torch.empty_like(x), torch.empty_like(x), torch.empty_like(x)
+    g = abi.Graph(cfg, wts, T, x, out, xb, xc, ws, stream, resid=x, keep=keep)
+    for _ in range(warmup):
+        g.launch(stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        g.launch(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert abi.moe_check_status(ws) == 0
+    g.destroy()
+    return e0.elapsed_time(e1) / steps
+
+
+def _eager_split(abi, cfg, wts, T, x, ws, stream):
+    """Per-kernel CUDA-event averages of one eager pass of the layers (moe_forward per layer)."""
+    import torch
+    out, nxt = torch.empty_like(x), torch.empty_like(x)
+    abi.timing_enable(True)
+    for w in wts:
+        abi.moe_forward(cfg, w, x, T, out, nxt, ws, stream, resid=x)
+    torch.cuda.synchronize()
+    abi.timing_enable(False)
+    res = {}
+    for name in abi.timing_classes():
+        n, ms = abi.timing_read(name)
+        if n:
+            res[name] = {"launches": n, "avg_us": round(1e3 * ms / n, 2)}
+    return res
+
+
+def run_workloads(args, dev, pg, peaks):
+    """The other two prefill workloads, each under its own key: T=1024 with Zipf(1.0) router
+    bias (one layer, HBM-bound by the roofline) and T=13,337 composed as 8192+4096+1024+25 with
+    Zipf(1.5) and four dead experts (four layers), with a per-piece split."""
+    import numpy as np
+    import torch
+    from sparse_moe_router_gb300 import abi, inputs
+
+    stream = torch.cuda.current_stream()
+    res = {}
+    for name in ("prefill1k", "prompt13337"):
+        wl = inputs.WORKLOADS[name]
+        shape, T, L = wl.shape, wl.T, wl.n_layers
+        layers, x = inputs.make(wl, device=dev)
+        cfg = abi.config_of(shape)
+        ws = abi.alloc_workspace(cfg, min(T, 8192))
+        wts = [abi.weights(l) for l in layers]
+        # realised routing of the first layer (touched experts, skew)
+        ids = torch.empty(T, shape.top_k, dtype=torch.int32, device=dev)
+        tw = torch.empty(T, shape.top_k, dtype=torch.float32, device=dev)
+        wsr = abi.alloc_workspace(cfg, T)
+        abi.moe_route(cfg, wts[0], x, T, None, ids, tw, wsr)
+        torch.cuda.synchronize()
+        del wsr
+        counts = np.bincount(ids.cpu().numpy().ravel(), minlength=shape.n_experts)
+        touched = int((counts > 0).sum())
+        ms = _max_over_ranks(pg, _graph_ms(abi, cfg, wts, T, x, ws, stream, max(20, args.steps // 4), args.warmup,
+                                           layers), dev)
+        us_layer = 1e3 * ms / L
+        alg = _algorithmic(shape, T, experts_touched=touched)
+        H, E, I, Is = shape.hidden, shape.n_experts, shape.inter, shape.shared_inter
+        layer_bytes = 2 * (touched * 3 * I * H + 3 * Is * H + E * H + 2 * T * H)
+        tflops = alg["total_flops"] / (us_layer * 1e-6) / 1e12
+        gbs = layer_bytes / (us_layer * 1e-6) / 1e9
+        r = {"workload": wl.note, "tokens": T, "layers": L, "us_per_layer": round(us_layer, 2),
+             "tokens_per_s": round(T / (us_layer * 1e-6), 1),
+             "layer_tokens_per_s": round(T * L / (ms * 1e-3), 1),
+             "tflops": round(tflops, 1), "tc_frac_of_burst": round(tflops / peaks["bf16_tflops"], 4),
+             "algorithmic_bytes_per_layer": layer_bytes, "gbs": round(gbs, 1),
+             "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+             "experts_touched": touched, "rows_per_expert_max": int(counts.max()),
+             "rows_per_expert_mean": round(float(counts.mean()), 1), "empty_experts": int((counts == 0).sum()),
+             "per_kernel_eager": _eager_split(abi, cfg, wts[:1], T, x, ws, stream),
+             "launch": "moe_graph_create of the %d moe_forward layers, one moe_graph_launch per step" % L}
+        if name == "prompt13337":
+            pieces, t0 = [], 0
+            for pc in abi.moe_plan_pieces(T):
+                xs = x[t0:t0 + pc]
+                pms = _max_over_ranks(pg, _graph_ms(abi, cfg, wts[:1], pc, xs, ws, stream, 20, args.warmup, layers),
+                                      dev)
+                pieces.append({"tokens": pc, "us": round(1e3 * pms, 2),
+                               "tokens_per_s": round(pc / (pms * 1e-3), 1)})
+                t0 += pc
+            r["pieces_one_layer"] = pieces
+            r["pieces_sum_us"] = round(sum(p["us"] for p in pieces), 2)
+        res[name] = r
+        del layers, wts, x, ws
+        torch.cuda.empty_cache()
     return res
 
 
@@ -602,6 +705,94 @@ def _parity_sample(wl, layer, x, hl, xs, orc, rows=512):
             "bound": {"max_abs": 2e-2, "rel_l2": 5e-3}}
 
 
+def run_oracle_table(args):
+    """--oracle-table: the CPU oracle timed on the host cores for every workload, single-thread and
+    on all allowed cores (T=8192 and T=13,337: all cores only), each interleaved with the GPU layer
+    in A/B/B/A order (oracle, GPU, GPU, oracle) as the paired-order method of "AIMA Intel PTL
+    Qwen3.6 35B U4 Engine" ("ABBA" blocks); the ratio is the median oracle time over the median
+    GPU time of the same layer.  One layer each; the oracle runs its own routing on all tokens."""
+    import numpy as np
+    import torch
+    from oracle import moe_oracle as orc
+    from sparse_moe_router_gb300 import abi, inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    abi.load()
+    stream = torch.cuda.current_stream()
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    all_threads = orc.threads(0)
+    plan = [("tiny", ("single-thread", "all-core")), ("decode", ("single-thread", "all-core")),
+            ("prefill1k", ("single-thread", "all-core")), ("prefill8k", ("single-thread", "all-core")),
+            ("prompt13337", ("single-thread", "all-core"))]
+    # single-thread on the two large workloads: the first 512 tokens (tokens are independent, so
+    # the per-token cost holds for the whole layer); about 15 s per oracle run
+    sample_single = {"prefill8k": 512, "prompt13337": 512}
+    rows = []
+    for name, modes in plan:
+        wl = inputs.WORKLOADS[name]
+        layers, x = inputs.make(wl, device=dev, n_layers=1)
+        cfg = abi.config_of(wl.shape)
+        T = wl.T
+        ws = abi.alloc_workspace(cfg, min(T, 8192))
+        wts = [abi.weights(layers[0])]
+        hl = inputs.layer_to_host(layers[0])
+        xs = np.ascontiguousarray(inputs.to_u16(x))
+        k = wl.shape.top_k
+
+        def gpu_us():
+            return 1e3 * _graph_ms(abi, cfg, wts, T, x, ws, stream, 20, 3, layers)
+
+        ref = {}
+
+        def oracle_s(nt, n_tok):
+            t0 = time.perf_counter()
+            r = orc.forward(np.ascontiguousarray(xs[:n_tok]), hl, k, n_threads=nt)
+            dt = time.perf_counter() - t0
+            if n_tok == T:
+                ref.setdefault("r", r)
+            return dt
+
+        def parity():
+            """The GPU layer (moe_forward) against the oracle's own run, over the rows whose expert
+            set the two select alike (a near-tie may flip a selection; those rows are counted)."""
+            out = torch.empty_like(x)
+            ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+            tw = torch.empty(T, k, dtype=torch.float32, device=dev)
+            wsr = abi.alloc_workspace(cfg, T)
+            abi.moe_forward(cfg, wts[0], x, T, out, None, ws)
+            abi.moe_route(cfg, wts[0], x, T, None, ids, tw, wsr)
+            torch.cuda.synchronize()
+            r = ref["r"]
+            same = np.all(np.sort(ids.cpu().numpy(), 1) == np.sort(r["ids"], 1), axis=1)
+            f = lambda u: (u.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            g, o = f(inputs.to_u16(out))[same], f(r["out"])[same]
+            return {"rows": int(same.sum()), "rows_other_selection": int((~same).sum()),
+                    "max_abs": float(np.abs(g - o).max()) if g.size else 0.0,
+                    "rel_l2": float(np.linalg.norm(g - o) / max(np.linalg.norm(o), 1e-30)) if g.size else 0.0}
+
+        for mode in reversed(modes):  # all-core first: its full run is the parity reference
+            nt = 1 if mode == "single-thread" else all_threads
+            n_tok = sample_single.get(name, T) if mode == "single-thread" else T
+            a1 = oracle_s(nt, n_tok)
+            b1, b2 = gpu_us(), gpu_us()
+            a2 = oracle_s(nt, n_tok)
+            a, b = statistics.median([a1, a2]), statistics.median([b1, b2])
+            o_tps, g_tps = n_tok / a, T / (b * 1e-6)
+            rows.append({"workload": name, "tokens": T, "oracle_tokens": n_tok, "mode": mode, "threads": nt,
+                         "parity": parity() if "r" in ref else None,
+                         "order": "oracle, GPU, GPU, oracle",
+                         "oracle_s": [round(a1, 4), round(a2, 4)], "gpu_us": [round(b1, 2), round(b2, 2)],
+                         "oracle_tokens_per_s": round(o_tps, 2), "gpu_tokens_per_s": round(g_tps, 1),
+                         "ratio_gpu_over_oracle": round(g_tps / o_tps, 1)})
+            print(json.dumps(rows[-1]), file=sys.stderr, flush=True)
+        del layers, wts, x, ws, hl
+        torch.cuda.empty_cache()
+    return {"oracle_table": rows, "host_cores_allowed": cores, "oracle_threads_all_core": all_threads,
+            "oracle": "plain C, fp64 accumulation, OpenMP over tokens; one layer, the oracle's own routing",
+            "gpu": "one moe_forward layer captured by moe_graph_create, mean of 20 replays"}
+
+
 def run_reference(args, world, rank):
     """--impl reference: the CPU oracle on the host cores, a bounded sample per step."""
     if rank != 0:
@@ -659,6 +850,8 @@ def main():
     ap.add_argument("--skip-decode", action="store_true")
     ap.add_argument("--skip-q8", action="store_true", help="skip the E4M3-weight decode measurement")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-workloads", action="store_true",
+                    help="skip the T=1024 and T=13,337 prefill workloads")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="prefill layers per step (default: the workload's 4); fewer only for profiler captures")
@@ -667,6 +860,8 @@ def main():
     ap.add_argument("--decode-layers", type=int, default=0,
                     help="decode layers (default: the workload's 40); fewer only for profiler captures")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--oracle-table", action="store_true",
+                    help="time the CPU oracle on every workload (single-thread and all cores, A/B/B/A with the GPU)")
     ap.add_argument("--ref-step-seconds", type=float, default=4.0)
     ap.add_argument("--ref-total-seconds", type=float, default=120.0,
                     help="bound on the reference arm's oracle work over all its warm-up and timed steps")
@@ -676,6 +871,8 @@ def main():
     world, rank, local, pg = _dist_init()
     if args.impl == "reference":
         res = run_reference(args, world, rank)
+    elif args.oracle_table:
+        res = run_oracle_table(args) if rank == 0 else None
     elif args.decode_only:
         res = run_decode_only(args, world, rank, local, pg)
     else:
