@@ -376,6 +376,10 @@ def run_ours(args, world, rank, local, pg):
     if not args.skip_workloads:
         workloads = run_workloads(args, dev, pg, peaks)
 
+    prefill_q8 = None
+    if not args.skip_q8:
+        prefill_q8 = run_prefill_q8(args, dev, pg, peaks)
+
     # --------------------------------------------------------------------- decode --
     decode = None
     if not args.skip_decode:
@@ -400,6 +404,7 @@ def run_ours(args, world, rank, local, pg):
            "layer_tflops": round(layer_tflops, 1),
            "roofline": roofline, "per_kernel": per_kernel, "gpu_launches": int(launches),
            "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "decode": decode, "workloads": workloads,
+           "prefill_e4m3_weights": prefill_q8,
            "peaks": peaks}
     return res
 
@@ -498,6 +503,80 @@ def run_workloads(args, dev, pg, peaks):
             r["pieces_sum_us"] = round(sum(p["us"] for p in pieces), 2)
         res[name] = r
         del layers, wts, x, ws
+        torch.cuda.empty_cache()
+    return res
+
+
+def run_prefill_q8(args, dev, pg, peaks):
+    """The prefill workloads with E4M3 expert weights (moe_forward_q8): the bf16 layers quantised on
+    the device (moe_quantize_e4m3), the layer stack captured as one CUDA graph."""
+    import torch
+    from sparse_moe_router_gb300 import abi, inputs
+
+    s = torch.cuda.Stream(device=dev)
+    res = {}
+    for name in ("prefill8k", "prefill1k"):
+        wl = inputs.WORKLOADS[name]
+        shape, T, L = wl.shape, wl.T, wl.n_layers
+        layers_bf, x0 = inputs.make(wl, device=dev)
+        with torch.cuda.stream(s):
+            layers = [abi.quantize_layer(l, s) for l in layers_bf]
+        torch.cuda.synchronize()
+        del layers_bf
+        cfg = abi.config_of(shape)
+        ws = abi.alloc_workspace(cfg, min(T, 8192))
+        wts = [abi.weights_q8(l) for l in layers]
+        bufs = [torch.empty_like(x0), torch.empty_like(x0)]
+        out = torch.empty_like(x0)
+
+        def chain():
+            x = x0
+            for l in range(L):
+                nxt = bufs[l % 2]
+                abi.moe_forward_q8(cfg, wts[l], x, T, out, nxt, ws, s, resid=x0)
+                x = nxt
+
+        with torch.cuda.stream(s):
+            chain()
+        torch.cuda.synchronize()
+        assert abi.moe_check_status(ws) == 0
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                chain()
+        torch.cuda.synchronize()
+        steps = max(20, args.steps // 4)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            for _ in range(args.warmup):
+                g.replay()
+            torch.cuda.synchronize()
+            e0.record(s)
+            for _ in range(steps):
+                g.replay()
+            e1.record(s)
+        torch.cuda.synchronize()
+        ms = _max_over_ranks(pg, e0.elapsed_time(e1) / steps, dev)
+        del g
+        abi.timing_enable(True)
+        with torch.cuda.stream(s):
+            abi.moe_forward_q8(cfg, wts[0], x0, T, out, bufs[0], ws, s, resid=x0)
+        torch.cuda.synchronize()
+        abi.timing_enable(False)
+        split = {}
+        for kn in abi.timing_classes():
+            n, t = abi.timing_read(kn)
+            if n:
+                split[kn] = {"launches": n, "avg_us": round(1e3 * t / n, 2)}
+        us_layer = 1e3 * ms / L
+        alg = _algorithmic(shape, T)
+        res[name] = {"tokens": T, "layers": L, "us_per_layer": round(us_layer, 2),
+                     "layer_tokens_per_s": round(T * L / (ms * 1e-3), 1),
+                     "tflops": round(alg["total_flops"] / (us_layer * 1e-6) / 1e12, 1),
+                     "per_kernel_eager": split,
+                     "weights": "E4M3 codes + fp32 row scales for every expert matrix (router bf16), quantised "
+                                "on the device from the bf16 workload"}
+        del layers, wts, ws
         torch.cuda.empty_cache()
     return res
 
@@ -848,7 +927,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-decode", action="store_true")
-    ap.add_argument("--skip-q8", action="store_true", help="skip the E4M3-weight decode measurement")
+    ap.add_argument("--skip-q8", action="store_true", help="skip the E4M3-weight measurements")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-workloads", action="store_true",
                     help="skip the T=1024 and T=13,337 prefill workloads")

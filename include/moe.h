@@ -202,6 +202,20 @@ moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const moe_bf
                        moe_bf16 *out, const moe_bf16 *resid, moe_bf16 *x_next, void *ws,
                        size_t ws_bytes, void *stream);
 
+/* moe_forward for a layer with quantised expert weights (moe_weights_q8): the same piece
+ * composition, router (bf16 weights), selection, permutation, rounding points and combine, with
+ * every expert matrix streamed as its E4M3 codes, one byte a weight ("AI MAX+ 395部署Qwen3大模型：
+ * GFX1151引擎实测优化解析", "两种权重格式：HGN 与 GGUF 的统一支持": 8-bit float weights for the large
+ * modules).  The grouped GEMMs widen each code exactly to bf16 in shared memory (every E4M3 value
+ * is a bf16 value), multiply with bf16 tokens into fp32, and scale each weight row's accumulator
+ * by its fp32 row scale; h = bf16(silu(g) * u) as in moe_forward.  Every piece, however short,
+ * takes this grouped path (there is no E4M3 variant of the 1-4-token kernels in moe_forward;
+ * moe_decode_chain_q8 is the quantised decode step).  Same arguments, workspace, alignment and
+ * errors as moe_forward. */
+moe_status moe_forward_q8(const moe_config *cfg, const moe_weights_q8 *w, const moe_bf16 *x, int T,
+                          moe_bf16 *out, const moe_bf16 *resid, moe_bf16 *x_next, void *ws,
+                          size_t ws_bytes, void *stream);
+
 /* A layer stack captured once as a CUDA graph and replayed (the resident prefill buckets of
  * "AIMA AMD395 Qwen3.6 35B Linux Engine", release boundary v1.5.0: one graph per bucket size,
  * kept resident with its workspace).  The graph holds n_layers (1..64) moe_forward calls on T

@@ -26,7 +26,7 @@ EXPORTS = ["moe_status_string", "moe_workspace_size", "moe_route", "moe_route_fr
            "moe_plan_pieces", "moe_launch_count", "moe_timing_enable", "moe_timing_read",
            "moe_timing_name", "moe_timing_classes", "moe_selftest_wait", "moe_decode_chain",
            "moe_decode_chain_q8", "moe_quantize_e4m3", "moe_graph_create", "moe_graph_launch",
-           "moe_graph_kernel_count", "moe_graph_destroy"]
+           "moe_graph_kernel_count", "moe_graph_destroy", "moe_forward_q8"]
 
 
 class MoeError(RuntimeError):
@@ -80,6 +80,7 @@ def load(path: str = LIB_PATH):
     L.moe_forward.argtypes = [C, W, _P, _I, _P, _P, _P, _P, _SZ, _P]
     L.moe_decode_chain.argtypes = [C, W, _I, _P, _P, _P, _P, _P, _SZ, _P]
     L.moe_decode_chain_q8.argtypes = [C, ctypes.POINTER(WeightsQ8), _I, _P, _P, _P, _P, _P, _SZ, _P]
+    L.moe_forward_q8.argtypes = [C, ctypes.POINTER(WeightsQ8), _P, _I, _P, _P, _P, _P, _SZ, _P]
     L.moe_quantize_e4m3.argtypes = [_P, _I, _I, _P, _P, _P]
     L.moe_check_status.argtypes = [_P, _SZ, ctypes.POINTER(_I), _P]
     L.moe_selftest_wait.argtypes = [_P, _SZ, ctypes.c_ulonglong, _I, _P]
@@ -101,7 +102,7 @@ def load(path: str = LIB_PATH):
                "moe_combine", "moe_forward", "moe_check_status", "moe_timing_enable",
                "moe_timing_read", "moe_timing_classes", "moe_selftest_wait", "moe_decode_chain",
                "moe_decode_chain_q8", "moe_quantize_e4m3", "moe_graph_create", "moe_graph_launch",
-               "moe_graph_destroy"):
+               "moe_graph_destroy", "moe_forward_q8"):
         getattr(L, fn).restype = _I
     _lib = L
     return L
@@ -254,6 +255,13 @@ class Graph:
             self.destroy()
         except Exception:
             pass
+
+
+def moe_forward_q8(cfg, w, x, T, out, x_next, ws, stream=None, resid=None):
+    """The layer with E4M3 expert weights (a WeightsQ8): x [T,H] -> out (and x_next)."""
+    st = lib().moe_forward_q8(ctypes.byref(cfg), ctypes.byref(w), _ptr(x), int(T), _ptr(out), _ptr(resid),
+                              _ptr(x_next), _ptr(ws), ws.numel(), _stream(stream))
+    _check("moe_forward_q8", st)
 
 
 def moe_decode_chain(cfg, layers, x0, out, x_last, ws, stream=None, resid=None):

@@ -38,6 +38,8 @@
 // tile) with the token tile fastest, so pairs sharing a weight tile run together; a shared-expert
 // group's tiles are spread evenly among the routed ones.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include <mutex>
 
@@ -67,19 +69,31 @@ constexpr int kPairStride = 36;
 // pair tile to the other roles of both CTAs (more than the tiles any role can run ahead).
 constexpr int kSchedDepth = 8;
 
-template <int EPI>
+// Q8: the weight operand arrives as E4M3 codes (one byte a weight, 8 KB per 128-row K block)
+// in a raw slot of the stage; converter warps widen the codes exactly to bf16 into the stage's
+// weight slot (the layout TMA would have written), and the epilogue multiplies each weight
+// row's accumulator by the row's fp32 scale.
+constexpr int kRawBytes = BM * BK;  // 8 KB
+constexpr int kConvBar = 8;         // named barrier of the converter warps
+
+template <int EPI, bool Q8 = false>
 struct Cfg {
     // K blocks per pipeline stage.  The long-K GEMMs (router, gate/up: K = H) take two, so the MMA
     // thread waits and commits once per 8 MMAs (each handshake costs the tensor pipe time it does
-    // not hide); the down GEMM (K = I, a few stages a tile) keeps one and the deeper ring.
-    static constexpr int kKB = (EPI == EPI_COMBINE) ? 1 : 2;
-    static constexpr int kStages = kPipeBytes / (kKB * kStepBytes);
-    static constexpr int kStageBytes = kKB * kStepBytes;
+    // not hide); the down GEMM (K = I, a few stages a tile) keeps one and the deeper ring, and so
+    // does the E4M3 variant (its stages carry the raw codes too).
+    static constexpr int kKB = (EPI == EPI_COMBINE || Q8) ? 1 : 2;
+    static constexpr int kStep = kStepBytes + (Q8 ? kRawBytes : 0);  // one K block in one CTA
+    static constexpr int kStages = kPipeBytes / (kKB * kStep);
+    static constexpr int kStageBytes = kKB * kStep;
     // epilogue warps: the weighted row scatter keeps many warps storing; the others need 8
     static constexpr int kEpiWarps = (EPI == EPI_COMBINE) ? 16 : 8;
-    static constexpr int kProdWarp0 = kEpiWarps;    // 4 producer warps
-    static constexpr int kMmaWarp = kEpiWarps + 4;  // TMEM allocation; lane 0 of the even CTA: MMA
-    static constexpr int kThreads = (kEpiWarps + 5) * 32;
+    static constexpr int kProdWarp0 = kEpiWarps;      // 4 producer warps (lane 0 of the first: TMA)
+    static constexpr int kConvWarp0 = kEpiWarps + 1;  // Q8: 4 converter warps
+    static constexpr int kConvWarps = Q8 ? 4 : 0;
+    // TMEM allocation; lane 0 of the even CTA: MMA
+    static constexpr int kMmaWarp = Q8 ? kConvWarp0 + kConvWarps : kEpiWarps + 4;
+    static constexpr int kThreads = (kMmaWarp + 1) * 32;
     static constexpr int kFT = (EPI == EPI_SWIGLU) ? 64 : BM;    // output features per CTA tile
     // SwiGLU: gate/up exchange, fp32 [2 sub-groups][16 rows][kStgStride];
     // combine: per-warp transpose buffers [warps][8 token pairs][kPairStride words]
@@ -87,9 +101,9 @@ struct Cfg {
         (EPI == EPI_SWIGLU) ? 2 * 16 * kStgStride * 4 : (EPI == EPI_COMBINE ? kEpiWarps * 8 * kPairStride * 4 : 0);
     // combine: per-tile (output row, weight) of the BN tile rows, double-buffered
     static constexpr int kMetaBytes = (EPI == EPI_COMBINE) ? 2 * BN * 8 : 0;
-    // full, empty per stage; acc_full, acc_empty per accumulator; drain; sched_full, sched_empty
-    // per slot of the tile ring
-    static constexpr int kBarBytes = (2 * kStages + 5 + 2 * kSchedDepth) * 8;
+    // full, empty, raw_full per stage; acc_full, acc_empty per accumulator; drain; sched_full,
+    // sched_empty per slot of the tile ring
+    static constexpr int kBarBytes = (3 * kStages + 5 + 2 * kSchedDepth) * 8;
     static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kPipeBytes + kStagingBytes +
                                       kMetaBytes + kBarBytes + 32 + 2 * (kMaxGroups + 1) * 4 +
                                       kSchedDepth * 4;
@@ -158,12 +172,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-template <int EPI>
-__global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
+template <int EPI, bool Q8>
+__global__ void __launch_bounds__(Cfg<EPI, Q8>::kThreads, 1)
     gemm_kernel(const GemmArgs p, const __grid_constant__ CUtensorMap tm_a0,
                 const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ TokenMaps tm_b,
                 const __grid_constant__ CUtensorMap tm_s0, const __grid_constant__ CUtensorMap tm_s1) {
-    using C = Cfg<EPI>;
+    using C = Cfg<EPI, Q8>;
+    constexpr int kStep = C::kStep;
     constexpr int kStages = C::kStages;
     constexpr int kStageBytes = C::kStageBytes;
     constexpr int kKB = C::kKB;
@@ -186,7 +201,8 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
     uint64_t *drain = acc_empty + 2;
     uint64_t *sched_full = drain + 1;                // [kSchedDepth], one arrival (the claimer)
     uint64_t *sched_empty = sched_full + kSchedDepth;  // [kSchedDepth], even CTA: every reader
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sched_empty + kSchedDepth);
+    uint64_t *raw_full = sched_empty + kSchedDepth;    // [kStages] Q8: this CTA's raw codes landed
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(raw_full + kStages);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     volatile int *epi_vote = reinterpret_cast<volatile int *>(tmem_holder + 2);  // 2 slots
     // stage fills issued by the producer / consumed by the MMA (read on abort), a zero flag
@@ -205,8 +221,10 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
-            ptx::mbar_init(&full[s], 1);
+            // Q8: the even producer's expect_tx (token rows) and every converter warp of both CTAs
+            ptx::mbar_init(&full[s], 1 + 2 * C::kConvWarps);
             ptx::mbar_init(&empty[s], 1);
+            ptx::mbar_init(&raw_full[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&acc_full[b], 1);
@@ -216,8 +234,8 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
         for (int i = 0; i < kSchedDepth; ++i) {
             ptx::mbar_init(&sched_full[i], 1);
             // readers of a slot: the even CTA's MMA thread, the odd CTA's producer, and every
-            // epilogue warp of both CTAs
-            ptx::mbar_init(&sched_empty[i], 2 + 2 * kEpiWarps);
+            // epilogue (and Q8: converter) warp of both CTAs
+            ptx::mbar_init(&sched_empty[i], 2 + 2 * kEpiWarps + 2 * C::kConvWarps);
         }
         *abort_flag = 0;
         epi_vote[0] = 0;
@@ -352,16 +370,28 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
                 const int nbox = own ? kTokenBoxes : (half + 15) >> 4;  // box rows / 16, 1..kTokenBoxes
                 const void *mb = own ? (const void *)&tm_b.shared : (const void *)&tm_b.m[nbox - 1];
                 const int brow = (own ? t.row0 - g_rows[G - 1] : t.row0) + (int)rank * half;
-                const uint32_t stage_tx = 2u * (uint32_t)kKB * (uint32_t)(kABytes + nbox * 16 * BK * 2);
+                // bytes the even CTA's full barrier counts: both CTAs' token rows, and (bf16 weights)
+                // both CTAs' weight rows; Q8 weight codes complete on each CTA's raw_full instead
+                const uint32_t stage_tx = 2u * (uint32_t)kKB * (uint32_t)((Q8 ? 0 : kABytes) + nbox * 16 * BK * 2);
                 for (int ks = 0; ks < nks; ++ks, ++it) {
                     if (!ptx::mbar_wait(&empty[s], ph ^ 1u, kWaitLimitNs, abort_flag)) { ok = false; break; }
                     const uint32_t bar = full_even + (uint32_t)(s * 8);
                     if (rank == 0) ptx::mbar_arrive_expect_tx(&full[s], stage_tx);
+                    if (Q8) ptx::mbar_arrive_expect_tx(&raw_full[s], (uint32_t)(kKB * kRawBytes));
 #pragma unroll
                     for (int j = 0; j < kKB; ++j) {
-                        uint8_t *st = smem + s * kStageBytes + j * kStepBytes;
+                        uint8_t *st = smem + s * kStageBytes + j * kStep;
                         const int kc = (ks * kKB + j) * BK;
-                        if (EPI == EPI_SWIGLU) {
+                        if (Q8) {
+                            // the codes of this CTA's weight rows, row-major 64 bytes a row
+                            uint8_t *raw = st + kStepBytes;
+                            if (EPI == EPI_SWIGLU) {
+                                ptx::tma_load_2d(raw, ma0, kc, arow, &raw_full[s]);
+                                ptx::tma_load_2d(raw + kRawBytes / 2, ma1, kc, arow, &raw_full[s]);
+                            } else {
+                                ptx::tma_load_2d(raw, ma0, kc, arow, &raw_full[s]);
+                            }
+                        } else if (EPI == EPI_SWIGLU) {
                             ptx::tma_load_2d_pair(st, ma0, kc, arow, bar);
                             ptx::tma_load_2d_pair(st + kABytes / 2, ma1, kc, arow, bar);
                         } else {
@@ -375,6 +405,69 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
                 if (claimer) tau = tau_next;
             }
             fills[0] = it;
+        } else if (Q8 && warp >= C::kConvWarp0) {
+            // ------------------------------------------------------- converters (Q8) --
+            // 16-byte chunk idx = ci + 128 i (i < 4) of a K block's raw codes holds codes
+            // 16 (idx % 4) .. +15 of weight row idx / 4.  They are widened exactly (E4M3 -> f16 ->
+            // f32 -> bf16: every E4M3 value is a bf16 value) into bf16 chunks 2 (idx % 4) and
+            // 2 (idx % 4) + 1 of that row, at their 128-byte-swizzled places (chunk c of row r at
+            // r * 128 + (c ^ r % 8) * 16, as TMA would write bf16 weights).  Each lane fences its
+            // writes for the async proxy; the warp then adds one arrival to the even CTA's full
+            // barrier of the stage (so no named barrier: a warp that gives up leaves alone).
+            const int ci = tid - C::kConvWarp0 * 32;
+            const uint32_t full_even = ptx::mapa_shared(ptx::smem_u32(full), 0);
+            int s = 0;
+            uint32_t ph = 0;
+            for (int n = 0; ok; ++n) {
+                int tau = total, okr = 1;
+                if (lane == 0) {
+                    okr = ring_get(n, tau) ? 1 : 0;
+                    if (okr) ring_release(n);
+                }
+                okr = __shfl_sync(0xffffffffu, okr, 0);
+                tau = __shfl_sync(0xffffffffu, tau, 0);
+                if (!okr) {
+                    ok = false;
+                    break;
+                }
+                if (tau >= total) break;
+                for (int ks = 0; ks < nks; ++ks) {
+                    const bool w_ok = __all_sync(0xffffffffu, ptx::mbar_wait(&raw_full[s], ph, kWaitLimitNs, abort_flag));
+                    if (!w_ok) {
+                        ok = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int jb = 0; jb < kKB; ++jb) {
+                        uint8_t *a = smem + s * kStageBytes + jb * kStep;
+                        const uint8_t *raw = a + kStepBytes;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int idx = ci + 128 * i, r = idx >> 2, q = idx & 3;
+                            const uint4 cw = *reinterpret_cast<const uint4 *>(raw + idx * 16);
+                            const __nv_fp8x2_storage_t *c2 = reinterpret_cast<const __nv_fp8x2_storage_t *>(&cw);
+                            uint32_t o[8];
+#pragma unroll
+                            for (int m = 0; m < 8; ++m) {
+                                const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(c2[m], __NV_E4M3);
+                                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
+                                o[m] = pack_bf16x2(f.x, f.y);
+                            }
+                            *reinterpret_cast<uint4 *>(a + r * 128 + (((2 * q) ^ (r & 7)) << 4)) =
+                                make_uint4(o[0], o[1], o[2], o[3]);
+                            *reinterpret_cast<uint4 *>(a + r * 128 + (((2 * q + 1) ^ (r & 7)) << 4)) =
+                                make_uint4(o[4], o[5], o[6], o[7]);
+                        }
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (rank == 0) ptx::mbar_arrive(&full[s]);
+                        else ptx::mbar_arrive_remote(full_even + (uint32_t)(s * 8));
+                    }
+                    if (++s == kStages) { s = 0; ph ^= 1u; }
+                }
+            }
         }
         if (!ok) {
             set_error(p.status, MOE_ERR_TIMEOUT);
@@ -414,7 +507,7 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
                     // and one K=16 slice is 32 bytes further along the swizzled 128-byte row
 #pragma unroll
                     for (int j = 0; j < kKB; ++j) {
-                        const uint64_t da = desc0 + (uint64_t)((s * kStageBytes + j * kStepBytes) >> 4);
+                        const uint64_t da = desc0 + (uint64_t)((s * kStageBytes + j * kStep) >> 4);
                         const uint64_t db = da + (uint64_t)(kABytes >> 4);
                         ptx::mma_bf16_pair(d_base, da, db, idesc, (ks | j) != 0 ? 1u : 0u);
 #pragma unroll
@@ -500,6 +593,20 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
                 const int f = ftile * BM + frow;
                 if (p.bias != nullptr && f < p.F) bias_f = __ldg(&p.bias[f]);
             }
+            // Q8: this lane's weight row scale (SwiGLU: lanes 0..63 gate rows, 64..127 the same
+            // features' up rows; the shared expert's group reads its own scale arrays)
+            float sc = 1.f;
+            if (Q8 && store) {
+                const bool shg = p.shared_last && t.g == G - 1;
+                const size_t gofs = shg ? 0 : (size_t)t.g * p.F;
+                if (EPI == EPI_SWIGLU) {
+                    const float *sp = frow < 64 ? (shg ? p.ws_scale0 : p.w_scale0) : (shg ? p.ws_scale1 : p.w_scale1);
+                    sc = __ldg(sp + gofs + ftile * 64 + (frow & 63));
+                } else {
+                    const int f = ftile * BM + frow;
+                    if (f < p.F) sc = __ldg((shg ? p.ws_scale0 : p.w_scale0) + gofs + f);
+                }
+            }
             // this warp's chunks are cidx = sub, sub + kSubs, ...; the TMEM load of the next
             // chunk is issued before the current one is processed, hiding its latency
             const int n_chunks = store ? (t.nvalid + 15) >> 4 : 0;
@@ -517,7 +624,7 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
                     // shared memory, then thread q computes token q/8, features 8*(q%8)..+7
                     // and writes them as one 16-byte store.
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) stg[jj * kStgStride + frow] = __uint_as_float(r[jj]);
+                    for (int jj = 0; jj < 16; ++jj) stg[jj * kStgStride + frow] = sc * __uint_as_float(r[jj]);
                     ptx::named_bar(2 + sub, 128);
                     const int q = frow;
                     const int jj = q >> 3, fg = (q & 7) * 8;
@@ -543,7 +650,7 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
 #pragma unroll
                         for (int jj = 0; jj < 16; ++jj)
                             if (j0 + jj < t.nvalid)
-                                o[(size_t)(t.row0 + j0 + jj) * p.ld + f] = __uint_as_float(r[jj]) + bias_f;
+                                o[(size_t)(t.row0 + j0 + jj) * p.ld + f] = sc * __uint_as_float(r[jj]) + bias_f;
                     }
                 } else {
                     // Weighted row scatter: tile row r is stored as bf16(w_r * D[:, r]) into
@@ -558,8 +665,10 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const float4 w4 = wv[q];
-                        const uint32_t lo = pack_bf16x2(w4.x * __uint_as_float(r[4 * q]), w4.y * __uint_as_float(r[4 * q + 1]));
-                        const uint32_t hi = pack_bf16x2(w4.z * __uint_as_float(r[4 * q + 2]), w4.w * __uint_as_float(r[4 * q + 3]));
+                        const uint32_t lo = pack_bf16x2(w4.x * (sc * __uint_as_float(r[4 * q])),
+                                                        w4.y * (sc * __uint_as_float(r[4 * q + 1])));
+                        const uint32_t hi = pack_bf16x2(w4.z * (sc * __uint_as_float(r[4 * q + 2])),
+                                                        w4.w * (sc * __uint_as_float(r[4 * q + 3])));
                         tb[(2 * q) * kPairStride + lane] = lo;
                         tb[(2 * q + 1) * kPairStride + lane] = hi;
                     }
@@ -622,11 +731,11 @@ __global__ void __launch_bounds__(Cfg<EPI>::kThreads, 1)
     }
 }
 
-template <int EPI>
+template <int EPI, bool Q8>
 cudaError_t launch_impl(const GemmArgs &a, const CUtensorMap &m0, const CUtensorMap &m1,
                         const TokenMaps &mb, const CUtensorMap &s0, const CUtensorMap &s1, int kc,
                         cudaStream_t s) {
-    using C = Cfg<EPI>;
+    using C = Cfg<EPI, Q8>;
     // per device: the shared-memory opt-in and how many CTA pairs fit on the GPU at once (set
     // once under a lock, so that two host threads' first launches do not race)
     static int max_pairs[64] = {0};
@@ -647,12 +756,12 @@ cudaError_t launch_impl(const GemmArgs &a, const CUtensorMap &m0, const CUtensor
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::unique_lock<std::mutex> lk(mu);
     if (max_pairs[dev] == 0) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<EPI, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemBytes);
         if (e != cudaSuccess) return e;
         cfg.gridDim = dim3(device_info().sm_count & ~1, 1, 1);
         int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<EPI>, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<EPI, Q8>, &cfg);
         if (e != cudaSuccess) return e;
         if (n < 1) return cudaErrorInvalidConfiguration;
         max_pairs[dev] = n;
@@ -667,7 +776,7 @@ cudaError_t launch_impl(const GemmArgs &a, const CUtensorMap &m0, const CUtensor
     if (pairs <= 0) return cudaSuccess;
     cfg.gridDim = dim3(2 * pairs, 1, 1);
     LaunchScope scope(kc, s);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_kernel<EPI>, a, m0, m1, mb, s0, s1);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_kernel<EPI, Q8>, a, m0, m1, mb, s0, s1);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -685,10 +794,20 @@ cudaError_t launch_gemm(GemmEpi epi, const GemmArgs &a, const CUtensorMap &tm_a0
     if (a.shared_b_own && !a.shared_last) return cudaErrorInvalidValue;
     if (epi == EPI_SWIGLU && (a.F % 64 != 0 || a.ld % 8 != 0)) return cudaErrorInvalidValue;
     if (epi == EPI_COMBINE && (a.F % BM != 0 || a.ld % 8 != 0)) return cudaErrorInvalidValue;
+    if (a.q8) {
+        if (!a.w_scale0 || (epi == EPI_SWIGLU && !a.w_scale1)) return cudaErrorInvalidValue;
+        if (a.shared_last && (!a.ws_scale0 || (epi == EPI_SWIGLU && !a.ws_scale1))) return cudaErrorInvalidValue;
+        switch (epi) {
+            case EPI_F32: return launch_impl<EPI_F32, true>(a, tm_a0, tm_a1, tm_b, tm_s0, tm_s1, kc, s);
+            case EPI_SWIGLU: return launch_impl<EPI_SWIGLU, true>(a, tm_a0, tm_a1, tm_b, tm_s0, tm_s1, kc, s);
+            case EPI_COMBINE: return launch_impl<EPI_COMBINE, true>(a, tm_a0, tm_a1, tm_b, tm_s0, tm_s1, kc, s);
+        }
+        return cudaErrorInvalidValue;
+    }
     switch (epi) {
-        case EPI_F32: return launch_impl<EPI_F32>(a, tm_a0, tm_a1, tm_b, tm_s0, tm_s1, kc, s);
-        case EPI_SWIGLU: return launch_impl<EPI_SWIGLU>(a, tm_a0, tm_a1, tm_b, tm_s0, tm_s1, kc, s);
-        case EPI_COMBINE: return launch_impl<EPI_COMBINE>(a, tm_a0, tm_a1, tm_b, tm_s0, tm_s1, kc, s);
+        case EPI_F32: return launch_impl<EPI_F32, false>(a, tm_a0, tm_a1, tm_b, tm_s0, tm_s1, kc, s);
+        case EPI_SWIGLU: return launch_impl<EPI_SWIGLU, false>(a, tm_a0, tm_a1, tm_b, tm_s0, tm_s1, kc, s);
+        case EPI_COMBINE: return launch_impl<EPI_COMBINE, false>(a, tm_a0, tm_a1, tm_b, tm_s0, tm_s1, kc, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -125,6 +125,12 @@ struct GemmArgs {
     // tile_counter NULL or dyn_tail 0: every tile round-robin.
     int *tile_counter;
     int dyn_tail;
+    // E4M3 weights: the weight maps are over byte codes (row-major, no swizzle, 64-byte boxes of
+    // 64 or 128 rows) and the accumulator of weight row f of group g is multiplied by
+    // w_scale0[g * F + f] (SwiGLU: gate rows; w_scale1: up rows); the shared expert's group by
+    // ws_scale0 / ws_scale1 [f]
+    bool q8;
+    const float *w_scale0, *w_scale1, *ws_scale0, *ws_scale1;
 };
 
 // Launch the persistent grouped GEMM.  tm_a0 (and tm_a1 for EPI_SWIGLU: the up projection)

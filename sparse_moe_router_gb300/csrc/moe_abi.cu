@@ -129,6 +129,12 @@ bool encode_token_maps(TokenMaps *tm, const void *base, uint64_t rows, uint64_t 
     return true;
 }
 
+// E4M3 weight codes [rows, cols] as a plain row-major byte map with box_rows x 64-byte boxes
+// (the raw slot layout the GEMM's converter warps read).
+bool encode_tmap_2d_u8(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    return encode_tmap_2d(map, base, rows, cols, box_rows, 64, false, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1);
+}
+
 // -------------------------------------------------------------- workspace layout --
 
 namespace {
@@ -210,6 +216,18 @@ moe_status check_weights(const moe_config *c, const moe_weights *w, bool router,
     return MOE_OK;
 }
 
+moe_status check_weights_q8(const moe_config *c, const moe_weights_q8 *w) {
+    if (!w) return MOE_ERR_INVALID_ARG;
+    if (!w->w_router || !aligned16(w->w_router) || !w->q_gate || !w->q_up || !w->q_down || !w->s_gate ||
+        !w->s_up || !w->s_down || !aligned16(w->q_gate) || !aligned16(w->q_up) || !aligned16(w->q_down))
+        return MOE_ERR_INVALID_ARG;
+    if (c->shared_inter > 0 &&
+        (!w->qs_gate || !w->qs_up || !w->qs_down || !w->ss_gate || !w->ss_up || !w->ss_down ||
+         !aligned16(w->qs_gate) || !aligned16(w->qs_up) || !aligned16(w->qs_down)))
+        return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
 moe_status check_ws(const moe_config *c, void *ws, size_t ws_bytes, int T) {
     if (!ws) return MOE_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_INVALID_ARG;
@@ -260,14 +278,20 @@ moe_status run_router_gemm(const moe_config &c, const moe_weights &w, const uint
 // Shared expert over T tokens: h_s = SwiGLU(x), then Ws_down h_s stored (not added) into
 // out (fp32 [T,H]).  Gate/up maps use 64-row boxes: a SwiGLU tile holds 64 features' gate
 // rows and the same features' up rows.
+// wq != NULL: the shared expert's E4M3 codes and row scales instead of w's bf16 matrices.
 moe_status run_shared(const moe_config &c, const moe_weights &w, const uint16_t *x, int T,
-                      uint16_t *h_s, float *out, int *status, cudaStream_t s) {
+                      uint16_t *h_s, float *out, int *status, cudaStream_t s, const moe_weights_q8 *wq = nullptr) {
     CUtensorMap tg, tu, td;
     TokenMaps tx, th;
-    if (!encode_tmap_2d_bf16(&tg, w.ws_gate, c.shared_inter, c.hidden, kTileM / 2, 64) ||
-        !encode_tmap_2d_bf16(&tu, w.ws_up, c.shared_inter, c.hidden, kTileM / 2, 64) ||
-        !encode_tmap_2d_bf16(&td, w.ws_down, c.hidden, c.shared_inter, kTileM, 64) ||
-        !encode_token_maps(&tx, x, (uint64_t)T, c.hidden) ||
+    const bool q8 = wq != nullptr;
+    if (q8 ? (!encode_tmap_2d_u8(&tg, wq->qs_gate, c.shared_inter, c.hidden, kTileM / 2) ||
+              !encode_tmap_2d_u8(&tu, wq->qs_up, c.shared_inter, c.hidden, kTileM / 2) ||
+              !encode_tmap_2d_u8(&td, wq->qs_down, c.hidden, c.shared_inter, kTileM))
+           : (!encode_tmap_2d_bf16(&tg, w.ws_gate, c.shared_inter, c.hidden, kTileM / 2, 64) ||
+              !encode_tmap_2d_bf16(&tu, w.ws_up, c.shared_inter, c.hidden, kTileM / 2, 64) ||
+              !encode_tmap_2d_bf16(&td, w.ws_down, c.hidden, c.shared_inter, kTileM, 64)))
+        return MOE_ERR_CUDA;
+    if (!encode_token_maps(&tx, x, (uint64_t)T, c.hidden) ||
         !encode_token_maps(&th, h_s, (uint64_t)T, c.shared_inter))
         return MOE_ERR_CUDA;
     GemmArgs a{};
@@ -279,6 +303,11 @@ moe_status run_shared(const moe_config &c, const moe_weights &w, const uint16_t 
     a.out = h_s;
     a.ld = c.shared_inter;
     a.status = status;
+    if (q8) {
+        a.q8 = true;
+        a.w_scale0 = wq->ss_gate;
+        a.w_scale1 = wq->ss_up;
+    }
     MOE_CUDA(launch_gemm(EPI_SWIGLU, a, tg, tu, tx, tg, tu, KC_SHARED_GATEUP, s));
     GemmArgs d{};
     d.b_src = h_s;
@@ -289,6 +318,10 @@ moe_status run_shared(const moe_config &c, const moe_weights &w, const uint16_t 
     d.out = out;
     d.ld = c.hidden;
     d.status = status;
+    if (q8) {
+        d.q8 = true;
+        d.w_scale0 = wq->ss_down;
+    }
     MOE_CUDA(launch_gemm(EPI_F32, d, td, td, th, td, td, KC_SHARED_DOWN, s));
     return MOE_OK;
 }
@@ -309,24 +342,34 @@ int dyn_tail_tiles() { return MOE_DYN_TAIL_WAVES * (device_info().sm_count / 2);
 moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t *x, int T,
                       const int32_t *offsets, const int32_t *tiles, const int32_t *row_tok,
                       const int32_t *perm, const float *row_w, uint16_t *xp, uint16_t *h, float *y_rows,
-                      uint16_t *y_pairs, int *status, int *sched, cudaStream_t s, bool with_shared = false) {
+                      uint16_t *y_pairs, int *status, int *sched, cudaStream_t s, bool with_shared = false,
+                      const moe_weights_q8 *wq = nullptr) {
     const uint64_t EI = (uint64_t)c.n_experts * c.inter;
     const uint64_t P = (uint64_t)T * c.top_k;
     const uint64_t rows = P + (with_shared ? (uint64_t)T : 0);
     CUtensorMap tg, tu, td, tsg, tsu, tsd;
     TokenMaps tx, th;
-    if (!encode_tmap_2d_bf16(&tg, w.w_gate, EI, c.hidden, kTileM / 2, 64) ||
-        !encode_tmap_2d_bf16(&tu, w.w_up, EI, c.hidden, kTileM / 2, 64) ||
-        !encode_tmap_2d_bf16(&td, w.w_down, (uint64_t)c.n_experts * c.hidden, c.inter, kTileM, 64) ||
-        !encode_token_maps(&tx, xp, P, c.hidden) || !encode_token_maps(&th, h, rows, c.inter))
+    const bool q8 = wq != nullptr;
+    const uint64_t EH = (uint64_t)c.n_experts * c.hidden;
+    if (q8 ? (!encode_tmap_2d_u8(&tg, wq->q_gate, EI, c.hidden, kTileM / 2) ||
+              !encode_tmap_2d_u8(&tu, wq->q_up, EI, c.hidden, kTileM / 2) ||
+              !encode_tmap_2d_u8(&td, wq->q_down, EH, c.inter, kTileM))
+           : (!encode_tmap_2d_bf16(&tg, w.w_gate, EI, c.hidden, kTileM / 2, 64) ||
+              !encode_tmap_2d_bf16(&tu, w.w_up, EI, c.hidden, kTileM / 2, 64) ||
+              !encode_tmap_2d_bf16(&td, w.w_down, EH, c.inter, kTileM, 64)))
+        return MOE_ERR_CUDA;
+    if (!encode_token_maps(&tx, xp, P, c.hidden) || !encode_token_maps(&th, h, rows, c.inter))
         return MOE_ERR_CUDA;
     // the shared expert's token rows are x itself, in order
     if (with_shared && !encode_tmap_2d_bf16(&tx.shared, x, (uint64_t)T, c.hidden, kTokenBoxRows, 64))
         return MOE_ERR_CUDA;
     if (with_shared) {
-        if (!encode_tmap_2d_bf16(&tsg, w.ws_gate, c.shared_inter, c.hidden, kTileM / 2, 64) ||
-            !encode_tmap_2d_bf16(&tsu, w.ws_up, c.shared_inter, c.hidden, kTileM / 2, 64) ||
-            !encode_tmap_2d_bf16(&tsd, w.ws_down, c.hidden, c.shared_inter, kTileM, 64))
+        if (q8 ? (!encode_tmap_2d_u8(&tsg, wq->qs_gate, c.shared_inter, c.hidden, kTileM / 2) ||
+                  !encode_tmap_2d_u8(&tsu, wq->qs_up, c.shared_inter, c.hidden, kTileM / 2) ||
+                  !encode_tmap_2d_u8(&tsd, wq->qs_down, c.hidden, c.shared_inter, kTileM))
+               : (!encode_tmap_2d_bf16(&tsg, w.ws_gate, c.shared_inter, c.hidden, kTileM / 2, 64) ||
+                  !encode_tmap_2d_bf16(&tsu, w.ws_up, c.shared_inter, c.hidden, kTileM / 2, 64) ||
+                  !encode_tmap_2d_bf16(&tsd, w.ws_down, c.hidden, c.shared_inter, kTileM, 64)))
             return MOE_ERR_CUDA;
     } else {
         tsg = tg;
@@ -349,6 +392,13 @@ moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t 
     a.shared_b_own = with_shared;
     a.tile_counter = sched;
     a.dyn_tail = dyn_tail_tiles();
+    if (q8) {
+        a.q8 = true;
+        a.w_scale0 = wq->s_gate;
+        a.w_scale1 = wq->s_up;
+        a.ws_scale0 = wq->ss_gate;
+        a.ws_scale1 = wq->ss_up;
+    }
     MOE_CUDA(launch_gemm(EPI_SWIGLU, a, tg, tu, tx, tsg, tsu, KC_GATEUP_GEMM, s));
     GemmArgs d{};
     d.b_src = h;
@@ -362,6 +412,11 @@ moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t 
     d.shared_last = with_shared;
     d.tile_counter = sched ? sched + 1 : nullptr;
     d.dyn_tail = dyn_tail_tiles();
+    if (q8) {
+        d.q8 = true;
+        d.w_scale0 = wq->s_down;
+        d.ws_scale0 = wq->ss_down;
+    }
     if (y_rows) {
         if (with_shared) return MOE_ERR_INVALID_ARG;
         d.out = y_rows;
@@ -378,7 +433,7 @@ moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t 
 // One prefill piece of T tokens (T >= 2), the whole layer.
 moe_status forward_piece(const moe_config &c, const moe_weights &w, const uint16_t *x, int T,
                          uint16_t *out, const uint16_t *resid, uint16_t *x_next, void *ws,
-                         cudaStream_t s) {
+                         cudaStream_t s, const moe_weights_q8 *wq = nullptr) {
     const Layout L = layout(c, T);
     int *status = at<int>(ws, L.status);
     float *logits = at<float>(ws, L.logits);
@@ -401,10 +456,11 @@ moe_status forward_piece(const moe_config &c, const moe_weights &w, const uint16
     MOE_CUDA(launch_permute(ids, T, c.n_experts, c.top_k, offsets, perm, inv, tiles, kTileN,
                             at<int32_t>(ws, L.chunks), topw, row_tok, row_w, status, s, merged ? T : 0, sched));
     uint16_t *y = at<uint16_t>(ws, L.y);
-    if (c.shared_inter > 0 && !merged) MOE_TRY(run_shared(c, w, x, T, h_s, acc, status, s));
+    if (c.shared_inter > 0 && !merged) MOE_TRY(run_shared(c, w, x, T, h_s, acc, status, s, wq));
     // y doubles as the expert-sorted copy of x: the gate/up GEMM is done reading it before the
     // down GEMM writes y (same stream)
-    MOE_TRY(run_routed(c, w, x, T, offsets, tiles, row_tok, perm, row_w, y, h, nullptr, y, status, sched, s, merged));
+    MOE_TRY(run_routed(c, w, x, T, offsets, tiles, row_tok, perm, row_w, y, h, nullptr, y, status, sched, s, merged,
+                       wq));
     const size_t P = (size_t)T * c.top_k;
     MOE_CUDA(launch_finalize(y, c.top_k, (c.shared_inter > 0 && !merged) ? acc : nullptr, resid, T, c.hidden, out,
                              x_next, s, merged ? y + P * c.hidden : nullptr));
@@ -641,6 +697,42 @@ moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const moe_bf
     return MOE_OK;
 }
 
+moe_status moe_forward_q8(const moe_config *cfg, const moe_weights_q8 *w, const moe_bf16 *x, int T,
+                          moe_bf16 *out, const moe_bf16 *resid, moe_bf16 *x_next, void *ws, size_t ws_bytes,
+                          void *stream) {
+    NvtxRange nvtx_range("moe_forward_q8");
+    MOE_TRY(check_config(cfg));
+    if (T < 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    MOE_TRY(check_weights_q8(cfg, w));
+    if (!x || !out || !aligned16(x) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+    if ((x_next && !aligned16(x_next)) || (resid && !aligned16(resid))) return MOE_ERR_INVALID_ARG;
+    if (!resid) resid = x;
+    const int Tmax = T < kMaxPiece ? T : kMaxPiece;
+    MOE_TRY(check_ws(cfg, ws, ws_bytes, Tmax));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int H = cfg->hidden;
+    // the bf16 router (the selection stays on bf16 weights)
+    moe_weights wr{};
+    wr.w_router = w->w_router;
+    wr.b_router = w->b_router;
+    static const int kBuckets[4] = {8192, 4096, 2048, 1024};
+    size_t t0 = 0;
+    for (int rem = T; rem > 0;) {
+        int Tp = rem;
+        for (int b = 0; b < 4; ++b)
+            if (rem >= kBuckets[b]) {
+                Tp = kBuckets[b];
+                break;
+            }
+        rem -= Tp;
+        MOE_TRY(forward_piece(*cfg, wr, x + t0 * H, Tp, out + t0 * H, resid + t0 * H,
+                              x_next ? x_next + t0 * H : nullptr, ws, s, w));
+        t0 += Tp;
+    }
+    return MOE_OK;
+}
+
 namespace {
 // The part of a chain launch both weight formats share: shape, token and workspace pointers.
 moe_status chain_common(const moe_config *cfg, int n_layers, const moe_bf16 *x0, const moe_bf16 *resid,
@@ -711,15 +803,7 @@ moe_status moe_decode_chain_q8(const moe_config *cfg, const moe_weights_q8 *laye
     static thread_local ChainParams p;
     MOE_TRY(chain_common(cfg, n_layers, x0, resid, out, x_last, ws, ws_bytes, p));
     const bool shared = cfg->shared_inter > 0;
-    for (int l = 0; l < n_layers; ++l) {
-        const moe_weights_q8 &w = layers[l];
-        if (!w.w_router || !aligned16(w.w_router) || !w.q_gate || !w.q_up || !w.q_down || !w.s_gate ||
-            !w.s_up || !w.s_down || !aligned16(w.q_gate) || !aligned16(w.q_up) || !aligned16(w.q_down))
-            return MOE_ERR_INVALID_ARG;
-        if (shared && (!w.qs_gate || !w.qs_up || !w.qs_down || !w.ss_gate || !w.ss_up || !w.ss_down ||
-                       !aligned16(w.qs_gate) || !aligned16(w.qs_up) || !aligned16(w.qs_down)))
-            return MOE_ERR_INVALID_ARG;
-    }
+    for (int l = 0; l < n_layers; ++l) MOE_TRY(check_weights_q8(cfg, &layers[l]));
     const int H = cfg->hidden;
     const uint32_t sl = (uint32_t)decode_slice(), br = (uint32_t)decode_box_rows();
     for (int l = 0; l < n_layers; ++l) {

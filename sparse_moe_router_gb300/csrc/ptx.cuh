@@ -159,6 +159,12 @@ __device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const void *tma
         : "memory");
 }
 
+// Orders this thread's shared-memory writes through the generic proxy (ordinary stores) before
+// later accesses of the async proxy (tcgen05 operand reads) that a release of it publishes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Fire-and-forget 16-byte vector add into global memory (no value returned, so the issuing
 // thread never waits on it).
 __device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {

@@ -134,3 +134,30 @@ def test_graph_entry_points_validate_on_the_host():
     assert L.moe_graph_launch(None, None) == 1
     assert L.moe_graph_kernel_count(None) == -1
     assert L.moe_graph_destroy(None) == 0
+
+
+def test_forward_q8_validates_on_the_host():
+    """moe_forward_q8 rejects a bad call before any device work: null/incomplete weights, a
+    missing shared expert's codes or scales, misaligned codes, a bad workspace; T == 0 succeeds."""
+    L = abi.load()
+    cfg = _cfg()
+    P = ctypes.c_void_p
+    fake = P(0x10000)
+    full = abi.WeightsQ8(*(0x10000 for _ in range(14)))
+    assert L.moe_forward_q8(ctypes.byref(cfg), None, fake, 4, fake, None, None, fake, 1 << 30, None) == 1
+    assert L.moe_forward_q8(ctypes.byref(cfg), None, None, 0, None, None, None, None, 0, None) == 0
+    assert L.moe_forward_q8(ctypes.byref(cfg), ctypes.byref(full), fake, -2, fake, None, None, fake, 1 << 30, None) == 1
+    for field in ("q_gate", "s_down", "qs_up", "ss_down"):
+        w = abi.WeightsQ8(*(0x10000 for _ in range(14)))
+        setattr(w, field, None)
+        assert L.moe_forward_q8(ctypes.byref(cfg), ctypes.byref(w), fake, 4, fake, None, None, fake, 1 << 30, None) == 1
+    w = abi.WeightsQ8(*(0x10000 for _ in range(14)))
+    w.q_down = 0x10008  # codes must be 16-byte aligned
+    assert L.moe_forward_q8(ctypes.byref(cfg), ctypes.byref(w), fake, 4, fake, None, None, fake, 1 << 30, None) == 1
+    assert L.moe_forward_q8(ctypes.byref(cfg), ctypes.byref(full), fake, 4, fake, None, None, fake, 1000, None) == 2
+    assert L.moe_forward_q8(ctypes.byref(cfg), ctypes.byref(full), fake, 4, fake, None, None, P(0x10010),
+                            1 << 30, None) == 1
+    # no shared expert: its pointers may be NULL
+    cfg0 = _cfg(shared_inter=0)
+    w0 = abi.WeightsQ8(*(0x10000 for _ in range(8)), None, None, None, None, None, None)
+    assert L.moe_forward_q8(ctypes.byref(cfg0), ctypes.byref(w0), fake, 4, fake, None, None, fake, 1000, None) == 2

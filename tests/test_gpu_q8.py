@@ -163,3 +163,52 @@ def test_chain_q8_argument_errors():
     assert call(good) == 0
     torch.cuda.synchronize()
     assert abi.moe_check_status(ws) == 0
+
+
+# ------------------------------------------------------------ prefill with E4M3 weights --
+
+def _forward_q8(shape, layer, x):
+    cfg = cfg_of(shape)
+    T = x.shape[0]
+    ws = abi.alloc_workspace(cfg, min(T, 8192))
+    out, xn = torch.empty_like(x), torch.empty_like(x)
+    abi.moe_forward_q8(cfg, abi.weights_q8(layer), x, T, out, xn, ws)
+    torch.cuda.synchronize()
+    assert abi.moe_check_status(ws) == 0
+    return out, xn
+
+
+@pytest.mark.parametrize("shape,T", [(TINY, 64), (TINY, 1), (TINY, 3), (TINY, 5), (TINY, 300), (TINY, 1025),
+                                     (inputs.Shape(512, 32, 4, 256, 0), 200),
+                                     (inputs.Shape(1024, 64, 8, 384, 256), 70),
+                                     (inputs.Shape(256, 16, 16, 128, 256), 40),
+                                     (inputs.Shape(384, 1, 1, 128, 0), 33)])
+def test_forward_q8_matches_oracle(shape, T):
+    """moe_forward_q8 (the grouped GEMMs widening E4M3 codes to bf16 in shared memory, row scales
+    in the epilogue) against the oracle's quantised layer on the GPU's routing: every row."""
+    layers, x = inputs.make_q8(inputs.custom(shape, T=T, seed=800 + T, router_std=0.02), device="cuda")
+    out, xn = _forward_q8(shape, layers[0], x)
+    compare_out(u16(out), _layer_ref_q8(shape, layers[0], x), what="forward_q8")
+    assert torch.equal(xn, (x.float() + out.float()).to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("T", [8192, 1000])
+def test_forward_q8_layer_shape_sampled(T):
+    """The 2048-wide, 256-expert top-8 layer with E4M3 weights quantised on the device from a bf16
+    layer (moe_quantize_e4m3, pinned bit-exact against the oracle's quantiser above), checked on
+    sampled rows (every piece edge included) against the oracle on the same codes."""
+    shape = DECODE
+    wl = inputs.custom(shape, T=T, seed=820 + T % 7, router_std=1.0 / np.sqrt(shape.hidden))
+    layers_bf, x = inputs.make(wl, device="cuda")
+    layer = abi.quantize_layer(layers_bf[0])
+    del layers_bf
+    torch.cuda.synchronize()
+    out, _ = _forward_q8(shape, layer, x)
+    logits, ids, w = route_gpu(shape, layer, x)
+    ids_o, _ = orc.route_from_logits(logits, shape.top_k)
+    assert np.array_equal(ids, ids_o)
+    rng = np.random.default_rng(T)
+    rows = np.unique(np.concatenate([[0, 1, T - 2, T - 1], rng.choice(T, size=64, replace=False)]))
+    ref = orc.forward_q8(np.ascontiguousarray(u16(x)[rows]), _host_q8(layer), shape.top_k,
+                         np.ascontiguousarray(ids[rows]), np.ascontiguousarray(w[rows]))
+    compare_out(u16(out)[rows], ref, what="forward_q8 layer shape")
