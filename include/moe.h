@@ -304,6 +304,12 @@ uint64_t moe_launch_count(void);
  * graph capture. */
 moe_status moe_timing_enable(int enable);
 moe_status moe_timing_read(const char *name, int *launches, double *total_ms);
+/* 1 when this library was built with MOE_DEBUG: every kernel then checks each index it reads from
+ * device data (permutation rows, caller-given expert offsets, combine rows, GEMM output rows)
+ * before using it, records MOE_ERR_INVALID_ARG in the workspace status word (moe_combine has
+ * none) and skips the access.  0 for the ordinary build, which does not check them. */
+int moe_debug_build(void);
+
 /* Name of kernel class i (0 <= i < moe_timing_classes()), or NULL. */
 const char *moe_timing_name(int i);
 int moe_timing_classes(void);

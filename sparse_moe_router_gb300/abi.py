@@ -26,7 +26,7 @@ EXPORTS = ["moe_status_string", "moe_workspace_size", "moe_route", "moe_route_fr
            "moe_plan_pieces", "moe_launch_count", "moe_timing_enable", "moe_timing_read",
            "moe_timing_name", "moe_timing_classes", "moe_selftest_wait", "moe_decode_chain",
            "moe_decode_chain_q8", "moe_quantize_e4m3", "moe_graph_create", "moe_graph_launch",
-           "moe_graph_kernel_count", "moe_graph_destroy", "moe_forward_q8"]
+           "moe_graph_kernel_count", "moe_graph_destroy", "moe_forward_q8", "moe_debug_build"]
 
 
 class MoeError(RuntimeError):
@@ -98,6 +98,8 @@ def load(path: str = LIB_PATH):
     L.moe_timing_name.argtypes = [_I]
     L.moe_timing_name.restype = ctypes.c_char_p
     L.moe_timing_classes.argtypes = []
+    L.moe_debug_build.argtypes = []
+    L.moe_debug_build.restype = _I
     for fn in ("moe_route", "moe_route_from_logits", "moe_permute", "moe_permute_noalloc", "moe_expert_ffn",
                "moe_combine", "moe_forward", "moe_check_status", "moe_timing_enable",
                "moe_timing_read", "moe_timing_classes", "moe_selftest_wait", "moe_decode_chain",

@@ -16,6 +16,8 @@ ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(HERE, "libmoe.so")
 BUILD = os.path.join(ROOT, "_build")
+# The same sources with MOE_DEBUG: every kernel checks the indices it reads from device data.
+OUT_DEBUG = os.path.join(HERE, "libmoe_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -40,23 +42,28 @@ def _deps():
     return files
 
 
-def up_to_date():
-    if not os.path.exists(OUT):
+def up_to_date(out=OUT):
+    if not os.path.exists(out):
         return False
-    t = os.path.getmtime(OUT)
+    t = os.path.getmtime(out)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build(force=False, verbose=False, extra=()):
-    """Compile the library if needed; returns the path of libmoe.so."""
-    if not force and up_to_date():
-        return OUT
+def build(force=False, verbose=False, extra=(), debug=False):
+    """Compile the library if needed; returns the path of libmoe.so (debug=True: libmoe_debug.so,
+    built with MOE_DEBUG)."""
+    out = OUT_DEBUG if debug else OUT
+    if not force and up_to_date(out):
+        return out
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    bdir = os.path.join(BUILD, "debug") if debug else BUILD
+    os.makedirs(bdir, exist_ok=True)
+    if debug:
+        extra = tuple(extra) + ("-DMOE_DEBUG",)
     objs = []
     cmds = []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(bdir, os.path.basename(src) + ".o")
         objs.append(obj)
         cmds.append([nvcc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj])
 
@@ -70,16 +77,16 @@ def build(force=False, verbose=False, extra=()):
                 sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
             if r.returncode != 0:
                 raise RuntimeError("nvcc failed for " + cmd[-3])
-    tmp = OUT + ".tmp%d" % os.getpid()
+    tmp = out + ".tmp%d" % os.getpid()
     link = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(link, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(" ".join(link) + "\n" + r.stdout + r.stderr)
         raise RuntimeError("link failed")
-    os.replace(tmp, OUT)
-    return OUT
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
-                extra=["-Xptxas", "-v"] if "--ptxas" in sys.argv else ()))
+                extra=["-Xptxas", "-v"] if "--ptxas" in sys.argv else (), debug="--debug" in sys.argv))

@@ -569,10 +569,14 @@ __global__ void __launch_bounds__(Cfg<EPI, Q8>::kThreads, 1)
                     if (p.shared_last && t.g == G - 1) {  // shared expert: in place, weight 1
                         orow = row;
                         w = 1.f;
-                    } else {
+                    } else if (MOE_DEBUG_OK(p.src_rows == 0 || (row >= 0 && row < p.src_rows), p.status)) {
                         orow = p.epi_tok ? __ldg(&p.epi_tok[row]) : row;
                         w = p.epi_w ? __ldg(&p.epi_w[row]) : 1.f;
+                    } else {
+                        orow = -1;
                     }
+                    // -1: the row is not stored
+                    if (orow >= 0 && !MOE_DEBUG_OK(p.out_rows == 0 || orow < p.out_rows, p.status)) orow = -1;
                 }
                 meta_row[buf * BN + j] = orow;
                 meta_w[buf * BN + j] = w;
@@ -628,7 +632,8 @@ __global__ void __launch_bounds__(Cfg<EPI, Q8>::kThreads, 1)
                     ptx::named_bar(2 + sub, 128);
                     const int q = frow;
                     const int jj = q >> 3, fg = (q & 7) * 8;
-                    if (j0 + jj < t.nvalid) {
+                    if (j0 + jj < t.nvalid &&
+                        MOE_DEBUG_OK(p.out_rows == 0 || t.row0 + j0 + jj < p.out_rows, p.status)) {
                         const float4 g0 = *reinterpret_cast<const float4 *>(&stg[jj * kStgStride + fg]);
                         const float4 g1 = *reinterpret_cast<const float4 *>(&stg[jj * kStgStride + fg + 4]);
                         const float4 u0 = *reinterpret_cast<const float4 *>(&stg[jj * kStgStride + 64 + fg]);
@@ -649,7 +654,8 @@ __global__ void __launch_bounds__(Cfg<EPI, Q8>::kThreads, 1)
                     if (f < p.F) {
 #pragma unroll
                         for (int jj = 0; jj < 16; ++jj)
-                            if (j0 + jj < t.nvalid)
+                            if (j0 + jj < t.nvalid &&
+                                MOE_DEBUG_OK(p.out_rows == 0 || t.row0 + j0 + jj < p.out_rows, p.status))
                                 o[(size_t)(t.row0 + j0 + jj) * p.ld + f] = sc * __uint_as_float(r[jj]) + bias_f;
                     }
                 } else {
@@ -683,10 +689,11 @@ __global__ void __launch_bounds__(Cfg<EPI, Q8>::kThreads, 1)
                     const uint4 e1 = make_uint4(__byte_perm(a.x, a.y, 0x7632), __byte_perm(a.z, a.w, 0x7632),
                                                 __byte_perm(c.x, c.y, 0x7632), __byte_perm(c.z, c.w, 0x7632));
                     const size_t col = (size_t)ftile * BM + quarter * 32 + seg * 8;
-                    if (j0 + 2 * m < t.nvalid)
-                        *reinterpret_cast<uint4 *>(&o[(size_t)meta_row[mb + 2 * m] * p.ld + col]) = e0;
-                    if (j0 + 2 * m + 1 < t.nvalid)
-                        *reinterpret_cast<uint4 *>(&o[(size_t)meta_row[mb + 2 * m + 1] * p.ld + col]) = e1;
+                    const int or0 = meta_row[mb + 2 * m], or1 = meta_row[mb + 2 * m + 1];
+                    if (j0 + 2 * m < t.nvalid && or0 >= 0)
+                        *reinterpret_cast<uint4 *>(&o[(size_t)or0 * p.ld + col]) = e0;
+                    if (j0 + 2 * m + 1 < t.nvalid && or1 >= 0)
+                        *reinterpret_cast<uint4 *>(&o[(size_t)or1 * p.ld + col]) = e1;
                     __syncwarp();
                 }
             }

@@ -77,6 +77,20 @@ bool encode_token_maps(TokenMaps *tm, const void *base, uint64_t rows, uint64_t 
 enum GemmEpi { EPI_F32 = 0, EPI_SWIGLU = 1, EPI_COMBINE = 2 };
 
 #ifdef __CUDACC__
+// MOE_DEBUG builds check every index a kernel reads from device data (permutation rows,
+// caller-given offsets, combine rows, GEMM output rows) before using it: an index outside its
+// buffer records MOE_ERR_INVALID_ARG in the status word (when the kernel has one) and the access
+// is skipped.  Ordinary builds compile the checks away.
+#ifdef MOE_DEBUG
+__device__ __forceinline__ bool moe_debug_ok(bool ok, int *status) {
+    if (!ok && status) atomicCAS(status, 0, (int)MOE_ERR_INVALID_ARG);
+    return ok;
+}
+#define MOE_DEBUG_OK(cond, status) moe_debug_ok((cond), (status))
+#else
+#define MOE_DEBUG_OK(cond, status) true
+#endif
+
 // Order-preserving map of fp32 onto uint32 (-0 folded onto +0, so equal values get equal keys)
 // and its inverse: top-k rounds compare logits with one integer warp reduction.
 __device__ __forceinline__ uint32_t order_key(float x) {
@@ -131,6 +145,8 @@ struct GemmArgs {
     // ws_scale0 / ws_scale1 [f]
     bool q8;
     const float *w_scale0, *w_scale1, *ws_scale0, *ws_scale1;
+    // MOE_DEBUG: rows of `out` and of the group row space (epi_tok / epi_w), 0 = unknown
+    int out_rows, src_rows;
 };
 
 // Launch the persistent grouped GEMM.  tm_a0 (and tm_a1 for EPI_SWIGLU: the up projection)
@@ -166,7 +182,7 @@ cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int32_t *off
 // zeroed tile counters, as launch_permute).
 cudaError_t launch_tile_prefix(const int32_t *offsets, int E, int32_t *tile_prefix, int tile_n,
                                const int32_t *perm, int P, int k, int32_t *row_tok,
-                               cudaStream_t s, int *sched = nullptr);
+                               cudaStream_t s, int *sched = nullptr, int *status = nullptr);
 // out[t] = bf16( sum_j y[t*k + j] + acc[t] ) with y bf16 [T*k, H] (the weighted expert rows in
 // pair order) and acc fp32 [T, H] (the shared expert, or NULL); when x_next != NULL also
 // x_next = bf16(resid + out).  The sum runs in fp32, slots in order, then the shared term.
@@ -183,6 +199,8 @@ cudaError_t launch_finalize(const uint16_t *y, int k, const float *acc, const ui
 cudaError_t launch_combine(const float *y_rows, const int32_t *inv, const float *topk_w,
                            const float *shared_y, int T, int H, int k, uint16_t *out,
                            cudaStream_t s);
+// true when the library was compiled with MOE_DEBUG (device index checks)
+bool debug_build();
 cudaError_t launch_zero(float *p, size_t n, cudaStream_t s);
 
 // ---- decode (T = 1) ------------------------------------------------------------------

@@ -387,6 +387,7 @@ moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t 
     a.F = c.inter;
     a.out = h;
     a.ld = c.inter;
+    a.out_rows = (int)rows;
     a.status = status;
     a.shared_last = with_shared;
     a.shared_b_own = with_shared;
@@ -417,6 +418,8 @@ moe_status run_routed(const moe_config &c, const moe_weights &w, const uint16_t 
         d.w_scale0 = wq->s_down;
         d.ws_scale0 = wq->ss_down;
     }
+    d.src_rows = (int)rows;
+    d.out_rows = (int)rows;  // y_rows [P, H] or the weighted rows [P + T, H]
     if (y_rows) {
         if (with_shared) return MOE_ERR_INVALID_ARG;
         d.out = y_rows;
@@ -574,7 +577,7 @@ moe_status moe_expert_ffn(const moe_config *cfg, const moe_weights *w, const moe
     int32_t *row_tok = at<int32_t>(ws, L.row_tok);
     int *sched = at<int>(ws, L.sched);
     MOE_CUDA(launch_tile_prefix(expert_offsets, cfg->n_experts, tiles, kTileN, perm, T * cfg->top_k,
-                                cfg->top_k, row_tok, s, sched));
+                                cfg->top_k, row_tok, s, sched, status));
     MOE_TRY(run_routed(*cfg, *w, x, T, expert_offsets, tiles, row_tok, perm, nullptr, at<uint16_t>(ws, L.y), h_rows,
                        y_rows, nullptr, status, sched, s));
     if (shared_y && cfg->shared_inter > 0)
@@ -977,5 +980,7 @@ moe_status moe_timing_read(const char *name, int *launches, double *total_ms) {
 const char *moe_timing_name(int i) { return kernel_class_name(i); }
 
 int moe_timing_classes(void) { return KC_COUNT; }
+
+int moe_debug_build(void) { return debug_build() ? 1 : 0; }
 
 }  // extern "C"

@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kPermThreads) perm_scatter_kernel(const int32_
                                                                      int32_t *__restrict__ inv,
                                                                      const float *__restrict__ topk_w,
                                                                      int32_t *__restrict__ row_tok,
-                                                                     float *__restrict__ row_w) {
+                                                                     float *__restrict__ row_w, int *status) {
     extern __shared__ int wh[];  // [kPermWarps][E]
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     for (int i = tid; i < kPermWarps * E; i += kPermThreads) wh[i] = 0;
@@ -277,6 +277,7 @@ __global__ void __launch_bounds__(kPermThreads) perm_scatter_kernel(const int32_
         if (e >= 0 && (grp & lt_mask) == 0) my[e] += __popc(grp);
         __syncwarp();
         if (p < P) {
+            if (row >= 0 && !MOE_DEBUG_OK(row < P, status)) row = -1;  // a corrupt count table
             inv[p] = row;
             if (row >= 0) {
                 perm[row] = p;
@@ -291,12 +292,17 @@ __global__ void __launch_bounds__(kPermThreads) perm_scatter_kernel(const int32_
 __global__ void __launch_bounds__(kPermThreads, 1)
     tile_prefix_kernel(const int32_t *__restrict__ offsets, int E, int32_t *__restrict__ tile_prefix,
                        int tile_n, const int32_t *__restrict__ perm, int P, int k,
-                       int32_t *__restrict__ row_tok, int *__restrict__ sched) {
+                       int32_t *__restrict__ row_tok, int *__restrict__ sched, int *status) {
     __shared__ int sh_warp[32];
     const int tid = threadIdx.x;
     if (sched && tid < kSchedCounters) sched[tid] = 0;
-    for (int r = tid; r < P; r += kPermThreads) row_tok[r] = perm[r] / k;
-    const int cnt = tid < E ? offsets[tid + 1] - offsets[tid] : 0;
+    for (int r = tid; r < P; r += kPermThreads) {
+        const int pr = perm[r];
+        row_tok[r] = MOE_DEBUG_OK(pr >= 0 && pr < P, status) ? pr / k : -1;  // -1: a zero row
+    }
+    int cnt = tid < E ? offsets[tid + 1] - offsets[tid] : 0;
+    // the caller's offsets: non-decreasing, from 0 to at most P (else no rows for this expert)
+    if (tid < E && !MOE_DEBUG_OK(cnt >= 0 && offsets[tid] >= 0 && offsets[tid + 1] <= P, status)) cnt = 0;
     const int tiles = tid < E ? token_tile_count(cnt) : 0;
     int total = 0;
     const int toff = block_excl_scan(tiles, sh_warp, &total);
@@ -374,7 +380,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int j = 0; j < k; ++j) {
             const int row = __ldg(&inv[(size_t)t * k + j]);
-            if (row < 0) continue;
+            if (row < 0 || !MOE_DEBUG_OK(row < T * k, nullptr)) continue;
             const float wj = __ldg(&topk_w[(size_t)t * k + j]);
             const float4 y = __ldg(reinterpret_cast<const float4 *>(y_rows + (size_t)row * H) + c);
             acc.x += wj * y.x;
@@ -464,15 +470,16 @@ cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int32_t *off
     }
     LaunchScope scope(KC_PERMUTE, s);
     perm_scatter_kernel<<<n_chunks, kPermThreads, kPermWarps * E * sizeof(int), s>>>(
-        ids, P, E, k, chunk_tab, perm, inv, topk_w, row_tok, row_w);
+        ids, P, E, k, chunk_tab, perm, inv, topk_w, row_tok, row_w, status);
     return cudaGetLastError();
 }
 
 cudaError_t launch_tile_prefix(const int32_t *offsets, int E, int32_t *tile_prefix, int tile_n,
                                const int32_t *perm, int P, int k, int32_t *row_tok,
-                               cudaStream_t s, int *sched) {
+                               cudaStream_t s, int *sched, int *status) {
     LaunchScope scope(KC_TILE_PREFIX, s);
-    tile_prefix_kernel<<<1, kPermThreads, 0, s>>>(offsets, E, tile_prefix, tile_n, perm, P, k, row_tok, sched);
+    tile_prefix_kernel<<<1, kPermThreads, 0, s>>>(offsets, E, tile_prefix, tile_n, perm, P, k, row_tok, sched,
+                                                  status);
     return cudaGetLastError();
 }
 
@@ -529,6 +536,14 @@ cudaError_t launch_combine(const float *y_rows, const int32_t *inv, const float 
     LaunchScope scope(KC_COMBINE, s);
     combine_kernel<<<grid_for(n, 256), 256, 0, s>>>(y_rows, inv, topk_w, shared_y, T, H, k, out);
     return cudaGetLastError();
+}
+
+bool debug_build() {
+#ifdef MOE_DEBUG
+    return true;
+#else
+    return false;
+#endif
 }
 
 cudaError_t launch_zero(float *p, size_t n, cudaStream_t s) {
