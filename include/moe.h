@@ -151,7 +151,7 @@ moe_status moe_permute(const moe_config *cfg, const int32_t *topk_ids, int T,
  * they route tokens (a serving process that reserves all device memory at start-up, host
  * code with no allocator at hand).  The pages have no counterpart: this is a convenience of
  * this library.  Same outputs as moe_permute (bit-identical), but the per-chunk count table
- * lives in a fixed array inside the library (128 KiB on every device that loads it, kept
+ * lives in a fixed array inside the library (160 KiB on every device that loads it, kept
  * until the process exits), so the call allocates nothing and takes no workspace.
  * Limits: T*k <= 65536 pairs, E <= 1024, k <= 32; larger problems return
  * MOE_ERR_UNSUPPORTED_SHAPE (use moe_permute).  Ids outside [0,E) get inv = -1 and are not

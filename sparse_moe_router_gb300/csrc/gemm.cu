@@ -214,6 +214,9 @@ __global__ void __launch_bounds__(Cfg<EPI, Q8>::kThreads, 1)
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
+    // the next kernels' count table, zeroed by every CTA (also those with no tile) before its work
+    if (p.zero_ptr)
+        for (int i = (int)blockIdx.x * kThreads + tid; i < p.zero_n; i += (int)gridDim.x * kThreads) p.zero_ptr[i] = 0;
     const int cap = p.tile_cap > 0 ? p.tile_cap : BN;  // token tile cap
     // CTA pair: rank 0 issues the pair's MMAs (M = 256: its 128 weight rows, then the peer's);
     // each CTA holds half of the tile's token rows and its own rows of the accumulator

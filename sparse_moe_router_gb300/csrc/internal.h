@@ -147,6 +147,9 @@ struct GemmArgs {
     const float *w_scale0, *w_scale1, *ws_scale0, *ws_scale1;
     // MOE_DEBUG: rows of `out` and of the group row space (epi_tok / epi_w), 0 = unknown
     int out_rows, src_rows;
+    // ints to zero before the GEMM's own work (the next kernels' count table), or NULL
+    int32_t *zero_ptr;
+    int zero_n;
 };
 
 // Launch the persistent grouped GEMM.  tm_a0 (and tm_a1 for EPI_SWIGLU: the up projection)
@@ -161,14 +164,32 @@ cudaError_t launch_gemm(GemmEpi epi, const GemmArgs &a, const CUtensorMap &tm_a0
 
 cudaError_t launch_topk(const float *logits, int T, int E, int k, int32_t *ids, float *w,
                         cudaStream_t s);
+// The same selection, and each chunk's expert counts added into chunk_tab (which must hold
+// zeros: permute_scratch_ints(T, E, k) of them), for launch_scan_scatter.
+cudaError_t launch_topk_hist(const float *logits, int T, int E, int k, int32_t *ids, float *w,
+                             int32_t *chunk_tab, cudaStream_t s);
+// The permutation from the counts launch_topk_hist left in chunk_tab, in one launch: every block
+// derives its chunk's first row per expert from the whole table (the offsets and the token-tile
+// prefix are written by block 0), then scatters its chunk as launch_permute does.  The table is
+// read only.
+cudaError_t launch_scan_scatter(const int32_t *ids, int T, int E, int k, int32_t *offsets, int32_t *perm,
+                                int32_t *inv, int32_t *tile_prefix, const int32_t *chunk_tab,
+                                const float *topk_w, int32_t *row_tok, float *row_w, int *status,
+                                cudaStream_t s, int extra_rows, int *sched);
 // chunk_tab: device scratch of permute_scratch_ints(T, E, k) ints.  When row_tok / row_w are
 // not NULL the scatter also writes, per row of the sorted order, the token (pair / k) and the
 // routing weight topk_w[pair] (what the expert GEMMs read per row).  extra_rows > 0 appends one
 // more group of that many rows after the experts (offsets[E+1], tile_prefix[E+1]): the shared
 // expert's rows when it runs inside the routed GEMMs.
-// Pairs per block of the permutation kernels: the chunk table holds one row of E counts per
-// chunk of this many consecutive pairs.
+// The permutation works on chunks of whole tokens: chunk c holds tokens [c*CT, (c+1)*CT) and so
+// pairs [c*CT*k, (c+1)*CT*k), with CT = perm_chunk_tokens(k) a multiple of 8 (the top-k kernel's
+// 8-token blocks each fall in one chunk) and CT*k <= kPermChunk pairs (one block of the scatter).
+// The chunk table holds one row of E counts per chunk.
 constexpr int kPermChunk = 2048;
+__host__ __device__ __forceinline__ int perm_chunk_tokens(int k) {
+    const int ct = (kPermChunk / k) & ~7;
+    return ct < 8 ? 8 : ct;
+}
 // Tile counters of the grouped GEMMs that follow a permutation (gate/up, down): `sched` (or
 // NULL) receives kSchedCounters zeros from the permutation's scan kernel.
 constexpr int kSchedCounters = 2;

@@ -253,8 +253,11 @@ moe_status cuda_status(cudaError_t e) {
 #define MOE_ROUTER_TILE_N 128
 #endif
 constexpr int kRouterTileN = MOE_ROUTER_TILE_N;
+// zero_ptr (or NULL): zero_n ints the GEMM's CTAs clear before their work (the count table the
+// top-k kernel that follows adds into).
 moe_status run_router_gemm(const moe_config &c, const moe_weights &w, const uint16_t *x, int T,
-                           float *logits, int *status, cudaStream_t s) {
+                           float *logits, int *status, cudaStream_t s, int32_t *zero_ptr = nullptr,
+                           int zero_n = 0) {
     CUtensorMap tm;
     TokenMaps tb;
     if (!encode_tmap_2d_bf16(&tm, w.w_router, (uint64_t)c.n_experts, (uint64_t)c.hidden, kTileM, 64) ||
@@ -271,6 +274,8 @@ moe_status run_router_gemm(const moe_config &c, const moe_weights &w, const uint
     a.ld = c.n_experts;
     a.bias = w.b_router;
     a.status = status;
+    a.zero_ptr = zero_ptr;
+    a.zero_n = zero_n;
     MOE_CUDA(launch_gemm(EPI_F32, a, tm, tm, tb, tm, tm, KC_ROUTER_GEMM, s));
     return MOE_OK;
 }
@@ -449,15 +454,19 @@ moe_status forward_piece(const moe_config &c, const moe_weights &w, const uint16
     uint16_t *h = at<uint16_t>(ws, L.h);
     uint16_t *h_s = at<uint16_t>(ws, L.h_s);
     float *acc = at<float>(ws, L.acc);
-    MOE_TRY(run_router_gemm(c, w, x, T, logits, status, s));
-    MOE_CUDA(launch_topk(logits, T, c.n_experts, c.top_k, ids, topw, s));
+    // routing in three launches: the router GEMM (which also zeroes the chunk count table), the
+    // top-k (which adds each chunk's expert counts into it), and the permutation's scan + scatter
+    int32_t *chunks = at<int32_t>(ws, L.chunks);
+    MOE_TRY(run_router_gemm(c, w, x, T, logits, status, s, chunks,
+                            (int)permute_scratch_ints(T, c.n_experts, c.top_k)));
+    MOE_CUDA(launch_topk_hist(logits, T, c.n_experts, c.top_k, ids, topw, chunks, s));
     int32_t *row_tok = at<int32_t>(ws, L.row_tok);
     float *row_w = at<float>(ws, L.row_w);
     // a shared expert as wide as the routed ones runs inside the routed GEMMs, as group E
     const bool merged = c.shared_inter > 0 && c.shared_inter == c.inter;
     int *sched = at<int>(ws, L.sched);
-    MOE_CUDA(launch_permute(ids, T, c.n_experts, c.top_k, offsets, perm, inv, tiles, kTileN,
-                            at<int32_t>(ws, L.chunks), topw, row_tok, row_w, status, s, merged ? T : 0, sched));
+    MOE_CUDA(launch_scan_scatter(ids, T, c.n_experts, c.top_k, offsets, perm, inv, tiles, chunks, topw, row_tok,
+                                 row_w, status, s, merged ? T : 0, sched));
     uint16_t *y = at<uint16_t>(ws, L.y);
     if (c.shared_inter > 0 && !merged) MOE_TRY(run_shared(c, w, x, T, h_s, acc, status, s, wq));
     // y doubles as the expert-sorted copy of x: the gate/up GEMM is done reading it before the

@@ -20,10 +20,12 @@
 namespace moe {
 namespace {
 
-// Largest problem the fixed table serves: T*k <= 65536 pairs and E <= 1024 experts.
+// Largest problem the fixed table serves: T*k <= 65536 pairs and E <= 1024 experts.  The
+// permutation cuts the pairs into chunks of whole tokens (at most kPermChunk pairs each, 8-token
+// granularity), which for T*k <= 65536 and any k <= 32 makes at most 36 chunks.
 constexpr int kNoAllocMaxPairs = 65536;
 constexpr int kNoAllocMaxExperts = 1024;
-constexpr int kNoAllocChunks = (kNoAllocMaxPairs + kPermChunk - 1) / kPermChunk;
+constexpr int kNoAllocChunks = 40;
 constexpr size_t kNoAllocTableInts = (size_t)kNoAllocChunks * kNoAllocMaxExperts;
 
 // The chunk count table: every entry a call reads is first written by that same call, so

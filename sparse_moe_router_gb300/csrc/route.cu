@@ -43,14 +43,10 @@ __device__ __forceinline__ void sort_desc(float (&v)[N], int (&e)[N]) {
     }
 }
 
-template <int PER_LANE>
-__global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ logits, int T, int E,
-                                                   int k, int32_t *__restrict__ ids,
-                                                   float *__restrict__ w) {
-    const int warp = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
-    const int lane = threadIdx.x & 31;
-    if (warp >= T) return;
-    const float *l = logits + (size_t)warp * E;
+// One token's selection (the warp's): sort, k rounds, the renormalised weights.
+template <int PER_LANE, bool HIST>
+__device__ __forceinline__ void topk_one(const float *__restrict__ l, int E, int k, int32_t *__restrict__ ids_t,
+                                         float *__restrict__ w_t, int lane, int *s_hist) {
     float v[PER_LANE];
     int e[PER_LANE];
 #pragma unroll
@@ -90,15 +86,44 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ log
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
     if (lane < k) {
-        ids[(size_t)warp * k + lane] = my_id;
-        w[(size_t)warp * k + lane] = ej / s;
+        ids_t[lane] = my_id;
+        w_t[lane] = ej / s;
+        if (HIST && my_id >= 0 && my_id < E) atomicAdd(&s_hist[my_id], 1);
     }
 }
 
+// HIST: the block's 8 tokens' expert counts are also added into row (8 * block) / CT of chunk_tab
+// (a table of zeros before the launch), the chunk counts the permutation starts from.
+template <int PER_LANE, bool HIST>
+__global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ logits, int T, int E,
+                                                   int k, int32_t *__restrict__ ids,
+                                                   float *__restrict__ w, int32_t *__restrict__ chunk_tab,
+                                                   int CT) {
+    extern __shared__ int s_hist[];  // HIST: [E]
+    const int warp = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (HIST) {
+        for (int i = threadIdx.x; i < E; i += blockDim.x) s_hist[i] = 0;
+        __syncthreads();
+    }
+    if (warp < T) topk_one<PER_LANE, HIST>(logits + (size_t)warp * E, E, k, ids + (size_t)warp * k,
+                                           w + (size_t)warp * k, lane, s_hist);
+    if (HIST) {
+        __syncthreads();
+        const int chunk = (int)(blockIdx.x * (blockDim.x >> 5)) / CT;
+        for (int i = threadIdx.x; i < E; i += blockDim.x) {
+            const int c = s_hist[i];
+            if (c) atomicAdd(&chunk_tab[(size_t)chunk * E + i], c);
+        }
+    }
+}
+
+
 // --------------------------------------------------------------------- permute --
-// Stable counting sort of the P = T*k pairs by expert in three launches, with no block ever
-// waiting on another:
-//   1. perm_hist:    block c counts the experts of its chunk of kChunk consecutive pairs;
+// Stable counting sort of the P = T*k pairs by expert, with no block ever waiting on another.
+// Chunk c is the pairs of tokens [c*CT, (c+1)*CT) (CT = perm_chunk_tokens(k), CP = CT*k pairs).
+// In three launches (moe_permute):
+//   1. perm_hist:    block c counts the experts of its chunk;
 //   2. perm_scan:    one block: per expert (a group of adjacent lanes, each summing a range
 //                    of chunks), the exclusive prefix over chunks, then the exclusive prefix
 //                    over experts (the offsets) and the token-tile prefix;
@@ -107,11 +132,14 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ log
 //                    chunk, per-warp counts give each warp its first row per expert, and a
 //                    pair's rank among equal ids earlier in its 32-pair batch (match_any)
 //                    finishes its row.
+// Inside a layer (moe_forward) the counts come from the top-k kernel itself (its 8-token blocks
+// add them into a table the router GEMM zeroed), and one launch, perm_scan_scatter, does the
+// rest: each block derives its own chunk's first rows from the whole table (a few KB) instead
+// of waiting for a separate scan.
 // Pairs of one expert therefore keep increasing pair order: the result is bit-exact.
 constexpr int kPermThreads = 1024;
 constexpr int kPermWarps = kPermThreads / 32;
-constexpr int kChunk = kPermChunk;           // pairs per block (64 per warp)
-static_assert(kChunk == 64 * kPermWarps, "the scatter gives each warp two 32-pair batches");
+static_assert(kPermChunk == 64 * kPermWarps, "the scatter gives each warp two 32-pair batches");
 
 __device__ __forceinline__ int block_excl_scan(int v, int *sh_warp, int *total) {
     // exclusive scan of one value per thread across the 1024-thread block
@@ -142,14 +170,14 @@ __device__ __forceinline__ int block_excl_scan(int v, int *sh_warp, int *total) 
 }
 
 __global__ void __launch_bounds__(kPermThreads) perm_hist_kernel(const int32_t *__restrict__ ids, int P,
-                                                                  int E, int32_t *__restrict__ chunk_tab,
+                                                                  int E, int CP, int32_t *__restrict__ chunk_tab,
                                                                   int *status) {
     extern __shared__ int cnt[];  // [E]
     const int tid = threadIdx.x;
     for (int i = tid; i < E; i += kPermThreads) cnt[i] = 0;
     __syncthreads();
-    const int beg = blockIdx.x * kChunk;
-    for (int p = beg + tid; p < min(P, beg + kChunk); p += kPermThreads) {
+    const int beg = blockIdx.x * CP;
+    for (int p = beg + tid; p < min(P, beg + CP); p += kPermThreads) {
         const int e = __ldg(&ids[p]);
         if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
         else if (status) atomicCAS(status, 0, (int)MOE_ERR_INVALID_ARG);
@@ -227,23 +255,24 @@ __global__ void __launch_bounds__(kPermThreads, 1)
     }
 }
 
-__global__ void __launch_bounds__(kPermThreads) perm_scatter_kernel(const int32_t *__restrict__ ids, int P,
-                                                                     int E, int k, const int32_t *__restrict__ chunk_tab,
-                                                                     int32_t *__restrict__ perm,
-                                                                     int32_t *__restrict__ inv,
-                                                                     const float *__restrict__ topk_w,
-                                                                     int32_t *__restrict__ row_tok,
-                                                                     float *__restrict__ row_w, int *status) {
-    extern __shared__ int wh[];  // [kPermWarps][E]
+// Block-wide scatter of chunk c's pairs [beg, end): base_e[e] is the first row of the chunk's
+// pairs of expert e; wh is shared memory for kPermWarps * E ints.  Warp w owns pairs
+// beg + [64w, 64w + 64); per-warp counts give each warp its first row per expert, and a pair's
+// rank among equal ids earlier in its 32-pair batch (match_any) finishes its row.
+__device__ __forceinline__ void scatter_chunk(const int32_t *__restrict__ ids, int P, int E, int k, int beg,
+                                              int end, const int32_t *base_e, int *wh,
+                                              int32_t *__restrict__ perm, int32_t *__restrict__ inv,
+                                              const float *__restrict__ topk_w, int32_t *__restrict__ row_tok,
+                                              float *__restrict__ row_w, int *status) {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     for (int i = tid; i < kPermWarps * E; i += kPermThreads) wh[i] = 0;
-    const int base = blockIdx.x * kChunk + wid * (kChunk / kPermWarps);
+    const int base = beg + wid * (kPermChunk / kPermWarps);
     const uint32_t lt_mask = (1u << lane) - 1u;
     int e2[2];
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
         const int p = base + 32 * b + lane;
-        int e = p < P ? __ldg(&ids[p]) : -1;
+        int e = p < end ? __ldg(&ids[p]) : -1;
         if (e >= E) e = -1;
         e2[b] = e;
     }
@@ -258,7 +287,7 @@ __global__ void __launch_bounds__(kPermThreads) perm_scatter_kernel(const int32_
     __syncthreads();
     // per expert: first row of each warp's pairs = chunk's first row + earlier warps' counts
     for (int e = tid; e < E; e += kPermThreads) {
-        int run = chunk_tab[(size_t)blockIdx.x * E + e];
+        int run = base_e[e];
         for (int w2 = 0; w2 < kPermWarps; ++w2) {
             const int c = wh[w2 * E + e];
             wh[w2 * E + e] = run;
@@ -276,7 +305,7 @@ __global__ void __launch_bounds__(kPermThreads) perm_scatter_kernel(const int32_
         __syncwarp();
         if (e >= 0 && (grp & lt_mask) == 0) my[e] += __popc(grp);
         __syncwarp();
-        if (p < P) {
+        if (p < end) {
             if (row >= 0 && !MOE_DEBUG_OK(row < P, status)) row = -1;  // a corrupt count table
             inv[p] = row;
             if (row >= 0) {
@@ -286,6 +315,85 @@ __global__ void __launch_bounds__(kPermThreads) perm_scatter_kernel(const int32_
             }
         }
     }
+}
+
+__global__ void __launch_bounds__(kPermThreads) perm_scatter_kernel(const int32_t *__restrict__ ids, int P,
+                                                                     int E, int k, int CP,
+                                                                     const int32_t *__restrict__ chunk_tab,
+                                                                     int32_t *__restrict__ perm,
+                                                                     int32_t *__restrict__ inv,
+                                                                     const float *__restrict__ topk_w,
+                                                                     int32_t *__restrict__ row_tok,
+                                                                     float *__restrict__ row_w, int *status) {
+    extern __shared__ int wh[];  // [kPermWarps][E]
+    const int beg = blockIdx.x * CP;
+    scatter_chunk(ids, P, E, k, beg, min(P, beg + CP), chunk_tab + (size_t)blockIdx.x * E, wh, perm, inv, topk_w,
+                  row_tok, row_w, status);
+}
+
+// The scan and the scatter in one launch, from the chunk table of counts (read only).  Block c:
+// per expert e (a group of tpe adjacent lanes, each summing a range of chunks) the total and the
+// count in chunks before c; the exclusive prefix over experts of the totals (the offsets); then
+// the first row of chunk c for e is offset_e + the count before c, and the chunk is scattered.
+// Block 0 also writes the offsets, the token-tile prefix (with one more group of extra_rows
+// after the experts, when asked) and zeroes the grouped GEMMs' tile counters.
+__global__ void __launch_bounds__(kPermThreads, 1)
+    perm_scan_scatter_kernel(const int32_t *__restrict__ chunk_tab, int n_chunks, const int32_t *__restrict__ ids,
+                             int P, int E, int k, int CP, int32_t *__restrict__ offsets,
+                             int32_t *__restrict__ tile_prefix, int extra_rows, int *__restrict__ sched,
+                             int32_t *__restrict__ perm, int32_t *__restrict__ inv,
+                             const float *__restrict__ topk_w, int32_t *__restrict__ row_tok,
+                             float *__restrict__ row_w, int *status) {
+    extern __shared__ int sm[];  // wh [kPermWarps][E], then the chunk's first rows [E]
+    int *wh = sm, *sbase = sm + kPermWarps * E;
+    __shared__ int sh_warp[32];
+    const int tid = threadIdx.x, c = (int)blockIdx.x;
+    if (c == 0 && sched && tid < kSchedCounters) sched[tid] = 0;
+    int tpe = 1;
+    while (tpe < 32 && E * tpe * 2 <= kPermThreads) tpe *= 2;
+    const int e = tid / tpe, sub = tid % tpe;
+    const bool live = e < E;
+    const int cpt = (n_chunks + tpe - 1) / tpe;
+    const int c0 = sub * cpt, c1 = min(n_chunks, c0 + cpt);
+    int part = 0, before = 0;
+    if (live)
+        for (int cc = c0; cc < c1; cc += 8) {
+            int h[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) h[u] = (cc + u < c1) ? chunk_tab[(size_t)(cc + u) * E + e] : 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                part += h[u];
+                if (cc + u < c) before += h[u];
+            }
+        }
+    for (int d = 1; d < tpe; d <<= 1) {
+        part += __shfl_xor_sync(0xffffffffu, part, d, tpe);
+        before += __shfl_xor_sync(0xffffffffu, before, d, tpe);
+    }
+    int total = 0;
+    const int off_first = block_excl_scan((live && sub == 0) ? part : 0, sh_warp, &total);
+    if (live && sub == 0) sbase[e] = off_first + before;
+    if (c == 0) {
+        const int tiles = (live && sub == 0) ? token_tile_count(part) : 0;
+        int total_tiles = 0;
+        const int toff = block_excl_scan(tiles, sh_warp, &total_tiles);
+        if (live && sub == 0) {
+            offsets[e] = off_first;
+            if (tile_prefix) tile_prefix[e] = toff;
+        }
+        if (tid == 0) {
+            offsets[E] = total;
+            if (tile_prefix) tile_prefix[E] = total_tiles;
+            if (extra_rows > 0) {
+                offsets[E + 1] = total + extra_rows;
+                if (tile_prefix) tile_prefix[E + 1] = total_tiles + token_tile_count(extra_rows);
+            }
+        }
+    }
+    __syncthreads();
+    const int beg = c * CP;
+    scatter_chunk(ids, P, E, k, beg, min(P, beg + CP), sbase, wh, perm, inv, topk_w, row_tok, row_w, status);
 }
 
 // Token-tile prefix from given offsets (for the unfused expert entry point).
@@ -417,24 +525,59 @@ int grid_for(size_t work, int per_block) {
 
 }  // namespace
 
-cudaError_t launch_topk(const float *logits, int T, int E, int k, int32_t *ids, float *w,
+namespace {
+template <bool HIST>
+cudaError_t topk_launch(const float *logits, int T, int E, int k, int32_t *ids, float *w, int32_t *chunk_tab,
                         cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
-    const int blocks = (T + 7) / 8;  // 8 warps per block
+    const int blocks = (T + 7) / 8;  // 8 warps (tokens) per block
+    const size_t smem = HIST ? (size_t)E * sizeof(int) : 0;
+    const int ct = perm_chunk_tokens(k);
     LaunchScope scope(KC_TOPK, s);
     const int per = (E + 31) / 32;
-    if (per <= 1) topk_kernel<1><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
-    else if (per <= 2) topk_kernel<2><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
-    else if (per <= 4) topk_kernel<4><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
-    else if (per <= 8) topk_kernel<8><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
-    else if (per <= 16) topk_kernel<16><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
-    else topk_kernel<32><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
+    if (per <= 1) topk_kernel<1, HIST><<<blocks, 256, smem, s>>>(logits, T, E, k, ids, w, chunk_tab, ct);
+    else if (per <= 2) topk_kernel<2, HIST><<<blocks, 256, smem, s>>>(logits, T, E, k, ids, w, chunk_tab, ct);
+    else if (per <= 4) topk_kernel<4, HIST><<<blocks, 256, smem, s>>>(logits, T, E, k, ids, w, chunk_tab, ct);
+    else if (per <= 8) topk_kernel<8, HIST><<<blocks, 256, smem, s>>>(logits, T, E, k, ids, w, chunk_tab, ct);
+    else if (per <= 16) topk_kernel<16, HIST><<<blocks, 256, smem, s>>>(logits, T, E, k, ids, w, chunk_tab, ct);
+    else topk_kernel<32, HIST><<<blocks, 256, smem, s>>>(logits, T, E, k, ids, w, chunk_tab, ct);
     return cudaGetLastError();
 }
 
+// the permutation kernels' shared-memory opt-in, once per device (under a lock: two host threads'
+// first calls would otherwise race on the flag)
+cudaError_t perm_attrs() {
+    static bool attr_done[64] = {false};
+    static std::mutex mu;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!attr_done[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(perm_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)(kPermWarps * 1024 * sizeof(int)));
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(perm_scan_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)((kPermWarps + 1) * 1024 * sizeof(int)));
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+    }
+    return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t launch_topk(const float *logits, int T, int E, int k, int32_t *ids, float *w, cudaStream_t s) {
+    return topk_launch<false>(logits, T, E, k, ids, w, nullptr, s);
+}
+
+cudaError_t launch_topk_hist(const float *logits, int T, int E, int k, int32_t *ids, float *w,
+                             int32_t *chunk_tab, cudaStream_t s) {
+    return topk_launch<true>(logits, T, E, k, ids, w, chunk_tab, s);
+}
+
 size_t permute_scratch_ints(int T, int E, int k) {
-    const long P = (long)T * k;
-    return (size_t)((P + kChunk - 1) / kChunk) * E;
+    const int ct = perm_chunk_tokens(k);
+    return (size_t)(((long)T + ct - 1) / ct) * E;
 }
 
 cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int32_t *offsets,
@@ -442,26 +585,13 @@ cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int32_t *off
                            int32_t *chunk_tab, const float *topk_w, int32_t *row_tok,
                            float *row_w, int *status, cudaStream_t s, int extra_rows, int *sched) {
     const int P = T * k;
-    const int n_chunks = (P + kChunk - 1) / kChunk;
-    // the scatter's shared-memory opt-in, once per device (under a lock: two host threads' first
-    // calls would otherwise race on the flag)
-    static bool attr_done[64] = {false};
-    static std::mutex mu;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    {
-        std::lock_guard<std::mutex> lk(mu);
-        if (!attr_done[dev]) {
-            cudaError_t e = cudaFuncSetAttribute(perm_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)(kPermWarps * 1024 * sizeof(int)));
-            if (e != cudaSuccess) return e;
-            attr_done[dev] = true;
-        }
-    }
+    const int ct = perm_chunk_tokens(k), cp = ct * k;
+    const int n_chunks = (T + ct - 1) / ct;
+    cudaError_t e = perm_attrs();
+    if (e != cudaSuccess) return e;
     {
         LaunchScope scope(KC_PERMUTE, s);
-        perm_hist_kernel<<<n_chunks, kPermThreads, E * sizeof(int), s>>>(ids, P, E, chunk_tab, status);
+        perm_hist_kernel<<<n_chunks, kPermThreads, E * sizeof(int), s>>>(ids, P, E, cp, chunk_tab, status);
     }
     {
         LaunchScope scope(KC_PERMUTE, s);
@@ -470,7 +600,23 @@ cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int32_t *off
     }
     LaunchScope scope(KC_PERMUTE, s);
     perm_scatter_kernel<<<n_chunks, kPermThreads, kPermWarps * E * sizeof(int), s>>>(
-        ids, P, E, k, chunk_tab, perm, inv, topk_w, row_tok, row_w, status);
+        ids, P, E, k, cp, chunk_tab, perm, inv, topk_w, row_tok, row_w, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scan_scatter(const int32_t *ids, int T, int E, int k, int32_t *offsets, int32_t *perm,
+                                int32_t *inv, int32_t *tile_prefix, const int32_t *chunk_tab,
+                                const float *topk_w, int32_t *row_tok, float *row_w, int *status,
+                                cudaStream_t s, int extra_rows, int *sched) {
+    const int P = T * k;
+    const int ct = perm_chunk_tokens(k), cp = ct * k;
+    const int n_chunks = (T + ct - 1) / ct;
+    cudaError_t e = perm_attrs();
+    if (e != cudaSuccess) return e;
+    LaunchScope scope(KC_PERMUTE, s);
+    perm_scan_scatter_kernel<<<n_chunks, kPermThreads, (kPermWarps + 1) * E * sizeof(int), s>>>(
+        chunk_tab, n_chunks, ids, P, E, k, cp, offsets, tile_prefix, extra_rows, sched, perm, inv, topk_w, row_tok,
+        row_w, status);
     return cudaGetLastError();
 }
 
