@@ -95,6 +95,29 @@ def test_forward_shapes(shape):
     check_layer(shape, layers1[0], x1)
 
 
+@pytest.mark.parametrize("shape,T", [(inputs.Shape(256, 24, 3, 128, 128), 2100),
+                                     (inputs.Shape(256, 40, 5, 128, 0), 1300),
+                                     (inputs.Shape(512, 64, 6, 128, 128), 1111)])
+def test_forward_top_k_not_dividing_the_chunk(shape, T):
+    """k = 3, 5, 6: the permutation's chunks are whole tokens (680 / 408 / 336 tokens, 2040 / 2040 /
+    2016 pairs), so chunk edges fall inside no token and the top-k kernel's 8-token blocks each land
+    in one chunk; several chunks and a ragged last one, through moe_forward (top-k counts, one
+    scan+scatter) and through moe_permute (three launches), both against the oracle."""
+    layers, x = make(shape, T, seed=70 + shape.top_k)
+    check_layer(shape, layers[0], x)
+    _, ids, _ = route_gpu(shape, layers[0], x)
+    cfg = cfg_of(shape)
+    ws = abi.alloc_workspace(cfg, T)
+    k = shape.top_k
+    offs = torch.empty(shape.n_experts + 1, dtype=torch.int32, device="cuda")
+    perm = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    inv = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    abi.moe_permute(cfg, torch.as_tensor(ids, device="cuda"), T, offs, perm, inv, ws)
+    torch.cuda.synchronize()
+    for g, o in zip((offs, perm, inv), orc.permute(ids, shape.n_experts)):
+        assert np.array_equal(g.cpu().numpy(), o)
+
+
 def test_forward_single_expert_is_dense_swiglu_library():
     """E=1, k=1, no shared expert: the layer is a dense SwiGLU MLP; check against torch."""
     shape = inputs.Shape(512, 1, 1, 256, 0)
