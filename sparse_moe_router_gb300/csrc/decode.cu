@@ -472,28 +472,40 @@ __global__ void __maxnreg__(NT == 1 ? 104 : 128)
             if (tid == 0 && !ptx::mbar_wait(&bar, ph, kWaitLimitNs, (volatile int *)&s_abort)) s_ok = 0;
             __syncthreads();
             if (!s_ok) break;
-            // rows is a multiple of 128, so every warp runs the same number of iterations
+            // rows is a multiple of 128, so every warp runs the same number of iterations.  The row's
+            // chunk order (cc + n/2) % 4 is the same for every row of this thread (rows tid + 512 i):
+            // with one token its h is read into registers once, in that order.
+            const int rot = (tid >> 1) & 3;
+            float hr[NT == 1 ? 32 : 1];
+            if constexpr (NT == 1) {
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) hr[cc * 8 + j] = hsl[((cc + rot) & 3) * 8 + j];
+            }
             for (int n = tid; n < rows; n += kK2Threads) {
                 const uint4 *rw = reinterpret_cast<const uint4 *>(wd + (size_t)n * kSlice);
                 // the row's four 16-byte chunks, read in an order rotated per row (against bank
                 // conflicts); chunk cc of q holds features 8*((cc + n/2) % 4) ..
                 uint4 q[4];
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) q[cc] = rw[(cc + (n >> 1)) & 3];
+                for (int cc = 0; cc < 4; ++cc) q[cc] = rw[(cc + rot) & 3];
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
                     if (t >= nt) break;  // the same for the whole block
                     float acc = 0.f;
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
-                        const int c = (cc + (n >> 1)) & 3;
+                        const int c = (cc + rot) & 3;
                         const __nv_bfloat162 *bq = reinterpret_cast<const __nv_bfloat162 *>(&q[cc]);
                         const float *hf = hsl + t * kSlice + c * 8;
 #pragma unroll
                         for (int m = 0; m < 4; ++m) {
                             const float2 fv = __bfloat1622float2(bq[m]);
-                            acc = fmaf(fv.x, hf[2 * m], acc);
-                            acc = fmaf(fv.y, hf[2 * m + 1], acc);
+                            const float h0 = NT == 1 ? hr[cc * 8 + 2 * m] : hf[2 * m];
+                            const float h1 = NT == 1 ? hr[cc * 8 + 2 * m + 1] : hf[2 * m + 1];
+                            acc = fmaf(fv.x, h0, acc);
+                            acc = fmaf(fv.y, h1, acc);
                         }
                     }
                     // lanes 4q..4q+3 hold rows n..n+3: one 16-byte reduction per four rows
@@ -924,13 +936,22 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
                 }
                 pending = false;
                 if constexpr (Q8) {
+                    // the row's halves are read in the order n % 2, (n % 2) ^ 1 (against bank conflicts);
+                    // n % 2 = tid % 2 for every row of this thread, so h is read into registers once
+                    const int hb = tid & 1;
+                    float hq[32];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        hq[j] = hsl[hb * 16 + j];
+                        hq[16 + j] = hsl[(hb ^ 1) * 16 + j];
+                    }
+                    const float *h0 = hq, *h1 = hq + 16;
 #pragma unroll
                     for (int i = 0; i < kChunkRows / kK2Threads; ++i) {
                         const int n = tid + i * kK2Threads;
                         if (n >= rows) break;  // rows is a multiple of 128: whole warps leave together
                         const uint4 *rw = reinterpret_cast<const uint4 *>(wd + (size_t)n * kSlice);
-                        const uint4 q0 = rw[n & 1], q1 = rw[(n & 1) ^ 1];  // alternate halves against bank conflicts
-                        const float *h0 = hsl + (n & 1) * 16, *h1 = hsl + ((n & 1) ^ 1) * 16;
+                        const uint4 q0 = rw[hb], q1 = rw[hb ^ 1];  // alternate halves against bank conflicts
                         const __nv_fp8x2_storage_t *c0 = reinterpret_cast<const __nv_fp8x2_storage_t *>(&q0);
                         const __nv_fp8x2_storage_t *c1 = reinterpret_cast<const __nv_fp8x2_storage_t *>(&q1);
                         float a = 0.f;
@@ -954,29 +975,37 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
                         const float v3 = __shfl_down_sync(0xffffffffu, a, 3);
                         if ((lane & 3) == 0) ptx::red_add_v4(&acc[r0 + n], wt * a, wt * v1, wt * v2, wt * v3);
                     }
-                } else
+                } else {
+                // row n's 16-byte chunks are read in the order (cc + n/2) % 4 (no bank conflicts);
+                // n/2 % 4 is the same for every row of this thread (rows tid + 512 i), so h is read
+                // into registers once, in that order
+                const int rot = (tid >> 1) & 3;
+                float hr[32];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) hr[cc * 8 + j] = hsl[((cc + rot) & 3) * 8 + j];
                 for (int n = tid; n < rows; n += kK2Threads) {
                     const uint4 *rw = reinterpret_cast<const uint4 *>(wd + (size_t)n * kSlice * 2);
                     uint4 q[4];
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) q[cc] = rw[(cc + (n >> 1)) & 3];
+                    for (int cc = 0; cc < 4; ++cc) q[cc] = rw[(cc + rot) & 3];
                     float a = 0.f;
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
-                        const int c = (cc + (n >> 1)) & 3;
                         const __nv_bfloat162 *bq = reinterpret_cast<const __nv_bfloat162 *>(&q[cc]);
-                        const float *hf = hsl + c * 8;
 #pragma unroll
                         for (int m = 0; m < 4; ++m) {
                             const float2 fv = __bfloat1622float2(bq[m]);
-                            a = fmaf(fv.x, hf[2 * m], a);
-                            a = fmaf(fv.y, hf[2 * m + 1], a);
+                            a = fmaf(fv.x, hr[cc * 8 + 2 * m], a);
+                            a = fmaf(fv.y, hr[cc * 8 + 2 * m + 1], a);
                         }
                     }
                     const float v1 = __shfl_down_sync(0xffffffffu, a, 1);
                     const float v2 = __shfl_down_sync(0xffffffffu, a, 2);
                     const float v3 = __shfl_down_sync(0xffffffffu, a, 3);
                     if ((lane & 3) == 0) ptx::red_add_v4(&acc[r0 + n], wt * a, wt * v1, wt * v2, wt * v3);
+                }
                 }
                 __syncthreads();  // the chunk buffer and hsl are free again
                 if (r0 + kChunkRows < H && warp == kLoadWarp) {
