@@ -156,12 +156,11 @@ class ClockSampler:
 # while the kernel has changed since the last capture: 1.41758 GB read + 72.72 MB written.
 GATEUP_DRAM_BYTES = 1_490_304_224
 # the same per layer for the one-token decode chain (decode_chain_kernel, H=2048, E=256, k=8,
-# I=I_s=512), or None until captured for the current kernel: a 2-layer launch read 115.44 MB and
-# wrote 2.99 MB.
-DECODE_CHAIN_DRAM_BYTES_PER_LAYER = 59_211_648
+# I=I_s=512), or None until captured for the current kernel.
+DECODE_CHAIN_DRAM_BYTES_PER_LAYER = None
 # the same for the chain on E4M3 expert weights (decode_chain_kernel<true>), or None until captured
-# for the current kernel: a 2-layer launch read 59.03 MB and wrote 0.50 MB.
-DECODE_CHAIN_Q8_DRAM_BYTES_PER_LAYER = 29_766_016
+# for the current kernel.
+DECODE_CHAIN_Q8_DRAM_BYTES_PER_LAYER = None
 
 
 def _algorithmic(shape, T, experts_touched=None):

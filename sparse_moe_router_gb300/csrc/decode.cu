@@ -189,21 +189,33 @@ __global__ void __launch_bounds__(kK1Block) decode_k1_kernel(DecodeArgs a) {
     }
 }
 
-// ---------------------------------------------------------------------- kernel 2 --
-// Warp-level top-k over the E logits (value descending, index ascending on ties) and the
-// renormalised softmax weights of the chosen k, into shared memory.  Lane L holds the logits
-// e = L + 32*i (i < PER) in registers and sorts them once; each of the k rounds is a warp
-// arg-max over the lanes' list heads, and the winner pops its head.  Ids are clamped into
-// [0, E) so that a corrupted logit vector can never make the block read outside the weights.
+// Warp-wide top-k over one token's E logits: value descending, lower expert index first on
+// equal values.  Lane L holds v[i] = logit of e = L + 32 i (i < PER; entries with e >= E are
+// ignored).  Each logit becomes one 64-bit key, its order bits above the complement of its
+// index, so that a single unsigned comparison orders value and index together (e >= E: key 0,
+// below every real key).  Every lane sorts its PER keys once with a bitonic network of selects
+// (no branches: a lone warp pays for divergence on every compare-exchange), then each of the k
+// rounds takes the largest list head with two warp reductions (the order bits, then the index
+// bits among the lanes whose head carries them) and the winning lane pops its head.  (The
+// prefill top-k kernel, one warp per token and thousands of warps, keeps float compares with
+// per-lane swaps: there throughput counts, and that form issues fewer instructions.)  Lane r < k
+// returns the r-th choice (*val its logit, *id its index); every lane returns the largest
+// logit in *top.
+__device__ __forceinline__ void topk_cx(unsigned long long &a, unsigned long long &b) {
+    const bool sw = b > a;
+    const unsigned long long hi = sw ? b : a, lo = sw ? a : b;
+    a = hi;
+    b = lo;
+}
+
 template <int PER>
-__device__ __forceinline__ void warp_topk_t(const float *logits, int E, int k, int *s_ids, float *s_w) {
-    const int lane = threadIdx.x & 31;
-    float v[PER];
-    int id[PER];
+__device__ __forceinline__ void warp_topk_select(const float (&v)[PER], int E, int k, int lane, float *val,
+                                                 int *id, float *top) {
+    unsigned long long q[PER];
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
-        id[i] = lane + 32 * i;
-        v[i] = id[i] < E ? logits[id[i]] : -INFINITY;
+        const int e = lane + 32 * i;
+        q[i] = e < E ? ((unsigned long long)order_key(v[i]) << 32) | (uint32_t)~(uint32_t)e : 0ull;
     }
 #pragma unroll
     for (int kk = 2; kk <= PER; kk <<= 1) {
@@ -213,41 +225,60 @@ __device__ __forceinline__ void warp_topk_t(const float *logits, int E, int k, i
             for (int i = 0; i < PER; ++i) {
                 const int l = i ^ j;
                 if (l > i) {
-                    const bool l_first = v[l] > v[i] || (v[l] == v[i] && id[l] < id[i]);
-                    if (((i & kk) == 0) ? l_first : !l_first) {
-                        const float tv = v[i]; v[i] = v[l]; v[l] = tv;
-                        const int ti = id[i]; id[i] = id[l]; id[l] = ti;
-                    }
+                    if ((i & kk) == 0) topk_cx(q[i], q[l]);
+                    else topk_cx(q[l], q[i]);
                 }
             }
         }
     }
-    float top = 0.f, my_val = 0.f;
+    float my_val = 0.f, t = 0.f;
     int my_id = 0;
     for (int r = 0; r < k; ++r) {
-        // two warp reductions a round: the largest head, then the lowest expert index among
-        // the lanes whose head equals it
-        const uint32_t key = order_key(v[0]);
-        const uint32_t mk = __reduce_max_sync(0xffffffffu, key);
-        const uint32_t cand = (key == mk && id[0] < E) ? (uint32_t)id[0] : 0xffffffffu;
-        const uint32_t sel = __reduce_min_sync(0xffffffffu, cand);
-        const float bv = key_value(mk);
-        const int bi = (int)sel;
-        if (sel != 0xffffffffu && (int)(sel & 31u) == lane) {
+        const uint32_t hi = (uint32_t)(q[0] >> 32), lo = (uint32_t)q[0];
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, hi);
+        const uint32_t ml = __reduce_max_sync(0xffffffffu, hi == mk ? lo : 0u);
+        const bool win = hi == mk && lo == ml;
 #pragma unroll
-            for (int i = 0; i + 1 < PER; ++i) { v[i] = v[i + 1]; id[i] = id[i + 1]; }
-            v[PER - 1] = -INFINITY;
-            id[PER - 1] = 0x7fffffff;
+        for (int i = 0; i + 1 < PER; ++i) q[i] = win ? q[i + 1] : q[i];
+        q[PER - 1] = win ? 0ull : q[PER - 1];
+        const float bv = key_value(mk);
+        if (r == 0) t = bv;
+        if (lane == r) {
+            my_val = bv;
+            my_id = (int)~ml;
         }
-        if (r == 0) top = bv;
-        if (lane == r) { my_val = bv; my_id = bi; }
     }
+    *val = my_val;
+    *id = my_id;
+    *top = t;
+}
+
+// ---------------------------------------------------------------------- kernel 2 --
+// Warp-level top-k over the E logits (value descending, index ascending on ties: the rounds of
+// warp_topk_select) and the renormalised softmax weights of the chosen k, into shared memory.
+// Ids are clamped into [0, E) so that a corrupted logit vector can never make the block read
+// outside the weights.
+template <int PER>
+__device__ __forceinline__ void warp_topk_regs(const float (&v)[PER], int E, int k, int *s_ids, float *s_w) {
+    const int lane = threadIdx.x & 31;
+    float my_val, top;
+    int my_id;
+    warp_topk_select<PER>(v, E, k, lane, &my_val, &my_id, &top);
     const float ej = lane < k ? expf(my_val - top) : 0.f;
     const float s = warp_sum(ej);
     if (lane < k) {
         s_ids[lane] = (my_id >= 0 && my_id < E) ? my_id : 0;
         s_w[lane] = ej / s;
     }
+}
+
+template <int PER>
+__device__ __forceinline__ void warp_topk_t(const float *logits, int E, int k, int *s_ids, float *s_w) {
+    const int lane = threadIdx.x & 31;
+    float v[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) v[i] = lane + 32 * i < E ? logits[lane + 32 * i] : 0.f;
+    warp_topk_regs<PER>(v, E, k, s_ids, s_w);
 }
 
 // The same selection for E > 256 without holding the logits in registers: they are staged in
@@ -603,11 +634,17 @@ cudaError_t decode_attrs() {
 // the layers are separated by two grid barriers instead of kernel boundaries:
 //   A  every block: x_l into shared memory (from the previous layer's accumulator), up to
 //      ceil(E / blocks) router rows (one warp each, the same dot as K1, so the logits are the
-//      same bits), its share of clearing this layer's accumulator; then it arrives at B1.
-//      A shared-expert block goes straight on to stream its slice: it needs only x_l.
-//   B  after B1 a routed block selects the top-k from the logits and streams its expert slice;
-//      every block adds its split-K down partial into the accumulator, then B2.
-// The accumulators alternate between layers, so clearing one never races with reading the other.
+//      same bits).  Each logit is stored as one 64-bit word with its layer's tag (l + 1) above
+//      the value bits, so a reader that sees the tag sees the value: no barrier between the
+//      router rows and the selection.  A shared-expert block goes straight on to stream its
+//      slice: it needs only x_l.
+//   B  a routed block reads the logits until all carry this layer's tag, selects the top-k and
+//      streams its expert slice; every block adds its split-K down partial into the
+//      accumulator, then B2.
+// Three accumulators rotate: the one cleared during layer l (for layer l + 1) last held layer
+// l - 2's sums, which every block read before B2 of layer l - 1, so no barrier is needed between
+// reading one and clearing another.  Layer 0 keeps one barrier, B1, after the blocks clear its
+// accumulator and before the first partial is added.
 // Barriers count arrivals on one word (release by the arriving block, acquire by the waiting
 // one); every spin is bounded and a block that gives up raises a flag the others see.
 constexpr uint64_t kBarLimitNs = 2000000000ull;
@@ -623,6 +660,61 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
 __device__ __forceinline__ void grid_arrive(unsigned *bar) {
     __syncthreads();
     if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(bar) : "memory");
+}
+
+// Tagged logits: the tag (the layer + 1) in the high word, the fp32 bits in the low one.  One
+// 64-bit access each way, so that the pair is written and read whole.
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Warp-wide: v[i] = logit e0 + lane + 32 i (i < 8, e < E; 0 past E) once every one of them
+// carries `tag`.  Bounded like grid_wait: false (for the whole warp) when the wait runs out or
+// another block gave up.
+__device__ __forceinline__ bool wait_logits(const unsigned long long *lgt, int e0, int E, uint32_t tag, float (&v)[8],
+                                            int *abort, int *status) {
+    const int lane = threadIdx.x & 31;
+    uint64_t t0 = 0;
+    for (uint32_t n = 0;; ++n) {
+        unsigned long long u[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = e0 + lane + 32 * i;
+            u[i] = e < E ? ld_relaxed_u64(lgt + e) : (unsigned long long)tag << 32;
+        }
+        bool got = true;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) got = got && (uint32_t)(u[i] >> 32) == tag;
+        if (__all_sync(0xffffffffu, got)) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = __uint_as_float((uint32_t)u[i]);
+            return true;
+        }
+        if (n == 0) {
+            t0 = ptx::globaltimer();
+        } else if ((n & 31u) == 0u) {  // the rest every 32 polls, decided by lane 0
+            int stop = 0;
+            if (lane == 0) {
+                if (*reinterpret_cast<volatile int *>(abort)) {
+                    stop = 1;
+                } else if (ptx::globaltimer() - t0 > kBarLimitNs) {
+                    stop = 1;
+                    atomicExch(abort, 1);
+                    if (status) atomicCAS(status, 0, (int)MOE_ERR_TIMEOUT);
+                }
+            }
+            if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+        }
+    }
+}
+
+__device__ __forceinline__ float *chain_acc(const ChainParams &p, int i) {
+    return i == 0 ? p.acc0 : (i == 1 ? p.acc1 : p.acc2);
 }
 
 // All threads of the block: true once `target` arrivals are counted; false (for the whole
@@ -757,7 +849,7 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
     __shared__ float s_lg[1024];
     __shared__ unsigned s_chosen[32];
     __shared__ __align__(8) uint64_t tbar;
-    __shared__ int s_ok, s_abort, s_flag;
+    __shared__ int s_ok, s_abort, s_flag, s_lgok;
     __shared__ int s_zero[1];  // the token list of one token: token 0
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int H = p.H, E = p.E, n16 = H / 8;
@@ -808,8 +900,8 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
     bool ok = true;
     for (int l = 0; l < p.L && ok; ++l) {
         const ChainLayer &ly = p.lay[l];
-        float *acc = (l & 1) ? p.acc1 : p.acc0;
-        const float *acc_prev = (l & 1) ? p.acc0 : p.acc1;
+        float *acc = chain_acc(p, l % 3);
+        const float *acc_prev = chain_acc(p, (l + 2) % 3);
         // ---------------------------------------------------------------- phase A --
         if (l == 0) {
             const uint4 *xg = reinterpret_cast<const uint4 *>(p.x0);
@@ -835,17 +927,21 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
             else dot1_row_t<1>(ly.w_router + (size_t)e * H, xs, n16, lane, 1, sc);
             const float bias = ly.b_router ? ly.b_router[e] : 0.f;
             const float v = warp_sum(sc[0]);
-            if (lane == 0) p.logits[e] = v + bias;
+            if (lane == 0)
+                st_relaxed_u64(p.logits + e, (unsigned long long)(l + 1) << 32 | __float_as_uint(v + bias));
         }
-        grid_arrive(p.bar);  // B1: the logits (and, at l = 0, the cleared accumulator)
-        const unsigned t_b1 = (++nbar) * (unsigned)nb;
+        unsigned t_b1 = 0;
+        if (l == 0) {
+            grid_arrive(p.bar);  // B1: the cleared first accumulator
+            t_b1 = (++nbar) * (unsigned)nb;
+        }
         if (l + 1 < p.L) {  // the next layer's router rows towards L2 while this layer streams
             const char *wr = reinterpret_cast<const char *>(p.lay[l + 1].w_router);
             for (int e = b + nb * warp; e < E; e += nb * kK2Warps)
                 for (int o = lane * 128; o < H * 2; o += 32 * 128) prefetch_l2(wr + (size_t)e * H * 2 + o);
         }
         // ---------------------------------------------------------------- phase B --
-        bool b1 = false, topk_done = false;
+        bool b1 = l > 0, topk_done = false;
         for (int w = b; w < n_items && ok; w += nb) {
             const bool shared_task = w < n_shared;
             const int i0 = shared_task ? w * kSlice : ((w - n_shared) % slices) * kSlice;
@@ -856,28 +952,33 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
             // Q8: the row scales of this item's gate/up rows and down rows
             const float *sgr = ly.ss_gate, *sur = ly.ss_up, *sdr = ly.ss_down;
             if (!shared_task) {
-                if (!b1) {
-                    if (!grid_wait(p.bar, t_b1, p.abort, p.status, (volatile int *)&s_flag)) { ok = false; break; }
-                    b1 = true;
-                }
                 if (!topk_done) {
                     if (warp == 0) {
-                        // the logits other blocks wrote, past L1, with eight loads in flight a lane
-                        for (int e0 = 0; e0 < E; e0 += 256) {
+                        // the logits other blocks wrote, once all carry this layer's tag
+                        const uint32_t tag = (uint32_t)(l + 1);
+                        bool got = true;
+                        if (E <= 256) {
                             float v[8];
+                            got = wait_logits(p.logits, 0, E, tag, v, p.abort, p.status);
+                            if (got) warp_topk_regs<8>(v, E, p.k, s_ids, s_w);
+                        } else {
+                            for (int e0 = 0; e0 < E && got; e0 += 256) {
+                                float v[8];
+                                got = wait_logits(p.logits, e0, E, tag, v, p.abort, p.status);
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const int e = e0 + lane + 32 * i;
-                                v[i] = e < E ? __ldcg(p.logits + e) : 0.f;
+                                for (int i = 0; i < 8; ++i)
+                                    if (got && e0 + lane + 32 * i < E) lg[e0 + lane + 32 * i] = v[i];
                             }
-#pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                if (e0 + lane + 32 * i < E) lg[e0 + lane + 32 * i] = v[i];
+                            __syncwarp();
+                            if (got) warp_topk(lg, E, p.k, s_ids, s_w, s_lg, s_chosen);
                         }
-                        __syncwarp();
-                        warp_topk(lg, E, p.k, s_ids, s_w, s_lg, s_chosen);
+                        if (lane == 0) s_lgok = got ? 1 : 0;
                     }
                     __syncthreads();
+                    if (!s_lgok) {
+                        ok = false;
+                        break;
+                    }
                     topk_done = true;
                 }
                 const int slot = (w - n_shared) / slices;
@@ -913,7 +1014,7 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
                 }
                 if (lane == 0) hsl[f] = __bfloat162float(__float2bfloat16_rn(silu_mul(gs, us)));
             }
-            if (!b1) {  // a shared-expert block: the accumulator is cleared once B1 completes
+            if (!b1) {  // layer 0: the accumulator is cleared once B1 completes
                 if (!grid_wait(p.bar, t_b1, p.abort, p.status, (volatile int *)&s_flag)) { ok = false; break; }
                 b1 = true;
             }
@@ -1020,10 +1121,10 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
             ok = false;
             break;
         }
-        // the next layer's accumulator held layer l-1's sums, which every block read into x_l
-        // before B1 (passed by now): clear it here; it is added into only after the next B1
+        // the next layer's accumulator held layer l-2's sums, which every block read into x_{l-1}
+        // before B2 of layer l-1: clear it here; it is added into only after this layer's B2
         if (l + 1 < p.L) {
-            float *acc_next = ((l + 1) & 1) ? p.acc1 : p.acc0;
+            float *acc_next = chain_acc(p, (l + 1) % 3);
             for (int i = b * kK2Threads + tid; i < H / 4; i += nb * kK2Threads)
                 reinterpret_cast<float4 *>(acc_next)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
@@ -1046,7 +1147,7 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
     }
     // after the last B2: out = bf16(acc), x_last = bf16(r + out); the first block writes them
     if (b == 0) {
-        const float *acc = ((p.L - 1) & 1) ? p.acc1 : p.acc0;
+        const float *acc = chain_acc(p, (p.L - 1) % 3);
         const uint2 *x2 = reinterpret_cast<const uint2 *>(xs);
         for (int i = tid; i < H / 4; i += kK2Threads) {
             const float4 a = __ldcg(reinterpret_cast<const float4 *>(acc) + i);
@@ -1137,8 +1238,13 @@ cudaError_t launch_decode_chain(const ChainParams &p, bool q8, cudaStream_t s) {
     const int n_items = p.Is / kSlice + p.k * (p.I / kSlice);
     int grid = per_sm[q8][dev] * device_info().sm_count;
     if (n_items < grid) grid = n_items;
-    cudaError_t e = cudaMemsetAsync(p.bar, 0, sizeof(unsigned), s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(p.abort, 0, sizeof(int), s);
+    // the barrier count and abort flag (adjacent words), and the logits' tags
+    cudaError_t e = reinterpret_cast<void *>(p.abort) == reinterpret_cast<void *>(p.bar + 1)
+                        ? cudaMemsetAsync(p.bar, 0, 2 * sizeof(unsigned), s)
+                        : cudaMemsetAsync(p.bar, 0, sizeof(unsigned), s);
+    if (e == cudaSuccess && reinterpret_cast<void *>(p.abort) != reinterpret_cast<void *>(p.bar + 1))
+        e = cudaMemsetAsync(p.abort, 0, sizeof(int), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p.logits, 0, (size_t)p.E * sizeof(unsigned long long), s);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

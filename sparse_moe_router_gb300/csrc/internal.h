@@ -282,8 +282,9 @@ struct ChainParams {
     const uint16_t *resid;  // [H] or NULL
     uint16_t *out;          // [H] the last layer's output
     uint16_t *x_last;       // [H] or NULL: bf16(r + out) after the last layer
-    float *logits;          // [E]
-    float *acc0, *acc1;     // [H] each; layer l adds into acc0 (l even) or acc1 (l odd)
+    // [E] tagged logits: (layer + 1) << 32 | fp32 bits, zero at launch
+    unsigned long long *logits;
+    float *acc0, *acc1, *acc2;  // [H] each; layer l adds into acc(l % 3)
     unsigned *bar;          // grid-barrier counter, zero at launch
     int *abort;             // zero at launch; set by a block that gives up
     int *status;            // device status word

@@ -164,7 +164,8 @@ Layout layout(const moe_config &c, int T) {
     const size_t Tt = (size_t)(T > 0 ? T : 1);
     L.status = take(256);
     L.sched = take(256);  // the grouped GEMMs' tile counters
-    L.logits = take(Tt * c.n_experts * 4);
+    // fp32 [T, E]; the decode chain's tagged logits take 8 bytes an expert
+    L.logits = take(Tt * c.n_experts * 4 > (size_t)c.n_experts * 8 ? Tt * c.n_experts * 4 : (size_t)c.n_experts * 8);
     L.ids = take(Tt * c.top_k * 4);
     L.topw = take(Tt * c.top_k * 4);
     // E + 2 entries: the experts and, when it runs inside the routed GEMMs, the shared expert
@@ -177,7 +178,7 @@ Layout layout(const moe_config &c, int T) {
     L.row_w = take(Tt * c.top_k * 4);
     L.h = take(Tt * (c.top_k + 1) * c.inter * 2);  // + the shared expert's rows
     L.h_s = take(Tt * (size_t)c.shared_inter * 2);
-    L.acc = take(Tt * c.hidden * 4);
+    L.acc = take((Tt > 3 ? Tt : 3) * c.hidden * 4);  // >= 3 rows: the decode chain's accumulators
     L.y = take(Tt * (c.top_k + 1) * c.hidden * 2);
     L.total = o;
     return L;
@@ -767,9 +768,10 @@ moe_status chain_common(const moe_config *cfg, int n_layers, const moe_bf16 *x0,
     p.resid = resid;
     p.out = out;
     p.x_last = x_last;
-    p.logits = at<float>(ws, L.logits);
+    p.logits = at<unsigned long long>(ws, L.logits);
     p.acc0 = at<float>(ws, L.acc);
-    p.acc1 = at<float>(ws, L.y);  // (k + 1) * H bf16 >= H fp32
+    p.acc1 = p.acc0 + cfg->hidden;
+    p.acc2 = p.acc1 + cfg->hidden;
     int *st = at<int>(ws, L.status);
     p.status = st;
     // st[1] is the one-layer path's ticket counter; the chain's barrier count and abort flag follow
