@@ -874,14 +874,20 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
             ptx::tma_load_2d(wd + (size_t)lane * kBoxRows * kSlice * kWB, tm, i0, base_row + r0 + lane * kBoxRows,
                              &tbar);
     };
-    // the router rows of warps 0..1 (e = b + nb * warp) are staged in shared memory while the
-    // previous layer finishes, when every block has at most two rows of moderate length
+    // the router rows of warps 0..1 (e = b + nb * warp) and their biases are staged in shared
+    // memory and registers while the previous layer's barrier completes, when every block has at
+    // most two rows of moderate length.  (Rows on warps 1..2, which leaves warp 0 free to poll
+    // for the logits at once, measured 2 us a layer slower: its polls crowd the lines the other
+    // blocks are writing.)
     const bool stage = E <= kStageRows * nb && H <= kStageH;
+    const int rw = warp;  // this warp's first router row is b + nb * rw
+    float sbias = 0.f;
     auto stage_rows = [&](int l) {
-        const int e = b + nb * warp;
-        if (warp < kStageRows && e < E) {
+        const int e = b + nb * rw;
+        if (rw >= 0 && rw < kStageRows && e < E) {
+            sbias = p.lay[l].b_router ? p.lay[l].b_router[e] : 0.f;
             const uint4 *src = reinterpret_cast<const uint4 *>(p.lay[l].w_router + (size_t)e * H);
-            uint4 *dst = wr_s + (size_t)warp * n16;
+            uint4 *dst = wr_s + (size_t)rw * n16;
             for (int c0 = lane; c0 < n16; c0 += 32 * 8) {
                 uint4 v[8];
 #pragma unroll
@@ -921,11 +927,11 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
             for (int i = b * kK2Threads + tid; i < H / 4; i += nb * kK2Threads)
                 reinterpret_cast<float4 *>(acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         __syncthreads();
-        for (int e = b + nb * warp; e < E; e += nb * kK2Warps) {
+        for (int e = b + nb * rw; rw >= 0 && e < E; e += nb * kK2Warps) {
             float sc[1] = {0.f};
-            if (stage) sc[0] = dot1_row_smem(wr_s + (size_t)warp * n16, xs, n16, lane);
+            if (stage) sc[0] = dot1_row_smem(wr_s + (size_t)rw * n16, xs, n16, lane);
             else dot1_row_t<1>(ly.w_router + (size_t)e * H, xs, n16, lane, 1, sc);
-            const float bias = ly.b_router ? ly.b_router[e] : 0.f;
+            const float bias = stage ? sbias : (ly.b_router ? ly.b_router[e] : 0.f);
             const float v = warp_sum(sc[0]);
             if (lane == 0)
                 st_relaxed_u64(p.logits + e, (unsigned long long)(l + 1) << 32 | __float_as_uint(v + bias));
@@ -1128,9 +1134,9 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
             for (int i = b * kK2Threads + tid; i < H / 4; i += nb * kK2Threads)
                 reinterpret_cast<float4 *>(acc_next)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        if (stage && l + 1 < p.L) stage_rows(l + 1);  // lands while the barrier completes
         grid_arrive(p.bar);  // B2: this layer's partials (and the next layer's cleared sums)
         const unsigned t_b2 = (++nbar) * (unsigned)nb;
+        if (stage && l + 1 < p.L) stage_rows(l + 1);  // lands while the barrier completes
         if (!grid_wait(p.bar, t_b2, p.abort, p.status, (volatile int *)&s_flag)) ok = false;
     }
     if (!ok || !s_ok) {
