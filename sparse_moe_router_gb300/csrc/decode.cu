@@ -1047,10 +1047,12 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
                     // n % 2 = tid % 2 for every row of this thread, so h is read into registers once
                     const int hb = tid & 1;
                     float hq[32];
+                    const float4 *h4 = reinterpret_cast<const float4 *>(hsl);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        hq[j] = hsl[hb * 16 + j];
-                        hq[16 + j] = hsl[(hb ^ 1) * 16 + j];
+                    for (int j = 0; j < 4; ++j) {
+                        const float4 u0 = h4[hb * 4 + j], u1 = h4[(hb ^ 1) * 4 + j];
+                        hq[4 * j] = u0.x, hq[4 * j + 1] = u0.y, hq[4 * j + 2] = u0.z, hq[4 * j + 3] = u0.w;
+                        hq[16 + 4 * j] = u1.x, hq[17 + 4 * j] = u1.y, hq[18 + 4 * j] = u1.z, hq[19 + 4 * j] = u1.w;
                     }
                     const float *h0 = hq, *h1 = hq + 16;
 #pragma unroll
@@ -1077,21 +1079,25 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
                             a = fmaf(fv.y, h1[2 * m + 1], a);
                         }
                         a *= sdn[i];
-                        const float v1 = __shfl_down_sync(0xffffffffu, a, 1);
-                        const float v2 = __shfl_down_sync(0xffffffffu, a, 2);
-                        const float v3 = __shfl_down_sync(0xffffffffu, a, 3);
-                        if ((lane & 3) == 0) ptx::red_add_v4(&acc[r0 + n], wt * a, wt * v1, wt * v2, wt * v3);
+                        atomicAdd(&acc[r0 + n], wt * a);  // the warp's 32 rows: one 128-byte reduction
                     }
                 } else {
                 // row n's 16-byte chunks are read in the order (cc + n/2) % 4 (no bank conflicts);
                 // n/2 % 4 is the same for every row of this thread (rows tid + 512 i), so h is read
-                // into registers once, in that order
+                // into registers once, in that order.  (This phase is bound by the shared-memory
+                // pipe, which also carries shuffles and narrow loads: h comes in 16-byte loads and
+                // each row is added on its own, the warp's 32 rows in one reduction.)
                 const int rot = (tid >> 1) & 3;
                 float hr[32];
+                const float4 *h4 = reinterpret_cast<const float4 *>(hsl);
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) hr[cc * 8 + j] = hsl[((cc + rot) & 3) * 8 + j];
+                    for (int j = 0; j < 2; ++j) {
+                        const float4 u = h4[((cc + rot) & 3) * 2 + j];
+                        hr[cc * 8 + 4 * j] = u.x, hr[cc * 8 + 4 * j + 1] = u.y;
+                        hr[cc * 8 + 4 * j + 2] = u.z, hr[cc * 8 + 4 * j + 3] = u.w;
+                    }
                 for (int n = tid; n < rows; n += kK2Threads) {
                     const uint4 *rw = reinterpret_cast<const uint4 *>(wd + (size_t)n * kSlice * 2);
                     uint4 q[4];
@@ -1108,10 +1114,7 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
                             a = fmaf(fv.y, hr[cc * 8 + 2 * m + 1], a);
                         }
                     }
-                    const float v1 = __shfl_down_sync(0xffffffffu, a, 1);
-                    const float v2 = __shfl_down_sync(0xffffffffu, a, 2);
-                    const float v3 = __shfl_down_sync(0xffffffffu, a, 3);
-                    if ((lane & 3) == 0) ptx::red_add_v4(&acc[r0 + n], wt * a, wt * v1, wt * v2, wt * v3);
+                    atomicAdd(&acc[r0 + n], wt * a);  // the warp's 32 rows: one 128-byte reduction
                 }
                 }
                 __syncthreads();  // the chunk buffer and hsl are free again
