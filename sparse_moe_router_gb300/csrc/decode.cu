@@ -345,7 +345,9 @@ __global__ void __maxnreg__(NT == 1 ? 104 : 128)
                      const __grid_constant__ CUtensorMap tm_sdown, int n_shared_blocks) {
     extern __shared__ uint8_t smem_raw[];
     // TMA destinations: align the dynamic shared memory up to 1024 bytes (the launch adds slack)
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // aligned by an offset from the shared array itself (not through an integer address), so that
+    // every access derived from it compiles to a shared-memory access rather than a generic one
+    uint8_t *smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
     uint16_t *wd = reinterpret_cast<uint16_t *>(smem);                           // [kChunkRows][kSlice]
     uint4 *xs = reinterpret_cast<uint4 *>(smem + (size_t)kChunkRows * kSlice * 2);  // [T][H] bf16
     float *hsl = reinterpret_cast<float *>(xs + (size_t)a.T * (a.H / 8));          // [NT][kSlice] fp32
@@ -838,7 +840,9 @@ template <bool Q8>
 __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __grid_constant__ ChainParams p) {
     constexpr int kWB = Q8 ? 1 : 2;  // bytes per expert weight
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // aligned by an offset from the shared array itself (not through an integer address), so that
+    // every access derived from it compiles to a shared-memory access rather than a generic one
+    uint8_t *smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *wd = smem;                                                          // [kChunkRows][kSlice] weights
     uint4 *xs = reinterpret_cast<uint4 *>(smem + (size_t)kChunkRows * kSlice * 2);  // [H] bf16: x_l
     float *hsl = reinterpret_cast<float *>(xs + p.H / 8);                          // [kSlice]

@@ -188,8 +188,9 @@ __global__ void __launch_bounds__(Cfg<EPI, Q8>::kThreads, 1)
     constexpr int kThreads = C::kThreads;
     constexpr int kSubs = kEpiWarps / 4;  // warps per TMEM lane quarter
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // aligned by an offset from the shared array itself (not through an integer address), so that
+    // every access derived from it compiles to a shared-memory access rather than a generic one
+    uint8_t *smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
     float *staging = reinterpret_cast<float *>(smem + kStages * kStageBytes);
     int32_t *meta_row = reinterpret_cast<int32_t *>(smem + kStages * kStageBytes + C::kStagingBytes);
     float *meta_w = reinterpret_cast<float *>(meta_row + 2 * BN);
