@@ -644,13 +644,12 @@ __global__ void __launch_bounds__(256)
         }
         const uint4 *src = x + (size_t)t * H8;
         int i = lane;
-        for (; i + 96 < H8; i += 128) {
-            const uint4 v0 = __ldg(&src[i]), v1 = __ldg(&src[i + 32]);
-            const uint4 v2 = __ldg(&src[i + 64]), v3 = __ldg(&src[i + 96]);
-            dst[i] = v0;
-            dst[i + 32] = v1;
-            dst[i + 64] = v2;
-            dst[i + 96] = v3;
+        for (; i + 224 < H8; i += 256) {  // eight 16-byte loads a lane in flight (a 4 KB row per warp)
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = __ldg(&src[i + 32 * u]);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) dst[i + 32 * u] = v[u];
         }
         for (; i < H8; i += 32) dst[i] = __ldg(&src[i]);
     }
