@@ -153,14 +153,15 @@ class ClockSampler:
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one gate/up launch (routed experts + the shared
 # expert, T=8192, H=2048, E=256, k=8, I=I_s=512) from an ncu capture of the current kernel, or None
-# while the kernel has changed since the last capture: 1.41758 GB read + 72.72 MB written.
-GATEUP_DRAM_BYTES = 1_490_304_224
+# while the kernel has changed since the last capture: 1.41722 GB read + 72.78 MB written.
+GATEUP_DRAM_BYTES = 1_490_004_032
 # the same per layer for the one-token decode chain (decode_chain_kernel, H=2048, E=256, k=8,
-# I=I_s=512), or None until captured for the current kernel.
-DECODE_CHAIN_DRAM_BYTES_PER_LAYER = None
+# I=I_s=512), or None until captured for the current kernel: a 2-layer launch read 115.42 MB and
+# wrote 3.02 MB.
+DECODE_CHAIN_DRAM_BYTES_PER_LAYER = 59_222_912
 # the same for the chain on E4M3 expert weights (decode_chain_kernel<true>), or None until captured
-# for the current kernel.
-DECODE_CHAIN_Q8_DRAM_BYTES_PER_LAYER = None
+# for the current kernel: a 2-layer launch read 59.02 MB and wrote 0.49 MB.
+DECODE_CHAIN_Q8_DRAM_BYTES_PER_LAYER = 29_755_136
 
 
 def _algorithmic(shape, T, experts_touched=None):
