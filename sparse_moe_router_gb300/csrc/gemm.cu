@@ -31,7 +31,8 @@
 //               tcgen05.mma (kind::f16, M = 256, bf16 -> fp32) and tcgen05.commit, whose
 //               arrivals go to both CTAs' barriers.
 // Pipelines: 192 KB of shared-memory stages (full/empty mbarriers): 3 stages of two 64-wide K
-// blocks for the long-K GEMMs (router, gate/up), 6 stages of one block for the down GEMM; and two
+// blocks for the fp32-output GEMMs (router), 6 stages of one block for the routed gate/up and down
+// GEMMs; and two
 // TMEM accumulators of 256 columns (acc_full/acc_empty; the odd CTA's epilogue releases an
 // accumulator with a remote arrive), so the epilogue of one tile overlaps the next main loop.
 // Pair tiles are walked statically (tile = pair + i*pairs), ordered (group, weight tile, token
@@ -78,11 +79,12 @@ constexpr int kConvBar = 8;         // named barrier of the converter warps
 
 template <int EPI, bool Q8 = false>
 struct Cfg {
-    // K blocks per pipeline stage.  The long-K GEMMs (router, gate/up: K = H) take two, so the MMA
-    // thread waits and commits once per 8 MMAs (each handshake costs the tensor pipe time it does
-    // not hide); the down GEMM (K = I, a few stages a tile) keeps one and the deeper ring, and so
-    // does the E4M3 variant (its stages carry the raw codes too).
-    static constexpr int kKB = (EPI == EPI_COMBINE || Q8) ? 1 : 2;
+    // K blocks per pipeline stage.  The router GEMM (K = H, a single wave of small tiles) takes two,
+    // so the MMA thread waits and commits once per 8 MMAs (each handshake costs the tensor pipe time
+    // it does not hide); the routed GEMMs keep one and the deeper ring (gate/up measured 275.3 us with
+    // six one-block stages against 276.1 with three two-block ones), and so does the E4M3 variant
+    // (its stages carry the raw codes too).
+    static constexpr int kKB = (EPI == EPI_F32 && !Q8) ? 2 : 1;
     static constexpr int kStep = kStepBytes + (Q8 ? kRawBytes : 0);  // one K block in one CTA
     static constexpr int kStages = kPipeBytes / (kKB * kStep);
     static constexpr int kStageBytes = kKB * kStep;
