@@ -412,3 +412,92 @@ void moe_ref_forward_q8(int H, int E, int k, int I, int Is, int T, const uint16_
     }
     free(hbuf); free(y); free(acc);
 }
+
+/* ------------------------------------------------------------ 4-bit integer blocks -- */
+/* GFX1151 page ("两种权重格式" section and its explanatory paragraph: Q4 is 4-bit integer
+ * quantisation, FP8 8-bit floating point); the block layout is the reading stated in the header. */
+
+void moe_ref_quantize_q4_rows(int rows, int cols, const uint16_t *w, uint8_t *q, float *scale) {
+    const int nb = cols / 32;
+    for (int r = 0; r < rows; ++r) {
+        const uint16_t *wr = w + (size_t)r * cols;
+        uint8_t *qr = q + (size_t)r * (cols / 2);
+        for (int b = 0; b < nb; ++b) {
+            float amax = 0.0f;
+            for (int c = 32 * b; c < 32 * b + 32; ++c) {
+                float a = (float)fabs(BF(wr[c]));
+                if (a > amax) amax = a;
+            }
+            float s = amax > 0.0f ? amax / 7.0f : 1.0f;
+            scale[(size_t)r * nb + b] = s;
+            for (int c = 32 * b; c < 32 * b + 32; ++c) {
+                float v = rintf((float)BF(wr[c]) / s);
+                if (v > 7.0f) v = 7.0f;
+                if (v < -7.0f) v = -7.0f;
+                int code = (int)v;
+                uint8_t nib = (uint8_t)(code & 15);
+                if (c % 2 == 0) qr[c / 2] = nib;
+                else qr[c / 2] = (uint8_t)(qr[c / 2] | (nib << 4));
+            }
+        }
+    }
+}
+
+int moe_ref_q4_code(const uint8_t *row, int c) {
+    int nib = (c % 2 == 0) ? (row[c / 2] & 15) : (row[c / 2] >> 4);
+    return nib >= 8 ? nib - 16 : nib;
+}
+
+/* One weight of a Q4 matrix with `cols` columns: scale * code. */
+static double q4_weight(const uint8_t *q, const float *scale, int cols, int r, int c) {
+    return (double)scale[(size_t)r * (cols / 32) + c / 32] * (double)moe_ref_q4_code(q + (size_t)r * (cols / 2), c);
+}
+
+/* h = bf16(silu(g) * u), y = Wd h with the Q4 weights (fp64 sums); as swiglu_ffn. */
+static void swiglu_ffn_q4(int H, int I, const uint16_t *xrow, const uint8_t *qg, const float *sg,
+                          const uint8_t *qu, const float *su, const uint8_t *qd, const float *sd,
+                          double *hbuf, double *y) {
+    for (int i = 0; i < I; ++i) {
+        double g = 0.0, u = 0.0;
+        for (int h = 0; h < H; ++h) {
+            double xv = BF(xrow[h]);
+            g += q4_weight(qg, sg, H, i, h) * xv;
+            u += q4_weight(qu, su, H, i, h) * xv;
+        }
+        hbuf[i] = BF(moe_ref_double_to_bf16(moe_ref_silu(g) * u));
+    }
+    for (int n = 0; n < H; ++n) {
+        double acc = 0.0;
+        for (int i = 0; i < I; ++i) acc += q4_weight(qd, sd, I, n, i) * hbuf[i];
+        y[n] = acc;
+    }
+}
+
+void moe_ref_forward_q4(int H, int E, int k, int I, int Is, int T, const uint16_t *x,
+                        const uint8_t *qg, const float *sg, const uint8_t *qu, const float *su,
+                        const uint8_t *qd, const float *sd, const uint8_t *qsg, const float *ssg,
+                        const uint8_t *qsu, const float *ssu, const uint8_t *qsd, const float *ssd,
+                        const int32_t *ids, const float *w, uint16_t *out) {
+    (void)E;
+    int maxI = I > Is ? I : Is;
+    double *hbuf = (double *)malloc(sizeof(double) * (size_t)(maxI > 0 ? maxI : 1));
+    double *y = (double *)malloc(sizeof(double) * (size_t)H);
+    double *acc = (double *)malloc(sizeof(double) * (size_t)H);
+    for (int t = 0; t < T; ++t) {
+        const uint16_t *xrow = x + (size_t)t * H;
+        for (int n = 0; n < H; ++n) acc[n] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            int e = ids[(size_t)t * k + j];
+            swiglu_ffn_q4(H, I, xrow, qg + (size_t)e * I * (H / 2), sg + (size_t)e * I * (H / 32),
+                          qu + (size_t)e * I * (H / 2), su + (size_t)e * I * (H / 32),
+                          qd + (size_t)e * H * (I / 2), sd + (size_t)e * H * (I / 32), hbuf, y);
+            for (int n = 0; n < H; ++n) acc[n] += (double)w[(size_t)t * k + j] * y[n];
+        }
+        if (Is > 0) {
+            swiglu_ffn_q4(H, Is, xrow, qsg, ssg, qsu, ssu, qsd, ssd, hbuf, y);
+            for (int n = 0; n < H; ++n) acc[n] += y[n];
+        }
+        for (int n = 0; n < H; ++n) out[(size_t)t * H + n] = moe_ref_double_to_bf16(acc[n]);
+    }
+    free(hbuf); free(y); free(acc);
+}

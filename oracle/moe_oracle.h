@@ -114,6 +114,26 @@ void moe_ref_forward_q8(int H, int E, int k, int I, int Is, int T, const uint16_
                         const uint8_t *qsu, const float *ssu, const uint8_t *qsd, const float *ssd,
                         const int32_t *ids, const float *w, uint16_t *out);
 
+/* 4-bit integer block quantisation ("Q4": 4-bit integer codes, as the GFX1151 page's explanatory
+ * paragraph on weight formats describes it).  Each row of a bf16 matrix [rows, cols] (cols a
+ * multiple of 32) is cut into blocks of 32 consecutive columns.  Block b of row r: scale[r, b] =
+ * fp32(max |w|) / 7 in fp32 (1 for an all-zero block); the code of w is round-half-even of
+ * fp32(w) / scale (fp32 division), clamped to [-7, 7], stored as a two's-complement nibble:
+ * column 2j in the low nibble and 2j+1 in the high nibble of byte j of the row (cols / 2 bytes a
+ * row).  The weight the layer uses is scale * code (exact in double). */
+void moe_ref_quantize_q4_rows(int rows, int cols, const uint16_t *w, uint8_t *q, float *scale);
+/* The value of code nibble c (column c) of a row of packed codes. */
+int moe_ref_q4_code(const uint8_t *row, int c);
+/* The layer for T tokens with Q4 expert weights on a given routing, with the rounding points of
+ * moe_ref_forward.  Routed: qg, qu [E, I, H/2] with sg, su [E, I, H/32]; qd [E, H, I/2] with
+ * sd [E, H, I/32].  Shared (Is > 0): qsg, qsu [Is, H/2] with ssg, ssu [Is, H/32]; qsd [H, Is/2]
+ * with ssd [H, Is/32]. */
+void moe_ref_forward_q4(int H, int E, int k, int I, int Is, int T, const uint16_t *x,
+                        const uint8_t *qg, const float *sg, const uint8_t *qu, const float *su,
+                        const uint8_t *qd, const float *sd, const uint8_t *qsg, const float *ssg,
+                        const uint8_t *qsu, const float *ssu, const uint8_t *qsd, const float *ssd,
+                        const int32_t *ids, const float *w, uint16_t *out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -58,6 +58,12 @@ def _declare(L):
     L.moe_ref_quantize_e4m3_rows.restype = None
     L.moe_ref_forward_q8.argtypes = [_I] * 6 + [_P] * 16
     L.moe_ref_forward_q8.restype = None
+    L.moe_ref_quantize_q4_rows.argtypes = [_I, _I, _P, _P, _P]
+    L.moe_ref_quantize_q4_rows.restype = None
+    L.moe_ref_q4_code.argtypes = [_P, _I]
+    L.moe_ref_q4_code.restype = _I
+    L.moe_ref_forward_q4.argtypes = [_I] * 6 + [_P] * 16
+    L.moe_ref_forward_q4.restype = None
 
 
 def _ptr(a):
@@ -260,6 +266,46 @@ def forward_q8(x, wq, k, ids, topk_w):
     ids, topk_w = _i32(ids), _f32(topk_w)
     out = np.empty((T, H), dtype=np.uint16)
     lib().moe_ref_forward_q8(H, E, k, I, Is, T, _ptr(x), _ptr(qg), _ptr(sg), _ptr(qu), _ptr(su), _ptr(qd),
+                             _ptr(sd), _ptr(qsg), _ptr(ssg), _ptr(qsu), _ptr(ssu), _ptr(qsd), _ptr(ssd),
+                             _ptr(ids), _ptr(topk_w), _ptr(out))
+    return out
+
+
+def quantize_q4_rows(w):
+    """bf16 bits [rows, cols] (cols % 32 == 0) -> (packed 4-bit codes uint8 [rows, cols/2], fp32
+    block scales [rows, cols/32])."""
+    w = _u16(w)
+    rows, cols = w.shape
+    q = np.empty((rows, cols // 2), dtype=np.uint8)
+    s = np.empty((rows, cols // 32), dtype=np.float32)
+    lib().moe_ref_quantize_q4_rows(rows, cols, _ptr(w), _ptr(q), _ptr(s))
+    return q, s
+
+
+def q4_codes(q_row):
+    """The signed codes of one packed row (the C oracle's decoder, nibble by nibble)."""
+    r = np.ascontiguousarray(q_row, dtype=np.uint8)
+    f = lib().moe_ref_q4_code
+    return np.array([f(_ptr(r), c) for c in range(2 * r.size)], dtype=np.int64)
+
+
+def forward_q4(x, wq, k, ids, topk_w):
+    """The layer with Q4 expert weights on a given routing.  ``wq`` holds packed codes q_gate,
+    q_up [E,I,H/2], q_down [E,H,I/2] with float32 block scales s_gate, s_up [E,I,H/32], s_down
+    [E,H,I/32], and optionally the shared expert's qs_gate, qs_up [Is,H/2], qs_down [H,Is/2]
+    with ss_gate, ss_up [Is,H/32], ss_down [H,Is/32].  Returns out (u16 [T,H])."""
+    x = _u16(x)
+    T, H = x.shape
+    u8 = lambda a: None if a is None else np.ascontiguousarray(a, dtype=np.uint8)
+    qg, qu, qd = u8(wq["q_gate"]), u8(wq["q_up"]), u8(wq["q_down"])
+    E, I = qg.shape[0], qg.shape[1]
+    sg, su, sd = _f32(wq["s_gate"]), _f32(wq["s_up"]), _f32(wq["s_down"])
+    qsg, qsu, qsd = u8(wq.get("qs_gate")), u8(wq.get("qs_up")), u8(wq.get("qs_down"))
+    ssg, ssu, ssd = _f32(wq.get("ss_gate")), _f32(wq.get("ss_up")), _f32(wq.get("ss_down"))
+    Is = 0 if qsg is None else qsg.shape[0]
+    ids, topk_w = _i32(ids), _f32(topk_w)
+    out = np.empty((T, H), dtype=np.uint16)
+    lib().moe_ref_forward_q4(H, E, k, I, Is, T, _ptr(x), _ptr(qg), _ptr(sg), _ptr(qu), _ptr(su), _ptr(qd),
                              _ptr(sd), _ptr(qsg), _ptr(ssg), _ptr(qsu), _ptr(ssu), _ptr(qsd), _ptr(ssd),
                              _ptr(ids), _ptr(topk_w), _ptr(out))
     return out
