@@ -156,12 +156,13 @@ class ClockSampler:
 # while the kernel has changed since the last capture: 1.42150 GB read + 72.92 MB written.
 GATEUP_DRAM_BYTES = 1_494_418_856
 # the same per layer for the one-token decode chain (decode_chain_kernel, H=2048, E=256, k=8,
-# I=I_s=512), or None until captured for the current kernel: a 2-layer launch read 115.42 MB and
-# wrote 3.02 MB.
-DECODE_CHAIN_DRAM_BYTES_PER_LAYER = 59_222_912
-# the same for the chain on E4M3 expert weights (decode_chain_kernel<true>), or None until captured
-# for the current kernel: a 2-layer launch read 59.02 MB and wrote 0.49 MB.
-DECODE_CHAIN_Q8_DRAM_BYTES_PER_LAYER = 29_755_136
+# I=I_s=512), or None until captured for the current kernel.
+DECODE_CHAIN_DRAM_BYTES_PER_LAYER = None
+# the same for the chain on E4M3 expert weights (decode_chain_kernel<1>), or None until captured
+# for the current kernel.
+DECODE_CHAIN_Q8_DRAM_BYTES_PER_LAYER = None
+# the same for the chain on 4-bit expert weights (decode_chain_kernel<2>), or None until captured.
+DECODE_CHAIN_Q4_DRAM_BYTES_PER_LAYER = None
 
 
 def _algorithmic(shape, T, experts_touched=None):
@@ -201,6 +202,14 @@ def _decode_bytes_q8(shape):
     weight of the k routed and the shared expert, and their fp32 row scales."""
     H, E, k, I, Is = shape.hidden, shape.n_experts, shape.top_k, shape.inter, shape.shared_inter
     return E * H * 2 + k * 3 * H * I + 3 * H * Is + 4 * (k * (2 * I + H) + (2 * Is + H if Is else 0))
+
+
+def _decode_bytes_q4(shape):
+    """The bytes one token reads with 4-bit expert weights: the bf16 router, half a byte per
+    expert weight of the k routed and the shared expert, and their fp32 block scales (one per 32)."""
+    H, E, k, I, Is = shape.hidden, shape.n_experts, shape.top_k, shape.inter, shape.shared_inter
+    n = k * 3 * H * I + 3 * H * Is
+    return E * H * 2 + n // 2 + 4 * (n // 32)
 
 
 def run_ours(args, world, rank, local, pg):
@@ -604,10 +613,10 @@ def run_decode(args, dev, pg, peaks):
     wts = [abi.weights(l) for l in layers]
     s = torch.cuda.Stream(device=dev)
 
-    def graph_time(x_start, one_launch=False, wts_q8=None):
+    def graph_time(x_start, one_launch=False, wts_q8=None, wts_q4=None):
         """Median time of the 40-layer chain for x_start's tokens, captured as one CUDA graph:
         one moe_forward call per layer, or (one_launch) one moe_decode_chain call for all, or
-        (wts_q8) one moe_decode_chain_q8 call on the E4M3 copies of the layers."""
+        (wts_q8 / wts_q4) one moe_decode_chain_q8 / _q4 call on the quantised copies of the layers."""
         T = x_start.shape[0]
         ws = abi.alloc_workspace(cfg, T)
         bufs = [x_start.clone(), torch.empty_like(x_start), torch.empty_like(x_start)]
@@ -617,6 +626,9 @@ def run_decode(args, dev, pg, peaks):
             # layer l+1 reads bf16(x_0 + out_l), fused into the layer's last kernel
             if wts_q8 is not None:
                 abi.moe_decode_chain_q8(cfg, wts_q8, bufs[0], out, bufs[1], ws, s, resid=bufs[0])
+                return
+            if wts_q4 is not None:
+                abi.moe_decode_chain_q4(cfg, wts_q4, bufs[0], out, bufs[1], ws, s, resid=bufs[0])
                 return
             if one_launch:
                 abi.moe_decode_chain(cfg, wts, bufs[0], out, bufs[1], ws, s, resid=bufs[0])
@@ -703,7 +715,24 @@ def run_decode(args, dev, pg, peaks):
         q8 = {"us_per_layer": round(us_q8, 3), "bytes_per_layer": nq,
               "roofline": {"bound": "hbm", "achieved": round(gq, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                            "frac": round(gq / peaks["hbm_gbs"], 4), "traffic": DECODE_CHAIN_Q8_DRAM_BYTES_PER_LAYER,
-                           "traffic_kernel": "decode_chain_kernel<true>"}}
+                           "traffic_kernel": "decode_chain_kernel<1>"}}
+    # and with 4-bit expert weights (scale per block of 32; the router stays bf16), quantised on the
+    # device from the bf16 layers, through moe_decode_chain_q4
+    q4 = None
+    if not args.skip_q8:
+        with torch.cuda.stream(s):
+            layers_q4 = [abi.quantize_layer_q4(l, s) for l in layers]
+        torch.cuda.synchronize()
+        tq = _max_over_ranks(pg, statistics.median(graph_time(x0, wts_q4=[abi.weights_q4(l) for l in layers_q4])[0]),
+                             dev)
+        del layers_q4
+        us_q4 = 1e3 * tq / L
+        nq = _decode_bytes_q4(shape)
+        gq = nq / (us_q4 * 1e-6) / 1e9
+        q4 = {"us_per_layer": round(us_q4, 3), "bytes_per_layer": nq,
+              "roofline": {"bound": "hbm", "achieved": round(gq, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                           "frac": round(gq / peaks["hbm_gbs"], 4), "traffic": DECODE_CHAIN_Q4_DRAM_BYTES_PER_LAYER,
+                           "traffic_kernel": "decode_chain_kernel<2>"}}
     return {"workload": "decode T=1, %d distinct layers (%.1f GB of weights), one moe_decode_chain launch "
                         "in a CUDA graph" % (L, L * _decode_layer_bytes(shape) / 1e9),
             "us_per_layer": round(us_layer, 3), "graph_ms": round(t_med, 4), "reps": reps,
@@ -713,9 +742,9 @@ def run_decode(args, dev, pg, peaks):
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
                          "frac_of_8000": round(gbs / 8000.0, 4), "bytes_per_layer": nbytes,
-                         "traffic": DECODE_CHAIN_DRAM_BYTES_PER_LAYER, "traffic_kernel": "decode_chain_kernel",
+                         "traffic": DECODE_CHAIN_DRAM_BYTES_PER_LAYER, "traffic_kernel": "decode_chain_kernel<0>",
                          "peak_source": peaks["source"] + " hbm copy"},
-            "eager_kernel_avg_us": split, "small_batch": small, "e4m3_weights": q8}
+            "eager_kernel_avg_us": split, "small_batch": small, "e4m3_weights": q8, "int4_weights": q4}
 
 
 def cpu_baseline(wl, seconds=12.0):
@@ -927,7 +956,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-decode", action="store_true")
-    ap.add_argument("--skip-q8", action="store_true", help="skip the E4M3-weight measurements")
+    ap.add_argument("--skip-q8", action="store_true", help="skip the quantised-weight (E4M3, 4-bit) measurements")
     ap.add_argument("--q8-workloads", default="prefill8k,prefill1k",
                     help="prefill workloads timed with E4M3 expert weights (comma list)")
     ap.add_argument("--skip-e2e", action="store_true")

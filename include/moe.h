@@ -102,6 +102,30 @@ typedef struct {
     const float *ss_down;     /* [H] */
 } moe_weights_q8;
 
+/* One layer with 4-bit integer expert weights ("Q4": 4-bit integer codes, as the GFX1151 page's
+ * explanatory paragraph on weight formats calls them; the block layout is this library's
+ * reading, the page gives none).  Each row of every expert matrix is cut into blocks of 32
+ * consecutive columns; a block has one fp32 scale and 32 codes in [-7, 7], two's-complement
+ * nibbles, column 2j in the low and 2j+1 in the high nibble of byte j of the row (cols / 2 bytes a
+ * row); weight = scale * code.  The router stays bf16.  H and I (and Is) multiples of 128; code
+ * arrays 16-byte aligned; moe_quantize_q4 produces them from bf16 matrices. */
+typedef struct {
+    const moe_bf16 *w_router; /* [E, H] bf16 */
+    const float *b_router;    /* [E] fp32, or NULL */
+    const uint8_t *q_gate;    /* [E, I, H/2] codes */
+    const uint8_t *q_up;      /* [E, I, H/2] */
+    const uint8_t *q_down;    /* [E, H, I/2] */
+    const float *s_gate;      /* [E, I, H/32] block scales */
+    const float *s_up;        /* [E, I, H/32] */
+    const float *s_down;      /* [E, H, I/32] */
+    const uint8_t *qs_gate;   /* [Is, H/2] (NULL when Is == 0) */
+    const uint8_t *qs_up;     /* [Is, H/2] */
+    const uint8_t *qs_down;   /* [H, Is/2] */
+    const float *ss_gate;     /* [Is, H/32] */
+    const float *ss_up;       /* [Is, H/32] */
+    const float *ss_down;     /* [H, Is/32] */
+} moe_weights_q4;
+
 /* Text for a status code (static storage). */
 const char *moe_status_string(moe_status s);
 
@@ -264,6 +288,22 @@ moe_status moe_decode_chain(const moe_config *cfg, const moe_weights *layers, in
 moe_status moe_decode_chain_q8(const moe_config *cfg, const moe_weights_q8 *layers, int n_layers,
                                const moe_bf16 *x0, const moe_bf16 *resid, moe_bf16 *out,
                                moe_bf16 *x_last, void *ws, size_t ws_bytes, void *stream);
+
+/* moe_decode_chain for layers with 4-bit expert weights (moe_weights_q4): every expert row
+ * streamed as its codes (a quarter of the bytes of bf16) and block scales, each block's codes
+ * dotted in fp32 and scaled; otherwise the same steps, rounding points, barriers and errors. */
+moe_status moe_decode_chain_q4(const moe_config *cfg, const moe_weights_q4 *layers, int n_layers,
+                               const moe_bf16 *x0, const moe_bf16 *resid, moe_bf16 *out,
+                               moe_bf16 *x_last, void *ws, size_t ws_bytes, void *stream);
+
+/* Block-wise 4-bit quantisation of a bf16 matrix w [rows, cols] (device pointers; cols a multiple
+ * of 32): per block of 32 columns, scale = max |w| / 7 (1 for an all-zero block) and code =
+ * round-half-even(w / scale) clamped to [-7, 7], in fp32 with IEEE division (a function of the
+ * block alone).  q [rows, cols/2] packed nibbles (column 2j low, 2j+1 high), scale [rows, cols/32]
+ * fp32.  Blocks holding an infinity or a NaN give unspecified codes.  Asynchronous on `stream`;
+ * rows or cols of 0 do nothing; a negative size, cols not a multiple of 32 or a NULL pointer is
+ * MOE_ERR_INVALID_ARG. */
+moe_status moe_quantize_q4(const moe_bf16 *w, int rows, int cols, uint8_t *q, float *scale, void *stream);
 
 /* Row-wise E4M3 quantisation of a bf16 matrix w [rows, cols] (device pointers): scale[r] =
  * max_c |w[r,c]| / 448 (1 for an all-zero row) and q[r,c] = the E4M3 code nearest to

@@ -26,7 +26,8 @@ EXPORTS = ["moe_status_string", "moe_workspace_size", "moe_route", "moe_route_fr
            "moe_plan_pieces", "moe_launch_count", "moe_timing_enable", "moe_timing_read",
            "moe_timing_name", "moe_timing_classes", "moe_selftest_wait", "moe_decode_chain",
            "moe_decode_chain_q8", "moe_quantize_e4m3", "moe_graph_create", "moe_graph_launch",
-           "moe_graph_kernel_count", "moe_graph_destroy", "moe_forward_q8", "moe_debug_build"]
+           "moe_graph_kernel_count", "moe_graph_destroy", "moe_forward_q8", "moe_debug_build",
+           "moe_decode_chain_q4", "moe_quantize_q4"]
 
 
 class MoeError(RuntimeError):
@@ -49,6 +50,11 @@ class WeightsQ8(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("w_router", "b_router", "q_gate", "q_up", "q_down", "s_gate", "s_up", "s_down",
                  "qs_gate", "qs_up", "qs_down", "ss_gate", "ss_up", "ss_down")]
+
+
+class WeightsQ4(ctypes.Structure):
+    # the same fields as WeightsQ8: packed 4-bit codes and per-block scales (include/moe.h)
+    _fields_ = WeightsQ8._fields_
 
 
 _P = ctypes.c_void_p
@@ -82,6 +88,8 @@ def load(path: str = LIB_PATH):
     L.moe_decode_chain_q8.argtypes = [C, ctypes.POINTER(WeightsQ8), _I, _P, _P, _P, _P, _P, _SZ, _P]
     L.moe_forward_q8.argtypes = [C, ctypes.POINTER(WeightsQ8), _P, _I, _P, _P, _P, _P, _SZ, _P]
     L.moe_quantize_e4m3.argtypes = [_P, _I, _I, _P, _P, _P]
+    L.moe_decode_chain_q4.argtypes = [C, ctypes.POINTER(WeightsQ4), _I, _P, _P, _P, _P, _P, _SZ, _P]
+    L.moe_quantize_q4.argtypes = [_P, _I, _I, _P, _P, _P]
     L.moe_check_status.argtypes = [_P, _SZ, ctypes.POINTER(_I), _P]
     L.moe_selftest_wait.argtypes = [_P, _SZ, ctypes.c_ulonglong, _I, _P]
     L.moe_graph_create.argtypes = [C, W, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P, ctypes.POINTER(_P)]
@@ -104,7 +112,7 @@ def load(path: str = LIB_PATH):
                "moe_combine", "moe_forward", "moe_check_status", "moe_timing_enable",
                "moe_timing_read", "moe_timing_classes", "moe_selftest_wait", "moe_decode_chain",
                "moe_decode_chain_q8", "moe_quantize_e4m3", "moe_graph_create", "moe_graph_launch",
-               "moe_graph_destroy", "moe_forward_q8"):
+               "moe_graph_destroy", "moe_forward_q8", "moe_decode_chain_q4", "moe_quantize_q4"):
         getattr(L, fn).restype = _I
     _lib = L
     return L
@@ -150,6 +158,17 @@ def weights_q8(layer: dict) -> WeightsQ8:
     """WeightsQ8 struct from a dict of device tensors (keys as in include/moe.h)."""
     w = WeightsQ8()
     for name, _ in WeightsQ8._fields_:
+        t = layer.get(name)
+        setattr(w, name, None if t is None else t.data_ptr())
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("weight %s must be a contiguous CUDA tensor" % name)
+    return w
+
+
+def weights_q4(layer: dict) -> WeightsQ4:
+    """WeightsQ4 struct from a dict of device tensors (keys as in include/moe.h)."""
+    w = WeightsQ4()
+    for name, _ in WeightsQ4._fields_:
         t = layer.get(name)
         setattr(w, name, None if t is None else t.data_ptr())
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
@@ -280,6 +299,38 @@ def moe_decode_chain_q8(cfg, layers_q8, x0, out, x_last, ws, stream=None, resid=
     st = lib().moe_decode_chain_q8(ctypes.byref(cfg), arr, len(layers_q8), _ptr(x0), _ptr(resid), _ptr(out),
                                    _ptr(x_last), _ptr(ws), ws.numel(), _stream(stream))
     _check("moe_decode_chain_q8", st)
+
+
+def moe_decode_chain_q4(cfg, layers_q4, x0, out, x_last, ws, stream=None, resid=None):
+    """One token through len(layers_q4) layers with 4-bit expert weights (WeightsQ4 list)."""
+    arr = (WeightsQ4 * len(layers_q4))(*layers_q4)
+    st = lib().moe_decode_chain_q4(ctypes.byref(cfg), arr, len(layers_q4), _ptr(x0), _ptr(resid), _ptr(out),
+                                   _ptr(x_last), _ptr(ws), ws.numel(), _stream(stream))
+    _check("moe_decode_chain_q4", st)
+
+
+def moe_quantize_q4(w, q, scale, stream=None):
+    """Block-wise 4-bit codes q (uint8, w's shape with the last dimension halved) and fp32 scales
+    (w's shape with the last dimension / 32) of a bf16 w whose last dimension is the row."""
+    rows, cols = (w.numel() // w.shape[-1]) if w.dim() > 1 else 1, w.shape[-1]
+    st = lib().moe_quantize_q4(_ptr(w), int(rows), int(cols), _ptr(q), _ptr(scale), _stream(stream))
+    _check("moe_quantize_q4", st)
+
+
+def quantize_layer_q4(layer: dict, stream=None) -> dict:
+    """A layer's expert matrices as 4-bit codes and block scales (the router kept as it is), on
+    the device, through moe_quantize_q4."""
+    out = {"w_router": layer["w_router"], "b_router": layer.get("b_router")}
+    for src, q, sc in (("w_gate", "q_gate", "s_gate"), ("w_up", "q_up", "s_up"), ("w_down", "q_down", "s_down"),
+                       ("ws_gate", "qs_gate", "ss_gate"), ("ws_up", "qs_up", "ss_up"),
+                       ("ws_down", "qs_down", "ss_down")):
+        w = layer.get(src)
+        if w is None:
+            continue
+        out[q] = torch.empty(w.shape[:-1] + (w.shape[-1] // 2,), dtype=torch.uint8, device=w.device)
+        out[sc] = torch.empty(w.shape[:-1] + (w.shape[-1] // 32,), dtype=torch.float32, device=w.device)
+        moe_quantize_q4(w, out[q], out[sc], stream)
+    return out
 
 
 def moe_quantize_e4m3(w, q, scale, stream=None):

@@ -27,6 +27,8 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
+#include <mutex>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -830,15 +832,68 @@ __device__ __forceinline__ float dot1_row_smem(const uint4 *w, const uint4 *xs, 
 constexpr int kStageRows = 2;
 constexpr int kStageH = 4096;
 
+// 4-bit codes: w8 is a word of 8 nibbles (columns 8k .. 8k+7, the lowest nibble first) with bit 3
+// of every nibble flipped, so that nibble j holds code + 8.  2^23 + (code + 8) is a float whose
+// low mantissa bits are that nibble; subtracting 2^23 + 8 leaves the code exactly.
+__device__ __forceinline__ float q4_val(uint32_t w8, int j) {
+    return __int_as_float(0x4B000000 | ((w8 >> (4 * j)) & 15u)) - 8388616.0f;
+}
+
+// the 32 codes of one block (16 bytes) against 32 fp32 values, in column order, fp32 sums
+__device__ __forceinline__ float q4_dot32(const uint4 &q, const float (&v)[32]) {
+    const uint32_t w[4] = {q.x ^ 0x88888888u, q.y ^ 0x88888888u, q.z ^ 0x88888888u, q.w ^ 0x88888888u};
+    float a = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a = fmaf(q4_val(w[k], j), v[8 * k + j], a);
+    return a;
+}
+
+// Four rows of H 4-bit codes (nblk = H / 32 blocks of 16 bytes, fp32 scale per block) against x
+// in shared memory (bf16): lane L takes blocks L, L + 32, ..., one at a time (the four rows' codes
+// of a block in flight together); acc[r] += scale * (the block's codes . x).
+__device__ __forceinline__ void dot4_rows_q4(const uint8_t *const (&rows)[4], const float *const (&sc)[4],
+                                             const uint4 *xs, int nblk, int lane, float (&acc)[4]) {
+    for (int c = lane; c < nblk; c += 32) {
+        uint4 w[4];
+        float s[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            w[r] = ld_stream(reinterpret_cast<const uint4 *>(rows[r]) + c);
+            s[r] = __ldg(sc[r] + c);
+        }
+        float xf[32];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 xv = xs[4 * c + i];
+            const __nv_bfloat162 *xb = reinterpret_cast<const __nv_bfloat162 *>(&xv);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float2 f = __bfloat1622float2(xb[m]);
+                xf[8 * i + 2 * m] = f.x;
+                xf[8 * i + 2 * m + 1] = f.y;
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[r] = fmaf(q4_dot32(w[r], xf), s[r], acc[r]);
+    }
+}
+
 __host__ __device__ __forceinline__ size_t chain_stage_off(int H, int E) {
     return ((size_t)kChunkRows * kSlice * 2 + (size_t)H * 2 + (size_t)kSlice * 4 + (size_t)E * 4 + 15) & ~(size_t)15;
 }
 
-// Q8: the expert weights are E4M3 codes with fp32 scales per output row (gate/up rows of H
-// bytes, the down slice 32 bytes a row); the router stays bf16.
-template <bool Q8>
+// The expert weight format WF: kChainBf16; kChainE4m3: E4M3 codes with fp32 scales per output
+// row (gate/up rows of H bytes, the down slice 32 bytes a row); kChainQ4: 4-bit codes with one
+// fp32 scale per block of 32 columns (gate/up rows of H/2 bytes, the down slice 16 bytes a row,
+// which is one block).  The router stays bf16.
+template <int WF>
 __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __grid_constant__ ChainParams p) {
-    constexpr int kWB = Q8 ? 1 : 2;  // bytes per expert weight
+    constexpr bool Q8 = WF == kChainE4m3, Q4 = WF == kChainQ4;
+    // bytes of an expert row of n weights, and of a row of the down slice (kSlice weights)
+    auto row_bytes = [](int n) { return Q4 ? n / 2 : (Q8 ? n : 2 * n); };
+    constexpr int kSliceBytes = Q4 ? kSlice / 2 : (Q8 ? kSlice : 2 * kSlice);
     extern __shared__ uint8_t smem_raw[];
     // aligned by an offset from the shared array itself (not through an integer address), so that
     // every access derived from it compiles to a shared-memory access rather than a generic one
@@ -871,12 +926,13 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
     }
     __syncthreads();
     // TMA of rows [r0, r0 + rows) of a slice's columns into shared memory (as in K2)
+    // (the map's columns are bytes for the code formats: the slice starts at byte row_bytes(i0))
     auto load_chunk = [&](const CUtensorMap *tm, int i0, int base_row, int r0, int rows) {
-        if (lane == 0) ptx::mbar_arrive_expect_tx(&tbar, (uint32_t)(rows * kSlice * kWB));
+        if (lane == 0) ptx::mbar_arrive_expect_tx(&tbar, (uint32_t)(rows * kSliceBytes));
         __syncwarp();
         if (lane < rows / kBoxRows)
-            ptx::tma_load_2d(wd + (size_t)lane * kBoxRows * kSlice * kWB, tm, i0, base_row + r0 + lane * kBoxRows,
-                             &tbar);
+            ptx::tma_load_2d(wd + (size_t)lane * kBoxRows * kSliceBytes, tm, WF == kChainBf16 ? i0 : row_bytes(i0),
+                             base_row + r0 + lane * kBoxRows, &tbar);
     };
     // the router rows of warps 0..1 (e = b + nb * warp) and their biases are staged in shared
     // memory and registers while the previous layer's barrier completes, when every block has at
@@ -995,18 +1051,40 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
                 const int e = s_ids[slot];
                 wt = s_w[slot];
                 base_row = e * H;
-                wg = static_cast<const uint8_t *>(ly.w_gate) + (size_t)e * p.I * H * kWB;
-                wu = static_cast<const uint8_t *>(ly.w_up) + (size_t)e * p.I * H * kWB;
+                wg = static_cast<const uint8_t *>(ly.w_gate) + (size_t)e * p.I * row_bytes(H);
+                wu = static_cast<const uint8_t *>(ly.w_up) + (size_t)e * p.I * row_bytes(H);
                 if (Q8) {
                     sgr = ly.s_gate + (size_t)e * p.I;
                     sur = ly.s_up + (size_t)e * p.I;
                     sdr = ly.s_down + (size_t)e * H;
                 }
+                if (Q4) {  // block scales: gate/up [I, H/32], down [H, I/32]
+                    sgr = ly.s_gate + (size_t)e * p.I * (H / 32);
+                    sur = ly.s_up + (size_t)e * p.I * (H / 32);
+                    sdr = ly.s_down + (size_t)e * H * (p.I / 32);
+                }
             }
             if (warp == kLoadWarp) load_chunk(tm, i0, base_row, 0, rows0);
             pending = true;
+            if constexpr (Q4) {
+                // h for features i0 + warp and i0 + warp + 16: both features' gate and up rows in
+                // flight at once (the rows are a quarter of the bf16 bytes)
+                const int nblk = H / 32;
+                const size_t r0w = (size_t)(i0 + warp), r1w = r0w + kK2Warps;
+                const uint8_t *rows4[4] = {wg + r0w * (H / 2), wu + r0w * (H / 2), wg + r1w * (H / 2),
+                                           wu + r1w * (H / 2)};
+                const float *sc4[4] = {sgr + r0w * nblk, sur + r0w * nblk, sgr + r1w * nblk, sur + r1w * nblk};
+                float a4[4] = {0.f, 0.f, 0.f, 0.f};
+                dot4_rows_q4(rows4, sc4, xs, nblk, lane, a4);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) a4[r] = warp_sum(a4[r]);
+                if (lane == 0) {
+                    hsl[warp] = __bfloat162float(__float2bfloat16_rn(silu_mul(a4[0], a4[1])));
+                    hsl[warp + kK2Warps] = __bfloat162float(__float2bfloat16_rn(silu_mul(a4[2], a4[3])));
+                }
+            }
             // h for features i0 .. i0+31: 16 warps x 2 features
-            for (int f = warp; f < kSlice; f += kK2Warps) {
+            for (int f = warp; f < (Q4 ? 0 : kSlice); f += kK2Warps) {
                 const size_t row = (size_t)(i0 + f);
                 float gs, us;
                 if constexpr (Q8) {
@@ -1039,6 +1117,14 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
                         sdn[i] = n < rows ? __ldg(sdr + r0 + n) : 0.f;
                     }
                 }
+                if constexpr (Q4) {  // row r0 + n's scale of the block this slice is: [rows, I/32]
+                    const int nb_row = (shared_task ? p.Is : p.I) / 32, blk = i0 / 32;
+#pragma unroll
+                    for (int i = 0; i < kChunkRows / kK2Threads; ++i) {
+                        const int n = tid + i * kK2Threads;
+                        sdn[i] = n < rows ? __ldg(sdr + (size_t)(r0 + n) * nb_row + blk) : 0.f;
+                    }
+                }
                 if (tid == 0 && !ptx::mbar_wait(&tbar, ph, kWaitLimitNs, (volatile int *)&s_abort)) s_ok = 0;
                 __syncthreads();
                 if (!s_ok) {
@@ -1046,7 +1132,25 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
                     break;
                 }
                 pending = false;
-                if constexpr (Q8) {
+                if constexpr (Q4) {
+                    // row n of the chunk: 16 bytes, the 32 codes of this slice's block (a warp's 32
+                    // consecutive rows: conflict-free 16-byte reads); h into registers once
+                    float hq[32];
+                    const float4 *h4 = reinterpret_cast<const float4 *>(hsl);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float4 u = h4[j];
+                        hq[4 * j] = u.x, hq[4 * j + 1] = u.y, hq[4 * j + 2] = u.z, hq[4 * j + 3] = u.w;
+                    }
+#pragma unroll
+                    for (int i = 0; i < kChunkRows / kK2Threads; ++i) {
+                        const int n = tid + i * kK2Threads;
+                        if (n >= rows) break;  // rows is a multiple of 128: whole warps leave together
+                        const uint4 q = *reinterpret_cast<const uint4 *>(wd + (size_t)n * kSliceBytes);
+                        const float a = q4_dot32(q, hq) * sdn[i];
+                        atomicAdd(&acc[r0 + n], wt * a);  // the warp's 32 rows: one 128-byte reduction
+                    }
+                } else if constexpr (Q8) {
                     // the row's halves are read in the order n % 2, (n % 2) ^ 1 (against bank conflicts);
                     // n % 2 = tid % 2 for every row of this thread, so h is read into registers once
                     const int hb = tid & 1;
@@ -1226,30 +1330,37 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &tm_down, const
     }
 }
 
-cudaError_t launch_decode_chain(const ChainParams &p, bool q8, cudaStream_t s) {
+cudaError_t launch_decode_chain(const ChainParams &p, int wf, cudaStream_t s) {
     if (p.L < 1 || p.L > kChainMaxLayers || p.H % kBoxRows != 0 || p.H > 16384 || p.E < 1 || p.E > 1024 ||
-        p.k < 1 || p.k > p.E || p.k > 32 || p.I % kSlice != 0 || p.Is % kSlice != 0)
+        p.k < 1 || p.k > p.E || p.k > 32 || p.I % kSlice != 0 || p.Is % kSlice != 0 || wf < 0 || wf > 2)
         return cudaErrorInvalidValue;
-    const void *fn = q8 ? reinterpret_cast<const void *>(decode_chain_kernel<true>)
-                        : reinterpret_cast<const void *>(decode_chain_kernel<false>);
+    const void *fn = wf == kChainE4m3 ? reinterpret_cast<const void *>(decode_chain_kernel<kChainE4m3>)
+                     : wf == kChainQ4 ? reinterpret_cast<const void *>(decode_chain_kernel<kChainQ4>)
+                                      : reinterpret_cast<const void *>(decode_chain_kernel<kChainBf16>);
     const size_t smem = chain_smem(p.H, p.E);
-    static int per_sm[2][64] = {{0}};
+    // per device and format: the shared-memory opt-in and the resident blocks per SM (set once,
+    // under a lock: two host threads' first launches would otherwise race)
+    static int per_sm[3][64] = {{0}};
+    static std::mutex mu;
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 64) return cudaErrorInvalidDevice;
-    if (per_sm[q8][dev] == 0) {
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::unique_lock<std::mutex> lk(mu);
+    if (per_sm[wf][dev] == 0) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)chain_smem(16384, 1024));
         if (e != cudaSuccess) return e;
         int n = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kK2Threads, chain_smem(16384, 1024));
         if (e != cudaSuccess) return e;
         if (n < 1) return cudaErrorInvalidConfiguration;
-        per_sm[q8][dev] = n;
+        per_sm[wf][dev] = n;
     }
+    const int resident = per_sm[wf][dev];
+    lk.unlock();
     // every block must be resident at once (the layers are separated by grid barriers): at most
     // the blocks the GPU holds, each walking items blockIdx.x + i * gridDim.x
     const int n_items = p.Is / kSlice + p.k * (p.I / kSlice);
-    int grid = per_sm[q8][dev] * device_info().sm_count;
+    int grid = resident * device_info().sm_count;
     if (n_items < grid) grid = n_items;
     // the barrier count and abort flag (adjacent words), and the logits' tags
     cudaError_t e = reinterpret_cast<void *>(p.abort) == reinterpret_cast<void *>(p.bar + 1)
@@ -1310,6 +1421,41 @@ cudaError_t launch_quantize_e4m3(const uint16_t *w, int rows, int cols, uint8_t 
     if (rows <= 0 || cols <= 0) return cudaSuccess;
     LaunchScope scope(KC_QUANTIZE, s);
     quantize_e4m3_kernel<<<rows, 256, 0, s>>>(w, cols, q, scale);
+    return cudaGetLastError();
+}
+
+namespace {
+// One warp per block of 32 columns: lane j holds column 32 b + j.  The block's largest magnitude
+// (a warp maximum), its scale, each lane's code, and the lanes' nibbles packed in pairs (column
+// 2m in the low nibble of byte m).  fp32 arithmetic with IEEE division, so the scale and every
+// code follow from the block's values alone.
+__global__ void __launch_bounds__(256) quantize_q4_kernel(const uint16_t *__restrict__ w, int rows, int cols,
+                                                          uint8_t *__restrict__ q, float *__restrict__ scale) {
+    const int nblk = cols / 32;
+    const size_t blk = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (blk >= (size_t)rows * nblk) return;  // the same for the whole warp
+    const int lane = threadIdx.x & 31;
+    const size_t r = blk / nblk, b = blk % nblk;
+    const float v = bf16_to_f(w[r * cols + 32 * b + lane]);
+    float amax = fabsf(v);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float sc = amax > 0.f ? __fdiv_rn(amax, 7.0f) : 1.0f;
+    float c = rintf(__fdiv_rn(v, sc));
+    c = fminf(fmaxf(c, -7.0f), 7.0f);
+    const uint32_t nib = (uint32_t)(int)c & 15u;
+    const uint32_t hi = __shfl_down_sync(0xffffffffu, nib, 1);
+    if ((lane & 1) == 0) q[r * (cols / 2) + 16 * b + lane / 2] = (uint8_t)(nib | (hi << 4));
+    if (lane == 0) scale[r * nblk + b] = sc;
+}
+}  // namespace
+
+cudaError_t launch_quantize_q4(const uint16_t *w, int rows, int cols, uint8_t *q, float *scale, cudaStream_t s) {
+    if (rows <= 0 || cols <= 0) return cudaSuccess;
+    if (cols % 32 != 0) return cudaErrorInvalidValue;
+    const size_t nblocks = (size_t)rows * (cols / 32);
+    LaunchScope scope(KC_QUANTIZE, s);
+    quantize_q4_kernel<<<(unsigned)((nblocks + 7) / 8), 256, 0, s>>>(w, rows, cols, q, scale);
     return cudaGetLastError();
 }
 

@@ -268,9 +268,11 @@ constexpr int kChainMaxLayers = 64;
 struct ChainLayer {
     const uint16_t *w_router;
     const float *b_router;
-    // bf16 expert rows, or (the E4M3 chain) their byte codes
+    // bf16 expert rows, or (the code formats) their codes
     const void *w_gate, *w_up, *ws_gate, *ws_up;
-    // E4M3 chain only: fp32 scales per output row (gate/up [E, I], down [E, H]; shared [Is], [H])
+    // E4M3: fp32 scales per output row (gate/up [E, I], down [E, H]; shared [Is], [H]);
+    // 4-bit codes: per block of 32 columns (gate/up [E, I, H/32], down [E, H, I/32]; shared
+    // [Is, H/32], [H, Is/32])
     const float *s_gate, *s_up, *s_down, *ss_gate, *ss_up, *ss_down;
 };
 struct ChainParams {
@@ -289,12 +291,18 @@ struct ChainParams {
     int *abort;             // zero at launch; set by a block that gives up
     int *status;            // device status word
 };
-// q8: expert weights as E4M3 codes with fp32 row scales (ChainLayer's s_*), W_d maps over bytes
-cudaError_t launch_decode_chain(const ChainParams &p, bool q8, cudaStream_t s);
+// The chain's expert weight formats: bf16; E4M3 codes with fp32 row scales (ChainLayer's s_*);
+// 4-bit codes with fp32 scales per block of 32 columns.  The code formats' W_d maps are over bytes.
+constexpr int kChainBf16 = 0, kChainE4m3 = 1, kChainQ4 = 2;
+cudaError_t launch_decode_chain(const ChainParams &p, int wf, cudaStream_t s);
 // Row-wise E4M3 quantisation: scale[r] = max_c |w[r,c]| / 448 (1 for a zero row),
 // q[r,c] = E4M3(w[r,c] / scale[r]), fp32 arithmetic, round to nearest even, saturating.
 cudaError_t launch_quantize_e4m3(const uint16_t *w, int rows, int cols, uint8_t *q, float *scale,
                                  cudaStream_t s);
+// Block-wise 4-bit quantisation (cols % 32 == 0): per block of 32 columns scale = max |w| / 7 (1 for
+// an all-zero block), code = round-half-even(w / scale) clamped to [-7, 7] (fp32, IEEE division),
+// packed two's-complement nibbles (column 2j low, 2j+1 high); q [rows, cols/2], scale [rows, cols/32].
+cudaError_t launch_quantize_q4(const uint16_t *w, int rows, int cols, uint8_t *q, float *scale, cudaStream_t s);
 
 // Token tiles of a group of c rows: ceil(c / 256) tiles of equal size rounded up to 16 (the
 // MMA's N granularity); the last tile takes the remainder.  Shared by the permutation (tile

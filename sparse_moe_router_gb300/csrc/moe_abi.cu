@@ -229,6 +229,18 @@ moe_status check_weights_q8(const moe_config *c, const moe_weights_q8 *w) {
     return MOE_OK;
 }
 
+moe_status check_weights_q4(const moe_config *c, const moe_weights_q4 *w) {
+    if (!w) return MOE_ERR_INVALID_ARG;
+    if (!w->w_router || !aligned16(w->w_router) || !w->q_gate || !w->q_up || !w->q_down || !w->s_gate ||
+        !w->s_up || !w->s_down || !aligned16(w->q_gate) || !aligned16(w->q_up) || !aligned16(w->q_down))
+        return MOE_ERR_INVALID_ARG;
+    if (c->shared_inter > 0 &&
+        (!w->qs_gate || !w->qs_up || !w->qs_down || !w->ss_gate || !w->ss_up || !w->ss_down ||
+         !aligned16(w->qs_gate) || !aligned16(w->qs_up) || !aligned16(w->qs_down)))
+        return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
 moe_status check_ws(const moe_config *c, void *ws, size_t ws_bytes, int T) {
     if (!ws) return MOE_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_INVALID_ARG;
@@ -805,7 +817,7 @@ moe_status moe_decode_chain(const moe_config *cfg, const moe_weights *layers, in
             p.tm_sdown[l] = p.tm_down[l];
         }
     }
-    MOE_CUDA(launch_decode_chain(p, false, static_cast<cudaStream_t>(stream)));
+    MOE_CUDA(launch_decode_chain(p, kChainBf16, static_cast<cudaStream_t>(stream)));
     return MOE_OK;
 }
 
@@ -835,7 +847,47 @@ moe_status moe_decode_chain_q8(const moe_config *cfg, const moe_weights_q8 *laye
             p.tm_sdown[l] = p.tm_down[l];
         }
     }
-    MOE_CUDA(launch_decode_chain(p, true, static_cast<cudaStream_t>(stream)));
+    MOE_CUDA(launch_decode_chain(p, kChainE4m3, static_cast<cudaStream_t>(stream)));
+    return MOE_OK;
+}
+
+moe_status moe_decode_chain_q4(const moe_config *cfg, const moe_weights_q4 *layers, int n_layers,
+                               const moe_bf16 *x0, const moe_bf16 *resid, moe_bf16 *out, moe_bf16 *x_last,
+                               void *ws, size_t ws_bytes, void *stream) {
+    NvtxRange nvtx_range("moe_decode_chain_q4");
+    if (!layers) return MOE_ERR_INVALID_ARG;
+    static thread_local ChainParams p;
+    MOE_TRY(chain_common(cfg, n_layers, x0, resid, out, x_last, ws, ws_bytes, p));
+    const bool shared = cfg->shared_inter > 0;
+    for (int l = 0; l < n_layers; ++l) MOE_TRY(check_weights_q4(cfg, &layers[l]));
+    const int H = cfg->hidden;
+    const uint32_t sl = (uint32_t)decode_slice(), br = (uint32_t)decode_box_rows();
+    for (int l = 0; l < n_layers; ++l) {
+        const moe_weights_q4 &w = layers[l];
+        p.lay[l] = ChainLayer{w.w_router, w.b_router, w.q_gate, w.q_up, w.qs_gate, w.qs_up,
+                              w.s_gate, w.s_up, w.s_down, w.ss_gate, w.ss_up, w.ss_down};
+        // W_d as byte rows of I/2 codes; a box is a slice's 16 bytes of kBoxRows rows
+        if (!encode_tmap_2d(&p.tm_down[l], w.q_down, (uint64_t)cfg->n_experts * H, cfg->inter / 2, br, sl / 2, false,
+                            CU_TENSOR_MAP_DATA_TYPE_UINT8, 1))
+            return MOE_ERR_CUDA;
+        if (shared) {
+            if (!encode_tmap_2d(&p.tm_sdown[l], w.qs_down, H, cfg->shared_inter / 2, br, sl / 2, false,
+                                CU_TENSOR_MAP_DATA_TYPE_UINT8, 1))
+                return MOE_ERR_CUDA;
+        } else {
+            p.tm_sdown[l] = p.tm_down[l];
+        }
+    }
+    MOE_CUDA(launch_decode_chain(p, kChainQ4, static_cast<cudaStream_t>(stream)));
+    return MOE_OK;
+}
+
+moe_status moe_quantize_q4(const moe_bf16 *w, int rows, int cols, uint8_t *q, float *scale, void *stream) {
+    NvtxRange nvtx_range("moe_quantize_q4");
+    if (rows < 0 || cols < 0 || cols % 32 != 0) return MOE_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return MOE_OK;
+    if (!w || !q || !scale) return MOE_ERR_INVALID_ARG;
+    MOE_CUDA(launch_quantize_q4(w, rows, cols, q, scale, static_cast<cudaStream_t>(stream)));
     return MOE_OK;
 }
 

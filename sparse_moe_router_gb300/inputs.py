@@ -167,6 +167,45 @@ def make_q8(w: Workload, device="cpu", n_layers: Optional[int] = None, T: Option
     return layers, x
 
 
+def _q4_bytes(gen, shape, device):
+    """Bytes of two 4-bit fields each uniform over the 15 patterns other than 8 (0b1000): bit
+    patterns only, nothing here decodes them."""
+    lo = torch.randint(0, 15, shape, generator=gen, device=device, dtype=torch.int32)
+    hi = torch.randint(0, 15, shape, generator=gen, device=device, dtype=torch.int32)
+    lo = lo + (lo >= 8).to(torch.int32)
+    hi = hi + (hi >= 8).to(torch.int32)
+    return (lo | (hi << 4)).to(torch.uint8)
+
+
+def make_q4(w: Workload, device="cpu", n_layers: Optional[int] = None, T: Optional[int] = None,
+            scale_base: float = 5e-3):
+    """Layers with 4-bit expert weights and the input x, for the 4-bit path.
+
+    Per layer, in this order: W_r and b as in ``make_layer``; then for W_g, W_u, W_d and the shared
+    expert's three matrices, the packed codes (each 4-bit field uniform over the 15 patterns other
+    than 0b1000) followed by one fp32 scale per block of 32 columns, uniform in [0.5, 1.5] *
+    scale_base.  The default base puts the weights near the bf16 workloads' 0.02.  Then x ~ N(0, 1).
+    Keys as in ``make_q8``: codes [rows, cols/2], scales [rows, cols/32].
+    """
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed)
+    s = w.shape
+    H, E, I, Is = s.hidden, s.n_experts, s.inter, s.shared_inter
+    layers = []
+    for _ in range(w.n_layers if n_layers is None else n_layers):
+        layer = _make_router(w, gen, device)
+        mats = [("q_gate", "s_gate", (E, I, H)), ("q_up", "s_up", (E, I, H)), ("q_down", "s_down", (E, H, I))]
+        if Is > 0:
+            mats += [("qs_gate", "ss_gate", (Is, H)), ("qs_up", "ss_up", (Is, H)), ("qs_down", "ss_down", (H, Is))]
+        for qn, sn, shp in mats:
+            layer[qn] = _q4_bytes(gen, shp[:-1] + (shp[-1] // 2,), device)
+            layer[sn] = _scales(gen, shp[:-1] + (shp[-1] // 32,), scale_base, device)
+        layers.append(layer)
+    TT = w.T if T is None else T
+    x = _normal_bf16(gen, (TT, w.shape.hidden), w.x_std, device)
+    return layers, x
+
+
 def custom(shape: Shape, T: int, seed: int, router_std: float = 0.02, zipf_s=None,
            n_dead: int = 0, n_layers: int = 1, name: str = "custom") -> Workload:
     return Workload(name, shape, T=T, n_layers=n_layers, seed=seed, router_std=router_std,
