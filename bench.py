@@ -155,14 +155,14 @@ class ClockSampler:
 # expert, T=8192, H=2048, E=256, k=8, I=I_s=512) from an ncu capture of the current kernel, or None
 # while the kernel has changed since the last capture: 1.42150 GB read + 72.92 MB written.
 GATEUP_DRAM_BYTES = 1_494_418_856
-# the same per layer for the one-token decode chain (decode_chain_kernel, H=2048, E=256, k=8,
-# I=I_s=512), or None until captured for the current kernel.
-DECODE_CHAIN_DRAM_BYTES_PER_LAYER = None
-# the same for the chain on E4M3 expert weights (decode_chain_kernel<1>), or None until captured
-# for the current kernel.
-DECODE_CHAIN_Q8_DRAM_BYTES_PER_LAYER = None
-# the same for the chain on 4-bit expert weights (decode_chain_kernel<2>), or None until captured.
-DECODE_CHAIN_Q4_DRAM_BYTES_PER_LAYER = None
+# the same per layer for the one-token decode chain on bf16 weights (decode_chain_kernel<0>,
+# H=2048, E=256, k=8, I=I_s=512; a 2-layer capture halved), or None until captured for the current
+# kernel: 115.42 MB read + 3.31 MB written for 2 layers.
+DECODE_CHAIN_DRAM_BYTES_PER_LAYER = 59_366_272
+# the same for the chain on E4M3 expert weights (decode_chain_kernel<1>): 59.02 MB + 0.52 MB.
+DECODE_CHAIN_Q8_DRAM_BYTES_PER_LAYER = 29_772_928
+# the same for the chain on 4-bit expert weights (decode_chain_kernel<2>): 37.58 MB + 0.02 MB.
+DECODE_CHAIN_Q4_DRAM_BYTES_PER_LAYER = 18_796_800
 
 
 def _algorithmic(shape, T, experts_touched=None):
