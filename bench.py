@@ -157,12 +157,12 @@ class ClockSampler:
 GATEUP_DRAM_BYTES = 1_494_418_856
 # the same per layer for the one-token decode chain on bf16 weights (decode_chain_kernel<0>,
 # H=2048, E=256, k=8, I=I_s=512; a 2-layer capture halved), or None until captured for the current
-# kernel: 115.42 MB read + 3.31 MB written for 2 layers.
-DECODE_CHAIN_DRAM_BYTES_PER_LAYER = 59_366_272
-# the same for the chain on E4M3 expert weights (decode_chain_kernel<1>): 59.02 MB + 0.52 MB.
-DECODE_CHAIN_Q8_DRAM_BYTES_PER_LAYER = 29_772_928
-# the same for the chain on 4-bit expert weights (decode_chain_kernel<2>): 37.58 MB + 0.02 MB.
-DECODE_CHAIN_Q4_DRAM_BYTES_PER_LAYER = 18_796_800
+# kernel: 115.68 MB read + 3.40 MB written for 2 layers.
+DECODE_CHAIN_DRAM_BYTES_PER_LAYER = 59_542_144
+# the same for the chain on E4M3 expert weights (decode_chain_kernel<1>): 59.02 MB + 0.55 MB.
+DECODE_CHAIN_Q8_DRAM_BYTES_PER_LAYER = 29_783_296
+# the same for the chain on 4-bit expert weights (decode_chain_kernel<2>): 37.70 MB + 0.03 MB.
+DECODE_CHAIN_Q4_DRAM_BYTES_PER_LAYER = 18_863_104
 
 
 def _algorithmic(shape, T, experts_touched=None):

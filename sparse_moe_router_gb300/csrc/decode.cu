@@ -61,17 +61,37 @@ __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// c + a * b for bf16 halves of two 32-bit words (HA, HB: 0 low, 1 high), in fp32 with one
+// rounding.  A product of two bf16 values is exact in fp32, so this is fmaf on the widened values.
+template <int HA, int HB>
+__device__ __forceinline__ float fma_bf16h(uint32_t a2, uint32_t b2, float c) {
+    float d;
+    if constexpr (HA == 0 && HB == 0)
+        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, a0, b0, %3;\n\t}" : "=f"(d) : "r"(a2), "r"(b2), "f"(c));
+    else if constexpr (HA == 0)
+        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, a0, b1, %3;\n\t}" : "=f"(d) : "r"(a2), "r"(b2), "f"(c));
+    else if constexpr (HB == 0)
+        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, a1, b0, %3;\n\t}" : "=f"(d) : "r"(a2), "r"(b2), "f"(c));
+    else
+        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, a1, b1, %3;\n\t}" : "=f"(d) : "r"(a2), "r"(b2), "f"(c));
+    return d;
+}
+
+// 8 bf16 weights against 8 bf16 values, in order, fp32 sums
 __device__ __forceinline__ float dot8(const uint4 &w, const uint4 &x) {
-    const __nv_bfloat162 *wp = reinterpret_cast<const __nv_bfloat162 *>(&w);
-    const __nv_bfloat162 *xp = reinterpret_cast<const __nv_bfloat162 *>(&x);
     float acc = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 a = __bfloat1622float2(wp[i]);
-        const float2 b = __bfloat1622float2(xp[i]);
-        acc = fmaf(a.x, b.x, acc);
-        acc = fmaf(a.y, b.y, acc);
-    }
+    acc = fma_bf16h<0, 0>(w.x, x.x, acc);
+    acc = fma_bf16h<1, 1>(w.x, x.x, acc);
+    acc = fma_bf16h<0, 0>(w.y, x.y, acc);
+    acc = fma_bf16h<1, 1>(w.y, x.y, acc);
+    acc = fma_bf16h<0, 0>(w.z, x.z, acc);
+    acc = fma_bf16h<1, 1>(w.z, x.z, acc);
+    acc = fma_bf16h<0, 0>(w.w, x.w, acc);
+    acc = fma_bf16h<1, 1>(w.w, x.w, acc);
     return acc;
 }
 
@@ -832,21 +852,39 @@ __device__ __forceinline__ float dot1_row_smem(const uint4 *w, const uint4 *xs, 
 constexpr int kStageRows = 2;
 constexpr int kStageH = 4096;
 
-// 4-bit codes: w8 is a word of 8 nibbles (columns 8k .. 8k+7, the lowest nibble first) with bit 3
-// of every nibble flipped, so that nibble j holds code + 8.  2^23 + (code + 8) is a float whose
-// low mantissa bits are that nibble; subtracting 2^23 + 8 leaves the code exactly.
-__device__ __forceinline__ float q4_val(uint32_t w8, int j) {
-    return __int_as_float(0x4B000000 | ((w8 >> (4 * j)) & 15u)) - 8388616.0f;
+// 4-bit codes: a word holds 8 nibbles, columns 8k .. 8k+7 with the lowest nibble first.  Flipping
+// bit 3 of every nibble turns the two's-complement code into code + 8.
+
+// Nibbles s and s + 4 of an offset-8 code word (two's-complement nibble ^ 8) as two bf16 codes:
+// 0x4300 | u is the bf16 value 128 + u (u < 16 fits its 7 fraction bits), and subtracting 136
+// leaves u - 8, the code, exactly.
+__device__ __forceinline__ uint32_t q4_pair_bf16(uint32_t w, int s) {
+    const uint32_t t = ((w >> (4 * s)) & 0x000F000Fu) | 0x43004300u;
+    uint32_t c;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(c) : "r"(t), "r"(0x43084308u));
+    return c;
 }
 
-// the 32 codes of one block (16 bytes) against 32 fp32 values, in column order, fp32 sums
-__device__ __forceinline__ float q4_dot32(const uint4 &q, const float (&v)[32]) {
+// the 32 codes of one block (16 bytes) against 32 bf16 values (16 words, column 2m in the low
+// half of word m), in column order, fp32 sums: the products and sums of fmaf on the widened
+// codes and values, bit for bit
+__device__ __forceinline__ float q4_dot32(const uint4 &q, const uint32_t (&v)[16]) {
     const uint32_t w[4] = {q.x ^ 0x88888888u, q.y ^ 0x88888888u, q.z ^ 0x88888888u, q.w ^ 0x88888888u};
     float a = 0.f;
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) a = fmaf(q4_val(w[k], j), v[8 * k + j], a);
+    for (int k = 0; k < 4; ++k) {
+        // c_s holds columns 8k + s (low) and 8k + s + 4 (high)
+        const uint32_t c0 = q4_pair_bf16(w[k], 0), c1 = q4_pair_bf16(w[k], 1);
+        const uint32_t c2 = q4_pair_bf16(w[k], 2), c3 = q4_pair_bf16(w[k], 3);
+        a = fma_bf16h<0, 0>(c0, v[4 * k], a);
+        a = fma_bf16h<0, 1>(c1, v[4 * k], a);
+        a = fma_bf16h<0, 0>(c2, v[4 * k + 1], a);
+        a = fma_bf16h<0, 1>(c3, v[4 * k + 1], a);
+        a = fma_bf16h<1, 0>(c0, v[4 * k + 2], a);
+        a = fma_bf16h<1, 1>(c1, v[4 * k + 2], a);
+        a = fma_bf16h<1, 0>(c2, v[4 * k + 3], a);
+        a = fma_bf16h<1, 1>(c3, v[4 * k + 3], a);
+    }
     return a;
 }
 
@@ -863,20 +901,14 @@ __device__ __forceinline__ void dot4_rows_q4(const uint8_t *const (&rows)[4], co
             w[r] = ld_stream(reinterpret_cast<const uint4 *>(rows[r]) + c);
             s[r] = __ldg(sc[r] + c);
         }
-        float xf[32];
+        uint32_t xw[16];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const uint4 xv = xs[4 * c + i];
-            const __nv_bfloat162 *xb = reinterpret_cast<const __nv_bfloat162 *>(&xv);
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const float2 f = __bfloat1622float2(xb[m]);
-                xf[8 * i + 2 * m] = f.x;
-                xf[8 * i + 2 * m + 1] = f.y;
-            }
+            xw[4 * i] = xv.x, xw[4 * i + 1] = xv.y, xw[4 * i + 2] = xv.z, xw[4 * i + 3] = xv.w;
         }
 #pragma unroll
-        for (int r = 0; r < 4; ++r) acc[r] = fmaf(q4_dot32(w[r], xf), s[r], acc[r]);
+        for (int r = 0; r < 4; ++r) acc[r] = fmaf(q4_dot32(w[r], xw), s[r], acc[r]);
     }
 }
 
@@ -1135,12 +1167,14 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
                 if constexpr (Q4) {
                     // row n of the chunk: 16 bytes, the 32 codes of this slice's block (a warp's 32
                     // consecutive rows: conflict-free 16-byte reads); h into registers once
-                    float hq[32];
+                    // (h is bf16-rounded: its fp32 words' high halves are its bf16 bits)
+                    uint32_t hq[16];
                     const float4 *h4 = reinterpret_cast<const float4 *>(hsl);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const float4 u = h4[j];
-                        hq[4 * j] = u.x, hq[4 * j + 1] = u.y, hq[4 * j + 2] = u.z, hq[4 * j + 3] = u.w;
+                        hq[2 * j] = __byte_perm(__float_as_uint(u.x), __float_as_uint(u.y), 0x7632);
+                        hq[2 * j + 1] = __byte_perm(__float_as_uint(u.z), __float_as_uint(u.w), 0x7632);
                     }
 #pragma unroll
                     for (int i = 0; i < kChunkRows / kK2Threads; ++i) {
@@ -1196,15 +1230,16 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
                 // pipe, which also carries shuffles and narrow loads: h comes in 16-byte loads and
                 // each row is added on its own, the warp's 32 rows in one reduction.)
                 const int rot = (tid >> 1) & 3;
-                float hr[32];
+                // h is bf16-rounded: its fp32 words' high halves are its bf16 bits, two a word
+                uint32_t hr[16];
                 const float4 *h4 = reinterpret_cast<const float4 *>(hsl);
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         const float4 u = h4[((cc + rot) & 3) * 2 + j];
-                        hr[cc * 8 + 4 * j] = u.x, hr[cc * 8 + 4 * j + 1] = u.y;
-                        hr[cc * 8 + 4 * j + 2] = u.z, hr[cc * 8 + 4 * j + 3] = u.w;
+                        hr[cc * 4 + 2 * j] = __byte_perm(__float_as_uint(u.x), __float_as_uint(u.y), 0x7632);
+                        hr[cc * 4 + 2 * j + 1] = __byte_perm(__float_as_uint(u.z), __float_as_uint(u.w), 0x7632);
                     }
                 for (int n = tid; n < rows; n += kK2Threads) {
                     const uint4 *rw = reinterpret_cast<const uint4 *>(wd + (size_t)n * kSlice * 2);
@@ -1214,12 +1249,11 @@ __global__ void __launch_bounds__(kK2Threads, 1) decode_chain_kernel(const __gri
                     float a = 0.f;
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
-                        const __nv_bfloat162 *bq = reinterpret_cast<const __nv_bfloat162 *>(&q[cc]);
+                        const uint32_t qw[4] = {q[cc].x, q[cc].y, q[cc].z, q[cc].w};
 #pragma unroll
                         for (int m = 0; m < 4; ++m) {
-                            const float2 fv = __bfloat1622float2(bq[m]);
-                            a = fmaf(fv.x, hr[cc * 8 + 2 * m], a);
-                            a = fmaf(fv.y, hr[cc * 8 + 2 * m + 1], a);
+                            a = fma_bf16h<0, 0>(qw[m], hr[cc * 4 + m], a);
+                            a = fma_bf16h<1, 1>(qw[m], hr[cc * 4 + m], a);
                         }
                     }
                     atomicAdd(&acc[r0 + n], wt * a);  // the warp's 32 rows: one 128-byte reduction

@@ -44,18 +44,30 @@ def residual_step(r_u16, out_u16):
     return np.array([orc.double_to_bf16(t) for t in v.ravel()], dtype=np.uint16).reshape(v.shape)
 
 
-def check_x_last(x_last_u16, r_u16, out_u16, fixed_resid):
-    """x_last = bf16(r + out).  With a fixed residual r the chain adds exactly that r: bit-exact.
-    Without one, r is the chain's own x_l, rebuilt inside the launch from the previous layer's
-    split-K sum, whose fp32 atomics may land one bf16 step away from the x_l the caller holds
-    (from a shorter run): then x_last may differ by one bf16 step at |x_last|."""
+def check_x_last(x_last_u16, r_u16, out_u16, exact):
+    """x_last = bf16(r + out).
+
+    exact: r is exactly the chain's last input (a fixed residual, or x_0 for a one-layer chain):
+    bit-exact.  Otherwise r is the caller's copy of x_{n-1}, taken from an earlier, shorter launch,
+    while the chain rebuilds its own x_{n-1} inside the launch.  The split-K down sums are fp32
+    atomics whose order changes from launch to launch, so the two copies of an x_l can differ by a
+    bf16 step in a few elements, and a changed input element moves every dot product of the next
+    layer: across layers such differences reach tens of elements of a 2048-wide row (measured up
+    to 65, about 1 in 3 repetitions at 3 layers).  Then x_last is checked in aggregate: relative L2
+    of x_last - bf16(r + out) within the layer tolerance's 5e-3, and at most 5 % of the elements
+    more than one bf16 step (at the larger of |r|, |x_last| and |bf16(r + out)|) away."""
     want = residual_step(r_u16, out_u16)
-    if fixed_resid:
+    if exact:
         np.testing.assert_array_equal(x_last_u16, want)
         return
     a, b = orc.bf16_to_f64(x_last_u16), orc.bf16_to_f64(want)
-    step = np.ldexp(1.0, np.frexp(np.maximum(np.maximum(np.abs(a), np.abs(b)), 2.0 ** -126))[1] - 8)
-    assert np.all(np.abs(a - b) <= step), "x_last: %d elements beyond one bf16 step" % int((np.abs(a - b) > step).sum())
+    r = orc.bf16_to_f64(r_u16)
+    mag = np.maximum(np.maximum(np.abs(a), np.abs(b)), np.abs(r))
+    step = np.ldexp(1.0, np.frexp(np.maximum(mag, 2.0 ** -126))[1] - 8)
+    n_over = int((np.abs(a - b) > step).sum())
+    rel = float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+    assert rel <= 5e-3, "x_last: relative L2 %.3g against bf16(r + out)" % rel
+    assert n_over <= 0.05 * a.size, "x_last: %d of %d elements beyond one bf16 step" % (n_over, a.size)
 
 
 def bf16_spacing(v_f64):
