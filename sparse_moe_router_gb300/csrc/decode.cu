@@ -531,12 +531,19 @@ __global__ void __maxnreg__(NT == 1 ? 104 : 128)
             // chunk order (cc + n/2) % 4 is the same for every row of this thread (rows tid + 512 i):
             // with one token its h is read into registers once, in that order.
             const int rot = (tid >> 1) & 3;
-            float hr[NT == 1 ? 32 : 1];
+            // one token: h (bf16-rounded, so its fp32 words' high halves are its bf16 bits) packed
+            // two features a word
+            uint32_t hr[NT == 1 ? 16 : 1];
             if constexpr (NT == 1) {
+                const float4 *h4 = reinterpret_cast<const float4 *>(hsl);
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) hr[cc * 8 + j] = hsl[((cc + rot) & 3) * 8 + j];
+                    for (int j = 0; j < 2; ++j) {
+                        const float4 u = h4[((cc + rot) & 3) * 2 + j];
+                        hr[cc * 4 + 2 * j] = __byte_perm(__float_as_uint(u.x), __float_as_uint(u.y), 0x7632);
+                        hr[cc * 4 + 2 * j + 1] = __byte_perm(__float_as_uint(u.z), __float_as_uint(u.w), 0x7632);
+                    }
             }
             for (int n = tid; n < rows; n += kK2Threads) {
                 const uint4 *rw = reinterpret_cast<const uint4 *>(wd + (size_t)n * kSlice);
@@ -551,16 +558,23 @@ __global__ void __maxnreg__(NT == 1 ? 104 : 128)
                     float acc = 0.f;
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
-                        const int c = (cc + rot) & 3;
-                        const __nv_bfloat162 *bq = reinterpret_cast<const __nv_bfloat162 *>(&q[cc]);
-                        const float *hf = hsl + t * kSlice + c * 8;
+                        if constexpr (NT == 1) {
+                            const uint32_t qw[4] = {q[cc].x, q[cc].y, q[cc].z, q[cc].w};
 #pragma unroll
-                        for (int m = 0; m < 4; ++m) {
-                            const float2 fv = __bfloat1622float2(bq[m]);
-                            const float h0 = NT == 1 ? hr[cc * 8 + 2 * m] : hf[2 * m];
-                            const float h1 = NT == 1 ? hr[cc * 8 + 2 * m + 1] : hf[2 * m + 1];
-                            acc = fmaf(fv.x, h0, acc);
-                            acc = fmaf(fv.y, h1, acc);
+                            for (int m = 0; m < 4; ++m) {
+                                acc = fma_bf16h<0, 0>(qw[m], hr[cc * 4 + m], acc);
+                                acc = fma_bf16h<1, 1>(qw[m], hr[cc * 4 + m], acc);
+                            }
+                        } else {
+                            const int c = (cc + rot) & 3;
+                            const __nv_bfloat162 *bq = reinterpret_cast<const __nv_bfloat162 *>(&q[cc]);
+                            const float *hf = hsl + t * kSlice + c * 8;
+#pragma unroll
+                            for (int m = 0; m < 4; ++m) {
+                                const float2 fv = __bfloat1622float2(bq[m]);
+                                acc = fmaf(fv.x, hf[2 * m], acc);
+                                acc = fmaf(fv.y, hf[2 * m + 1], acc);
+                            }
                         }
                     }
                     // lanes 4q..4q+3 hold rows n..n+3: one 16-byte reduction per four rows

@@ -696,10 +696,12 @@ __global__ void __launch_bounds__(Cfg<EPI, Q8>::kThreads, 1)
                                                 __byte_perm(c.x, c.y, 0x7632), __byte_perm(c.z, c.w, 0x7632));
                     const size_t col = (size_t)ftile * BM + quarter * 32 + seg * 8;
                     const int or0 = meta_row[mb + 2 * m], or1 = meta_row[mb + 2 * m + 1];
+                    // y is read once, by the finalise: streaming stores leave L2 to the weight and
+                    // h tiles that the next tiles read again
                     if (j0 + 2 * m < t.nvalid && or0 >= 0)
-                        *reinterpret_cast<uint4 *>(&o[(size_t)or0 * p.ld + col]) = e0;
+                        __stcs(reinterpret_cast<uint4 *>(&o[(size_t)or0 * p.ld + col]), e0);
                     if (j0 + 2 * m + 1 < t.nvalid && or1 >= 0)
-                        *reinterpret_cast<uint4 *>(&o[(size_t)or1 * p.ld + col]) = e1;
+                        __stcs(reinterpret_cast<uint4 *>(&o[(size_t)or1 * p.ld + col]), e1);
                     __syncwarp();
                 }
             }

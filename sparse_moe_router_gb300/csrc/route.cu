@@ -432,8 +432,9 @@ __global__ void __launch_bounds__(256) finalize_kernel(const uint16_t *__restric
         const size_t t = i / H8, c = i % H8;
         float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         const uint4 *yr = reinterpret_cast<const uint4 *>(y) + (t * k) * H8 + c;
+        // the weighted rows are read once: evict-first loads leave L2 to the data read again
         for (int j = 0; j < k; ++j) {
-            const uint4 q = __ldg(yr + (size_t)j * H8);
+            const uint4 q = __ldcs(yr + (size_t)j * H8);
             const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&q);
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
@@ -461,7 +462,8 @@ __global__ void __launch_bounds__(256) finalize_kernel(const uint16_t *__restric
         __align__(16) __nv_bfloat16 o[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) o[j] = __float2bfloat16_rn(v[j]);
-        reinterpret_cast<uint4 *>(out)[i] = *reinterpret_cast<const uint4 *>(o);
+        // out is not read again in a layer stack (x_next is): a streaming store
+        __stcs(reinterpret_cast<uint4 *>(out) + i, *reinterpret_cast<const uint4 *>(o));
         if (x_next) {
             const uint4 xr = reinterpret_cast<const uint4 *>(resid)[i];
             const __nv_bfloat16 *xb = reinterpret_cast<const __nv_bfloat16 *>(&xr);
@@ -644,14 +646,16 @@ __global__ void __launch_bounds__(256)
         }
         const uint4 *src = x + (size_t)t * H8;
         int i = lane;
+        // x is read k times and stays in L2; the copies (k times its size) are written with
+        // streaming stores so that they do not push it out
         for (; i + 224 < H8; i += 256) {  // eight 16-byte loads a lane in flight (a 4 KB row per warp)
             uint4 v[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) v[u] = __ldg(&src[i + 32 * u]);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) dst[i + 32 * u] = v[u];
+            for (int u = 0; u < 8; ++u) __stcs(&dst[i + 32 * u], v[u]);
         }
-        for (; i < H8; i += 32) dst[i] = __ldg(&src[i]);
+        for (; i < H8; i += 32) __stcs(&dst[i], __ldg(&src[i]));
     }
 }
 
