@@ -1,5 +1,6 @@
 // decode.cu -- the single-token (T = 1) layer: every weight byte the token needs is streamed
-// from HBM once with 128-bit loads (or TMA), fp32 accumulation.
+// from HBM once with 128-bit loads (or TMA), fp32 accumulation.  A bf16 product is taken by the
+// mixed-precision FMA (bf16 x bf16 into an fp32 sum), with no widening of the operands first.
 //
 // Batch-1 decode is the pages' execution mode ("AIMA AMD395 Qwen3.6 35B Windows Engine",
 // "产品定位": batch size 1, greedy decode).  At T = 1 each selected expert is a matrix-vector
